@@ -1,0 +1,370 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: values the pages print,
+closed forms, a textbook library routine, brute force on tiny inputs, finite differences,
+or an invariant. A plausible slip in the oracle (a dropped term, a wrong index or sign, a
+transposed operand, a wrong tie rule, a non-causal summary) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import pisa_oracle as po
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed, scale=1.0):
+    r = np.random.default_rng(seed)
+    # bf16-exact values, like the real inputs
+    return torch.from_numpy(r.standard_normal(shape) * scale).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------- pyramid geometry
+def test_level_counts_match_printed_values():
+    with open(os.path.join(GOLD, "level_counts.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        sizes = po.level_sizes(c["N"], c["C"])
+        if "levels" in c:
+            assert len(sizes) == c["levels"]
+            assert sizes[0] == c["leaves"]
+        if "pooled_levels" in c:
+            assert len(sizes) - 1 == c["pooled_levels"]
+            assert len(sizes) - 1 == math.ceil(math.log2(c["N"] / c["C"]))
+
+
+@pytest.mark.parametrize("N,C", [(64, 4), (67, 4), (40, 8), (8, 8), (1, 8), (129, 16)])
+def test_pyramid_sums_are_direct_range_means(N, C):
+    K = _rand((N, 5), 1)
+    sums = po.pyramid_sums(K, C)
+    # merge factor 2: a parent is the sum of its two children (closed form)
+    for l in range(1, len(sums)):
+        for m in range(len(sums[l])):
+            kids = [c for c in (2 * m, 2 * m + 1) if c < len(sums[l - 1])]
+            np.testing.assert_allclose(sums[l][m], sum(sums[l - 1][c] for c in kids), rtol=1e-12, atol=1e-12)
+    # leaf means against pure-Python token loops
+    for t in range(len(sums[0])):
+        toks = [j for j in range(N) if j // C == t]
+        ref = [sum(K[j, k] for j in toks) / len(toks) for k in range(5)]
+        np.testing.assert_allclose(sums[0][t] / len(toks), ref, rtol=1e-12, atol=1e-12)
+    assert len(sums[-1]) == 1
+    np.testing.assert_allclose(sums[-1][0], K.sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_mean_pooling_equals_library_avg_pool():
+    N, C, d = 256, 8, 6
+    K = _rand((N, d), 2)
+    sums = po.pyramid_sums(K, C)
+    x = torch.from_numpy(K.T.copy()).unsqueeze(0)             # [1, d, N]
+    for l in range(len(sums)):
+        pooled = torch.nn.functional.avg_pool1d(x, kernel_size=C << l, stride=C << l)[0].T.numpy()
+        np.testing.assert_allclose(sums[l] / (C << l), pooled, rtol=1e-12, atol=1e-12)
+
+
+def test_causal_means_match_direct_prefix_means():
+    N, C, d = 45, 4, 3
+    K = _rand((N, d), 3)
+    summ = po.CausalKeySummaries(K, C)
+    for l, n in enumerate(summ.sizes):
+        for m in range(n):
+            s, e = po.node_range(l, m, C, N)
+            for i in range(N):
+                if s > i:
+                    assert not summ.visible(l, m, i)
+                    continue
+                assert summ.visible(l, m, i)
+                ref = K[s:min(e, i + 1)].mean(axis=0)
+                np.testing.assert_allclose(summ.means(l, np.array([m]), i)[0], ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- descent vs brute force
+def _bf_mean(K, l, m, i, C):
+    N = K.shape[0]
+    toks = [j for j in range(m * (C << l), min((m + 1) * (C << l), N)) if j <= i]
+    return [sum(K[j, k] for j in toks) / len(toks) for k in range(K.shape[1])]
+
+
+def _bf_score(q, K, l, m, i, C, s):
+    """Independent scalar-loop enumerator of S_i(l, m)."""
+    N = K.shape[0]
+    tot = 0.0
+    for h in range(q.shape[0]):
+        if l == 0:
+            vals = [s * sum(q[h, k] * K[j, k] for k in range(K.shape[1]))
+                    for j in range(m * C, min((m + 1) * C, N)) if j <= i]
+        else:
+            vals = []
+            for c in (2 * m, 2 * m + 1):
+                if c * (C << (l - 1)) <= i and c * (C << (l - 1)) < N:
+                    mu = _bf_mean(K, l - 1, c, i, C)
+                    vals.append(s * sum(q[h, k] * mu[k] for k in range(K.shape[1])))
+        mx = max(vals)
+        tot += mx + math.log(sum(math.exp(v - mx) for v in vals))
+    return tot
+
+
+def _bf_select(q, K, i, C, Ksel, s):
+    N = K.shape[0]
+    n = [-(-N // C)]
+    while n[-1] > 1:
+        n.append(-(-n[-1] // 2))
+    table = {}
+    for l in range(len(n)):
+        for m in range(n[l]):
+            if m * (C << l) <= i:
+                table[(l, m)] = _bf_score(q, K, l, m, i, C, s)
+    kept = {0}
+    for l in range(len(n) - 2, -1, -1):
+        cand = sorted({c for a in kept for c in (2 * a, 2 * a + 1) if (l, c) in table})
+        if len(cand) > Ksel or l == 0:
+            cand.sort(key=lambda c: (-table[(l, c)], c))
+            kept = set(cand[:Ksel])
+        else:
+            kept = set(cand)
+    if len(n) == 1:
+        kept = {0}
+    leaves = sorted(kept)
+    return leaves, [table[(0, t)] for t in leaves]
+
+
+@pytest.mark.parametrize("N,C,Ksel,G,seed", [
+    (64, 4, 1, 1, 0), (64, 4, 2, 2, 1), (96, 4, 3, 2, 2), (72, 8, 2, 1, 3),
+    (128, 8, 3, 2, 4), (61, 4, 2, 2, 5), (200, 8, 1, 2, 6), (256, 4, 3, 1, 7)])
+def test_descent_matches_brute_force(N, C, Ksel, G, seed):
+    d = 4
+    Q = _rand((1, N, G, d), 10 + seed, scale=2.0)
+    K = _rand((1, N, 1, d), 20 + seed, scale=2.0)
+    s = 0.7
+    out = po.select(Q, K, C, Ksel, scale=s)
+    rng = np.random.default_rng(seed)
+    for i in sorted(set(rng.integers(0, N, 12).tolist()) | {0, N - 1}):
+        leaves, scores = _bf_select(Q[0, i], K[0, :, 0, :], i, C, Ksel, s)
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == leaves, (i, got, leaves)
+        np.testing.assert_allclose(out["score"][0, 0, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
+        assert np.all(out["score"][0, 0, i, len(leaves):] == -np.inf)
+
+
+def test_descent_invariants():
+    N, C, Ksel, G, d = 512, 4, 3, 2, 4
+    Q = _rand((1, N, G, d), 30)
+    K = _rand((1, N, 1, d), 31)
+    summ = po.CausalKeySummaries(K[0, :, 0, :], C)
+    for i in range(0, N, 7):
+        u = po.select_unit(Q[0, i], i, summ, Ksel, 0.5)
+        assert all(c <= 2 * Ksel for c in u.cand_sizes)            # at most gK candidates per level
+        assert np.all(u.leaves <= i // C) and np.all(np.diff(u.leaves) > 0)
+        assert set(u.leaves.tolist()) <= set(u.leaf_candidates.tolist())
+        parents = {int(t) // 2 for t in u.leaf_candidates}
+        assert len(parents) <= Ksel                                 # candidates are children of <= K kept nodes
+        assert len(u.leaves) == min(Ksel, i // C + 1)
+
+
+# ---------------------------------------------------------------- special cases
+def test_zero_query_closed_form():
+    with open(os.path.join(GOLD, "zero_query.json")) as f:
+        g = json.load(f)
+    sh = g["shape"]
+    Q = np.zeros((1, sh["N"], sh["G"], sh["d"]))
+    K = _rand((1, sh["N"], 1, sh["d"]), 40)
+    for c in g["cases"]:
+        out = po.select(Q, K, sh["C"], c["K"], queries=[c["i"]])
+        got = out["idx"][0, 0, c["i"]]
+        assert list(got[got >= 0]) == c["leaves"]
+        want = [eval(x, {"log": math.log}) for x in c["scores"]]
+        np.testing.assert_allclose(out["score"][0, 0, c["i"], :len(want)], want, rtol=0, atol=1e-12)
+
+
+def test_keep_all_returns_every_visible_leaf():
+    with open(os.path.join(GOLD, "keep_all.json")) as f:
+        g = json.load(f)
+    sh = g["shape"]
+    Q = _rand((1, sh["N"], sh["G"], sh["d"]), 41)
+    K = _rand((1, sh["N"], 1, sh["d"]), 42)
+    out = po.select(Q, K, sh["C"], sh["K"])
+    flat = po.select_flat(Q, K, sh["C"], sh["K"])
+    for c in g["cases"]:
+        for o in (out, flat):
+            got = o["idx"][0, 0, c["i"]]
+            assert list(got[got >= 0]) == c["leaves"]
+    # and for every query of a larger random case
+    N, C = 300, 8
+    Q = _rand((1, N, 2, 8), 43)
+    K = _rand((1, N, 1, 8), 44)
+    out = po.select(Q, K, C, 38)
+    for i in range(N):
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == list(range(i // C + 1))
+
+
+def test_no_intermediate_pruning_equals_exhaustive():
+    # K >= number of level-1 nodes: no intermediate level prunes, so the leaf stage sees
+    # every visible leaf and PISA reduces to exhaustive exact scoring + top-K.
+    N, C, G, d = 128, 4, 2, 4
+    Ksel = 16                      # n0 = 32, n1 = 16
+    Q = _rand((1, N, G, d), 50, 1.5)
+    K = _rand((1, N, 1, d), 51, 1.5)
+    a = po.select(Q, K, C, Ksel)
+    b = po.select_exhaustive(Q, K, C, Ksel)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_allclose(a["score"], b["score"], rtol=1e-12, atol=1e-12)
+
+
+def test_planted_block_wins():
+    N, C, G, d = 256, 8, 2, 8
+    Q = _rand((1, N, G, d), 60)
+    K = _rand((1, N, 1, d), 61) * 0.1
+    direction = Q[0, N - 1].sum(axis=0)
+    star = 13
+    K[0, star * C:(star + 1) * C, 0, :] += 4.0 * direction / np.linalg.norm(direction)
+    out = po.select(Q, K, C, 1, queries=[N - 1])
+    assert list(out["idx"][0, 0, N - 1]) == [star]
+
+
+def test_exact_ties_go_to_lower_index():
+    N, C, G, d = 128, 4, 2, 4
+    Q = _rand((1, N, G, d), 70)
+    blk = _rand((C, d), 71)
+    K = np.tile(blk, (N // C, 1))[None, :, None, :]      # every leaf holds the same keys
+    out = po.select(Q, K, C, 3, queries=[N - 1, 77])
+    assert list(out["idx"][0, 0, N - 1]) == [0, 1, 2]
+    assert list(out["idx"][0, 0, 77]) == [0, 1, 2]
+
+
+def test_constant_leaves_closed_forms():
+    # Keys constant inside each leaf: mu_i(0,t) = k_t, so the flat score is s sum_h q_h.k_t
+    # and the exact leaf score is sum_h (s q_h.k_t + log n_t), n_t = visible keys of t.
+    N, C, G, d, Ksel = 96, 8, 2, 6, 3
+    Q = _rand((1, N, G, d), 80)
+    kt = _rand((N // C, d), 81)
+    K = np.repeat(kt, C, axis=0)[None, :, None, :]
+    s = 0.4
+    qs = [5, 40, 95]
+    flat = po.select_flat(Q, K, C, Ksel, scale=s, queries=qs)
+    exh = po.select_exhaustive(Q, K, C, Ksel, scale=s, queries=qs)
+    for i in qs:
+        vis = np.arange(i // C + 1)
+        base = s * torch.from_numpy(Q[0, i]).sum(0).numpy() @ kt[vis].T          # library matmul
+        n_t = np.array([min((t + 1) * C, i + 1) - t * C for t in vis])
+        exact = base + G * np.log(n_t)
+        for o, sc in ((flat, base), (exh, exact)):
+            order = sorted(range(len(vis)), key=lambda r: (-sc[r], r))[:Ksel]
+            got = o["idx"][0, 0, i]
+            assert list(got[got >= 0]) == sorted(order)
+            np.testing.assert_allclose(o["score"][0, 0, i, :len(order)], sc[sorted(order)], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- attention
+def _sdpa_dense(Q, K, V, s):
+    G = Q.shape[2] // K.shape[2]
+    q = torch.from_numpy(Q).permute(0, 2, 1, 3)
+    k = torch.from_numpy(K).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    v = torch.from_numpy(V).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    return q, k, v
+
+
+def test_attention_all_selected_equals_sdpa():
+    B, N, Hq, Hkv, d, C = 2, 70, 4, 2, 8, 8
+    Q, K, V = _rand((B, N, Hq, d), 90), _rand((B, N, Hkv, d), 91), _rand((B, N, Hkv, d), 92)
+    s = 0.3
+    n0 = -(-N // C)
+    idx = np.tile(np.arange(n0, dtype=np.int32), (B, Hkv, N, 1))
+    O, lse = po.sparse_attn_fwd(Q, K, V, idx, C, scale=s)
+    q, k, v = _sdpa_dense(Q, K, V, s)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=s)
+    np.testing.assert_allclose(O, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+    logits = (q @ k.transpose(-1, -2)) * s
+    logits = logits.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_masks_unselected_blocks():
+    # Only leaf 1 selected: the output must be the softmax over exactly its visible keys.
+    B, N, Hq, Hkv, d, C = 1, 32, 2, 1, 4, 8
+    Q, K, V = _rand((B, N, Hq, d), 93), _rand((B, N, Hkv, d), 94), _rand((B, N, Hkv, d), 95)
+    idx = np.full((B, Hkv, N, 2), -1, dtype=np.int32)
+    idx[..., 0] = 1
+    O, _ = po.sparse_attn_fwd(Q, K, V, idx, C, scale=1.0, queries=[12, 31])
+    for i in (12, 31):
+        J = list(range(8, min(16, i + 1)))
+        for h in range(Hq):
+            w = np.exp([Q[0, i, h] @ K[0, j, 0] for j in J])
+            w /= w.sum()
+            np.testing.assert_allclose(O[0, i, h], w @ V[0, J, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_backward_all_selected_equals_autograd():
+    B, N, Hq, Hkv, d, C = 1, 40, 4, 2, 8, 8
+    Q, K, V = _rand((B, N, Hq, d), 100), _rand((B, N, Hkv, d), 101), _rand((B, N, Hkv, d), 102)
+    dO = _rand((B, N, Hq, d), 103)
+    s = 0.35
+    idx = np.tile(np.arange(N // C, dtype=np.int32), (B, Hkv, N, 1))
+    dQ, dK, dV = po.sparse_attn_bwd(Q, K, V, dO, idx, C, scale=s)
+    q = torch.from_numpy(Q).requires_grad_()
+    k = torch.from_numpy(K).requires_grad_()
+    v = torch.from_numpy(V).requires_grad_()
+    G = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        q.permute(0, 2, 1, 3), k.repeat_interleave(G, 2).permute(0, 2, 1, 3),
+        v.repeat_interleave(G, 2).permute(0, 2, 1, 3), is_causal=True, scale=s)
+    (o.permute(0, 2, 1, 3) * torch.from_numpy(dO)).sum().backward()
+    np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dK, k.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dV, v.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_backward_finite_differences_sparse():
+    B, N, Hq, Hkv, d, C = 1, 24, 2, 1, 4, 4
+    Q, K, V = _rand((B, N, Hq, d), 110), _rand((B, N, Hkv, d), 111), _rand((B, N, Hkv, d), 112)
+    dO = _rand((B, N, Hq, d), 113)
+    sel = po.select(Q, K, C, 2)
+    idx = sel["idx"]
+    dQ, dK, dV = po.sparse_attn_bwd(Q, K, V, dO, idx, C, scale=0.5)
+
+    def loss(Q_, K_, V_):
+        O, _ = po.sparse_attn_fwd(Q_, K_, V_, idx, C, scale=0.5)
+        return float((O * dO).sum())
+
+    eps = 1e-6
+    rng = np.random.default_rng(0)
+    for name, X, G_ in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        for _ in range(6):
+            pos = tuple(int(rng.integers(0, n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[pos] += eps
+            Xm[pos] -= eps
+            args_p = {"Q": (Xp, K, V), "K": (Q, Xp, V), "V": (Q, K, Xp)}[name]
+            args_m = {"Q": (Xm, K, V), "K": (Q, Xm, V), "V": (Q, K, Xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - G_[pos]) < 1e-6 * max(1.0, abs(fd)), (name, pos, fd, G_[pos])
+
+
+# ---------------------------------------------------------------- decode
+def test_decode_incremental_pyramid_equals_rebuilt_and_prefill():
+    B, Ncap, Hq, Hkv, d, C, Ksel = 2, 96, 4, 2, 4, 4, 2
+    L0, steps = 37, 11
+    Kc, Vc = _rand((B, Ncap, Hkv, d), 120), _rand((B, Ncap, Hkv, d), 121)
+    Kc[:, L0:] = 0.0
+    Vc[:, L0:] = 0.0
+    qs, ks, vs = _rand((steps, B, Hq, d), 122), _rand((steps, B, Hkv, d), 123), _rand((steps, B, Hkv, d), 124)
+    st = po.DecodeState(Kc, Vc, L0, C)
+    for t in range(steps):
+        o, idx, score, _ = st.step(qs[t], ks[t], vs[t], Ksel, scale=0.5)
+        p = L0 + t
+        # the incrementally maintained pyramid equals one rebuilt from the cache
+        rb = po.DecodeState(st.K, st.V, p + 1, C)
+        for l in range(len(st.sums)):
+            np.testing.assert_allclose(st.sums[l], rb.sums[l], rtol=1e-12, atol=1e-12)
+        # decode at step p equals prefill's query p (a shorter pyramid: height invariance)
+        Qp = np.zeros((B, p + 1, Hq, d))
+        Qp[:, p] = qs[t]
+        pre = po.select(Qp, st.K[:, :p + 1], C, Ksel, scale=0.5, queries=[p])
+        np.testing.assert_array_equal(idx, pre["idx"][:, :, p])
+        np.testing.assert_allclose(score, pre["score"][:, :, p], rtol=1e-10, atol=1e-10)
+        Op, _ = po.sparse_attn_fwd(Qp, st.K[:, :p + 1], st.V[:, :p + 1], pre["idx"], C, scale=0.5, queries=[p])
+        np.testing.assert_allclose(o, Op[:, p], rtol=1e-10, atol=1e-12)
