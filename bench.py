@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""PISA select+attend throughput on GB300.
+
+Default workload (one GPU): prefill over N = 65536 tokens, B = 1, Hq = 16, Hkv = 2, d = 128,
+leaf C = 64, K = 16, g = 2, Qtile = 4, bf16 N(0,1) inputs with 8 needle leaf blocks per KV
+head. One step = pyramid build + pyramid Top-K selection + causal block-sparse attention
+forward over the selection, on inputs already resident in HBM; tokens/s = B*N / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill_64k|prefill_4k|sweep|decode|train] [--sweep-n 4096,...]
+
+Under torchrun each rank runs the same workload on its own GPU (independent problems, no
+collective on the data path: weak scaling); the timed region is bracketed by barriers and
+the slowest rank's time is reported. `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle legs run single-threaded
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pisa_synth as syn  # noqa: E402
+
+WORKLOADS = {
+    "prefill_64k": dict(B=1, N=65536, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
+    "prefill_4k": dict(B=1, N=4096, Hq=4, Hkv=1, d=64, C=64, K=8, g=2, qtile=1, needles=False),
+    "sweep": dict(B=1, N=65536, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=4, needles=True),
+    "train": dict(B=4, N=16384, Hq=16, Hkv=4, d=128, C=64, K=16, g=2, qtile=4, needles=False),
+    "decode": dict(B=32, N=131072, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=1, needles=False),
+}
+METRIC = "PISA select+attend tokens/s vs N (4K-256K) on 1 GB300; % of HBM/TC roofline"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_64k", choices=sorted(WORKLOADS))
+    ap.add_argument("--sweep-n", default="4096,16384,65536,131072,262144")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ environment helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[k] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:  # malformed file: fall back, and say so
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pisa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "pyramid_top_selection_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, units_per_launch: float):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(kernel)
+        if not e or e.get("source_hash") != source_hash():
+            return None
+        return e["dram_bytes_per_unit"] * units_per_launch
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ algorithmic work
+def algorithmic(kernel, cfg, idx_host=None):
+    """(bound, per-launch amount, unit, units processed, per-unit figure) of a kernel."""
+    B, N, Hq, Hkv, d, C, K = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K"))
+    G = Hq // Hkv
+    n0 = -(-N // C)
+    i = torch.arange(N, dtype=torch.float64)
+    if kernel in ("build_leaves",):
+        units = B * N * Hkv
+        per = d * 2 + (n0 * 4 * d * (1 + 0.5 + 0.25 + 0.125)) / N
+        return "hbm", units * per, "bytes", units, per
+    if kernel == "route":
+        sizes = [n0]
+        while sizes[-1] > 1:
+            sizes.append(-(-sizes[-1] // 2))
+        lvl = sum(1 for l in range(1, len(sizes) - 1) if sizes[l] > K)   # levels that prune
+        units = B * Hkv * N
+        per = lvl * (2 * K) * 2 * G * 2 * d   # 2K candidates x 2 children x G heads x 2d flops
+        return "tensor", units * per, "flops", units, per
+    if kernel == "leaf_score":
+        cands = torch.clamp(torch.floor(i / C) + 1, max=2 * K).sum().item()
+        units = B * Hkv * cands
+        per = G * C * 2 * d
+        return "tensor", units * per, "flops", units, per
+    if kernel == "attn_fwd_partial" and idx_host is not None:
+        keys = selected_keys(idx_host, C, N)
+        units = keys * G
+        per = 4 * d
+        return "tensor", units * per, "flops", units, per
+    if kernel == "attn_combine":
+        units = B * N * Hq
+        per = K * (2 * d + 4) + 2 * d + 4 + K * 4
+        return "hbm", units * per, "bytes", units, per
+    return None
+
+
+def selected_keys(idx: torch.Tensor, C: int, N: int) -> float:
+    """Number of (query, visible key) pairs inside the selection, over all KV heads."""
+    B, Hkv, N_, K = idx.shape
+    i = torch.arange(N_, dtype=torch.int64).view(1, 1, N_, 1)
+    t = idx.to(torch.int64)
+    start = t * C
+    cnt = torch.clamp(torch.minimum(start + C, i + 1) - start, min=0)
+    cnt = torch.where(t >= 0, cnt, torch.zeros_like(cnt))
+    return float(cnt.sum().item())
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, cfg, rank, world, local):
+    import pyramid_top_selection_gb300 as pisa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, N, Hq, Hkv, d, C, K, g, qtile = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile"))
+    Q, Kt, V = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0, needles=cfg["needles"], device=dev)
+    shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, g, qtile)
+    _, _, nodes = pisa.pyramid_layout(shape)
+    pyr = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=dev)
+    idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    score = torch.empty(B, Hkv, N, K, dtype=torch.float32, device=dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    ws_sel = pisa.workspace(shape, 0, dev)
+    ws_att = pisa.workspace(shape, 2, dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(Qs, Ks, Vs):
+        pisa.build_pyramid(Ks, shape, out=pyr)
+        pisa.select(Qs, Ks, pyr, shape, ws=ws_sel, idx=idx, score=score)
+        pisa.sparse_attn_fwd(Qs, Ks, Vs, idx, shape, ws=ws_att, out=O, lse=lse)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step(Q, Kt, V)
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.zero_()                        # L2 flush, outside the timed events
+            ev[k][0].record(stream)
+            step(Q, Kt, V)
+            ev[k][1].record(stream)
+        barrier()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = B * N * world / (ms / 1e3)
+
+    # per-kernel times (events around every launch, on the launch stream)
+    pisa.profile_start()
+    for k in range(args.steps):
+        flush.zero_()
+        step(Q, Kt, V)
+    torch.cuda.synchronize()
+    pisa.profile_stop()
+    prof = pisa.profile_read()
+    launches = sum(v[0] for v in prof.values())
+    per_step_launches = launches / args.steps
+    kernels = {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": 0.0} for k, v in prof.items()}
+    tot = sum(v[1] for v in prof.values())
+    for k, v in prof.items():
+        kernels[k]["share"] = v[1] / tot if tot else 0.0
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+
+    idx_host = idx.cpu()
+    pk, psrc = peaks()
+    roof = None
+    alg = algorithmic(dom, cfg, idx_host)
+    if alg is not None:
+        bound, amount, unit, units, per = alg
+        avg_s = kernels[dom]["avg_ms"] / 1e3
+        if unit == "bytes":
+            achieved = amount / avg_s / 1e9
+            peak = pk["hbm_gbs"]
+            u = "GB/s"
+        else:
+            achieved = amount / avg_s / 1e12
+            peak = pk["bf16_tflops"]
+            u = "TFLOP/s"
+        roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": u,
+                "frac": achieved / peak, "peak_source": psrc,
+                "traffic": traffic_for(dom, units), "units_per_launch": units, "per_unit": per,
+                "per_unit_kind": unit}
+
+    # e2e through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hQ, hK, hV = (x.cpu().pin_memory() for x in (Q, Kt, V))
+        dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Kt), torch.empty_like(V)
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        hidx = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True)
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        for _ in range(2):
+            dQ.copy_(hQ, non_blocking=True); dK.copy_(hK, non_blocking=True); dV.copy_(hV, non_blocking=True)
+            step(dQ, dK, dV)
+        barrier()
+        for k in range(args.steps):
+            flush.zero_()
+            e2e_ev[k][0].record(stream)
+            dQ.copy_(hQ, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            step(dQ, dK, dV)
+            hO.copy_(O, non_blocking=True)
+            hidx.copy_(idx, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            e2e_ev[k][1].record(stream)
+        barrier()
+        e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV))
+        d2h = sum(x.numel() * x.element_size() for x in (hO, hidx, hlse))
+        e2e = {"value": B * N * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, *(x.cpu().double().numpy() for x in (Q, Kt, V)), budget_s=12.0)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, 8 needle leaf blocks per KV head)",
+            "config": {"workload": f"prefill select+attend, N={N}", "B": B, "N": N, "Hq": Hq, "Hkv": Hkv,
+                       "d": d, "C": C, "K": K, "g": g, "qtile": qtile,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "step": "build_pyramid + select + sparse_attn_fwd", "parallelism": f"replica x{world}"},
+            "gpu_launches": int(round(per_step_launches * args.steps)),
+            "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        if clk.summary() is not None:
+            line["clocks"] = clk.summary()
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ oracle legs
+def oracle_sample(cfg, Q, Kt, V, n_queries, seed=0):
+    """Run the oracle's select + attention on a sample of queries (all KV heads)."""
+    from oracle import pisa_oracle as po
+    N, C, K = cfg["N"], cfg["C"], cfg["K"]
+    g = torch.Generator().manual_seed(seed)
+    qs = sorted(torch.randperm(N, generator=g)[:n_queries].tolist())
+    t0 = time.perf_counter()
+    ora = po.select(Q, Kt, C, K, queries=qs)
+    po.sparse_attn_fwd(Q, Kt, V, ora["idx"], C, queries=qs)
+    return time.perf_counter() - t0, qs
+
+
+def oracle_setup_time(cfg, Kt):
+    from oracle import pisa_oracle as po
+    t0 = time.perf_counter()
+    for b in range(cfg["B"]):
+        for kv in range(cfg["Hkv"]):
+            po.CausalKeySummaries(Kt[b, :, kv, :], cfg["C"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, Q, Kt, V, budget_s=12.0):
+    """The oracle as it stands, single-threaded on the host, on a bounded query sample.
+
+    tokens/s = sampled queries / (their select+attend time + the per-head summary set-up
+    time scaled by sample/N, i.e. amortised as over the full workload)."""
+    n = 8
+    setup = oracle_setup_time(cfg, Kt)
+    t_run, _ = oracle_sample(cfg, Q, Kt, V, n)
+    per_q = max(t_run - setup, 1e-6) / n
+    n = max(8, min(cfg["N"], int((budget_s - setup) / per_q)))
+    t_run, qs = oracle_sample(cfg, Q, Kt, V, n, seed=1)
+    t_q = max(t_run - setup, 1e-9)
+    value = n / (t_q + setup * n / cfg["N"])
+    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} random queries of the N={cfg['N']} workload (all {cfg['Hkv']} KV heads), "
+                      f"fp64 numpy, 1 thread; per-head summary set-up {setup:.2f}s amortised over N"}
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    B, N, Hq, Hkv, d, C = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C"))
+    Q, Kt, V = (x.double().numpy() for x in syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0,
+                                                              needles=cfg["needles"]))
+    setup = oracle_setup_time(cfg, Kt)
+    n = 16
+    for w in range(args.warmup):
+        oracle_sample(cfg, Q, Kt, V, 2, seed=100 + w)
+    times = []
+    for k in range(args.steps):
+        t, _ = oracle_sample(cfg, Q, Kt, V, n, seed=k)
+        times.append(max(t - setup, 1e-9))
+    per_step = sum(times) / len(times) + setup * n / N
+    value = n / per_step
+    cpu = {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} random queries per step of the N={N} workload (all {Hkv} KV heads), fp64 "
+                     f"numpy, 1 thread; summary set-up {setup:.2f}s amortised over N"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, 8 needle leaf blocks per KV head)",
+            "config": {"workload": f"prefill select+attend, N={N}", **{k: cfg[k] for k in
+                       ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")}},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ extra workloads
+def run_sweep(args, cfg, local):
+    """Pyramid selection vs the flat comparator over N (one JSON line per N)."""
+    import pyramid_top_selection_gb300 as pisa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for N in [int(x) for x in args.sweep_n.split(",")]:
+        c = dict(cfg, N=N)
+        Q, Kt, _ = syn.make_prefill(c["B"], N, c["Hq"], c["Hkv"], c["d"], C=c["C"], seed=0,
+                                    needles=True, device=dev)
+        shape = pisa.make_shape(c["B"], N, c["Hq"], c["Hkv"], c["d"], c["C"], c["K"], c["g"], c["qtile"])
+        pyr = pisa.build_pyramid(Kt, shape)
+        idx = torch.empty(c["B"], c["Hkv"], N, c["K"], dtype=torch.int32, device=dev)
+        ws_p, ws_f = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 1, dev)
+        out = {}
+        for name, fn, ws in (("pyramid", pisa.select, ws_p), ("flat", pisa.select_flat, ws_f)):
+            for _ in range(max(1, args.warmup)):
+                fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            out[name] = statistics.median(ts)
+        print(json.dumps({"workload": "selection sweep", "N": N, "B": c["B"], "Hq": c["Hq"], "Hkv": c["Hkv"],
+                          "d": c["d"], "K": c["K"], "pyramid_select_ms": out["pyramid"],
+                          "flat_select_ms": out["flat"], "flat_over_pyramid": out["flat"] / out["pyramid"],
+                          "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3)}), flush=True)
+        del Q, Kt, pyr, idx, ws_p, ws_f
+        torch.cuda.empty_cache()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        return
+    if args.workload == "sweep":
+        if rank == 0:
+            run_sweep(args, cfg, local)
+        return
+    run_ours(args, cfg, rank, world, local)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,356 @@
+// Single-kernel decode step: append, ancestor-path pyramid update, all-level selection
+// and sparse attention for one new token per sequence, in ONE launch.
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference
+// value of the work": decoding fuses all pyramid levels in a single kernel to avoid
+// repeated launches, and the cached mean pyramid is updated only on the ancestor path of
+// the current token, amortised O(log N) per step.
+//
+// One CTA per (KV head, sequence), 8 warps. The cached pyramid holds key SUMS over the
+// tokens present so far (absent tokens count as zero), so the node that holds the new
+// token p already carries the causal prefix sum; its mean is the sum over its present
+// token count. Arithmetic order of the update matches the pyramid build kernel exactly
+// (leaf: fp32 sum of the leaf's keys in token order; parent = left + right), so the
+// incrementally maintained pyramid equals one rebuilt from the cache, bit for bit.
+#include "device.cuh"
+#include "profile.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCand = 64;
+
+struct DecodeSmem {
+  // offsets in floats inside dynamic shared memory
+  int q32, S, lh, red, dots;
+  int total;
+};
+
+__host__ __device__ inline DecodeSmem decode_smem(int G, int D, int K) {
+  DecodeSmem m{};
+  int o = 0;
+  m.q32 = o;  o += G * D;
+  m.S = o;    o += 2 * K * 64 * G;
+  m.lh = o;   o += 2 * K * G;
+  m.red = o;  o += kWarps * G * D;
+  m.dots = o; o += kMaxCand * 2 * G;
+  m.total = o;
+  return m;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* Kc,
+              __nv_bfloat16* Vc, float* pyr, const __nv_bfloat16* __restrict__ qn,
+              const __nv_bfloat16* __restrict__ kn, const __nv_bfloat16* __restrict__ vn,
+              __nv_bfloat16* __restrict__ o_out, int32_t* __restrict__ idx_out,
+              float* __restrict__ score_out, int32_t* __restrict__ status) {
+  constexpr int KS = D / 16;
+  extern __shared__ __align__(16) float sm[];
+  __shared__ int s_cand[kMaxCand];
+  __shared__ int s_kept[kMaxCand];
+  __shared__ float s_sc[kMaxCand];
+  __shared__ int s_sel[kMaxCand / 2];    // selected candidate slots, ascending leaf order
+  __shared__ float s_lse[8];
+  __shared__ int s_n[2];
+
+  const int kv = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, pq = lane & 3;
+  const int G = s.G, Ksel = s.K, C = s.C, Ncap = s.N;
+  const int p = pos[b];
+  if (p < 0 || p >= Ncap) {
+    if (tid == 0) atomicOr(status, 1);
+    return;
+  }
+  const DecodeSmem L = decode_smem(G, D, Ksel);
+  float* q32 = sm + L.q32;
+  float* Sb = sm + L.S;
+  float* lh = sm + L.lh;
+  float* red = sm + L.red;
+  float* dots = sm + L.dots;
+
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  float* pyr_h = pyr + head * geo.nodes * D;
+  auto krow = [&](int64_t j) { return Kc + ((static_cast<int64_t>(b) * Ncap + j) * s.Hkv + kv) * D; };
+  auto vrow = [&](int64_t j) { return Vc + ((static_cast<int64_t>(b) * Ncap + j) * s.Hkv + kv) * D; };
+
+  // 1. append k/v at slot p; q to shared memory
+  if (tid < D / 8) {
+    reinterpret_cast<uint4*>(krow(p))[tid] = ldg_u4(kn + head * D + tid * 8);
+    reinterpret_cast<uint4*>(vrow(p))[tid] = ldg_u4(vn + head * D + tid * 8);
+  }
+  const __nv_bfloat16* qg = qn + (static_cast<int64_t>(b) * s.Hq + kv * G) * D;
+  for (int it = tid; it < G * D; it += kThreads) q32[it] = __bfloat162float(qg[it]);
+  __syncthreads();
+
+  // 2. leaf recompute (token order) and ancestor path (left + right)
+  const int tp = p / C;
+  if (tid < D) {
+    float acc = 0.0f;
+    for (int64_t j = static_cast<int64_t>(tp) * C; j <= p; ++j) acc += __bfloat162float(krow(j)[tid]);
+    pyr_h[(geo.off[0] + tp) * D + tid] = acc;
+    int m = tp;
+    float v = acc;
+    for (int l = 1; l < geo.n_levels; ++l) {
+      const int sib = m ^ 1;
+      if (sib < geo.size[l - 1]) {
+        const float sv = pyr_h[(geo.off[l - 1] + sib) * D + tid];
+        v = (m & 1) ? (sv + v) : (v + sv);
+      }
+      m >>= 1;
+      pyr_h[(geo.off[l] + m) * D + tid] = v;
+    }
+  }
+  __syncthreads();
+
+  // 3. intermediate levels
+  if (tid == 0) { s_kept[0] = 0; s_n[0] = 1; }
+  __syncthreads();
+  const int Lv = geo.n_levels;
+  for (int lam = Lv - 2; lam >= 1; --lam) {
+    const int64_t span = static_cast<int64_t>(C) << lam;
+    if (tid == 0) {
+      int nc = 0;
+      for (int k = 0; k < s_n[0]; ++k) {
+        const int a = s_kept[k];
+        s_cand[nc++] = 2 * a;
+        if (static_cast<int64_t>(2 * a + 1) * span <= p) s_cand[nc++] = 2 * a + 1;
+      }
+      s_n[1] = nc;
+    }
+    __syncthreads();
+    const int nc = s_n[1];
+    if (nc <= Ksel) {
+      if (tid < nc) s_kept[tid] = s_cand[tid];
+      __syncthreads();
+      if (tid == 0) s_n[0] = nc;
+      __syncthreads();
+      continue;
+    }
+    const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
+    for (int it = tid; it < nc * 2 * G; it += kThreads) {
+      const int cs = it / (2 * G), e = (it / G) & 1, h = it % G;
+      const int64_t ch = 2LL * s_cand[cs] + e;
+      const int64_t st = ch * cspan;
+      if (st > p) { dots[it] = neg_inf(); continue; }
+      const float4* row = reinterpret_cast<const float4*>(pyr_h + (geo.off[lam - 1] + ch) * D);
+      const float4* qq = reinterpret_cast<const float4*>(q32 + h * D);
+      float acc = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < D / 4; ++k) {
+        const float4 x = row[k], y = qq[k];
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+        acc = fmaf(x.z, y.z, acc);
+        acc = fmaf(x.w, y.w, acc);
+      }
+      const float cnt = static_cast<float>(min(st + cspan, static_cast<int64_t>(p) + 1) - st);
+      dots[it] = s.scale * acc / cnt;
+    }
+    __syncthreads();
+    if (tid < nc) {
+      float tot = 0.f;
+      for (int h = 0; h < G; ++h) {
+        const float x0 = dots[(tid * 2) * G + h], x1 = dots[(tid * 2 + 1) * G + h];
+        if (x1 == neg_inf()) {
+          tot += x0;
+        } else {
+          const float mx = fmaxf(x0, x1);
+          tot += mx + logf(expf(x0 - mx) + expf(x1 - mx));
+        }
+      }
+      s_sc[tid] = tot;
+    }
+    __syncthreads();
+    if (tid < nc) {
+      const float my = s_sc[tid];
+      const int mi = s_cand[tid];
+      int rank = 0;
+      for (int o = 0; o < nc; ++o) rank += beats(s_sc[o], s_cand[o], my, mi) ? 1 : 0;
+      if (rank < Ksel) s_kept[rank] = mi;
+    }
+    __syncthreads();
+    if (tid == 0) s_n[0] = Ksel;
+    __syncthreads();
+  }
+
+  // 4. leaf candidates and exact leaf LSE (MMA: rows = keys, columns = heads)
+  if (tid == 0) {
+    int nc = 0;
+    if (Lv == 1) {
+      s_cand[nc++] = 0;
+    } else {
+      for (int k = 0; k < s_n[0]; ++k) {
+        const int a = s_kept[k];
+        s_cand[nc++] = 2 * a;
+        if (static_cast<int64_t>(2 * a + 1) * C <= p) s_cand[nc++] = 2 * a + 1;
+      }
+    }
+    s_n[1] = nc;
+  }
+  __syncthreads();
+  const int nlc = s_n[1];
+  {
+    uint32_t qb[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint2 v = g < G ? ldg_u2(qg + static_cast<int64_t>(g) * D + 16 * ks + 4 * pq) : make_uint2(0, 0);
+      qb[ks][0] = v.x;
+      qb[ks][1] = v.y;
+    }
+    for (int cs = warp; cs < nlc; cs += kWarps) {
+      const int64_t t0 = static_cast<int64_t>(s_cand[cs]) * C;
+      for (int mt = 0; mt < 4; ++mt) {
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        const bool v0 = t0 + r0 <= p, v1 = t0 + r1 <= p;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint2 x0 = v0 ? ldg_u2(krow(t0 + r0) + 16 * ks + 4 * pq) : make_uint2(0, 0);
+          const uint2 x1 = v1 ? ldg_u2(krow(t0 + r1) + 16 * ks + 4 * pq) : make_uint2(0, 0);
+          const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+          mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
+        }
+        float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * pq + e;
+          if (h < G) {
+            Sr[r0 * G + h] = v0 ? s.scale * acc[e] : neg_inf();
+            Sr[r1 * G + h] = v1 ? s.scale * acc[2 + e] : neg_inf();
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int it = tid; it < nlc * G; it += kThreads) {
+    const int cs = it / G, h = it % G;
+    const float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
+    float mx = neg_inf();
+    for (int k = 0; k < 64; ++k) mx = fmaxf(mx, Sr[k * G + h]);
+    float sum = 0.f;
+    for (int k = 0; k < 64; ++k) sum += expf(Sr[k * G + h] - mx);
+    lh[it] = mx + logf(sum);
+  }
+  __syncthreads();
+  if (tid < nlc) {
+    float tot = 0.f;
+    for (int h = 0; h < G; ++h) tot += lh[tid * G + h];
+    s_sc[tid] = tot;
+  }
+  __syncthreads();
+  // 5. top K leaves, ascending
+  if (tid < nlc) {
+    const float my = s_sc[tid];
+    const int mi = s_cand[tid];
+    int rank = 0;
+    for (int o = 0; o < nlc; ++o) rank += beats(s_sc[o], s_cand[o], my, mi) ? 1 : 0;
+    s_kept[tid] = rank < Ksel ? 1 : 0;
+  }
+  __syncthreads();
+  if (tid < nlc && s_kept[tid]) {
+    int posn = 0;
+    for (int o = 0; o < nlc; ++o) posn += (s_kept[o] && s_cand[o] < s_cand[tid]) ? 1 : 0;
+    s_sel[posn] = tid;
+    idx_out[head * Ksel + posn] = s_cand[tid];
+    if (score_out) score_out[head * Ksel + posn] = s_sc[tid];
+  }
+  const int nsel = min(nlc, Ksel);
+  if (tid >= nsel && tid < Ksel) {
+    idx_out[head * Ksel + tid] = -1;
+    if (score_out) score_out[head * Ksel + tid] = neg_inf();
+  }
+  __syncthreads();
+  // 6. attention over the selected leaves, reusing the leaf logits S
+  if (tid < G) {
+    float mx = neg_inf();
+    for (int k = 0; k < nsel; ++k) mx = fmaxf(mx, lh[s_sel[k] * G + tid]);
+    float sum = 0.f;
+    for (int k = 0; k < nsel; ++k) sum += expf(lh[s_sel[k] * G + tid] - mx);
+    s_lse[tid] = mx + logf(sum);
+  }
+  __syncthreads();
+  {
+    constexpr int PER = D / 32;
+    float acc[8][PER];
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+#pragma unroll
+      for (int u = 0; u < PER; ++u) acc[h][u] = 0.f;
+    for (int k = warp; k < nsel; k += kWarps) {
+      const int cs = s_sel[k];
+      const int64_t t0 = static_cast<int64_t>(s_cand[cs]) * C;
+      const float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
+      for (int key = 0; key < 64 && t0 + key <= p; ++key) {
+        const __nv_bfloat16* vr = vrow(t0 + key) + lane * PER;
+        float vv[PER];
+        if (PER == 4) {
+          const uint2 x = *reinterpret_cast<const uint2*>(vr);
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x);
+#pragma unroll
+          for (int u = 0; u < PER; ++u) vv[u] = __bfloat162float(e[u]);
+        } else {
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(vr);
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x);
+#pragma unroll
+          for (int u = 0; u < PER; ++u) vv[u] = __bfloat162float(e[u]);
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          if (h < G) {
+            const float pw = expf(Sr[key * G + h] - s_lse[h]);
+#pragma unroll
+            for (int u = 0; u < PER; ++u) acc[h][u] = fmaf(pw, vv[u], acc[h][u]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      if (h < G)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) red[(warp * G + h) * D + lane * PER + u] = acc[h][u];
+  }
+  __syncthreads();
+  for (int it = tid; it < G * D; it += kThreads) {
+    const int h = it / D, k = it % D;
+    float v = 0.f;
+    for (int w = 0; w < kWarps; ++w) v += red[(w * G + h) * D + k];
+    o_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * D + k] = __float2bfloat16_rn(v);
+  }
+}
+
+}  // namespace
+
+int launch_decode_step(const Dims& s, int32_t Ncap, const Geo& g, const int32_t* pos, void* Kc,
+                       void* Vc, float* pyr, const void* q, const void* k_new, const void* v_new,
+                       void* o, int32_t* idx, float* score, int32_t* status, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Dims d = s;
+  d.N = Ncap;
+  const DecodeSmem L = decode_smem(s.G, s.d, s.K);
+  const size_t smem = static_cast<size_t>(L.total) * sizeof(float);
+  dim3 grid(s.Hkv, s.B);
+  ProfScope ps(st, "decode_step");
+  if (s.d == 128) {
+    cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    decode_kernel<128><<<grid, kThreads, smem, st>>>(
+        d, g, pos, static_cast<__nv_bfloat16*>(Kc), static_cast<__nv_bfloat16*>(Vc), pyr,
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
+        static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(o), idx, score, status);
+  } else {
+    cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    decode_kernel<64><<<grid, kThreads, smem, st>>>(
+        d, g, pos, static_cast<__nv_bfloat16*>(Kc), static_cast<__nv_bfloat16*>(Vc), pyr,
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
+        static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(o), idx, score, status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pisa

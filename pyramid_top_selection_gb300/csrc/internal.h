@@ -1,0 +1,77 @@
+// Host-side declarations shared by the C ABI (api.cpp) and the kernel launchers (*.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/pisa.h"
+
+namespace pisa {
+
+// Pyramid geometry of one (batch, KV head): level l holds size[l] nodes starting at node
+// offset off[l]; level 0 = leaves of C tokens, every level halves (rounding up).
+struct Geo {
+  int32_t n_levels;
+  int32_t size[PISA_MAX_LEVELS];
+  int64_t off[PISA_MAX_LEVELS];
+  int64_t nodes;
+};
+
+inline Geo make_geo(int64_t N, int C) {
+  Geo g{};
+  int64_t n = (N + C - 1) / C;
+  int64_t off = 0;
+  int l = 0;
+  while (true) {
+    g.size[l] = static_cast<int32_t>(n);
+    g.off[l] = off;
+    off += n;
+    ++l;
+    if (n <= 1 || l >= PISA_MAX_LEVELS) break;
+    n = (n + 1) / 2;
+  }
+  g.n_levels = l;
+  g.nodes = off;
+  return g;
+}
+
+// Plain-old-data view of a prefill shape with derived values, passed to kernels by value.
+struct Dims {
+  int32_t B, N, Hq, Hkv, d, C, K, G, n0;
+  float scale;
+};
+
+// Workspace carving for each op; every sub-buffer is 256-byte aligned.
+struct SelectWs {
+  size_t split, cand, cscore, counts, cursor, list, total;
+};
+struct AttnFwdWs {
+  size_t counts, cursor, list, part_o, part_lse, total;
+};
+struct AttnBwdWs {
+  size_t counts, cursor, list, delta, part_dq, total;
+};
+SelectWs select_ws(const Dims& s, const Geo& g);
+AttnFwdWs attn_fwd_ws(const Dims& s);
+AttnBwdWs attn_bwd_ws(const Dims& s);
+size_t flat_ws(const Dims& s, const Geo& g);
+
+// Launchers: return 0 or a cudaError_t value.
+int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32_t* len,
+                         int64_t tokens_per_seq, float* pyr, void* stream);
+int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
+                  int32_t* idx, float* score, char* ws, void* stream);
+int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
+                       const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
+int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
+                    const int32_t* idx, void* O, float* lse, char* ws, void* stream);
+int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, const void* O,
+                    const float* lse, const void* dO, const int32_t* idx, void* dQ, void* dK,
+                    void* dV, char* ws, void* stream);
+int launch_decode_step(const Dims& s, int32_t Ncap, const Geo& g, const int32_t* pos,
+                       void* Kc, void* Vc, float* pyr, const void* q, const void* k_new,
+                       const void* v_new, void* o, int32_t* idx, float* score, int32_t* status,
+                       void* stream);
+const char* cuda_error_string(int err);
+
+}  // namespace pisa

@@ -1,0 +1,136 @@
+// Key pyramid build: leaf sums over C tokens, then parents = left + right.
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Method key
+// points": leaf blocks of C tokens, mean pooling upward with merge factor 2, O(log N)
+// levels. The kernels store SUMS (a node's mean is its sum over its token count), so a
+// parent is exactly the fp32 sum of its two children, and the decode step can rebuild a
+// leaf and its ancestors with the identical arithmetic.
+//
+// Fixed summation order (relied upon by the decode kernel for bit-exact updates):
+//   leaf:   acc = 0.0f; for tokens j ascending: acc += float(k_j)     (per dimension)
+//   parent: S(l,m) = S(l-1,2m) + S(l-1,2m+1), or S(l-1,2m) when 2m+1 does not exist.
+// Bound: HBM. One launch reads N*Hkv*d*2 bytes of K and writes ~2*n0*Hkv*d*4 bytes.
+#include "device.cuh"
+#include "profile.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kLeavesPerCta = 8;   // leaves reduced by one CTA; levels 1..3 finish in-CTA
+constexpr int kInCtaLevels = 3;
+
+// Grid (ceil(n0/8), Hkv, B); block (D/8) * 8 threads: thread = (leaf, 8-dim chunk).
+template <int D>
+__global__ void __launch_bounds__(D)
+build_leaves_kernel(const __nv_bfloat16* __restrict__ K, const int32_t* __restrict__ len,
+                    int64_t T, int Hkv, int C, Geo geo, float* __restrict__ pyr) {
+  constexpr int CH = D / 8;
+  __shared__ __align__(16) float sm[2][kLeavesPerCta][D];
+  const int b = blockIdx.z, kv = blockIdx.y;
+  const int leaf0 = blockIdx.x * kLeavesPerCta;
+  const int ll = threadIdx.x / CH, ch = threadIdx.x % CH;
+  const int t = leaf0 + ll;
+  const int64_t present = len ? min(static_cast<int64_t>(max(len[b], 0)), T) : T;
+  const int64_t head = static_cast<int64_t>(b) * Hkv + kv;
+  float* pyr_h = pyr + head * geo.nodes * D;
+
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  if (t < geo.size[0]) {
+    const int64_t s = static_cast<int64_t>(t) * C;
+    const int64_t e_ = min(s + C, present);
+    const __nv_bfloat16* base = K + (static_cast<int64_t>(b) * T * Hkv + kv) * D + ch * 8;
+    const int64_t stride = static_cast<int64_t>(Hkv) * D;
+    int64_t j = s;
+    for (; j + 4 <= e_; j += 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = ldg_u4(base + (j + u) * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v[u]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __bfloat162float(h[e]);
+      }
+    }
+    for (; j < e_; ++j) {
+      uint4 v = ldg_u4(base + j * stride);
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += __bfloat162float(h[e]);
+    }
+    float4* out = reinterpret_cast<float4*>(pyr_h + (geo.off[0] + t) * D + ch * 8);
+    out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sm[0][ll][ch * 8 + e] = acc[e];
+  __syncthreads();
+
+  // Levels 1..3: node m at level l covers leaves [m<<l, (m+1)<<l), all inside this CTA.
+  int cur = 0;
+  for (int l = 1; l <= kInCtaLevels && l < geo.n_levels; ++l) {
+    const int here = kLeavesPerCta >> l;
+    for (int it = threadIdx.x; it < here * D; it += blockDim.x) {
+      const int nl = it / D, k = it % D;
+      const int m = (leaf0 >> l) + nl;
+      float v = sm[cur][2 * nl][k];
+      if (2 * m + 1 < geo.size[l - 1]) v = v + sm[cur][2 * nl + 1][k];
+      sm[cur ^ 1][nl][k] = v;
+      if (m < geo.size[l]) pyr_h[(geo.off[l] + m) * D + k] = v;
+    }
+    cur ^= 1;
+    __syncthreads();
+  }
+}
+
+// Levels 4.. for one (batch, KV head) per CTA, level by level.
+template <int D>
+__global__ void __launch_bounds__(256)
+build_upper_kernel(int Hkv, Geo geo, float* __restrict__ pyr) {
+  const int64_t head = static_cast<int64_t>(blockIdx.y) * Hkv + blockIdx.x;
+  float* pyr_h = pyr + head * geo.nodes * D;
+  for (int l = kInCtaLevels + 1; l < geo.n_levels; ++l) {
+    const float* src = pyr_h + geo.off[l - 1] * D;
+    float* dst = pyr_h + geo.off[l] * D;
+    const int n = geo.size[l], nc = geo.size[l - 1];
+    for (int it = threadIdx.x; it < n * D; it += blockDim.x) {
+      const int m = it / D, k = it % D;
+      float v = src[(2 * m) * D + k];
+      if (2 * m + 1 < nc) v = v + src[(2 * m + 1) * D + k];
+      dst[it] = v;
+    }
+    __syncthreads();
+  }
+}
+
+template <int D>
+int build_impl(const Dims& s, const Geo& g, const void* K, const int32_t* len, int64_t T,
+               float* pyr, cudaStream_t st) {
+  dim3 grid((g.size[0] + kLeavesPerCta - 1) / kLeavesPerCta, s.Hkv, s.B);
+  { ProfScope ps(st, "build_leaves");
+  build_leaves_kernel<D><<<grid, (D / 8) * kLeavesPerCta, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(K), len, T, s.Hkv, s.C, g, pyr); }
+  if (g.n_levels > kInCtaLevels + 1) {
+    ProfScope ps(st, "build_upper");
+    build_upper_kernel<D><<<dim3(s.Hkv, s.B), 256, 0, st>>>(s.Hkv, g, pyr);
+  }
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32_t* len,
+                         int64_t tokens_per_seq, float* pyr, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s.d == 128) return build_impl<128>(s, g, K, len, tokens_per_seq, pyr, st);
+  return build_impl<64>(s, g, K, len, tokens_per_seq, pyr, st);
+}
+
+const char* cuda_error_string(int err) {
+  return cudaGetErrorString(static_cast<cudaError_t>(err));
+}
+
+}  // namespace pisa

@@ -1,0 +1,820 @@
+// Pyramid Top-K selection (two stages) and the flat comparator.
+//
+// "Block Sparse Attention with Log-Linear Complexity":
+//  * abstract (arxivdaily page): coarse-to-fine hierarchy of pooled keys, selection from
+//    the coarsest level, LogSumExp scoring of a bounded candidate set at every level down
+//    to the finest, without materialising the query-key score matrix;
+//  * daily digest page, "Method key points": candidate set starts with 1 node, at most gK
+//    candidates per level, keep top K, expand only kept nodes; leaves scored by exact LSE
+//    over raw keys, intermediate nodes by LSE over children's mean summaries; GQA heads
+//    of one KV head share the selection; prefill runs in two stages: intermediate-level
+//    routing first, then queries grouped per leaf key block so the block's keys are read
+//    once per tile ("Reference value of the work").
+//
+// Stage 1 (route_kernel): one warp per (b, KV head, query i). The candidates' children
+//   are contracted against the G query heads with bf16 MMAs on a hi/lo split of the fp32
+//   key sums (fp32-accurate dots), LSE per head, sum over heads, warp top-K by rank.
+//   The node that contains i is causal-partial: its dot is q . (sum of keys j <= i in it),
+//   built bottom-up from the query's own-leaf prefix and the full left siblings on the
+//   ancestor path. Output: <= 2K leaf candidates per query.
+// Grouping: counting sort of (leaf, query) pairs into per-leaf lists.
+// Stage 2 (leaf_score_kernel): one CTA per leaf block; its 64 keys sit in shared memory
+//   and every query that has the leaf as a candidate is scored against them with MMAs.
+// Finish (topk_kernel): top K of the <= 2K exact leaf scores, output ascending.
+#include "device.cuh"
+#include "profile.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMaxCand = 64;   // 2K for K <= 32
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}.
+__global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4) {
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n4;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 v = src[q];
+    __nv_bfloat16 h[4], l[4];
+    split_bf16(v.x, h[0], l[0]);
+    split_bf16(v.y, h[1], l[1]);
+    split_bf16(v.z, h[2], l[2]);
+    split_bf16(v.w, h[3], l[3]);
+    uint4 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(h[0]) | ((uint32_t)__bfloat16_as_ushort(h[1]) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(h[2]) | ((uint32_t)__bfloat16_as_ushort(h[3]) << 16);
+    o.z = (uint32_t)__bfloat16_as_ushort(l[0]) | ((uint32_t)__bfloat16_as_ushort(l[1]) << 16);
+    o.w = (uint32_t)__bfloat16_as_ushort(l[2]) | ((uint32_t)__bfloat16_as_ushort(l[3]) << 16);
+    dst[q] = o;
+  }
+}
+
+// Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid; invalid
+// rows contribute zeros.
+template <int KS>
+__device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0, bool v0,
+                                               const uint4* r1, bool v1, int p,
+                                               const uint32_t (&qb)[KS][2]) {
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint4 x0 = v0 ? __ldg(r0 + 4 * ks + p) : make_uint4(0, 0, 0, 0);
+    uint4 x1 = v1 ? __ldg(r1 + 4 * ks + p) : make_uint4(0, 0, 0, 0);
+    uint32_t ahi[4] = {x0.x, x1.x, x0.y, x1.y};
+    uint32_t alo[4] = {x0.z, x1.z, x0.w, x1.w};
+    mma_bf16(acc, ahi, qb[ks][0], qb[ks][1]);
+    mma_bf16(acc, alo, qb[ks][0], qb[ks][1]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
+             const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl,
+             int32_t* __restrict__ cand_out) {
+  constexpr int KS = D / 16;
+  constexpr int RQ = D / 4;     // uint4 chunks per split row
+  __shared__ int s_cand[kWarps][kMaxCand];
+  __shared__ int s_kept[kWarps][kMaxCand / 2];
+  __shared__ float s_sc[kWarps][kMaxCand];
+  __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
+  __shared__ float s_pd[kWarps][PISA_MAX_LEVELS][8];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+  const int b = blockIdx.z, kv = blockIdx.y;
+  const int i = blockIdx.x * kWarps + warp;
+  if (i >= s.N) return;                   // no block-wide barriers below
+  const int G = s.G, Ksel = s.K, C = s.C;
+  const int ti = i / C;
+  const int L = geo.n_levels;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const uint4* spl_h = spl + head * geo.nodes * RQ;
+
+  // q of the G heads as MMA B fragments (column n = head g; heads >= G are zero).
+  uint32_t qb[KS][2];
+  {
+    const __nv_bfloat16* qrow =
+        Q + ((static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + min(g, G - 1)) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint2 v = g < G ? ldg_u2(qrow + 16 * ks + 4 * p) : make_uint2(0, 0);
+      qb[ks][0] = v.x;
+      qb[ks][1] = v.y;
+    }
+  }
+
+  // pd0[h] = sum over keys j in [ti*C, i] of q_h . k_j  (keys are exact bf16).
+  float pda = 0.f, pdb = 0.f;
+  {
+    const int64_t j0 = static_cast<int64_t>(ti) * C;
+    const int nkeys = i - static_cast<int>(j0) + 1;
+    for (int mt = 0; mt * 16 < nkeys; ++mt) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int r0 = mt * 16 + g, r1 = r0 + 8;
+      const __nv_bfloat16* k0 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r0) * s.Hkv + kv) * D;
+      const __nv_bfloat16* k1 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r1) * s.Hkv + kv) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint2 x0 = r0 < nkeys ? ldg_u2(k0 + 16 * ks + 4 * p) : make_uint2(0, 0);
+        uint2 x1 = r1 < nkeys ? ldg_u2(k1 + 16 * ks + 4 * p) : make_uint2(0, 0);
+        uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+        mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
+      }
+      pda += acc[0] + acc[2];
+      pdb += acc[1] + acc[3];
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      pda += __shfl_xor_sync(0xffffffffu, pda, o);
+      pdb += __shfl_xor_sync(0xffffffffu, pdb, o);
+    }
+  }
+
+  // Dots with the full left sibling of the ancestor at every level l < L-1 whose
+  // ancestor index is odd; prefix sums over levels give q . (keys j <= i of ancestor l).
+  for (int base = 0; base < L - 1; base += 16) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int l0 = base + g, l1 = base + g + 8;
+    const bool v0 = l0 < L - 1 && ((ti >> l0) & 1);
+    const bool v1 = l1 < L - 1 && ((ti >> l1) & 1);
+    const uint4* r0 = spl_h + (v0 ? (geo.off[l0] + (ti >> l0) - 1) * RQ : 0);
+    const uint4* r1 = spl_h + (v1 ? (geo.off[l1] + (ti >> l1) - 1) * RQ : 0);
+    mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
+    if (l0 < PISA_MAX_LEVELS) {
+      s_sib[warp][l0][2 * p] = v0 ? acc[0] : 0.f;
+      s_sib[warp][l0][2 * p + 1] = v0 ? acc[1] : 0.f;
+    }
+    if (l1 < PISA_MAX_LEVELS) {
+      s_sib[warp][l1][2 * p] = v1 ? acc[2] : 0.f;
+      s_sib[warp][l1][2 * p + 1] = v1 ? acc[3] : 0.f;
+    }
+  }
+  __syncwarp();
+  {
+    // lane h < 8 takes head h: pd0 of head h = 2p' + e sits in lane p' (g = 0), as pda
+    // for e = 0 and pdb for e = 1 (identical in every g after the reduction above)
+    const float va = __shfl_sync(0xffffffffu, pda, (lane & 7) >> 1);
+    const float vb = __shfl_sync(0xffffffffu, pdb, (lane & 7) >> 1);
+    if (lane < 8) {
+      float v = (lane & 1) ? vb : va;
+      s_pd[warp][0][lane] = v;
+      for (int l = 1; l < L; ++l) {
+        v = v + s_sib[warp][l - 1][lane];
+        s_pd[warp][l][lane] = v;
+      }
+    }
+  }
+  __syncwarp();
+
+  int* cand = s_cand[warp];
+  int* kept = s_kept[warp];
+  float* sc = s_sc[warp];
+  int nkept = 1;
+  if (lane == 0) kept[0] = 0;
+  __syncwarp();
+
+  const unsigned ltm = lanemask_lt();
+  for (int lam = L - 2; lam >= 1; --lam) {
+    // candidates at level lam: visible children of the kept nodes of level lam+1
+    const int64_t span = static_cast<int64_t>(C) << lam;
+    int nc;
+    {
+      const int a = lane < nkept ? kept[lane] : -1;
+      const bool c0 = a >= 0;
+      const bool c1 = a >= 0 && static_cast<int64_t>(2 * a + 1) * span <= i;
+      const unsigned m0 = __ballot_sync(0xffffffffu, c0), m1 = __ballot_sync(0xffffffffu, c1);
+      const int pos = __popc(m0 & ltm) + __popc(m1 & ltm);
+      __syncwarp();
+      if (c0) cand[pos] = 2 * a;
+      if (c1) cand[pos + 1] = 2 * a + 1;
+      nc = __popc(m0) + __popc(m1);
+    }
+    __syncwarp();
+    if (nc <= Ksel) {
+      if (lane < nc) kept[lane] = cand[lane];
+      nkept = nc;
+      __syncwarp();
+      continue;
+    }
+    // score every candidate with its (<= 2) visible children at level lam-1
+    const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
+    const int pathc = ti >> (lam - 1);
+    const float pd0 = s_pd[warp][lam - 1][2 * p], pd1 = s_pd[warp][lam - 1][2 * p + 1];
+    for (int mt = 0; mt * 8 < nc; ++mt) {
+      const int cs = mt * 8 + g;
+      const int c = cs < nc ? cand[cs] : -1;
+      const int ch0 = 2 * c, ch1 = 2 * c + 1;
+      const bool v0 = c >= 0;
+      const bool v1 = c >= 0 && static_cast<int64_t>(ch1) * cspan <= i;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* r0 = spl_h + (v0 ? (geo.off[lam - 1] + ch0) * RQ : 0);
+      const uint4* r1 = spl_h + (v1 ? (geo.off[lam - 1] + ch1) * RQ : 0);
+      mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
+      float cnt0, cnt1;
+      {
+        const int64_t st0 = static_cast<int64_t>(ch0) * cspan, st1 = static_cast<int64_t>(ch1) * cspan;
+        if (ch0 == pathc) {
+          acc[0] = pd0; acc[1] = pd1;
+          cnt0 = static_cast<float>(i - st0 + 1);
+        } else {
+          cnt0 = static_cast<float>(min(st0 + cspan, static_cast<int64_t>(s.N)) - st0);
+        }
+        if (ch1 == pathc) {
+          acc[2] = pd0; acc[3] = pd1;
+          cnt1 = static_cast<float>(i - st1 + 1);
+        } else {
+          cnt1 = static_cast<float>(min(st1 + cspan, static_cast<int64_t>(s.N)) - st1);
+        }
+      }
+      float part = 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float x0 = s.scale * acc[e] / cnt0;
+        float l;
+        if (v1) {
+          const float x1 = s.scale * acc[2 + e] / cnt1;
+          const float mx = fmaxf(x0, x1);
+          l = mx + logf(expf(x0 - mx) + expf(x1 - mx));
+        } else {
+          l = x0;
+        }
+        if (2 * p + e < G) part += l;
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (p == 0 && cs < nc) sc[cs] = part;
+    }
+    __syncwarp();
+    for (int s2 = lane; s2 < nc; s2 += 32) {
+      const float my = sc[s2];
+      const int mi = cand[s2];
+      int rank = 0;
+      for (int o = 0; o < nc; ++o) rank += beats(sc[o], cand[o], my, mi) ? 1 : 0;
+      if (rank < Ksel) kept[rank] = mi;
+    }
+    nkept = Ksel;
+    __syncwarp();
+  }
+
+  // leaf candidates: visible children of the kept level-1 nodes (or the single leaf)
+  int32_t* out = cand_out + ((head * s.N) + i) * (2 * Ksel);
+  if (L == 1) {
+    for (int q = lane; q < 2 * Ksel; q += 32) out[q] = q == 0 ? 0 : -1;
+    return;
+  }
+  {
+    const int a = lane < nkept ? kept[lane] : -1;
+    const bool c0 = a >= 0;
+    const bool c1 = a >= 0 && static_cast<int64_t>(2 * a + 1) * C <= i;
+    const unsigned m0 = __ballot_sync(0xffffffffu, c0), m1 = __ballot_sync(0xffffffffu, c1);
+    const int pos = __popc(m0 & ltm) + __popc(m1 & ltm);
+    const int nc = __popc(m0) + __popc(m1);
+    if (c0) out[pos] = 2 * a;
+    if (c1) out[pos + 1] = 2 * a + 1;
+    for (int q = nc + lane; q < 2 * Ksel; q += 32) out[q] = -1;
+  }
+}
+
+// ---------------------------------------------------------------------------- grouping
+__global__ void group_count_kernel(const int32_t* __restrict__ cand, int64_t total, int W, int N,
+                                   int n0, int32_t* __restrict__ counts) {
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = cand[e];
+    if (t >= 0) {
+      const int64_t bk = (e / W) / N;
+      atomicAdd(&counts[bk * n0 + t], 1);
+    }
+  }
+}
+
+// Exclusive scan of n counts into off[0..n] by one 1024-thread block.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* counts, int n, int32_t* off) {
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x;
+  const int per = (n + 1023) / 1024;
+  const int s0 = min(tid * per, n), s1 = min(s0 + per, n);
+  int32_t local = 0;
+  for (int k = s0; k < s1; ++k) local += counts[k];
+  // inclusive scan of `local` over the block
+  const int lane = tid & 31, w = tid >> 5;
+  int32_t v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) warp_tot[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int32_t t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  int32_t run = v - local + (w > 0 ? warp_tot[w - 1] : 0);
+  for (int k = s0; k < s1; ++k) {   // in place is safe: each thread reads then writes its own chunk
+    const int32_t c = counts[k];
+    off[k] = run;
+    run += c;
+  }
+  if (tid == 1023) off[n] = run;
+}
+
+__global__ void group_scatter_kernel(const int32_t* __restrict__ cand, int64_t total, int W, int N,
+                                     int n0, const int32_t* __restrict__ off,
+                                     int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = cand[e];
+    if (t >= 0) {
+      const int64_t unit = e / W;
+      const int slot = static_cast<int>(e - unit * W);
+      const int i = static_cast<int>(unit % N);
+      const int64_t bin = (unit / N) * n0 + t;
+      const int32_t pos = off[bin] + atomicAdd(&cursor[bin], 1);
+      list[pos] = (i << 6) | slot;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- stage 2
+// One CTA per (leaf t, KV head, batch): exact leaf LSE for every (query, head) row whose
+// query has t among its candidates. Keys in smem (row stride D+16 bf16: conflict-free
+// 8-byte fragment loads); rows = (list entry, head), 16 per MMA tile.
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+leaf_score_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+                  const int32_t* __restrict__ off, const int32_t* __restrict__ list, int W,
+                  float* __restrict__ pair_score) {
+  constexpr int KS = D / 16, KROW = D + 16, QPT = 16 / G;
+  __shared__ __align__(16) __nv_bfloat16 sK[64 * KROW];
+  const int t = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const int64_t bin = head * s.n0 + t;
+  const int beg = off[bin], end = off[bin + 1];
+  if (beg == end) return;
+  for (int it = threadIdx.x; it < 64 * (D / 8); it += blockDim.x) {
+    const int r = it / (D / 8), c = it % (D / 8);
+    const int64_t j = static_cast<int64_t>(t) * 64 + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j < s.N) v = ldg_u4(K + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8);
+    *reinterpret_cast<uint4*>(&sK[r * KROW + c * 8]) = v;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+  const int n_ent = end - beg;
+  const int n_mt = (n_ent + QPT - 1) / QPT;
+  const int kbase = t * 64;
+  for (int mt = warp; mt < n_mt; mt += kWarps) {
+    const int e0 = mt * QPT + g / G, h0 = g % G;
+    const int e1 = mt * QPT + (g + 8) / G, h1 = (g + 8) % G;
+    const bool ok0 = e0 < n_ent, ok1 = e1 < n_ent;
+    const int pk0 = ok0 ? list[beg + e0] : 0, pk1 = ok1 ? list[beg + e1] : 0;
+    const int i0 = pk0 >> 6, i1 = pk1 >> 6;
+    const __nv_bfloat16* q0 = Q + ((static_cast<int64_t>(b) * s.N + i0) * s.Hq + kv * G + h0) * D;
+    const __nv_bfloat16* q1 = Q + ((static_cast<int64_t>(b) * s.N + i1) * s.Hq + kv * G + h1) * D;
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint2 x0 = ok0 ? ldg_u2(q0 + 16 * ks + 4 * p) : make_uint2(0, 0);
+      const uint2 x1 = ok1 ? ldg_u2(q1 + 16 * ks + 4 * p) : make_uint2(0, 0);
+      const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const uint2 bb = *reinterpret_cast<const uint2*>(&sK[(nt * 8 + g) * KROW + 16 * ks + 4 * p]);
+        mma_bf16(acc[nt], a, bb.x, bb.y);
+      }
+    }
+    float m0 = neg_inf(), m1 = neg_inf();
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kbase + nt * 8 + 2 * p + e;
+        acc[nt][e] = key <= i0 ? s.scale * acc[nt][e] : neg_inf();
+        acc[nt][2 + e] = key <= i1 ? s.scale * acc[nt][2 + e] : neg_inf();
+        m0 = fmaxf(m0, acc[nt][e]);
+        m1 = fmaxf(m1, acc[nt][2 + e]);
+      }
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    const float ms0 = m0 == neg_inf() ? 0.f : m0, ms1 = m1 == neg_inf() ? 0.f : m1;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        s0 += expf(acc[nt][e] - ms0);
+        s1 += expf(acc[nt][2 + e] - ms1);
+      }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    float l0 = ms0 + logf(s0), l1 = ms1 + logf(s1);
+#pragma unroll
+    for (int o = 4; o < 4 * G; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    if (p == 0 && h0 == 0 && ok0)
+      pair_score[(head * s.N + i0) * W + (pk0 & 63)] = l0;
+    if (p == 0 && h1 == 0 && ok1)
+      pair_score[(head * s.N + i1) * W + (pk1 & 63)] = l1;
+  }
+}
+
+// ---------------------------------------------------------------------------- finish
+// One warp per (b, KV head, query): top K of the <= W candidate scores; ascending output.
+__global__ void __launch_bounds__(kWarps * 32)
+topk_kernel(int64_t units, int W, int Ksel, const int32_t* __restrict__ cand,
+            const float* __restrict__ csc, int32_t* __restrict__ idx, float* __restrict__ score) {
+  __shared__ int s_i[kWarps][kMaxCand];
+  __shared__ float s_s[kWarps][kMaxCand];
+  __shared__ int s_k[kWarps][kMaxCand];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = blockIdx.x * static_cast<int64_t>(kWarps) + warp;
+  if (u >= units) return;
+  for (int q = lane; q < W; q += 32) {
+    const int c = cand[u * W + q];
+    s_i[warp][q] = c;
+    s_s[warp][q] = c >= 0 ? csc[u * W + q] : neg_inf();
+  }
+  __syncwarp();
+  for (int q = lane; q < W; q += 32) {
+    const int mi = s_i[warp][q];
+    int rank = 0;
+    if (mi >= 0)
+      for (int o = 0; o < W; ++o)
+        rank += (s_i[warp][o] >= 0 && beats(s_s[warp][o], s_i[warp][o], s_s[warp][q], mi)) ? 1 : 0;
+    s_k[warp][q] = (mi >= 0 && rank < Ksel) ? 1 : 0;
+  }
+  __syncwarp();
+  int nk = 0;
+  for (int q = 0; q < W; ++q) nk += s_k[warp][q];
+  for (int q = lane; q < W; q += 32) {
+    if (!s_k[warp][q]) continue;
+    const int mi = s_i[warp][q];
+    int pos = 0;
+    for (int o = 0; o < W; ++o) pos += (s_k[warp][o] && s_i[warp][o] < mi) ? 1 : 0;
+    idx[u * Ksel + pos] = mi;
+    if (score) score[u * Ksel + pos] = s_s[warp][q];
+  }
+  for (int q = nk + lane; q < Ksel; q += 32) {
+    idx[u * Ksel + q] = -1;
+    if (score) score[u * Ksel + q] = neg_inf();
+  }
+}
+
+// ---------------------------------------------------------------------------- flat BSA
+// One CTA per (query leaf block tq, KV head, batch), 4 warps x 16 queries. Leaf t < tq is
+// scored by s * qbar . S(0,t) / C with qbar = sum_h q_h (a dot product is linear, so the
+// head sum moves inside) using a 3-term bf16 split (hi*hi + hi*lo + lo*hi); the query's own
+// leaf by s * sum_{j<=i} qbar . k_j / (i - tq*C + 1). Each lane keeps a streaming top-K for
+// its two rows in shared memory; the four lanes of a row are merged at the end.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+            const uint4* __restrict__ spl, int32_t* __restrict__ idx, float* __restrict__ score) {
+  constexpr int KS = D / 16, RQ = D / 4;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int s_keep[kWarps][2 * kMaxCand];
+  const int Ksel = s.K;
+  // lists: [warp][row 0..1][k][lane] scores and indices
+  float* ls = reinterpret_cast<float*>(smem_raw);
+  int* li = reinterpret_cast<int*>(ls + kWarps * 2 * Ksel * 32);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+  const int tq = gridDim.x - 1 - blockIdx.x;
+  const int kv = blockIdx.y, b = blockIdx.z;
+  const int C = s.C, G = s.G;
+  const int qbase = tq * C + warp * 16;
+  if (qbase >= s.N) return;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const int i0 = qbase + g, i1 = qbase + g + 8;
+  const bool ok0 = i0 < s.N, ok1 = i1 < s.N;
+
+  uint32_t ahi[KS][4], alo[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int h = 0; h < G; ++h) {
+      if (ok0) {
+        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i0) * s.Hq + kv * G + h) * D + 16 * ks + 4 * p);
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+        for (int u = 0; u < 4; ++u) f0[u] += __bfloat162float(e[u]);
+      }
+      if (ok1) {
+        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i1) * s.Hq + kv * G + h) * D + 16 * ks + 4 * p);
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+        for (int u = 0; u < 4; ++u) f1[u] += __bfloat162float(e[u]);
+      }
+    }
+    __nv_bfloat16 h0[4], l0[4], h1[4], l1[4];
+    for (int u = 0; u < 4; ++u) {
+      split_bf16(f0[u], h0[u], l0[u]);
+      split_bf16(f1[u], h1[u], l1[u]);
+    }
+    auto pk = [](__nv_bfloat16 x, __nv_bfloat16 y) {
+      return (uint32_t)__bfloat16_as_ushort(x) | ((uint32_t)__bfloat16_as_ushort(y) << 16);
+    };
+    ahi[ks][0] = pk(h0[0], h0[1]); ahi[ks][2] = pk(h0[2], h0[3]);
+    ahi[ks][1] = pk(h1[0], h1[1]); ahi[ks][3] = pk(h1[2], h1[3]);
+    alo[ks][0] = pk(l0[0], l0[1]); alo[ks][2] = pk(l0[2], l0[3]);
+    alo[ks][1] = pk(l1[0], l1[1]); alo[ks][3] = pk(l1[2], l1[3]);
+  }
+
+  // streaming lists
+  float* L0s = ls + (warp * 2 + 0) * Ksel * 32;
+  float* L1s = ls + (warp * 2 + 1) * Ksel * 32;
+  int* L0i = li + (warp * 2 + 0) * Ksel * 32;
+  int* L1i = li + (warp * 2 + 1) * Ksel * 32;
+  int n0c = 0, n1c = 0, w0 = 0, w1 = 0;   // counts and worst slots
+  auto insert = [&](float* Ls, int* Li, int& n, int& w, float sv, int iv) {
+    if (n < Ksel) {
+      Ls[n * 32 + lane] = sv;
+      Li[n * 32 + lane] = iv;
+      if (n == 0 || beats(Ls[w * 32 + lane], Li[w * 32 + lane], sv, iv)) w = n;
+      ++n;
+      return;
+    }
+    if (!beats(sv, iv, Ls[w * 32 + lane], Li[w * 32 + lane])) return;
+    Ls[w * 32 + lane] = sv;
+    Li[w * 32 + lane] = iv;
+    int nw = 0;
+    for (int k = 1; k < Ksel; ++k)
+      if (beats(Ls[nw * 32 + lane], Li[nw * 32 + lane], Ls[k * 32 + lane], Li[k * 32 + lane])) nw = k;
+    w = nw;
+  };
+
+  const float inv_c = s.scale / static_cast<float>(C);
+  const uint4* spl0 = spl + (head * geo.nodes + geo.off[0]) * RQ;
+  for (int nt = 0; nt * 8 < tq; ++nt) {
+    const int tl = nt * 8 + g;
+    const bool vb = tl < tq;
+    const uint4* row = spl0 + static_cast<int64_t>(vb ? tl : 0) * RQ;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint4 x = vb ? __ldg(row + 4 * ks + p) : make_uint4(0, 0, 0, 0);
+      mma_bf16(acc, ahi[ks], x.x, x.y);
+      mma_bf16(acc, ahi[ks], x.z, x.w);
+      mma_bf16(acc, alo[ks], x.x, x.y);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = nt * 8 + 2 * p + e;
+      if (t < tq) {
+        if (ok0) insert(L0s, L0i, n0c, w0, acc[e] * inv_c, t);
+        if (ok1) insert(L1s, L1i, n1c, w1, acc[2 + e] * inv_c, t);
+      }
+    }
+  }
+  // own leaf tq: prefix over keys j <= i
+  {
+    float r0 = 0.f, r1 = 0.f;
+    const int64_t kb = static_cast<int64_t>(tq) * C;
+    for (int nt = 0; nt < 8; ++nt) {
+      const int64_t j = kb + nt * 8 + g;
+      const bool vk = j < s.N;
+      const __nv_bfloat16* kr = K + ((static_cast<int64_t>(b) * s.N + (vk ? j : 0)) * s.Hkv + kv) * D;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 x = vk ? ldg_u2(kr + 16 * ks + 4 * p) : make_uint2(0, 0);
+        mma_bf16(acc, ahi[ks], x.x, x.y);
+        mma_bf16(acc, alo[ks], x.x, x.y);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t key = kb + nt * 8 + 2 * p + e;
+        if (key <= i0) r0 += acc[e];
+        if (key <= i1) r1 += acc[2 + e];
+      }
+    }
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+    if (p == 0) {
+      if (ok0) insert(L0s, L0i, n0c, w0, s.scale * r0 / static_cast<float>(i0 - kb + 1), tq);
+      if (ok1) insert(L1s, L1i, n1c, w1, s.scale * r1 / static_cast<float>(i1 - kb + 1), tq);
+    }
+  }
+  // pad unused list slots
+  for (int k = n0c; k < Ksel; ++k) { L0s[k * 32 + lane] = neg_inf(); L0i[k * 32 + lane] = -1; }
+  for (int k = n1c; k < Ksel; ++k) { L1s[k * 32 + lane] = neg_inf(); L1i[k * 32 + lane] = -1; }
+  __syncwarp();
+
+  // merge: row r (0..15) lives in lanes 4*(r&7) + {0..3}, list (r>>3); E = 4K entries
+  const int E = 4 * Ksel;
+  int* keep = s_keep[warp];
+  for (int r = 0; r < 16; ++r) {
+    const int i = qbase + r;
+    if (i >= s.N) break;
+    const float* Ls = ls + (warp * 2 + (r >> 3)) * Ksel * 32;
+    const int* Li = li + (warp * 2 + (r >> 3)) * Ksel * 32;
+    const int lbase = 4 * (r & 7);
+    int myi[2] = {-1, -1};
+    float mys[2] = {0.f, 0.f};
+    for (int rep = 0; rep < 2; ++rep) {
+      const int eidx = lane + 32 * rep;
+      if (eidx >= E) continue;
+      const int ln = lbase + (eidx & 3), k = eidx >> 2;
+      mys[rep] = Ls[k * 32 + ln];
+      myi[rep] = Li[k * 32 + ln];
+      int kept = 0;
+      if (myi[rep] >= 0) {
+        int rank = 0;
+        for (int o = 0; o < E; ++o) {
+          const int lo_ = lbase + (o & 3), ko = o >> 2;
+          const int io = Li[ko * 32 + lo_];
+          if (io >= 0 && beats(Ls[ko * 32 + lo_], io, mys[rep], myi[rep])) ++rank;
+        }
+        kept = rank < Ksel;
+      }
+      keep[eidx] = kept ? myi[rep] : -1;
+    }
+    __syncwarp();
+    int nk = 0;
+    for (int o = 0; o < E; ++o) nk += keep[o] >= 0 ? 1 : 0;
+    int32_t* orow = idx + (head * s.N + i) * Ksel;
+    float* srow = score ? score + (head * s.N + i) * Ksel : nullptr;
+    for (int rep = 0; rep < 2; ++rep) {
+      const int eidx = lane + 32 * rep;
+      if (eidx >= E || keep[eidx] < 0) continue;
+      int pos = 0;
+      for (int o = 0; o < E; ++o) pos += (keep[o] >= 0 && keep[o] < myi[rep]) ? 1 : 0;
+      orow[pos] = myi[rep];
+      if (srow) srow[pos] = mys[rep];
+    }
+    for (int q = nk + lane; q < Ksel; q += 32) {
+      orow[q] = -1;
+      if (srow) srow[q] = neg_inf();
+    }
+    __syncwarp();
+  }
+}
+
+template <int D, int G>
+void leaf_launch(const Dims& s, dim3 grid, const void* Q, const void* K, const int32_t* off,
+                 const int32_t* list, int W, float* pair_score, cudaStream_t st) {
+  ProfScope ps(st, "leaf_score");
+  leaf_score_kernel<D, G><<<grid, kWarps * 32, 0, st>>>(
+      s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), off, list, W,
+      pair_score);
+}
+
+template <int D>
+void leaf_dispatch(const Dims& s, dim3 grid, const void* Q, const void* K, const int32_t* off,
+                   const int32_t* list, int W, float* pair_score, cudaStream_t st) {
+  switch (s.G) {
+    case 1: leaf_launch<D, 1>(s, grid, Q, K, off, list, W, pair_score, st); break;
+    case 2: leaf_launch<D, 2>(s, grid, Q, K, off, list, W, pair_score, st); break;
+    case 4: leaf_launch<D, 4>(s, grid, Q, K, off, list, W, pair_score, st); break;
+    default: leaf_launch<D, 8>(s, grid, Q, K, off, list, W, pair_score, st); break;
+  }
+}
+
+inline int grid_for(int64_t n, int threads) {
+  int64_t b = (n + threads - 1) / threads;
+  return static_cast<int>(b < 1 ? 1 : (b > 152 * 32 ? 152 * 32 : b));
+}
+
+}  // namespace
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+SelectWs select_ws(const Dims& s, const Geo& g) {
+  SelectWs w{};
+  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
+  const size_t W = 2 * static_cast<size_t>(s.K);
+  const size_t bins = static_cast<size_t>(s.B) * s.Hkv * s.n0;
+  size_t o = 0;
+  w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
+  w.cand = o;   o += align256(units * W * 4);
+  w.cscore = o; o += align256(units * W * 4);
+  w.counts = o; o += align256((bins + 1) * 4);
+  w.cursor = o; o += align256((bins + 1) * 4);
+  w.list = o;   o += align256(units * W * 4);
+  w.total = o;
+  return w;
+}
+
+size_t flat_ws(const Dims& s, const Geo& g) {
+  return align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
+}
+
+// Groups the (leaf, query) pairs of cand [units, W] (-1 entries skipped) by leaf: after
+// the call, off[bin..bin+1] delimits list entries (i << 6 | slot) of bin = head*n0 + leaf.
+int launch_group(const Dims& s, const int32_t* cand, int W, int32_t* counts, int32_t* cursor,
+                 int32_t* list, cudaStream_t st) {
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  const int64_t total = units * W;
+  const int bins = s.B * s.Hkv * s.n0;
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (bins + 1), st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * (bins + 1), st);
+  if (e != cudaSuccess) return e;
+  {
+    ProfScope ps(st, "group_count");
+    group_count_kernel<<<grid_for(total, 256), 256, 0, st>>>(cand, total, W, s.N, s.n0, counts);
+  }
+  {
+    ProfScope ps(st, "group_scan");
+    scan_kernel<<<1, 1024, 0, st>>>(counts, bins, counts);   // counts -> offsets, in place
+  }
+  {
+    ProfScope ps(st, "group_scatter");
+    group_scatter_kernel<<<grid_for(total, 256), 256, 0, st>>>(cand, total, W, s.N, s.n0, counts,
+                                                                cursor, list);
+  }
+  return cudaGetLastError();
+}
+
+int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
+  const int64_t n4 = static_cast<int64_t>(s.B) * s.Hkv * g.nodes * s.d / 4;
+  ProfScope ps(st, "split_pyramid");
+  split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4);
+  return cudaGetLastError();
+}
+
+int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
+                  int32_t* idx, float* score, char* ws, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const SelectWs w = select_ws(s, g);
+  uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
+  int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
+  float* cscore = reinterpret_cast<float*>(ws + w.cscore);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
+  int32_t* cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
+  int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+  int err = launch_split(s, g, pyr, spl, st);
+  if (err) return err;
+  dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
+  {
+  ProfScope ps(st, "route");
+  if (s.d == 128)
+    route_kernel<128><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
+                                                     static_cast<const __nv_bfloat16*>(K), spl, cand);
+  else
+    route_kernel<64><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
+                                                    static_cast<const __nv_bfloat16*>(K), spl, cand);
+  }
+  if ((err = cudaGetLastError())) return err;
+  const int W = 2 * s.K;
+  if ((err = launch_group(s, cand, W, counts, cursor, list, st))) return err;
+  dim3 lgrid(s.n0, s.Hkv, s.B);
+  if (s.d == 128) leaf_dispatch<128>(s, lgrid, Q, K, counts, list, W, cscore, st);
+  else leaf_dispatch<64>(s, lgrid, Q, K, counts, list, W, cscore, st);
+  if ((err = cudaGetLastError())) return err;
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  {
+    ProfScope ps(st, "topk");
+    topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+        units, W, s.K, cand, cscore, idx, score);
+  }
+  return cudaGetLastError();
+}
+
+int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
+                       const float* pyr, int32_t* idx, float* score, char* ws, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint4* spl = reinterpret_cast<uint4*>(ws);
+  int err = launch_split(s, g, pyr, spl, st);
+  if (err) return err;
+  dim3 grid(s.n0, s.Hkv, s.B);
+  const size_t smem = static_cast<size_t>(kWarps) * 2 * s.K * 32 * 8;
+  ProfScope ps(st, "flat_select");
+  if (s.d == 128) {
+    cudaFuncSetAttribute(flat_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    flat_kernel<128><<<grid, kWarps * 32, smem, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
+                                                      static_cast<const __nv_bfloat16*>(K), spl, idx, score);
+  } else {
+    cudaFuncSetAttribute(flat_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    flat_kernel<64><<<grid, kWarps * 32, smem, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
+                                                     static_cast<const __nv_bfloat16*>(K), spl, idx, score);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pisa

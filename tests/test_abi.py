@@ -1,0 +1,86 @@
+"""C-ABI contract tests that need no GPU: the library loads, exports every symbol that
+include/pisa.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import pyramid_top_selection_gb300 as pisa
+from pyramid_top_selection_gb300 import _pisa
+from oracle import pisa_oracle as po
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "pisa.h")).read()
+    return sorted(set(re.findall(r"\b(pisa_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = pisa.lib()
+    decl = _declared()
+    assert len(decl) >= 12
+    for name in decl:
+        assert hasattr(L, name), name
+    assert set(decl) == set(_pisa.EXPORTS)
+    assert L.pisa_version() == 1
+
+
+@pytest.mark.parametrize("N,C", [(4096, 64), (65536, 64), (262144, 64), (1, 64), (65, 64), (130, 64)])
+def test_layout_matches_oracle_geometry(N, C):
+    n, off, nodes = pisa.pyramid_layout(pisa.make_shape(1, N, 4, 1, 64, C, 8))
+    sizes = po.level_sizes(N, C)
+    assert n == len(sizes)
+    assert nodes == sum(sizes)
+    assert off == [sum(sizes[:l]) for l in range(len(sizes))]
+
+
+def _rc(fn, *args):
+    rc = fn(*args)
+    return rc, pisa.lib().pisa_last_error().decode()
+
+
+def test_host_validation_before_any_cuda_call():
+    L = pisa.lib()
+    A = 1 << 20        # fake, 16-byte aligned addresses: must never be dereferenced
+    good = pisa.make_shape(1, 4096, 4, 1, 64, 64, 8)
+    ws = pisa.workspace_size(good, _pisa.OP_SELECT)
+    cases = [
+        (pisa.make_shape(1, 4096, 4, 1, 96, 64, 8), _pisa.PISA_EUNSUPPORTED, "head dim"),
+        (pisa.make_shape(1, 4096, 4, 1, 64, 32, 8), _pisa.PISA_EUNSUPPORTED, "leaf block"),
+        (pisa.make_shape(1, 4096, 4, 1, 64, 64, 8, g=4), _pisa.PISA_EUNSUPPORTED, "fan-out"),
+        (pisa.make_shape(1, 4096, 4, 1, 64, 64, 33), _pisa.PISA_EUNSUPPORTED, "K=33"),
+        (pisa.make_shape(1, 4096, 6, 4, 64, 64, 8), _pisa.PISA_EINVAL, "multiple"),
+        (pisa.make_shape(1, 4096, 32, 1, 64, 64, 8), _pisa.PISA_EUNSUPPORTED, "GQA group"),
+        (pisa.make_shape(0, 4096, 4, 1, 64, 64, 8), _pisa.PISA_EINVAL, "positive"),
+        (pisa.make_shape(1, 4096, 4, 1, 64, 64, 8, scale=-1.0), _pisa.PISA_EINVAL, "scale"),
+    ]
+    for shape, code, text in cases:
+        rc, msg = _rc(L.pisa_select, ctypes.byref(shape), A, A, A, A, None, A, 1 << 40, None)
+        assert rc == code and text in msg, (rc, msg)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), None, A, A, A, None, A, ws, None)
+    assert rc == _pisa.PISA_EINVAL and "Q is NULL" in msg
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A + 8, A, A, A, None, A, ws, None)
+    assert rc == _pisa.PISA_EINVAL and "aligned" in msg
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, A, ws - 1, None)
+    assert rc == _pisa.PISA_EWORKSPACE
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, None, ws, None)
+    assert rc == _pisa.PISA_EWORKSPACE
+    rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, A, A, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EINVAL and "V is NULL" in msg
+    rc, msg = _rc(L.pisa_build_pyramid, None, A, A, None)
+    assert rc == _pisa.PISA_EINVAL
+    dshape = pisa.make_decode_shape(2, 1000, 8, 2, 128, 64, 16)
+    rc, msg = _rc(L.pisa_decode_step, ctypes.byref(dshape), A, A, A, A, A, A, A, A, A, None, None, None)
+    assert rc == _pisa.PISA_EINVAL and "status" in msg
+    rc, msg = _rc(L.pisa_workspace_size, ctypes.byref(good), 7, ctypes.byref(ctypes.c_size_t()))
+    assert rc == _pisa.PISA_EINVAL
+
+
+def test_workspace_sizes_grow_with_problem():
+    a = pisa.make_shape(1, 4096, 16, 2, 128, 64, 16)
+    b = pisa.make_shape(1, 65536, 16, 2, 128, 64, 16)
+    for op in range(3):
+        assert 0 < pisa.workspace_size(a, op) < pisa.workspace_size(b, op)
