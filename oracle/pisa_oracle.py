@@ -495,3 +495,51 @@ class DecodeState:
                 P = np.exp(logits - _logsumexp(logits, axis=1)[:, None])
                 o[b, hs, :] = P @ self.V[b, J, kv, :]
         return o, idx, score, margin
+
+
+def sparse_attn_bwd_sampled(Q, K, V, dO, idx, C: int, scale: float | None = None,
+                            queries=(), leaves=()):
+    """The backward's definitions evaluated only where asked: dQ of the listed queries (all
+    heads) and dK/dV of the keys of the listed (b, KV head, leaf) triples. dK/dV of a key
+    sums over every (query, head) whose selection holds the key's leaf and sees the key.
+
+    Returns (dQ {(b, i): [Hq, d]}, dK {(b, kv, t): [n_keys, d]}, dV {...})."""
+    Q, K, V, dO = _as64(Q), _as64(K), _as64(V), _as64(dO)
+    idx = np.asarray(idx)
+    B, N, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    G = Hq // Hkv
+    s = default_scale(d) if scale is None else float(scale)
+
+    def row_terms(b, kv, i):
+        hs = slice(kv * G, (kv + 1) * G)
+        J = selected_keys(idx[b, kv, i], i, C, N)
+        q, kJ, vJ, do = Q[b, i, hs, :], K[b, J, kv, :], V[b, J, kv, :], dO[b, i, hs, :]
+        logits = s * (q @ kJ.T)
+        P = np.exp(logits - _logsumexp(logits, axis=1)[:, None])
+        D = np.sum(do * (P @ vJ), axis=1)
+        dS = P * (do @ vJ.T - D[:, None])
+        return J, q, kJ, do, P, dS
+
+    dQ = {}
+    for (b, i) in queries:
+        out = np.zeros((Hq, d))
+        for kv in range(Hkv):
+            J, q, kJ, do, P, dS = row_terms(b, kv, i)
+            out[kv * G:(kv + 1) * G] = s * (dS @ kJ)
+        dQ[(b, i)] = out
+    dK, dV = {}, {}
+    for (b, kv, t) in leaves:
+        s0, e0 = node_range(0, t, C, N)
+        gk = np.zeros((e0 - s0, d))
+        gv = np.zeros((e0 - s0, d))
+        users = np.nonzero((idx[b, kv] == t).any(axis=-1))[0]
+        for i in users:
+            J, q, kJ, do, P, dS = row_terms(b, kv, int(i))
+            for c, j in enumerate(J):
+                if s0 <= j < e0:
+                    gk[j - s0] += s * (dS[:, c] @ q)
+                    gv[j - s0] += P[:, c] @ do
+        dK[(b, kv, t)] = gk
+        dV[(b, kv, t)] = gv
+    return dQ, dK, dV

@@ -82,3 +82,22 @@ def query_subsample(N: int, every: int = 7, tail: int = 4096) -> torch.Tensor:
     """Deterministic query subsample for full-size parity: every `every`-th query + the last `tail`."""
     idx = set(range(0, N, every)) | set(range(max(0, N - tail), N))
     return torch.tensor(sorted(idx), dtype=torch.int64)
+
+
+def random_selection(B: int, Hkv: int, N: int, C: int, K: int, seed: int, device="cpu") -> torch.Tensor:
+    """A uniformly random valid selection: for every (b, KV head, query i), K distinct leaves
+    among the visible ones 0..floor(i/C) (all of them if fewer), ascending, -1 padded.
+    Returns int32 [B, Hkv, N, K]."""
+    n0 = (N + C - 1) // C
+    g = _gen(device, seed)
+    r = torch.rand(B, Hkv, N, n0, generator=g, device=device)
+    vis = torch.arange(n0, device=device).view(1, 1, 1, n0) <= (torch.arange(N, device=device) // C).view(1, 1, N, 1)
+    r = torch.where(vis, r, torch.full_like(r, -1.0))
+    k = min(K, n0)
+    val, pick = torch.topk(r, k, dim=-1)
+    pick = torch.where(val >= 0, pick, torch.full_like(pick, n0 + 1))
+    pick = torch.sort(pick, dim=-1).values
+    pick = torch.where(pick > n0, torch.full_like(pick, -1), pick)
+    out = torch.full((B, Hkv, N, K), -1, dtype=torch.int32, device=device)
+    out[..., :k] = pick.to(torch.int32)
+    return out

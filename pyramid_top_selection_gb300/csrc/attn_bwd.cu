@@ -1,20 +1,381 @@
-// Backward of the selected attention (placeholder until the block-major kernel lands).
+// Backward of the causal block-sparse attention; the discrete selection takes no gradient.
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference value
+// of the work": during training the gradient passes only through the selected attention,
+// so the block selection can be dropped into an existing model as a sparse module.
+//
+// With P = exp(s q.k - lse) (lse from the forward), D_i = dO_i . O_i and
+// dS = P (dO . v - D):  dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO.
+//
+// Block-major: the selected (leaf, query) pairs are grouped by leaf and one CTA owns one
+// leaf block of one KV head, so that block's dK/dV are complete inside the CTA (no atomics)
+// and summed over all rows = (query, head of the group) that selected it. Each of the 4
+// warps owns 16 of the 64 keys and keeps their dK/dV in registers across all row chunks;
+// rows come in chunks of 32, staged in shared memory row-major and transposed. dQ of a
+// (row, block) pair is a partial written to the workspace; a second kernel sums the <= K
+// partials of every row.
 #include "device.cuh"
+#include "profile.h"
 
 namespace pisa {
 
+int launch_group(const Dims& s, const int32_t* cand, int W, int32_t* counts, int32_t* cursor,
+                 int32_t* list, cudaStream_t st);
 size_t align256(size_t x);
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kRows = 32;       // rows per chunk
+
+template <int D>
+struct BwdSmem {
+  static constexpr int KROW = D + 16;     // row-major tiles (8-byte fragment loads)
+  static constexpr int TROW = 64 + 8;     // transposed K tile [dim][key]
+  static constexpr int RROW = kRows + 8;  // transposed row tiles [dim][row]
+  static constexpr int SROW = 64 + 8;     // dS [row][key]
+  static constexpr int oK = 0;
+  static constexpr int oV = oK + 64 * KROW;
+  static constexpr int oKt = oV + 64 * KROW;
+  static constexpr int oQ = oKt + D * TROW;
+  static constexpr int odO = oQ + kRows * KROW;
+  static constexpr int oQt = odO + kRows * KROW;
+  static constexpr int odOt = oQt + D * RROW;
+  static constexpr int odS = odOt + D * RROW;
+  static constexpr int n_bf16 = odS + kRows * SROW;
+  static constexpr int bytes = n_bf16 * 2 + kRows * (4 + 4 + 4 + 4 + 4);
+};
+
+// D_row = dO_row . O_row (fp32), one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+delta_kernel(int64_t rows, const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+             float* __restrict__ delta) {
+  const int64_t row = blockIdx.x * 8LL + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int PER = D / 32;
+  float acc = 0.f;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int64_t o = row * D + lane * PER + u;
+    acc += __bfloat162float(O[o]) * __bfloat162float(dO[o]);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) delta[row] = acc;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_bwd_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+                const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ dO,
+                const float* __restrict__ lse, const float* __restrict__ delta,
+                const int32_t* __restrict__ off, const int32_t* __restrict__ list,
+                __nv_bfloat16* __restrict__ part_dq, __nv_bfloat16* __restrict__ dK,
+                __nv_bfloat16* __restrict__ dV) {
+  using L = BwdSmem<D>;
+  constexpr int KS = D / 16, ND = D / 8, QPC = kRows / G;
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smraw);
+  __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sKt = sb + L::oKt, *sQ = sb + L::oQ,
+                *sdO = sb + L::odO, *sQt = sb + L::oQt, *sdOt = sb + L::odOt, *sdS = sb + L::odS;
+  float* s_lse = reinterpret_cast<float*>(sb + L::n_bf16);
+  float* s_D = s_lse + kRows;
+  int* s_i = reinterpret_cast<int*>(s_D + kRows);
+  int* s_slot = s_i + kRows;
+  int* s_h = s_slot + kRows;
+
+  const int t = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const int64_t bin = head * s.n0 + t;
+  const int beg = off[bin], end = off[bin + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+  const int kbase = t * 64;
+
+  // leaf tiles: K, V row-major, K transposed
+  for (int it = threadIdx.x; it < 64 * (D / 8); it += blockDim.x) {
+    const int r = it / (D / 8), c = it % (D / 8);
+    const int64_t j = static_cast<int64_t>(kbase) + r;
+    uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    if (j < s.N && beg < end) {
+      const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8;
+      kk = ldg_u4(K + o);
+      vv = ldg_u4(V + o);
+    }
+    *reinterpret_cast<uint4*>(&sK[r * L::KROW + c * 8]) = kk;
+    *reinterpret_cast<uint4*>(&sV[r * L::KROW + c * 8]) = vv;
+    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kk);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sKt[(c * 8 + e) * L::TROW + r] = ke[e];
+  }
+
+  float dv[ND][4], dk[ND][4];
+#pragma unroll
+  for (int nd = 0; nd < ND; ++nd)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dv[nd][e] = dk[nd][e] = 0.f;
+
+  const int n_ent = end - beg;
+  const int key0 = 16 * warp;        // this warp's keys: key0 + g, key0 + g + 8
+  for (int e0 = 0; e0 < n_ent; e0 += QPC) {
+    __syncthreads();                 // previous chunk fully consumed
+    // stage the chunk's rows (query, head): row r = entry r / G, head r % G
+    for (int it = threadIdx.x; it < kRows * (D / 8); it += blockDim.x) {
+      const int r = it / (D / 8), c = it % (D / 8);
+      const int e = e0 + r / G, h = r % G;
+      uint4 qq = make_uint4(0, 0, 0, 0), oo = make_uint4(0, 0, 0, 0);
+      if (e < n_ent) {
+        const int pk = list[beg + e];
+        const int64_t row = (static_cast<int64_t>(b) * s.N + (pk >> 6)) * s.Hq + kv * G + h;
+        qq = ldg_u4(Q + row * D + c * 8);
+        oo = ldg_u4(dO + row * D + c * 8);
+      }
+      *reinterpret_cast<uint4*>(&sQ[r * L::KROW + c * 8]) = qq;
+      *reinterpret_cast<uint4*>(&sdO[r * L::KROW + c * 8]) = oo;
+      const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(&qq);
+      const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&oo);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        sQt[(c * 8 + u) * L::RROW + r] = qe[u];
+        sdOt[(c * 8 + u) * L::RROW + r] = oe[u];
+      }
+    }
+    if (threadIdx.x < kRows) {
+      const int r = threadIdx.x, e = e0 + r / G, h = r % G;
+      if (e < n_ent) {
+        const int pk = list[beg + e];
+        const int i = pk >> 6;
+        const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
+        s_lse[r] = lse[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i];
+        s_D[r] = delta[row];
+        s_i[r] = i;
+        s_slot[r] = pk & 63;
+        s_h[r] = h;
+      } else {
+        s_lse[r] = __int_as_float(0x7f800000);   // +inf: P = 0 on padding rows
+        s_D[r] = 0.f;
+        s_i[r] = -1;
+        s_slot[r] = 0;
+        s_h[r] = 0;
+      }
+    }
+    __syncthreads();
+
+    // S^T and dP^T for keys key0+{g, g+8} x the 32 rows (4 n-tiles of 8 rows)
+    float st[4][4], dp[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st[nt][e] = dp[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint2 k0 = *reinterpret_cast<const uint2*>(&sK[(key0 + g) * L::KROW + 16 * ks + 4 * p]);
+      const uint2 k1 = *reinterpret_cast<const uint2*>(&sK[(key0 + g + 8) * L::KROW + 16 * ks + 4 * p]);
+      const uint2 v0 = *reinterpret_cast<const uint2*>(&sV[(key0 + g) * L::KROW + 16 * ks + 4 * p]);
+      const uint2 v1 = *reinterpret_cast<const uint2*>(&sV[(key0 + g + 8) * L::KROW + 16 * ks + 4 * p]);
+      const uint32_t ak[4] = {k0.x, k1.x, k0.y, k1.y};
+      const uint32_t av[4] = {v0.x, v1.x, v0.y, v1.y};
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint2 q = *reinterpret_cast<const uint2*>(&sQ[(nt * 8 + g) * L::KROW + 16 * ks + 4 * p]);
+        const uint2 o = *reinterpret_cast<const uint2*>(&sdO[(nt * 8 + g) * L::KROW + 16 * ks + 4 * p]);
+        mma_bf16(st[nt], ak, q.x, q.y);
+        mma_bf16(dp[nt], av, o.x, o.y);
+      }
+    }
+    // P^T, dS^T (in place: st <- P, dp <- dS)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = nt * 8 + 2 * p + (e & 1);
+        const int key = kbase + key0 + g + ((e >> 1) << 3);
+        const float pr = (s_i[r] >= 0 && key <= s_i[r]) ? expf(s.scale * st[nt][e] - s_lse[r]) : 0.f;
+        st[nt][e] = pr;
+        dp[nt][e] = pr * (dp[nt][e] - s_D[r]);
+      }
+    // dV += P^T dO, dK += dS^T Q   (contraction over the 32 rows: 2 k-steps)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t ap[4] = {pack_bf16(st[2 * kk][0], st[2 * kk][1]), pack_bf16(st[2 * kk][2], st[2 * kk][3]),
+                              pack_bf16(st[2 * kk + 1][0], st[2 * kk + 1][1]),
+                              pack_bf16(st[2 * kk + 1][2], st[2 * kk + 1][3])};
+      const uint32_t as[4] = {pack_bf16(dp[2 * kk][0], dp[2 * kk][1]), pack_bf16(dp[2 * kk][2], dp[2 * kk][3]),
+                              pack_bf16(dp[2 * kk + 1][0], dp[2 * kk + 1][1]),
+                              pack_bf16(dp[2 * kk + 1][2], dp[2 * kk + 1][3])};
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const __nv_bfloat16* orow = &sdOt[(nd * 8 + g) * L::RROW + 16 * kk + 2 * p];
+        const __nv_bfloat16* qrow = &sQt[(nd * 8 + g) * L::RROW + 16 * kk + 2 * p];
+        mma_bf16(dv[nd], ap, *reinterpret_cast<const uint32_t*>(orow), *reinterpret_cast<const uint32_t*>(orow + 8));
+        mma_bf16(dk[nd], as, *reinterpret_cast<const uint32_t*>(qrow), *reinterpret_cast<const uint32_t*>(qrow + 8));
+      }
+    }
+    // dS -> shared memory as [row][key] for dQ
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = nt * 8 + 2 * p + (e & 1);
+        const int key = key0 + g + ((e >> 1) << 3);
+        sdS[r * L::SROW + key] = __float2bfloat16_rn(dp[nt][e]);
+      }
+    __syncthreads();
+    // dQ partial = s dS K for 16 rows x D/2 dims per warp
+    {
+      const int r0 = (warp & 1) * 16, d0 = (warp >> 1) * (D / 2);
+      float dq[ND / 2][4];
+#pragma unroll
+      for (int nd = 0; nd < ND / 2; ++nd)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dq[nd][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const __nv_bfloat16* a0 = &sdS[(r0 + g) * L::SROW + 16 * kk + 2 * p];
+        const __nv_bfloat16* a1 = &sdS[(r0 + g + 8) * L::SROW + 16 * kk + 2 * p];
+        const uint32_t a[4] = {*reinterpret_cast<const uint32_t*>(a0), *reinterpret_cast<const uint32_t*>(a1),
+                               *reinterpret_cast<const uint32_t*>(a0 + 8), *reinterpret_cast<const uint32_t*>(a1 + 8)};
+#pragma unroll
+        for (int nd = 0; nd < ND / 2; ++nd) {
+          const __nv_bfloat16* br = &sKt[(d0 + nd * 8 + g) * L::TROW + 16 * kk + 2 * p];
+          mma_bf16(dq[nd], a, *reinterpret_cast<const uint32_t*>(br), *reinterpret_cast<const uint32_t*>(br + 8));
+        }
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int r = r0 + g + 8 * half;
+        if (s_i[r] < 0) continue;
+        const int64_t row = (static_cast<int64_t>(b) * s.N + s_i[r]) * s.Hq + kv * G + s_h[r];
+        __nv_bfloat16* dst = part_dq + (row * s.K + s_slot[r]) * D + d0;
+#pragma unroll
+        for (int nd = 0; nd < ND / 2; ++nd)
+          *reinterpret_cast<uint32_t*>(dst + nd * 8 + 2 * p) =
+              pack_bf16(s.scale * dq[nd][2 * half], s.scale * dq[nd][2 * half + 1]);
+      }
+    }
+  }
+  // dK, dV of this leaf block (zero when no query selected it)
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int64_t j = static_cast<int64_t>(kbase) + key0 + g + 8 * half;
+    if (j >= s.N) continue;
+    const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D;
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      *reinterpret_cast<uint32_t*>(dK + o + nd * 8 + 2 * p) =
+          pack_bf16(s.scale * dk[nd][2 * half], s.scale * dk[nd][2 * half + 1]);
+      *reinterpret_cast<uint32_t*>(dV + o + nd * 8 + 2 * p) = pack_bf16(dv[nd][2 * half], dv[nd][2 * half + 1]);
+    }
+  }
+}
+
+// dQ_row = sum over the row's valid slots of the partials; one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+dq_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_dq,
+                  __nv_bfloat16* __restrict__ dQ) {
+  constexpr int PER = D / 32;
+  const int64_t row = blockIdx.x * 8LL + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<int64_t>(s.B) * s.N * s.Hq) return;
+  const int h = static_cast<int>(row % s.Hq);
+  const int64_t bi = row / s.Hq;
+  const int i = static_cast<int>(bi % s.N), b = static_cast<int>(bi / s.N);
+  const int32_t* id = idx + ((static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i) * s.K;
+  float acc[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) acc[u] = 0.f;
+  for (int q = 0; q < s.K; ++q) {
+    if (id[q] < 0) continue;
+    const __nv_bfloat16* src = part_dq + (row * s.K + q) * D + lane * PER;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) acc[u] += __bfloat162float(src[u]);
+  }
+  __nv_bfloat16* dst = dQ + row * D + lane * PER;
+#pragma unroll
+  for (int u = 0; u < PER; u += 2) *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u], acc[u + 1]);
+}
+
+template <int D, int G>
+int bwd_launch(const Dims& s, const void* Q, const void* K, const void* V, const void* dO,
+               const float* lse, const float* delta, const int32_t* off, const int32_t* list,
+               __nv_bfloat16* pdq, void* dK, void* dV, cudaStream_t st) {
+  const int smem = BwdSmem<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ProfScope ps(st, "attn_bwd");
+  attn_bwd_kernel<D, G><<<dim3(s.n0, s.Hkv, s.B), kWarps * 32, smem, st>>>(
+      s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+      static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(dO), lse, delta, off, list,
+      pdq, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
+  return cudaGetLastError();
+}
+
+template <int D>
+int bwd_dispatch(const Dims& s, const void* Q, const void* K, const void* V, const void* dO,
+                 const float* lse, const float* delta, const int32_t* off, const int32_t* list,
+                 __nv_bfloat16* pdq, void* dK, void* dV, cudaStream_t st) {
+  switch (s.G) {
+    case 1: return bwd_launch<D, 1>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
+    case 2: return bwd_launch<D, 2>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
+    case 4: return bwd_launch<D, 4>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
+    default: return bwd_launch<D, 8>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
+  }
+}
+
+}  // namespace
 
 AttnBwdWs attn_bwd_ws(const Dims& s) {
   AttnBwdWs w{};
-  (void)s;
-  w.total = 256;
+  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
+  const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
+  const size_t bins = static_cast<size_t>(s.B) * s.Hkv * s.n0;
+  size_t o = 0;
+  w.counts = o;  o += align256((bins + 1) * 4);
+  w.cursor = o;  o += align256((bins + 1) * 4);
+  w.list = o;    o += align256(units * s.K * 4);
+  w.delta = o;   o += align256(rows * 4);
+  w.part_dq = o; o += align256(rows * s.K * s.d * 2);
+  w.total = o;
   return w;
 }
 
-int launch_attn_bwd(const Dims&, const void*, const void*, const void*, const void*, const float*,
-                    const void*, const int32_t*, void*, void*, void*, char*, void*) {
-  return static_cast<int>(cudaErrorNotSupported);
+int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, const void* O,
+                    const float* lse, const void* dO, const int32_t* idx, void* dQ, void* dK,
+                    void* dV, char* ws, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const AttnBwdWs w = attn_bwd_ws(s);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
+  int32_t* cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
+  int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  __nv_bfloat16* pdq = reinterpret_cast<__nv_bfloat16*>(ws + w.part_dq);
+  int err = launch_group(s, idx, s.K, counts, cursor, list, st);
+  if (err) return err;
+  const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
+  const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+  {
+    ProfScope ps(st, "attn_bwd_delta");
+    if (s.d == 128)
+      delta_kernel<128><<<blocks, 256, 0, st>>>(rows, static_cast<const __nv_bfloat16*>(O),
+                                                static_cast<const __nv_bfloat16*>(dO), delta);
+    else
+      delta_kernel<64><<<blocks, 256, 0, st>>>(rows, static_cast<const __nv_bfloat16*>(O),
+                                               static_cast<const __nv_bfloat16*>(dO), delta);
+  }
+  if ((err = cudaGetLastError())) return err;
+  err = s.d == 128 ? bwd_dispatch<128>(s, Q, K, V, dO, lse, delta, counts, list, pdq, dK, dV, st)
+                   : bwd_dispatch<64>(s, Q, K, V, dO, lse, delta, counts, list, pdq, dK, dV, st);
+  if (err) return err;
+  {
+    ProfScope ps(st, "attn_bwd_dq");
+    if (s.d == 128)
+      dq_combine_kernel<128><<<blocks, 256, 0, st>>>(s, idx, pdq, static_cast<__nv_bfloat16*>(dQ));
+    else
+      dq_combine_kernel<64><<<blocks, 256, 0, st>>>(s, idx, pdq, static_cast<__nv_bfloat16*>(dQ));
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace pisa

@@ -634,10 +634,13 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
     const float* Ls = ls + (warp * 2 + (r >> 3)) * Ksel * 32;
     const int* Li = li + (warp * 2 + (r >> 3)) * Ksel * 32;
     const int lbase = 4 * (r & 7);
-    int myi[2] = {-1, -1};
-    float mys[2] = {0.f, 0.f};
-    for (int rep = 0; rep < 2; ++rep) {
+    constexpr int kReps = (2 * kMaxCand) / 32;      // E <= 4*32 entries, 32 per pass
+    int myi[kReps];
+    float mys[kReps];
+    for (int rep = 0; rep < kReps; ++rep) {
       const int eidx = lane + 32 * rep;
+      myi[rep] = -1;
+      mys[rep] = 0.f;
       if (eidx >= E) continue;
       const int ln = lbase + (eidx & 3), k = eidx >> 2;
       mys[rep] = Ls[k * 32 + ln];
@@ -659,7 +662,7 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
     for (int o = 0; o < E; ++o) nk += keep[o] >= 0 ? 1 : 0;
     int32_t* orow = idx + (head * s.N + i) * Ksel;
     float* srow = score ? score + (head * s.N + i) * Ksel : nullptr;
-    for (int rep = 0; rep < 2; ++rep) {
+    for (int rep = 0; rep < kReps; ++rep) {
       const int eidx = lane + 32 * rep;
       if (eidx >= E || keep[eidx] < 0) continue;
       int pos = 0;

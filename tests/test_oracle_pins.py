@@ -368,3 +368,20 @@ def test_decode_incremental_pyramid_equals_rebuilt_and_prefill():
         np.testing.assert_allclose(score, pre["score"][:, :, p], rtol=1e-10, atol=1e-10)
         Op, _ = po.sparse_attn_fwd(Qp, st.K[:, :p + 1], st.V[:, :p + 1], pre["idx"], C, scale=0.5, queries=[p])
         np.testing.assert_allclose(o, Op[:, p], rtol=1e-10, atol=1e-12)
+
+
+def test_sampled_backward_equals_full_backward():
+    B, N, Hq, Hkv, d, C = 2, 50, 4, 2, 4, 8
+    Q, K, V = _rand((B, N, Hq, d), 130), _rand((B, N, Hkv, d), 131), _rand((B, N, Hkv, d), 132)
+    dO = _rand((B, N, Hq, d), 133)
+    idx = po.select(Q, K, C, 2)["idx"]
+    dQ, dK, dV = po.sparse_attn_bwd(Q, K, V, dO, idx, C, scale=0.4)
+    qs = [(0, 0), (1, 17), (0, 49)]
+    ls = [(0, 0, 0), (1, 1, 3), (0, 1, 6)]
+    sq, sk, sv = po.sparse_attn_bwd_sampled(Q, K, V, dO, idx, C, scale=0.4, queries=qs, leaves=ls)
+    for (b, i) in qs:
+        np.testing.assert_allclose(sq[(b, i)], dQ[b, i], rtol=1e-12, atol=1e-13)
+    for (b, kv, t) in ls:
+        s0, e0 = po.node_range(0, t, C, N)
+        np.testing.assert_allclose(sk[(b, kv, t)], dK[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(sv[(b, kv, t)], dV[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
