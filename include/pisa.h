@@ -110,6 +110,23 @@ int pisa_build_pyramid(const pisa_shape_t* shape, const void* K, float* pyr_sum,
 int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const float* pyr_sum,
                 int32_t* idx, float* score, void* ws, size_t ws_bytes, void* stream);
 
+/* pisa_select without a caller workspace (the pages have no counterpart: this is an
+ * integration aid). For callers that cannot hand the library device memory at call time,
+ * for instance code running under an engine that owns a fixed device-memory arena and
+ * forbids allocations on the serving path, or a plugin whose host exposes no allocator.
+ * Same arguments, results and errors as pisa_select minus ws/ws_bytes; it allocates
+ * nothing and calls no allocating routine. Its scratch is one fixed 32 MiB array inside
+ * the library's device image, held on every GPU that loads the library until the process
+ * exits. Shapes whose pisa_workspace_size(shape, PISA_OP_SELECT) exceeds 32 MiB are
+ * rejected with PISA_EUNSUPPORTED before any CUDA call (about B*Hkv*N <= 80K units at
+ * K = 16). The first call on a device looks up the array's device address (with that
+ * device current) and should come before any stream capture. Every call shares the one
+ * array and it keeps the last call's contents: the call clears on its stream whatever must
+ * start at zero, and calls whose GPU work overlaps in time (different streams or host
+ * threads on one device) race on the array. */
+int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
+                        const float* pyr_sum, int32_t* idx, float* score, void* stream);
+
 /* Flat block selection, the O(N^2/C) comparator (digest page, "Motivation": conventional
  * selection scores every query-block pair): leaf t scores sum_h s q_{i,h} . mu_i(0,t)
  * over every visible leaf; top K with the same tie rule and output layout as

@@ -25,6 +25,7 @@ EXPORTS = (
     "pisa_build_pyramid", "pisa_select", "pisa_select_flat", "pisa_sparse_attn_fwd",
     "pisa_sparse_attn_bwd", "pisa_decode_pyramid_layout", "pisa_decode_build_pyramid",
     "pisa_decode_step", "pisa_profile_start", "pisa_profile_stop", "pisa_profile_read",
+    "pisa_select_noalloc",
 )
 
 

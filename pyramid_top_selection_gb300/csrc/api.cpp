@@ -155,6 +155,27 @@ int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const f
                  "pisa_select");
 }
 
+int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
+                        const float* pyr_sum, int32_t* idx, float* score, void* stream) {
+  PISA_CHECK(check_shape(shape));
+  PISA_CHECK(check_ptr(Q, "Q"));
+  PISA_CHECK(check_ptr(K, "K"));
+  PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
+  PISA_CHECK(check_ptr(idx, "idx"));
+  PISA_CHECK(check_ptr(score, "score", true));
+  const pisa::Dims d = dims_of(shape);
+  const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  const size_t need = pisa::select_ws(d, g).total;
+  if (need > pisa::noalloc_scratch_bytes())
+    return fail(PISA_EUNSUPPORTED,
+                "pisa_select_noalloc: this shape needs %zu bytes of scratch, more than the fixed %zu; "
+                "use pisa_select with a caller workspace", need, pisa::noalloc_scratch_bytes());
+  void* ws = nullptr;
+  PISA_CHECK(cuda_rc(pisa::noalloc_scratch(&ws), "pisa_select_noalloc scratch set-up"));
+  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
+                 "pisa_select_noalloc");
+}
+
 int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
                      const float* pyr_sum, int32_t* idx, float* score, void* ws,
                      size_t ws_bytes, void* stream) {

@@ -73,5 +73,7 @@ int launch_decode_step(const Dims& s, int32_t Ncap, const Geo& g, const int32_t*
                        const void* v_new, void* o, int32_t* idx, float* score, int32_t* status,
                        void* stream);
 const char* cuda_error_string(int err);
+size_t noalloc_scratch_bytes();
+int noalloc_scratch(void** out);
 
 }  // namespace pisa
