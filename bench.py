@@ -193,7 +193,7 @@ def algorithmic(kernel, cfg, idx_host=None):
         units = B * Hkv * cands
         per = G * C * 2 * d
         return "tensor", units * per, "flops", units, per
-    if kernel == "attn_fwd_partial" and idx_host is not None:
+    if kernel in ("attn_fwd", "attn_fwd_partial") and idx_host is not None:
         keys = selected_keys(idx_host, C, N)
         units = keys * G
         per = 4 * d

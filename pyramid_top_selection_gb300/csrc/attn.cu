@@ -6,19 +6,20 @@
 // groups the queries that use the same leaf key block into tiles so the block's keys are
 // read once per tile.
 //
-// Forward, block-major: the selected (leaf, query) pairs are grouped by leaf; one CTA per
-// leaf block keeps the block's K (row-major) and V (transposed) in shared memory and runs
-// S = Q K^T and O = P V on MMAs for 16-row tiles of (query, head) rows. Each (row, block)
-// yields a normalised partial output and its block LSE; a combine kernel merges the
-// <= K partials of every row: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
+// Forward, block-major: the selected (leaf, query) pairs are grouped by (KV head, query
+// chunk, leaf) and cut into work items; one CTA per item keeps the leaf block's K
+// (row-major) and V (transposed) in shared memory and runs S = Q K^T and O = P V on MMAs
+// for 16-row tiles of (query, head) rows. Each (row, block) yields a normalised partial
+// output and its block LSE. Every query counts its finished blocks with one atomic; the
+// warp that finishes a query's last block merges that query's <= K partials right away,
+// while they are still in L2: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t,
+// then discards the merged partials' L2 lines (they are dead) so they are never written
+// back to HBM. Nothing waits on anything: the counter only decides who merges.
 #include "device.cuh"
+#include "group.h"
 #include "profile.h"
 
 namespace pisa {
-
-int launch_group(const Dims& s, const int32_t* cand, int W, int32_t* counts, int32_t* cursor,
-                 int32_t* list, cudaStream_t st);
-size_t align256(size_t x);
 
 namespace {
 
@@ -45,25 +46,78 @@ __device__ __forceinline__ void load_kv_tiles(const Dims& s, int b, int kv, int 
   }
 }
 
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Merge the nsel block partials of query i (all G heads of KV head kv) -- one warp.
+template <int D, int G>
+__device__ __forceinline__ void merge_query(const Dims& s, int b, int kv, int i, int nsel,
+                                            __nv_bfloat16* part_o, const float* part_lse,
+                                            __nv_bfloat16* O, float* lse_out, int lane) {
+  constexpr int PER = D / 32;
+  for (int h = 0; h < G; ++h) {
+    const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
+    const float* pl = part_lse + row * s.K;
+    float m = neg_inf();
+    for (int q = 0; q < nsel; ++q) m = fmaxf(m, __ldcg(pl + q));
+    float den = 0.f, acc[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) acc[u] = 0.f;
+    for (int q = 0; q < nsel; ++q) {
+      const float w = m == neg_inf() ? 0.f : expf(__ldcg(pl + q) - m);
+      den += w;
+      const __nv_bfloat16* src = part_o + (row * s.K + q) * D + lane * PER;
+      if (PER == 4) {
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(src));
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) acc[u] += w * __bfloat162float(e[u]);
+      } else {
+        const unsigned int v = __ldcg(reinterpret_cast<const unsigned int*>(src));
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) acc[u] += w * __bfloat162float(e[u]);
+      }
+    }
+    const float r = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16* dst = O + row * D + lane * PER;
+#pragma unroll
+    for (int u = 0; u < PER; u += 2)
+      *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
+    if (lane == 0)
+      lse_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
+    // the merged partials (whole 128-byte lines of this row only) are dead: drop them from L2
+    __syncwarp();
+    const int lines = nsel * D * 2 / 128;
+    const char* base = reinterpret_cast<const char*>(part_o + row * s.K * D);
+    if ((reinterpret_cast<uintptr_t>(base) & 127) == 0)
+      for (int k = lane; k < lines; k += 32) discard_l2_line(base + k * 128);
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32)
-attn_fwd_partial_kernel(Dims s, const __nv_bfloat16* __restrict__ Q,
-                        const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-                        const int32_t* __restrict__ off, const int32_t* __restrict__ list,
-                        __nv_bfloat16* __restrict__ part_o, float* __restrict__ part_lse) {
+attn_fwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
+                const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
+                const int32_t* __restrict__ idx, const int32_t* __restrict__ list,
+                const int4* __restrict__ items, const int32_t* __restrict__ n_items,
+                __nv_bfloat16* part_o, float* part_lse, int32_t* __restrict__ counter,
+                __nv_bfloat16* __restrict__ O, float* __restrict__ lse_out) {
   constexpr int KS = D / 16, KROW = D + 16, VROW = 64 + 8, QPT = 16 / G, ND = D / 8;
   __shared__ __align__(16) __nv_bfloat16 sK[64 * KROW];
   __shared__ __align__(16) __nv_bfloat16 sVt[D * VROW];
-  const int t = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
-  const int64_t bin = head * s.n0 + t;
-  const int beg = off[bin], end = off[bin + 1];
-  if (beg == end) return;
+  if (static_cast<int>(blockIdx.x) >= *n_items) return;
+  const int4 it = items[blockIdx.x];
+  const int64_t bin = it.x;
+  const int beg = it.y, n_ent = it.z;
+  const int t = gp.leaf_of(bin);
+  const int64_t head = gp.head_of(bin);
+  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
   load_kv_tiles<D>(s, b, kv, t, K, V, sK, sVt);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
-  const int n_ent = end - beg;
   const int n_mt = (n_ent + QPT - 1) / QPT;
   const int kbase = t * 64;
   const int Ksel = s.K;
@@ -143,7 +197,8 @@ attn_fwd_partial_kernel(Dims s, const __nv_bfloat16* __restrict__ Q,
         mma_bf16(oacc[nd], a, b0, b1);
       }
     }
-    const float r0 = 1.f / l0, r1 = 1.f / l1;
+    // a block with no key visible to the row (not a valid selection) contributes nothing
+    const float r0 = l0 > 0.f ? 1.f / l0 : 0.f, r1 = l1 > 0.f ? 1.f / l1 : 0.f;
     const int slot0 = pk0 & 63, slot1 = pk1 & 63;
     __nv_bfloat16* po0 = part_o + (row0 * Ksel + slot0) * D;
     __nv_bfloat16* po1 = part_o + (row1 * Ksel + slot1) * D;
@@ -155,94 +210,76 @@ attn_fwd_partial_kernel(Dims s, const __nv_bfloat16* __restrict__ Q,
         *reinterpret_cast<uint32_t*>(po1 + nd * 8 + 2 * p) = pack_bf16(oacc[nd][2] * r1, oacc[nd][3] * r1);
     }
     if (p == 0) {
-      if (ok0) part_lse[row0 * Ksel + slot0] = ms0 + logf(l0);
-      if (ok1) part_lse[row1 * Ksel + slot1] = ms1 + logf(l1);
+      if (ok0) part_lse[row0 * Ksel + slot0] = l0 > 0.f ? ms0 + logf(l0) : neg_inf();
+      if (ok1) part_lse[row1 * Ksel + slot1] = l1 > 0.f ? ms1 + logf(l1) : neg_inf();
+    }
+    // arrival: lane e < QPT reports entry mt*QPT + e (all its G rows are in this tile)
+    __threadfence();
+    __syncwarp();
+    int qi = -1, nsel = 0, last = 0;
+    if (lane < QPT) {
+      const int e = mt * QPT + lane;
+      if (e < n_ent) {
+        qi = list[beg + e] >> 6;
+        const int64_t unit = head * s.N + qi;
+        const int32_t* id = idx + unit * Ksel;
+        for (int q = 0; q < Ksel; ++q) nsel += id[q] >= 0 ? 1 : 0;
+        last = atomicAdd(&counter[unit], 1) == nsel - 1;
+      }
+    }
+    unsigned lm = __ballot_sync(0xffffffffu, last);
+    if (lm) __threadfence();
+    while (lm) {
+      const int src = __ffs(lm) - 1;
+      lm &= lm - 1;
+      const int i = __shfl_sync(0xffffffffu, qi, src);
+      const int ns = __shfl_sync(0xffffffffu, nsel, src);
+      merge_query<D, G>(s, b, kv, i, ns, part_o, part_lse, O, lse_out, lane);
     }
   }
-}
-
-// One warp per (b, query, head) row: merges the row's <= K block partials.
-template <int D>
-__global__ void __launch_bounds__(256)
-attn_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_o,
-                    const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ O,
-                    float* __restrict__ lse_out) {
-  constexpr int PER = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = blockIdx.x * 8LL + warp;     // (b*N + i)*Hq + h
-  const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
-  if (row >= rows) return;
-  const int h = static_cast<int>(row % s.Hq);
-  const int64_t bi = row / s.Hq;
-  const int i = static_cast<int>(bi % s.N), b = static_cast<int>(bi / s.N);
-  const int kv = h / s.G;
-  const int32_t* id = idx + ((static_cast<int64_t>(b) * s.Hkv + kv) * s.N + i) * s.K;
-  const float* pl = part_lse + row * s.K;
-  float m = neg_inf();
-  for (int q = 0; q < s.K; ++q)
-    if (id[q] >= 0) m = fmaxf(m, pl[q]);
-  float den = 0.f;
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int q = 0; q < s.K; ++q) {
-    if (id[q] < 0) continue;
-    const float w = expf(pl[q] - m);
-    den += w;
-    const __nv_bfloat16* src = part_o + (row * s.K + q) * D + lane * PER;
-    if (PER == 4) {
-      const uint2 v = *reinterpret_cast<const uint2*>(src);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-      for (int u = 0; u < PER; ++u) acc[u] += w * __bfloat162float(e[u]);
-    } else {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-      for (int u = 0; u < PER; ++u) acc[u] += w * __bfloat162float(e[u]);
-    }
-  }
-  const float r = 1.f / den;
-  __nv_bfloat16* dst = O + row * D + lane * PER;
-#pragma unroll
-  for (int u = 0; u < PER; u += 2)
-    *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
-  if (lane == 0) lse_out[(static_cast<int64_t>(b) * s.Hq + h) * s.N + i] = m + logf(den);
 }
 
 template <int D, int G>
-void fwd_launch(const Dims& s, const void* Q, const void* K, const void* V, const int32_t* off,
-                const int32_t* list, __nv_bfloat16* po, float* pl, cudaStream_t st) {
-  ProfScope ps(st, "attn_fwd_partial");
-  attn_fwd_partial_kernel<D, G><<<dim3(s.n0, s.Hkv, s.B), kWarps * 32, 0, st>>>(
-      s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
-      static_cast<const __nv_bfloat16*>(V), off, list, po, pl);
+void fwd_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+                __nv_bfloat16* po, float* pl, int32_t* counter, void* O, float* lse, cudaStream_t st) {
+  ProfScope ps(st, "attn_fwd");
+  attn_fwd_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, 0, st>>>(
+      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+      static_cast<const __nv_bfloat16*>(V), idx, list, items, n_items, po, pl, counter,
+      static_cast<__nv_bfloat16*>(O), lse);
 }
 
 template <int D>
-void fwd_dispatch(const Dims& s, const void* Q, const void* K, const void* V, const int32_t* off,
-                  const int32_t* list, __nv_bfloat16* po, float* pl, cudaStream_t st) {
+void fwd_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                  const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+                  __nv_bfloat16* po, float* pl, int32_t* counter, void* O, float* lse, cudaStream_t st) {
   switch (s.G) {
-    case 1: fwd_launch<D, 1>(s, Q, K, V, off, list, po, pl, st); break;
-    case 2: fwd_launch<D, 2>(s, Q, K, V, off, list, po, pl, st); break;
-    case 4: fwd_launch<D, 4>(s, Q, K, V, off, list, po, pl, st); break;
-    default: fwd_launch<D, 8>(s, Q, K, V, off, list, po, pl, st); break;
+    case 1: fwd_launch<D, 1>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st); break;
+    case 2: fwd_launch<D, 2>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st); break;
+    case 4: fwd_launch<D, 4>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st); break;
+    default: fwd_launch<D, 8>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st); break;
   }
+}
+
+// Query chunk so that one chunk's block partials take about 64 MiB (they live in L2 until
+// merged); about 1024 (query, head) rows per work item.
+GroupPlan fwd_plan(const Dims& s) {
+  const int64_t per_query = static_cast<int64_t>(s.G) * s.K * s.d * 2;
+  return make_group_plan(s, s.K, (int64_t(64) << 20) / per_query, 1024 / s.G);
 }
 
 }  // namespace
 
 AttnFwdWs attn_fwd_ws(const Dims& s) {
   AttnFwdWs w{};
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
+  const GroupPlan gp = fwd_plan(s);
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
-  const size_t bins = static_cast<size_t>(s.B) * s.Hkv * s.n0;
-  size_t o = 0;
-  w.counts = o;   o += align256((bins + 1) * 4);
-  w.cursor = o;   o += align256((bins + 1) * 4);
-  w.list = o;     o += align256(units * s.K * 4);
+  const GroupWs g = group_ws(gp, 0);
+  size_t o = g.end;
   w.part_o = o;   o += align256(rows * s.K * s.d * 2);
   w.part_lse = o; o += align256(rows * s.K * 4);
+  w.counter = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * s.N * 4);
   w.total = o;
   return w;
 }
@@ -251,23 +288,20 @@ int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
                     const int32_t* idx, void* O, float* lse, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnFwdWs w = attn_fwd_ws(s);
-  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
-  int32_t* cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
-  int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+  const GroupPlan gp = fwd_plan(s);
+  const GroupWs g = group_ws(gp, 0);
+  int err = launch_group_items(gp, idx, ws, g, st);
+  if (err) return err;
+  int32_t* counter = reinterpret_cast<int32_t*>(ws + w.counter);
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t) * s.B * s.Hkv * s.N, st);
+  if (e != cudaSuccess) return e;
+  const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
+  const int4* items = reinterpret_cast<const int4*>(ws + g.items);
+  const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
   __nv_bfloat16* po = reinterpret_cast<__nv_bfloat16*>(ws + w.part_o);
   float* pl = reinterpret_cast<float*>(ws + w.part_lse);
-  int err = launch_group(s, idx, s.K, counts, cursor, list, st);
-  if (err) return err;
-  if (s.d == 128) fwd_dispatch<128>(s, Q, K, V, counts, list, po, pl, st);
-  else fwd_dispatch<64>(s, Q, K, V, counts, list, po, pl, st);
-  if ((err = cudaGetLastError())) return err;
-  const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
-  const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-  ProfScope ps(st, "attn_combine");
-  if (s.d == 128)
-    attn_combine_kernel<128><<<blocks, 256, 0, st>>>(s, idx, po, pl, static_cast<__nv_bfloat16*>(O), lse);
-  else
-    attn_combine_kernel<64><<<blocks, 256, 0, st>>>(s, idx, po, pl, static_cast<__nv_bfloat16*>(O), lse);
+  if (s.d == 128) fwd_dispatch<128>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st);
+  else fwd_dispatch<64>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, O, lse, st);
   return cudaGetLastError();
 }
 

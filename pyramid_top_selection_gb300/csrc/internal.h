@@ -43,10 +43,10 @@ struct Dims {
 
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.
 struct SelectWs {
-  size_t split, cand, cscore, counts, cursor, list, total;
+  size_t split, cand, cscore, group, total;
 };
 struct AttnFwdWs {
-  size_t counts, cursor, list, part_o, part_lse, total;
+  size_t part_o, part_lse, counter, total;
 };
 struct AttnBwdWs {
   size_t counts, cursor, list, delta, part_dq, total;

@@ -17,11 +17,13 @@
 //   The node that contains i is causal-partial: its dot is q . (sum of keys j <= i in it),
 //   built bottom-up from the query's own-leaf prefix and the full left siblings on the
 //   ancestor path. Output: <= 2K leaf candidates per query.
-// Grouping: counting sort of (leaf, query) pairs into per-leaf lists.
-// Stage 2 (leaf_score_kernel): one CTA per leaf block; its 64 keys sit in shared memory
-//   and every query that has the leaf as a candidate is scored against them with MMAs.
+// Grouping: counting sort of (leaf, query) pairs into (KV head, query chunk, leaf) bins,
+//   cut into work items (group.cu).
+// Stage 2 (leaf_score_kernel): one CTA per work item; the leaf's 64 keys sit in shared
+//   memory and every query of the item is scored against them with MMAs.
 // Finish (topk_kernel): top K of the <= 2K exact leaf scores, output ascending.
 #include "device.cuh"
+#include "group.h"
 #include "profile.h"
 
 namespace pisa {
@@ -355,16 +357,18 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ cand, int64_t t
 // 8-byte fragment loads); rows = (list entry, head), 16 per MMA tile.
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32)
-leaf_score_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
-                  const int32_t* __restrict__ off, const int32_t* __restrict__ list, int W,
+leaf_score_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
+                  const __nv_bfloat16* __restrict__ K, const int32_t* __restrict__ list,
+                  const int4* __restrict__ items, const int32_t* __restrict__ n_items, int W,
                   float* __restrict__ pair_score) {
   constexpr int KS = D / 16, KROW = D + 16, QPT = 16 / G;
   __shared__ __align__(16) __nv_bfloat16 sK[64 * KROW];
-  const int t = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
-  const int64_t bin = head * s.n0 + t;
-  const int beg = off[bin], end = off[bin + 1];
-  if (beg == end) return;
+  if (static_cast<int>(blockIdx.x) >= *n_items) return;
+  const int4 item = items[blockIdx.x];
+  const int beg = item.y;
+  const int t = gp.leaf_of(item.x);
+  const int64_t head = gp.head_of(item.x);
+  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
   for (int it = threadIdx.x; it < 64 * (D / 8); it += blockDim.x) {
     const int r = it / (D / 8), c = it % (D / 8);
     const int64_t j = static_cast<int64_t>(t) * 64 + r;
@@ -375,7 +379,7 @@ leaf_score_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
-  const int n_ent = end - beg;
+  const int n_ent = item.z;
   const int n_mt = (n_ent + QPT - 1) / QPT;
   const int kbase = t * 64;
   for (int mt = warp; mt < n_mt; mt += kWarps) {
@@ -679,23 +683,30 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
 }
 
 template <int D, int G>
-void leaf_launch(const Dims& s, dim3 grid, const void* Q, const void* K, const int32_t* off,
-                 const int32_t* list, int W, float* pair_score, cudaStream_t st) {
+void leaf_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                 const int4* items, const int32_t* n_items, int W, float* pair_score, cudaStream_t st) {
   ProfScope ps(st, "leaf_score");
-  leaf_score_kernel<D, G><<<grid, kWarps * 32, 0, st>>>(
-      s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), off, list, W,
-      pair_score);
+  leaf_score_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, 0, st>>>(
+      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), list, items,
+      n_items, W, pair_score);
 }
 
 template <int D>
-void leaf_dispatch(const Dims& s, dim3 grid, const void* Q, const void* K, const int32_t* off,
-                   const int32_t* list, int W, float* pair_score, cudaStream_t st) {
+void leaf_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, cudaStream_t st) {
   switch (s.G) {
-    case 1: leaf_launch<D, 1>(s, grid, Q, K, off, list, W, pair_score, st); break;
-    case 2: leaf_launch<D, 2>(s, grid, Q, K, off, list, W, pair_score, st); break;
-    case 4: leaf_launch<D, 4>(s, grid, Q, K, off, list, W, pair_score, st); break;
-    default: leaf_launch<D, 8>(s, grid, Q, K, off, list, W, pair_score, st); break;
+    case 1: leaf_launch<D, 1>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
+    case 2: leaf_launch<D, 2>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
+    case 4: leaf_launch<D, 4>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
+    default: leaf_launch<D, 8>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
   }
+}
+
+// Stage-2 grouping: query chunks of about 16 MiB of one head's query rows; about 1024
+// (query, head) rows per work item.
+GroupPlan leaf_plan(const Dims& s) {
+  const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2;
+  return make_group_plan(s, 2 * s.K, (int64_t(16) << 20) / per_query, 1024 / s.G);
 }
 
 inline int grid_for(int64_t n, int threads) {
@@ -711,14 +722,12 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   SelectWs w{};
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   const size_t W = 2 * static_cast<size_t>(s.K);
-  const size_t bins = static_cast<size_t>(s.B) * s.Hkv * s.n0;
   size_t o = 0;
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
-  w.counts = o; o += align256((bins + 1) * 4);
-  w.cursor = o; o += align256((bins + 1) * 4);
-  w.list = o;   o += align256(units * W * 4);
+  w.group = o;
+  o = group_ws(leaf_plan(s), o).end;
   w.total = o;
   return w;
 }
@@ -768,9 +777,8 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
   int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
-  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
-  int32_t* cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
-  int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+  const GroupPlan gp = leaf_plan(s);
+  const GroupWs gw = group_ws(gp, w.group);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
@@ -785,10 +793,12 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   }
   if ((err = cudaGetLastError())) return err;
   const int W = 2 * s.K;
-  if ((err = launch_group(s, cand, W, counts, cursor, list, st))) return err;
-  dim3 lgrid(s.n0, s.Hkv, s.B);
-  if (s.d == 128) leaf_dispatch<128>(s, lgrid, Q, K, counts, list, W, cscore, st);
-  else leaf_dispatch<64>(s, lgrid, Q, K, counts, list, W, cscore, st);
+  if ((err = launch_group_items(gp, cand, ws, gw, st))) return err;
+  const int32_t* list = reinterpret_cast<const int32_t*>(ws + gw.list);
+  const int4* items = reinterpret_cast<const int4*>(ws + gw.items);
+  const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + gw.icount) + gp.bins;
+  if (s.d == 128) leaf_dispatch<128>(s, gp, Q, K, list, items, n_items, W, cscore, st);
+  else leaf_dispatch<64>(s, gp, Q, K, list, items, n_items, W, cscore, st);
   if ((err = cudaGetLastError())) return err;
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
