@@ -7,7 +7,8 @@ head. One step = pyramid build + pyramid Top-K selection + causal block-sparse a
 forward over the selection, on inputs already resident in HBM; tokens/s = B*N / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill_64k|prefill_4k|sweep|decode|train] [--sweep-n 4096,...]
+                  [--workload prefill_64k|prefill_32k|prefill_4k|sweep|decode|train]
+                  [--sweep-n 4096,...]
 
 Under torchrun each rank runs the same workload on its own GPU (independent problems, no
 collective on the data path: weak scaling); the timed region is bracketed by barriers and
@@ -40,6 +41,7 @@ import pisa_synth as syn  # noqa: E402
 WORKLOADS = {
     "prefill_64k": dict(B=1, N=65536, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "prefill_4k": dict(B=1, N=4096, Hq=4, Hkv=1, d=64, C=64, K=8, g=2, qtile=1, needles=False),
+    "prefill_32k": dict(B=1, N=32768, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "sweep": dict(B=1, N=65536, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "train": dict(B=4, N=16384, Hq=16, Hkv=4, d=128, C=64, K=16, g=2, qtile=4, needles=False),
     "decode": dict(B=32, N=131072, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=1, needles=False),
@@ -193,7 +195,7 @@ def algorithmic(kernel, cfg, idx_host=None):
         units = B * Hkv * cands
         per = G * C * 2 * d
         return "tensor", units * per, "flops", units, per
-    if kernel in ("attn_fwd", "attn_fwd_partial") and idx_host is not None:
+    if kernel in ("attn_fwd", "attn_fwd_tc", "attn_fwd_partial") and idx_host is not None:
         keys = selected_keys(idx_host, C, N)
         units = keys * G
         per = 4 * d

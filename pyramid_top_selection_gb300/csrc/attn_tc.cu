@@ -1,0 +1,368 @@
+// Causal block-sparse attention forward on the fifth-generation tensor cores (tcgen05).
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference value
+// of the work": queries that use the same leaf key block are grouped into tiles so the
+// block's keys are read once per tile, and attention runs only over the selected blocks.
+// One CTA takes one work item (a leaf block of one KV head and up to 2048 (query, head)
+// rows that selected it) in tiles of 128 rows:
+//   * the item's pair list is staged in shared memory; the leaf's K (64 x d) and V^T
+//     (d x 64) are staged once in the K-major 128-byte-swizzled layout;
+//   * the next tile's 128 query rows are gathered with cp.async into the other half of a
+//     double-buffered Q tile while the current tile computes;
+//   * S = Q K^T (M=128, N=64) and O = P V (M=128, N=d) run as tcgen05.mma issued by one
+//     thread, accumulating in TMEM; completion is tracked with mbarriers;
+//   * each thread owns one row: it reads its S row from TMEM, applies the causal mask and
+//     the block softmax, writes P (bf16) into the first K-block of the current Q buffer
+//     (Q is no longer needed once S is done), then reads its O row, normalises it and
+//     stores the (row, block) partial and the block LSE;
+//   * at the end of the item every query of the item counts this block with one atomic;
+//     the item that completes a query merges its partials (lse = log sum_t exp(lse_t),
+//     o = sum_t exp(lse_t - lse) o_t), one warp per query, and then drops the merged
+//     partials' lines from L2 so they are not written back.
+// Every mbarrier wait is bounded: if one gives up, the kernel records PISA_ETIMEOUT in the
+// status word, lets its outstanding copies finish, frees its TMEM and returns.
+#include "device.cuh"
+#include "group.h"
+#include "profile.h"
+#include "tc.cuh"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kMaxItem = 1024;       // entries per work item (queries)
+
+__device__ __forceinline__ void discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+template <int D>
+struct TcFwdSmem {
+  static constexpr int KB = D / 64;                 // K-blocks along the head dim
+  static constexpr int Q_BYTES = KB * kRows * 128;  // one Q tile
+  static constexpr int K_BYTES = KB * 64 * 128;
+  static constexpr int V_BYTES = D * 128;           // V^T: D rows of 64 keys
+  static constexpr int oQ0 = 0, oK = 2 * Q_BYTES, oV = oK + K_BYTES;
+  static constexpr int bytes = oV + V_BYTES + 1024; // + alignment slack
+  static constexpr int tmem_cols = (64 + D) <= 128 ? 128 : 256;
+};
+
+// Merge the nsel block partials of query i (its G rows) with one warp: lanes split the
+// rows and, within a row, the head dimension, so every lane keeps its loads in flight.
+template <int D, int G>
+__device__ __forceinline__ void merge_query(const Dims& s, int b, int kv, int i, int nsel,
+                                            __nv_bfloat16* part_o, const float* part_lse,
+                                            __nv_bfloat16* O, float* lse_out, int lane) {
+  constexpr int LPR = 32 / G;          // lanes per row
+  constexpr int DPL = D / LPR;         // dims per lane (>= 2)
+  constexpr int U = DPL >= 8 ? 8 : (DPL >= 4 ? 4 : 2);
+  const int h = lane / LPR, sub = lane % LPR;
+  const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
+  const float* pl = part_lse + row * s.K;
+  float lv[32];
+  float m = neg_inf();
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    lv[q] = q < nsel ? __ldcg(pl + q) : neg_inf();
+    m = fmaxf(m, lv[q]);
+  }
+  float den = 0.f;
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    lv[q] = (q < nsel && m != neg_inf()) ? expf(lv[q] - m) : 0.f;
+    den += lv[q];
+  }
+  const float r = den > 0.f ? 1.f / den : 0.f;
+  const __nv_bfloat16* src = part_o + row * s.K * D + sub * DPL;
+#pragma unroll
+  for (int c = 0; c < DPL; c += U) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      if (q < nsel) {
+        const __nv_bfloat16* p = src + q * D + c;
+        if constexpr (U == 8) {
+          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        } else if constexpr (U == 4) {
+          const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        } else {
+          const unsigned int v = __ldcg(reinterpret_cast<const unsigned int*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        }
+      }
+    }
+    __nv_bfloat16* dst = O + row * D + sub * DPL + c;
+#pragma unroll
+    for (int u = 0; u < U; u += 2)
+      *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
+  }
+  if (sub == 0)
+    lse_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
+  __syncwarp();
+  // the merged partials (whole 128-byte lines of these rows only) are dead: drop them from L2
+  const char* base = reinterpret_cast<const char*>(part_o + row * s.K * D);
+  if ((reinterpret_cast<uintptr_t>(base) & 127) == 0) {
+    const int lines = nsel * D * 2 / 128;
+    for (int k = sub; k < lines; k += LPR) discard_line(base + k * 128);
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kRows, 1)
+attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
+                   const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
+                   const int32_t* __restrict__ list, const int4* __restrict__ items,
+                   const int32_t* __restrict__ n_items, __nv_bfloat16* part_o, float* part_lse,
+                   int32_t* __restrict__ counter, const int32_t* __restrict__ nsel_of,
+                   __nv_bfloat16* __restrict__ O, float* __restrict__ lse_out, int32_t* status) {
+  using L = TcFwdSmem<D>;
+  constexpr int EPT = kRows / G;          // entries (queries) per tile
+  constexpr int CH = D / 8;               // 16-byte chunks per row
+  extern __shared__ unsigned char smraw[];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_list[kMaxItem];        // the item's (query << 6 | slot) entries
+  __shared__ int s_merge[kMaxItem];       // queries whose last block is this item's
+  __shared__ int s_nmerge, s_abort;
+
+  if (static_cast<int>(blockIdx.x) >= *n_items) return;
+  const int4 item = items[blockIdx.x];
+  const int beg = item.y, n_ent = item.z;
+  const int t = gp.leaf_of(item.x);
+  const int64_t head = gp.head_of(item.x);
+  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Ksel = s.K;
+  const int kbase = t * 64;
+  const int n_tiles = (n_ent + EPT - 1) / EPT;
+
+  unsigned char* sm = smraw + ((1024 - (tc::su32(smraw) & 1023)) & 1023);
+  const uint32_t aQ0 = tc::su32(sm + L::oQ0);     // Q buffer `buf` starts at aQ0 + buf * Q_BYTES
+  const uint32_t aK = tc::su32(sm + L::oK), aV = tc::su32(sm + L::oV);
+  constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
+
+  if (tid == 0) {
+    tc::bar_init(&bar[0], 1);
+    tc::bar_init(&bar[1], 1);
+    tc::fence_bar_init();
+    s_abort = 0;
+    s_nmerge = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, L::tmem_cols);
+  for (int e = tid; e < n_ent; e += kRows) s_list[e] = list[beg + e];
+  // entry e of tile j: query s_list[j*EPT + e] >> 6, slot & 63 (query -1 past the end)
+  auto entry_query = [&](int j, int e) {
+    const int ge = j * EPT + e;
+    return ge < n_ent ? (s_list[ge] >> 6) : -1;
+  };
+  auto gather_q = [&](int j, int buf) {
+    const uint32_t dstb = aQ0 + buf * L::Q_BYTES;
+    for (int lin = tid; lin < kRows * CH; lin += kRows) {
+      const int r = lin / CH, c = lin % CH;
+      const int i = entry_query(j, r / G);
+      const __nv_bfloat16* src =
+          Q + ((static_cast<int64_t>(b) * s.N + (i < 0 ? 0 : i)) * s.Hq + kv * G + (r % G)) * D + c * 8;
+      tc::cp_async16(dstb + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8), src, i >= 0);
+    }
+  };
+  __syncthreads();
+  gather_q(0, 0);
+  // leaf K tile (async) and V^T, transposed by the threads (lanes walk keys: no bank conflicts)
+  for (int lin = tid; lin < 64 * CH; lin += kRows) {
+    const int r = lin / CH, c = lin % CH;
+    const int64_t j = static_cast<int64_t>(kbase) + r;
+    const bool ok = j < s.N;
+    const __nv_bfloat16* src = K + ((static_cast<int64_t>(b) * s.N + (ok ? j : 0)) * s.Hkv + kv) * D + c * 8;
+    tc::cp_async16(aK + (c >> 3) * (64 * 128) + tc::sw128(r, (c & 7) * 8), src, ok);
+  }
+  tc::cp_async_commit();
+  for (int lin = tid; lin < 64 * CH; lin += kRows) {
+    const int r = lin % 64, c = lin / 64;   // key r, dims c*8 .. c*8+7
+    const int64_t j = static_cast<int64_t>(kbase) + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j < s.N) v = ldg_u4(V + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8);
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<__nv_bfloat16*>(sm + L::oV + tc::sw128(c * 8 + u, r)) = e[u];
+  }
+  tc::before_sync();
+  __syncthreads();
+  tc::after_sync();
+  const uint32_t tS = tmem_base, tO = tmem_base + 64;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+
+  for (int jt = 0; jt < n_tiles; ++jt) {
+    const int buf = jt & 1;
+    const uint32_t aQb = aQ0 + buf * L::Q_BYTES;
+    // prefetch the next tile's rows into the other buffer (its last reader, the previous
+    // tile's P V MMA, has completed)
+    if (jt + 1 < n_tiles) gather_q(jt + 1, buf ^ 1);
+    tc::cp_async_commit();
+    tc::cp_async_wait<1>();              // this tile's rows (and the K tile) have landed
+    tc::fence_async_smem();
+    tc::before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::after_sync();
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        tc::mma(tS, tc::desc(aQb + (ks >> 2) * (kRows * 128) + (ks & 3) * 32),
+                tc::desc(aK + (ks >> 2) * (64 * 128) + (ks & 3) * 32), idS, ks > 0);
+      tc::commit(&bar[0]);
+    }
+    if (!tc::bar_wait(&bar[0], jt & 1)) atomicOr(&s_abort, 1);
+    tc::after_sync();
+    // softmax of this thread's row; P goes into the (now free) first K-block of Q[buf]
+    const int r = tid, e = r / G, h = r % G;
+    const int qi = entry_query(jt, e);
+    float m, l = 0.f;
+    {
+      float sv[64];
+      tc::tmem_ld64(tS + lane_off, sv);
+      float mx = neg_inf();
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        sv[c] = (kbase + c <= qi) ? s.scale * sv[c] : neg_inf();
+        mx = fmaxf(mx, sv[c]);
+      }
+      m = mx == neg_inf() ? 0.f : mx;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        sv[c] = expf(sv[c] - m);
+        l += sv[c];
+      }
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4 pk;
+        pk.x = pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]);
+        pk.y = pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]);
+        pk.z = pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]);
+        pk.w = pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]);
+        *reinterpret_cast<uint4*>(sm + L::oQ0 + buf * L::Q_BYTES + tc::sw128(r, cc * 8)) = pk;
+      }
+    }
+    tc::fence_async_smem();
+    tc::before_sync();
+    __syncthreads();
+    if (s_abort) break;
+    if (tid == 0) {
+      tc::after_sync();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma(tO, tc::desc(aQb + kk * 32), tc::desc(aV + kk * 32), idO, kk > 0);
+      tc::commit(&bar[1]);
+    }
+    if (!tc::bar_wait(&bar[1], jt & 1)) atomicOr(&s_abort, 1);
+    tc::after_sync();
+    // epilogue: this thread's normalised partial row and its block LSE
+    const int64_t row = (static_cast<int64_t>(b) * s.N + (qi < 0 ? 0 : qi)) * s.Hq + kv * G + h;
+    const int slot = qi >= 0 ? (s_list[jt * EPT + e] & 63) : 0;
+    const float rl = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* dst = part_o + (row * Ksel + slot) * D;
+#pragma unroll
+    for (int half = 0; half < D / 64; ++half) {
+      float ov[64];
+      tc::tmem_ld64(tO + lane_off + half * 64, ov);
+      if (qi >= 0) {
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 pk;
+          pk.x = pack_bf16(ov[cc * 8 + 0] * rl, ov[cc * 8 + 1] * rl);
+          pk.y = pack_bf16(ov[cc * 8 + 2] * rl, ov[cc * 8 + 3] * rl);
+          pk.z = pack_bf16(ov[cc * 8 + 4] * rl, ov[cc * 8 + 5] * rl);
+          pk.w = pack_bf16(ov[cc * 8 + 6] * rl, ov[cc * 8 + 7] * rl);
+          *reinterpret_cast<uint4*>(dst + half * 64 + cc * 8) = pk;
+        }
+      }
+    }
+    if (qi >= 0) part_lse[row * Ksel + slot] = l > 0.f ? m + logf(l) : neg_inf();
+    tc::before_sync();
+    __syncthreads();
+    if (s_abort) break;
+  }
+  if (!s_abort) {
+    // arrival, once per item: every query of the item counts this block; the last one merges
+    __threadfence();
+    __syncthreads();
+    for (int e = tid; e < n_ent; e += kRows) {
+      const int qi = s_list[e] >> 6;
+      const int64_t unit = head * s.N + qi;
+      if (atomicAdd(&counter[unit], 1) == nsel_of[unit] - 1) s_merge[atomicAdd(&s_nmerge, 1)] = qi;
+    }
+    __syncthreads();
+    if (s_nmerge > 0) {
+      __threadfence();
+      for (int k = warp; k < s_nmerge; k += kRows / 32) {
+        const int qi = s_merge[k];
+        merge_query<D, G>(s, b, kv, qi, nsel_of[head * s.N + qi], part_o, part_lse, O, lse_out, lane);
+      }
+    }
+  }
+  tc::cp_async_wait<0>();
+  tc::before_sync();
+  __syncthreads();
+  if (s_abort && tid == 0) atomicOr(status, PISA_ETIMEOUT);
+  if (warp == 0) tc::tmem_free(tmem_base, L::tmem_cols);
+}
+
+// nsel[unit] = number of selected leaves of (b, KV head, query) = valid entries of idx.
+__global__ void nsel_kernel(int64_t units, int K, const int32_t* __restrict__ idx, int32_t* __restrict__ nsel) {
+  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int n = 0;
+    for (int q = 0; q < K; ++q) n += idx[u * K + q] >= 0 ? 1 : 0;
+    nsel[u] = n;
+  }
+}
+
+template <int D, int G>
+int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+              const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+              __nv_bfloat16* po, float* pl, int32_t* counter, int32_t* nsel, void* O, float* lse,
+              int32_t* status, cudaStream_t st) {
+  const int smem = TcFwdSmem<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  {
+    ProfScope ps(st, "attn_nsel");
+    const int64_t blocks = units / 256 + 1;
+    nsel_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(units, s.K, idx, nsel);
+  }
+  ProfScope ps(st, "attn_fwd_tc");
+  attn_fwd_tc_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kRows, smem, st>>>(
+      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+      static_cast<const __nv_bfloat16*>(V), list, items, n_items, po, pl, counter, nsel,
+      static_cast<__nv_bfloat16*>(O), lse, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Tensor-core forward for d in {64, 128} and G in {1, 2, 4, 8}.
+int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                       const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+                       __nv_bfloat16* po, float* pl, int32_t* counter, int32_t* nsel, void* O, float* lse,
+                       int32_t* status, cudaStream_t st) {
+#define PISA_TC_CASE(DD, GG)                                                                          \
+  if (s.d == DD && s.G == GG)                                                                         \
+    return tc_launch<DD, GG>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, nsel, O, lse, status, st);
+  PISA_TC_CASE(128, 1) PISA_TC_CASE(128, 2) PISA_TC_CASE(128, 4) PISA_TC_CASE(128, 8)
+  PISA_TC_CASE(64, 1) PISA_TC_CASE(64, 2) PISA_TC_CASE(64, 4) PISA_TC_CASE(64, 8)
+#undef PISA_TC_CASE
+  return static_cast<int>(cudaErrorNotSupported);
+}
+
+}  // namespace pisa
