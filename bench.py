@@ -467,6 +467,146 @@ def run_sweep(args, cfg, local):
         torch.cuda.empty_cache()
 
 
+# ------------------------------------------------------------------ decode and training
+def profile_kernels(pisa, step, steps, flush=None):
+    """Per-kernel CUDA-event times over `steps` calls of `step` (events on the launch stream)."""
+    pisa.profile_start()
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    pisa.profile_stop()
+    prof = pisa.profile_read()
+    tot = sum(v[1] for v in prof.values()) or 1.0
+    kernels = {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / tot} for k, v in prof.items()}
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    return kernels, dom, sum(v[0] for v in prof.values())
+
+
+def roofline_entry(kernel, bound, amount, unit_kind, avg_ms, units, per):
+    pk, psrc = peaks()
+    sec = avg_ms / 1e3
+    if unit_kind == "bytes":
+        achieved, peak, u = amount / sec / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, u = amount / sec / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": u,
+            "frac": achieved / peak, "peak_source": psrc, "traffic": traffic_for(kernel, units),
+            "units_per_launch": units, "per_unit": per, "per_unit_kind": unit_kind}
+
+
+def run_decode(args, cfg, rank, world, local):
+    """Autoregressive decode: a batch of sequences with a long cache, one fused step per token."""
+    import pyramid_top_selection_gb300 as pisa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, L0, Hq, Hkv, d, C, K = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K"))
+    total = 256                                      # steps the cache has room for
+    Ncap = L0 + total
+    steps = max(1, min(args.steps, total - args.warmup - 8))
+    Kc = syn.randn_bf16((B, Ncap, Hkv, d), 1, dev)
+    Vc = syn.randn_bf16((B, Ncap, Hkv, d), 2, dev)
+    qs, ks, vs = syn.make_decode_stream(B, total, Hq, Hkv, d, seed=0, device=dev)
+    shape = pisa.make_decode_shape(B, Ncap, Hq, Hkv, d, C, K)
+    length = torch.full((B,), L0, dtype=torch.int32, device=dev)
+    pyr = pisa.decode_build_pyramid(Kc, length, shape)
+    pos = (L0 + torch.arange(total, device=dev, dtype=torch.int32)).view(total, 1).repeat(1, B).contiguous()
+    o = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(B, Hkv, K, dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    cur = [0]
+
+    def step():
+        t = cur[0]
+        pisa.decode_step(shape, pos[t], Kc, Vc, pyr, qs[t], ks[t], vs[t], o=o, idx=idx, status=status)
+        cur[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b_) / steps
+    prof_steps = min(8, total - cur[0])
+    kernels, dom, launches = profile_kernels(pisa, step, prof_steps)
+    assert int(status.sum()) == 0
+    sizes = [-(-Ncap // C)]
+    while sizes[-1] > 1:
+        sizes.append(-(-sizes[-1] // 2))
+    lv = sum(1 for l in range(1, len(sizes) - 1) if sizes[l] > K)
+    per = (2 * K * C * d * 2 + K * C * d * 2 + lv * 2 * K * 2 * d * 4 + C * d * 2 + len(sizes) * 3 * d * 4)
+    units = B * Hkv
+    roof = roofline_entry("decode_step", "hbm", units * per, "bytes", kernels["decode_step"]["avg_ms"], units, per)
+    if rank == 0:
+        line = {"workload": "decode", "metric": "decode tokens/s (one fused kernel per step)",
+                "value": B * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                "config": {"B": B, "cache_tokens": L0, "Ncap": Ncap, "Hq": Hq, "Hkv": Hkv, "d": d, "C": C, "K": K,
+                           "l2": "working set per step larger than L2 (no flush)"},
+                "gpu_launches": steps, "kernels": kernels, "roofline": roof}
+        if clk.summary() is not None:
+            line["clocks"] = clk.summary()
+        print(json.dumps(line), flush=True)
+
+
+def run_train(args, cfg, rank, world, local):
+    """Training step: pyramid + selection (no gradient) + sparse attention forward and backward."""
+    import pyramid_top_selection_gb300 as pisa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, N, Hq, Hkv, d, C, K, g, qtile = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile"))
+    Q, Kt, V = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0, needles=cfg["needles"], device=dev)
+    dO = syn.make_grad_out(B, N, Hq, d, seed=0, device=dev)
+    shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, g, qtile)
+    _, _, nodes = pisa.pyramid_layout(shape)
+    pyr = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=dev)
+    idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    ws_sel, ws_f, ws_b = (pisa.workspace(shape, op, dev) for op in (0, 2, 3))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        pisa.build_pyramid(Kt, shape, out=pyr)
+        pisa.select(Q, Kt, pyr, shape, ws=ws_sel, want_score=False, idx=idx)
+        pisa.sparse_attn_fwd(Q, Kt, V, idx, shape, ws=ws_f, out=O, lse=lse)
+        pisa.sparse_attn_bwd(Q, Kt, V, O, lse, dO, idx, shape, ws=ws_b)
+
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    kernels, dom, launches = profile_kernels(pisa, step, args.steps, flush)
+    keys = selected_keys(idx.cpu(), C, N)
+    units = keys * (Hq // Hkv)
+    roof = roofline_entry("attn_bwd", "tensor", units * 10 * d, "flops", kernels["attn_bwd"]["avg_ms"], units, 10 * d)
+    if rank == 0:
+        line = {"workload": "train", "metric": "training tokens/s (select + sparse attention fwd + bwd)",
+                "value": B * N * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                "config": {k: cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
+                "gpu_launches": int(round(launches)), "kernels": kernels, "dominant": dom, "roofline": roof}
+        if clk.summary() is not None:
+            line["clocks"] = clk.summary()
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -480,7 +620,12 @@ def main():
         if rank == 0:
             run_sweep(args, cfg, local)
         return
-    run_ours(args, cfg, rank, world, local)
+    if args.workload == "decode":
+        run_decode(args, cfg, rank, world, local)
+    elif args.workload == "train":
+        run_train(args, cfg, rank, world, local)
+    else:
+        run_ours(args, cfg, rank, world, local)
     if world > 1:
         torch.distributed.destroy_process_group()
 
