@@ -9,11 +9,8 @@
 // Forward, block-major: the selected (leaf, query) pairs are grouped by (KV head, query
 // chunk, leaf) and cut into work items (group.cu); the tensor-core kernel (attn_tc.cu)
 // takes one item per CTA. Each (row, block) yields a normalised partial output and its
-// block LSE. Every query counts its finished blocks with one atomic; the block that
-// finishes a query's last leaf merges that query's <= K partials right away, while they
-// are still in L2: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t, then
-// discards the merged partials' L2 lines (they are dead) so they are never written back
-// to HBM. Nothing waits on anything: the counter only decides who merges.
+// block LSE; a combine kernel then merges the <= K partials of every row:
+// lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -22,13 +19,12 @@ namespace pisa {
 
 int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
-                       __nv_bfloat16* po, float* pl, int32_t* counter, int32_t* nsel, void* O, float* lse,
-                       int32_t* status, cudaStream_t st);
+                       __nv_bfloat16* po, float* pl, void* O, float* lse, int32_t* status, cudaStream_t st);
 
 namespace {
 
-// Query chunk so that one chunk's block partials take about 64 MiB (merged while the chunk
-// is being processed); about 2048 (query, head) rows (at most 1024 queries) per work item.
+// Query chunk so that one chunk's query rows stay in L2 while its leaves are swept; about
+// 2048 (query, head) rows (at most 1024 queries) per work item.
 GroupPlan fwd_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.K * s.d * 2;
   const int cap = (2048 / s.G) < 1024 ? 2048 / s.G : 1024;
@@ -41,12 +37,9 @@ AttnFwdWs attn_fwd_ws(const Dims& s) {
   AttnFwdWs w{};
   const GroupPlan gp = fwd_plan(s);
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   size_t o = group_ws(gp, 0).end;
   w.part_o = o;   o += align256(rows * s.K * s.d * 2);
   w.part_lse = o; o += align256(rows * s.K * 4);
-  w.counter = o;  o += align256(units * 4);
-  w.nsel = o;     o += align256(units * 4);
   w.status = o;   o += 256;
   w.total = o;
   return w;
@@ -60,17 +53,14 @@ int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
   const GroupWs g = group_ws(gp, 0);
   int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;
-  int32_t* counter = reinterpret_cast<int32_t*>(ws + w.counter);
-  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t) * s.B * s.Hkv * s.N, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws + w.status, 0, 256, st);
+  cudaError_t e = cudaMemsetAsync(ws + w.status, 0, 256, st);
   if (e != cudaSuccess) return e;
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
   const int4* items = reinterpret_cast<const int4*>(ws + g.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
   return launch_attn_fwd_tc(s, gp, Q, K, V, idx, list, items, n_items,
                             reinterpret_cast<__nv_bfloat16*>(ws + w.part_o),
-                            reinterpret_cast<float*>(ws + w.part_lse), counter,
-                            reinterpret_cast<int32_t*>(ws + w.nsel), O, lse,
+                            reinterpret_cast<float*>(ws + w.part_lse), O, lse,
                             reinterpret_cast<int32_t*>(ws + w.status), st);
 }
 

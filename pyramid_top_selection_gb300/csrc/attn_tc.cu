@@ -15,10 +15,8 @@
 //     the block softmax, writes P (bf16) into the first K-block of the current Q buffer
 //     (Q is no longer needed once S is done), then reads its O row, normalises it and
 //     stores the (row, block) partial and the block LSE;
-//   * at the end of the item every query of the item counts this block with one atomic;
-//     the item that completes a query merges its partials (lse = log sum_t exp(lse_t),
-//     o = sum_t exp(lse_t - lse) o_t), one warp per query, and then drops the merged
-//     partials' lines from L2 so they are not written back.
+//   * a second kernel merges every query's block partials, one warp per query with all of
+//     its rows and slots in flight: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
 // Every mbarrier wait is bounded: if one gives up, the kernel records PISA_ETIMEOUT in the
 // status word, lets its outstanding copies finish, frees its TMEM and returns.
 #include "device.cuh"
@@ -33,10 +31,6 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kMaxItem = 1024;       // entries per work item (queries)
 
-__device__ __forceinline__ void discard_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 template <int D>
 struct TcFwdSmem {
   static constexpr int KB = D / 64;                 // K-blocks along the head dim
@@ -48,84 +42,13 @@ struct TcFwdSmem {
   static constexpr int tmem_cols = (64 + D) <= 128 ? 128 : 256;
 };
 
-// Merge the nsel block partials of query i (its G rows) with one warp: lanes split the
-// rows and, within a row, the head dimension, so every lane keeps its loads in flight.
-template <int D, int G>
-__device__ __forceinline__ void merge_query(const Dims& s, int b, int kv, int i, int nsel,
-                                            __nv_bfloat16* part_o, const float* part_lse,
-                                            __nv_bfloat16* O, float* lse_out, int lane) {
-  constexpr int LPR = 32 / G;          // lanes per row
-  constexpr int DPL = D / LPR;         // dims per lane (>= 2)
-  constexpr int U = DPL >= 8 ? 8 : (DPL >= 4 ? 4 : 2);
-  const int h = lane / LPR, sub = lane % LPR;
-  const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
-  const float* pl = part_lse + row * s.K;
-  float lv[32];
-  float m = neg_inf();
-#pragma unroll
-  for (int q = 0; q < 32; ++q) {
-    lv[q] = q < nsel ? __ldcg(pl + q) : neg_inf();
-    m = fmaxf(m, lv[q]);
-  }
-  float den = 0.f;
-#pragma unroll
-  for (int q = 0; q < 32; ++q) {
-    lv[q] = (q < nsel && m != neg_inf()) ? expf(lv[q] - m) : 0.f;
-    den += lv[q];
-  }
-  const float r = den > 0.f ? 1.f / den : 0.f;
-  const __nv_bfloat16* src = part_o + row * s.K * D + sub * DPL;
-#pragma unroll
-  for (int c = 0; c < DPL; c += U) {
-    float acc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = 0.f;
-#pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      if (q < nsel) {
-        const __nv_bfloat16* p = src + q * D + c;
-        if constexpr (U == 8) {
-          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        } else if constexpr (U == 4) {
-          const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        } else {
-          const unsigned int v = __ldcg(reinterpret_cast<const unsigned int*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        }
-      }
-    }
-    __nv_bfloat16* dst = O + row * D + sub * DPL + c;
-#pragma unroll
-    for (int u = 0; u < U; u += 2)
-      *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
-  }
-  if (sub == 0)
-    lse_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
-  __syncwarp();
-  // the merged partials (whole 128-byte lines of these rows only) are dead: drop them from L2
-  const char* base = reinterpret_cast<const char*>(part_o + row * s.K * D);
-  if ((reinterpret_cast<uintptr_t>(base) & 127) == 0) {
-    const int lines = nsel * D * 2 / 128;
-    for (int k = sub; k < lines; k += LPR) discard_line(base + k * 128);
-  }
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(kRows, 1)
 attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
                    const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                    const int32_t* __restrict__ list, const int4* __restrict__ items,
-                   const int32_t* __restrict__ n_items, __nv_bfloat16* part_o, float* part_lse,
-                   int32_t* __restrict__ counter, const int32_t* __restrict__ nsel_of,
-                   __nv_bfloat16* __restrict__ O, float* __restrict__ lse_out, int32_t* status) {
+                   const int32_t* __restrict__ n_items, __nv_bfloat16* __restrict__ part_o,
+                   float* __restrict__ part_lse, int32_t* status) {
   using L = TcFwdSmem<D>;
   constexpr int EPT = kRows / G;          // entries (queries) per tile
   constexpr int CH = D / 8;               // 16-byte chunks per row
@@ -133,8 +56,7 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_list[kMaxItem];        // the item's (query << 6 | slot) entries
-  __shared__ int s_merge[kMaxItem];       // queries whose last block is this item's
-  __shared__ int s_nmerge, s_abort;
+  __shared__ int s_abort;
 
   if (static_cast<int>(blockIdx.x) >= *n_items) return;
   const int4 item = items[blockIdx.x];
@@ -142,7 +64,7 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
   const int t = gp.leaf_of(item.x);
   const int64_t head = gp.head_of(item.x);
   const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int Ksel = s.K;
   const int kbase = t * 64;
   const int n_tiles = (n_ent + EPT - 1) / EPT;
@@ -157,7 +79,6 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
     tc::bar_init(&bar[1], 1);
     tc::fence_bar_init();
     s_abort = 0;
-    s_nmerge = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, L::tmem_cols);
   for (int e = tid; e < n_ent; e += kRows) s_list[e] = list[beg + e];
@@ -292,24 +213,6 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
     __syncthreads();
     if (s_abort) break;
   }
-  if (!s_abort) {
-    // arrival, once per item: every query of the item counts this block; the last one merges
-    __threadfence();
-    __syncthreads();
-    for (int e = tid; e < n_ent; e += kRows) {
-      const int qi = s_list[e] >> 6;
-      const int64_t unit = head * s.N + qi;
-      if (atomicAdd(&counter[unit], 1) == nsel_of[unit] - 1) s_merge[atomicAdd(&s_nmerge, 1)] = qi;
-    }
-    __syncthreads();
-    if (s_nmerge > 0) {
-      __threadfence();
-      for (int k = warp; k < s_nmerge; k += kRows / 32) {
-        const int qi = s_merge[k];
-        merge_query<D, G>(s, b, kv, qi, nsel_of[head * s.N + qi], part_o, part_lse, O, lse_out, lane);
-      }
-    }
-  }
   tc::cp_async_wait<0>();
   tc::before_sync();
   __syncthreads();
@@ -317,35 +220,105 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
   if (warp == 0) tc::tmem_free(tmem_base, L::tmem_cols);
 }
 
-// nsel[unit] = number of selected leaves of (b, KV head, query) = valid entries of idx.
-__global__ void nsel_kernel(int64_t units, int K, const int32_t* __restrict__ idx, int32_t* __restrict__ nsel) {
-  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int n = 0;
-    for (int q = 0; q < K; ++q) n += idx[u * K + q] >= 0 ? 1 : 0;
-    nsel[u] = n;
+// Merge the nsel block partials of query i (its G rows) with one warp: lanes split the
+// rows and, within a row, the head dimension, so every lane keeps its loads in flight.
+template <int D, int G>
+__device__ __forceinline__ void merge_query(const Dims& s, int b, int kv, int i, int nsel,
+                                            const __nv_bfloat16* __restrict__ part_o,
+                                            const float* __restrict__ part_lse, __nv_bfloat16* O,
+                                            float* lse_out, int lane) {
+  constexpr int LPR = 32 / G;          // lanes per row
+  constexpr int DPL = D / LPR;         // dims per lane (>= 2)
+  constexpr int U = DPL >= 8 ? 8 : (DPL >= 4 ? 4 : 2);
+  const int h = lane / LPR, sub = lane % LPR;
+  const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
+  const float* pl = part_lse + row * s.K;
+  float lv[32];
+  float m = neg_inf();
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    lv[q] = q < nsel ? __ldg(pl + q) : neg_inf();
+    m = fmaxf(m, lv[q]);
   }
+  float den = 0.f;
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    lv[q] = (q < nsel && m != neg_inf()) ? expf(lv[q] - m) : 0.f;
+    den += lv[q];
+  }
+  const float r = den > 0.f ? 1.f / den : 0.f;
+  const __nv_bfloat16* src = part_o + row * s.K * D + sub * DPL;
+#pragma unroll
+  for (int c = 0; c < DPL; c += U) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      if (q < nsel) {
+        const __nv_bfloat16* p = src + q * D + c;
+        if constexpr (U == 8) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        } else if constexpr (U == 4) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        } else {
+          const unsigned int v = __ldg(reinterpret_cast<const unsigned int*>(p));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
+        }
+      }
+    }
+    __nv_bfloat16* dst = O + row * D + sub * DPL + c;
+#pragma unroll
+    for (int u = 0; u < U; u += 2)
+      *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
+  }
+  if (sub == 0)
+    lse_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
 }
+
+// One warp per (b, KV head, query): merges the query's block partials for its G rows.
+template <int D, int G>
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_o,
+                    const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ O,
+                    float* __restrict__ lse_out) {
+  const int64_t unit = blockIdx.x * 8LL + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (unit >= static_cast<int64_t>(s.B) * s.Hkv * s.N) return;
+  const int i = static_cast<int>(unit % s.N);
+  const int64_t head = unit / s.N;
+  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
+  const bool valid = lane < s.K && idx[unit * s.K + lane] >= 0;
+  const int nsel = __popc(__ballot_sync(0xffffffffu, valid));
+  merge_query<D, G>(s, b, kv, i, nsel, part_o, part_lse, O, lse_out, lane);
+}
+
 
 template <int D, int G>
 int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
               const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
-              __nv_bfloat16* po, float* pl, int32_t* counter, int32_t* nsel, void* O, float* lse,
-              int32_t* status, cudaStream_t st) {
+              __nv_bfloat16* po, float* pl, void* O, float* lse, int32_t* status, cudaStream_t st) {
   const int smem = TcFwdSmem<D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
-    ProfScope ps(st, "attn_nsel");
-    const int64_t blocks = units / 256 + 1;
-    nsel_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(units, s.K, idx, nsel);
+    ProfScope ps(st, "attn_fwd_tc");
+    attn_fwd_tc_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kRows, smem, st>>>(
+        s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+        static_cast<const __nv_bfloat16*>(V), list, items, n_items, po, pl, status);
   }
-  ProfScope ps(st, "attn_fwd_tc");
-  attn_fwd_tc_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kRows, smem, st>>>(
-      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
-      static_cast<const __nv_bfloat16*>(V), list, items, n_items, po, pl, counter, nsel,
-      static_cast<__nv_bfloat16*>(O), lse, status);
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  ProfScope ps(st, "attn_combine");
+  attn_combine_kernel<D, G><<<static_cast<unsigned>((units + 7) / 8), 256, 0, st>>>(
+      s, idx, po, pl, static_cast<__nv_bfloat16*>(O), lse);
   return cudaGetLastError();
 }
 
@@ -354,11 +327,10 @@ int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, 
 // Tensor-core forward for d in {64, 128} and G in {1, 2, 4, 8}.
 int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
-                       __nv_bfloat16* po, float* pl, int32_t* counter, int32_t* nsel, void* O, float* lse,
-                       int32_t* status, cudaStream_t st) {
+                       __nv_bfloat16* po, float* pl, void* O, float* lse, int32_t* status, cudaStream_t st) {
 #define PISA_TC_CASE(DD, GG)                                                                          \
   if (s.d == DD && s.G == GG)                                                                         \
-    return tc_launch<DD, GG>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, counter, nsel, O, lse, status, st);
+    return tc_launch<DD, GG>(s, gp, Q, K, V, idx, list, items, n_items, po, pl, O, lse, status, st);
   PISA_TC_CASE(128, 1) PISA_TC_CASE(128, 2) PISA_TC_CASE(128, 4) PISA_TC_CASE(128, 8)
   PISA_TC_CASE(64, 1) PISA_TC_CASE(64, 2) PISA_TC_CASE(64, 4) PISA_TC_CASE(64, 8)
 #undef PISA_TC_CASE

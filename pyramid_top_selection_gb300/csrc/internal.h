@@ -46,7 +46,7 @@ struct SelectWs {
   size_t split, cand, cscore, group, total;
 };
 struct AttnFwdWs {
-  size_t part_o, part_lse, counter, nsel, status, total;
+  size_t part_o, part_lse, status, total;
 };
 struct AttnBwdWs {
   size_t counts, cursor, list, delta, part_dq, total;
