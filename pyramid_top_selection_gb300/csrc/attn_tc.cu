@@ -15,8 +15,8 @@
 //     the block softmax, writes P (bf16) into the first K-block of the current Q buffer
 //     (Q is no longer needed once S is done), then reads its O row, normalises it and
 //     stores the (row, block) partial and the block LSE;
-//   * a second kernel merges every query's block partials, one warp per query with all of
-//     its rows and slots in flight: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
+//   * a second kernel merges every row's block partials, one warp per row with all of its
+//     slots in flight: lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
 // Every mbarrier wait is bounded: if one gives up, the kernel records PISA_ETIMEOUT in the
 // status word, lets its outstanding copies finish, frees its TMEM and returns.
 #include "device.cuh"
@@ -220,87 +220,54 @@ attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
   if (warp == 0) tc::tmem_free(tmem_base, L::tmem_cols);
 }
 
-// Merge the nsel block partials of query i (its G rows) with one warp: lanes split the
-// rows and, within a row, the head dimension, so every lane keeps its loads in flight.
-template <int D, int G>
-__device__ __forceinline__ void merge_query(const Dims& s, int b, int kv, int i, int nsel,
-                                            const __nv_bfloat16* __restrict__ part_o,
-                                            const float* __restrict__ part_lse, __nv_bfloat16* O,
-                                            float* lse_out, int lane) {
-  constexpr int LPR = 32 / G;          // lanes per row
-  constexpr int DPL = D / LPR;         // dims per lane (>= 2)
-  constexpr int U = DPL >= 8 ? 8 : (DPL >= 4 ? 4 : 2);
-  const int h = lane / LPR, sub = lane % LPR;
-  const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
-  const float* pl = part_lse + row * s.K;
-  float lv[32];
-  float m = neg_inf();
-#pragma unroll
-  for (int q = 0; q < 32; ++q) {
-    lv[q] = q < nsel ? __ldg(pl + q) : neg_inf();
-    m = fmaxf(m, lv[q]);
-  }
-  float den = 0.f;
-#pragma unroll
-  for (int q = 0; q < 32; ++q) {
-    lv[q] = (q < nsel && m != neg_inf()) ? expf(lv[q] - m) : 0.f;
-    den += lv[q];
-  }
-  const float r = den > 0.f ? 1.f / den : 0.f;
-  const __nv_bfloat16* src = part_o + row * s.K * D + sub * DPL;
-#pragma unroll
-  for (int c = 0; c < DPL; c += U) {
-    float acc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = 0.f;
-#pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      if (q < nsel) {
-        const __nv_bfloat16* p = src + q * D + c;
-        if constexpr (U == 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        } else if constexpr (U == 4) {
-          const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        } else {
-          const unsigned int v = __ldg(reinterpret_cast<const unsigned int*>(p));
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) acc[u] += lv[q] * __bfloat162float(e[u]);
-        }
-      }
-    }
-    __nv_bfloat16* dst = O + row * D + sub * DPL + c;
-#pragma unroll
-    for (int u = 0; u < U; u += 2)
-      *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
-  }
-  if (sub == 0)
-    lse_out[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
-}
-
-// One warp per (b, KV head, query): merges the query's block partials for its G rows.
-template <int D, int G>
+// One warp per (b, query, head) row: merges the row's <= K block partials. Lane q < K
+// holds slot q's LSE, the weights come from warp reductions, and each lane then owns D/32
+// dimensions, with every slot's load issued before any is used.
+template <int D>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_o,
                     const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ O,
                     float* __restrict__ lse_out) {
-  const int64_t unit = blockIdx.x * 8LL + (threadIdx.x >> 5);
+  constexpr int PER = D / 32;
+  const int64_t row = blockIdx.x * 8LL + (threadIdx.x >> 5);       // (b*N + i)*Hq + h
   const int lane = threadIdx.x & 31;
-  if (unit >= static_cast<int64_t>(s.B) * s.Hkv * s.N) return;
-  const int i = static_cast<int>(unit % s.N);
-  const int64_t head = unit / s.N;
-  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
+  if (row >= static_cast<int64_t>(s.B) * s.N * s.Hq) return;
+  const int h = static_cast<int>(row % s.Hq);
+  const int64_t bi = row / s.Hq;
+  const int i = static_cast<int>(bi % s.N), b = static_cast<int>(bi / s.N);
+  const int64_t unit = (static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i;
   const bool valid = lane < s.K && idx[unit * s.K + lane] >= 0;
-  const int nsel = __popc(__ballot_sync(0xffffffffu, valid));
-  merge_query<D, G>(s, b, kv, i, nsel, part_o, part_lse, O, lse_out, lane);
+  const float my = valid ? part_lse[row * s.K + lane] : neg_inf();
+  float m = my;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float w = (valid && m != neg_inf()) ? expf(my - m) : 0.f;
+  const float den = warp_sum(w);
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  const float r = den > 0.f ? 1.f / den : 0.f;
+  const __nv_bfloat16* src = part_o + row * s.K * D + lane * PER;
+  float acc[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) acc[u] = 0.f;
+  uint2 v[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if ((vmask >> q) & 1u) v[q] = __ldg(reinterpret_cast<const uint2*>(src + q * D));
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, w, q);
+    if ((vmask >> q) & 1u) {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[q]);
+#pragma unroll
+      for (int u = 0; u < PER; ++u) acc[u] += wq * __bfloat162float(e[u]);
+    }
+  }
+  __nv_bfloat16* dst = O + row * D + lane * PER;
+#pragma unroll
+  for (int u = 0; u < PER; u += 2) *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u] * r, acc[u + 1] * r);
+  if (lane == 0)
+    lse_out[(static_cast<int64_t>(b) * s.Hq + h) * s.N + i] = den > 0.f ? m + logf(den) : neg_inf();
 }
-
 
 template <int D, int G>
 int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
@@ -315,9 +282,9 @@ int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, 
         s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
         static_cast<const __nv_bfloat16*>(V), list, items, n_items, po, pl, status);
   }
-  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
   ProfScope ps(st, "attn_combine");
-  attn_combine_kernel<D, G><<<static_cast<unsigned>((units + 7) / 8), 256, 0, st>>>(
+  attn_combine_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
       s, idx, po, pl, static_cast<__nv_bfloat16*>(O), lse);
   return cudaGetLastError();
 }

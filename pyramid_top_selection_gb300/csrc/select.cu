@@ -87,6 +87,10 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   __shared__ float s_sc[kWarps][kMaxCand];
   __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
   __shared__ float s_pd[kWarps][PISA_MAX_LEVELS][8];
+  // dots of every candidate's two children (q . key sum, per head), two level buffers
+  __shared__ float s_cdot[kWarps][2][kMaxCand][2][8];
+  __shared__ int s_kslot[kWarps][kMaxCand / 2];   // candidate slot each kept node came from
+  __shared__ int s_par[kWarps][kMaxCand];         // 2 * (kept slot of the parent) + which child
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
@@ -183,8 +187,16 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   __syncwarp();
 
   const unsigned ltm = lanemask_lt();
+  // Right-child shortcut: the key sum of a node is the sum of its children's, so once a
+  // level has been scored the dot of every next candidate c is known, and for c's children
+  // only the left one needs loading: q.S(2c+1) = q.S(c) - q.S(2c). The node on the query's
+  // path uses its causal prefix dot instead.
+  bool have_pdot = false;   // dots of the current candidates are known (previous level scored)
+  int cur = 0;              // s_cdot buffer written by the previous scored level
+  int* kslot = s_kslot[warp];
   for (int lam = L - 2; lam >= 1; --lam) {
-    // candidates at level lam: visible children of the kept nodes of level lam+1
+    // candidates at level lam: visible children of the kept nodes of level lam+1; candidate
+    // 2k(+1) of kept node k records (kept slot, which child) for its parent dot
     const int64_t span = static_cast<int64_t>(C) << lam;
     int nc;
     {
@@ -194,54 +206,45 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const unsigned m0 = __ballot_sync(0xffffffffu, c0), m1 = __ballot_sync(0xffffffffu, c1);
       const int pos = __popc(m0 & ltm) + __popc(m1 & ltm);
       __syncwarp();
-      if (c0) cand[pos] = 2 * a;
-      if (c1) cand[pos + 1] = 2 * a + 1;
+      if (c0) { cand[pos] = 2 * a; s_par[warp][pos] = lane * 2 + 0; }
+      if (c1) { cand[pos + 1] = 2 * a + 1; s_par[warp][pos + 1] = lane * 2 + 1; }
       nc = __popc(m0) + __popc(m1);
     }
     __syncwarp();
     if (nc <= Ksel) {
       if (lane < nc) kept[lane] = cand[lane];
       nkept = nc;
+      have_pdot = false;
       __syncwarp();
       continue;
     }
-    // score every candidate with its (<= 2) visible children at level lam-1
     const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
     const int pathc = ti >> (lam - 1);
     const float pd0 = s_pd[warp][lam - 1][2 * p], pd1 = s_pd[warp][lam - 1][2 * p + 1];
-    for (int mt = 0; mt * 8 < nc; ++mt) {
-      const int cs = mt * 8 + g;
-      const int c = cs < nc ? cand[cs] : -1;
+    const int nxt = cur ^ 1;
+    float (*cd)[2][8] = s_cdot[warp][nxt];
+    float (*pdots)[2][8] = s_cdot[warp][cur];
+    // child dots for one candidate slot cs (lane's two heads): returns the score part
+    auto finish = [&](int cs, int c, float l0, float l1, float r0, float r1, bool rv) {
       const int ch0 = 2 * c, ch1 = 2 * c + 1;
-      const bool v0 = c >= 0;
-      const bool v1 = c >= 0 && static_cast<int64_t>(ch1) * cspan <= i;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint4* r0 = spl_h + (v0 ? (geo.off[lam - 1] + ch0) * RQ : 0);
-      const uint4* r1 = spl_h + (v1 ? (geo.off[lam - 1] + ch1) * RQ : 0);
-      mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
+      const int64_t st0 = static_cast<int64_t>(ch0) * cspan, st1 = static_cast<int64_t>(ch1) * cspan;
       float cnt0, cnt1;
-      {
-        const int64_t st0 = static_cast<int64_t>(ch0) * cspan, st1 = static_cast<int64_t>(ch1) * cspan;
-        if (ch0 == pathc) {
-          acc[0] = pd0; acc[1] = pd1;
-          cnt0 = static_cast<float>(i - st0 + 1);
-        } else {
-          cnt0 = static_cast<float>(min(st0 + cspan, static_cast<int64_t>(s.N)) - st0);
-        }
-        if (ch1 == pathc) {
-          acc[2] = pd0; acc[3] = pd1;
-          cnt1 = static_cast<float>(i - st1 + 1);
-        } else {
-          cnt1 = static_cast<float>(min(st1 + cspan, static_cast<int64_t>(s.N)) - st1);
-        }
+      if (ch0 == pathc) { l0 = pd0; l1 = pd1; cnt0 = static_cast<float>(i - st0 + 1); }
+      else cnt0 = static_cast<float>(min(st0 + cspan, static_cast<int64_t>(s.N)) - st0);
+      if (ch1 == pathc) { r0 = pd0; r1 = pd1; cnt1 = static_cast<float>(i - st1 + 1); }
+      else cnt1 = static_cast<float>(min(st1 + cspan, static_cast<int64_t>(s.N)) - st1);
+      if (cs < nc) {
+        cd[cs][0][2 * p] = l0; cd[cs][0][2 * p + 1] = l1;
+        cd[cs][1][2 * p] = r0; cd[cs][1][2 * p + 1] = r1;
       }
       float part = 0.f;
+      const float lv[2] = {l0, l1}, rvv[2] = {r0, r1};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float x0 = s.scale * acc[e] / cnt0;
+        const float x0 = s.scale * lv[e] / cnt0;
         float l;
-        if (v1) {
-          const float x1 = s.scale * acc[2 + e] / cnt1;
+        if (rv) {
+          const float x1 = s.scale * rvv[e] / cnt1;
           const float mx = fmaxf(x0, x1);
           l = mx + logf(expf(x0 - mx) + expf(x1 - mx));
         } else {
@@ -249,9 +252,56 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         }
         if (2 * p + e < G) part += l;
       }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (p == 0 && cs < nc) sc[cs] = part;
+      return part;
+    };
+    if (have_pdot) {
+      // 16 candidates per MMA tile: row g and g+8 are the left children of two candidates
+      for (int mt = 0; mt * 16 < nc; ++mt) {
+        const int csa = mt * 16 + g, csb = csa + 8;
+        const int ca = csa < nc ? cand[csa] : -1, cb = csb < nc ? cand[csb] : -1;
+        const bool la = ca >= 0 && 2 * ca != pathc, lb = cb >= 0 && 2 * cb != pathc;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4* ra = spl_h + (la ? (geo.off[lam - 1] + 2 * ca) * RQ : 0);
+        const uint4* rb = spl_h + (lb ? (geo.off[lam - 1] + 2 * cb) * RQ : 0);
+        mma_split_rows<KS>(acc, ra, la, rb, lb, p, qb);
+        float pa = 0.f, pb = 0.f;
+        if (ca >= 0) {
+          const int ps = s_par[warp][csa];
+          const float q0 = pdots[kslot[ps >> 1]][ps & 1][2 * p], q1 = pdots[kslot[ps >> 1]][ps & 1][2 * p + 1];
+          const bool rv = static_cast<int64_t>(2 * ca + 1) * cspan <= i;
+          pa = finish(csa, ca, acc[0], acc[1], q0 - acc[0], q1 - acc[1], rv);
+        }
+        if (cb >= 0) {
+          const int ps = s_par[warp][csb];
+          const float q0 = pdots[kslot[ps >> 1]][ps & 1][2 * p], q1 = pdots[kslot[ps >> 1]][ps & 1][2 * p + 1];
+          const bool rv = static_cast<int64_t>(2 * cb + 1) * cspan <= i;
+          pb = finish(csb, cb, acc[2], acc[3], q0 - acc[2], q1 - acc[3], rv);
+        }
+        pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+        pa += __shfl_xor_sync(0xffffffffu, pa, 2);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+        if (p == 0 && csa < nc) sc[csa] = pa;
+        if (p == 0 && csb < nc) sc[csb] = pb;
+      }
+    } else {
+      // 8 candidates per MMA tile: row g and g+8 are candidate g's two children
+      for (int mt = 0; mt * 8 < nc; ++mt) {
+        const int cs = mt * 8 + g;
+        const int c = cs < nc ? cand[cs] : -1;
+        const int ch0 = 2 * c, ch1 = 2 * c + 1;
+        const bool v0 = c >= 0;
+        const bool v1 = c >= 0 && static_cast<int64_t>(ch1) * cspan <= i;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4* r0 = spl_h + (v0 ? (geo.off[lam - 1] + ch0) * RQ : 0);
+        const uint4* r1 = spl_h + (v1 ? (geo.off[lam - 1] + ch1) * RQ : 0);
+        mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
+        float part = 0.f;
+        if (c >= 0) part = finish(cs, c, acc[0], acc[1], acc[2], acc[3], v1);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (p == 0 && cs < nc) sc[cs] = part;
+      }
     }
     __syncwarp();
     for (int s2 = lane; s2 < nc; s2 += 32) {
@@ -259,9 +309,11 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const int mi = cand[s2];
       int rank = 0;
       for (int o = 0; o < nc; ++o) rank += beats(sc[o], cand[o], my, mi) ? 1 : 0;
-      if (rank < Ksel) kept[rank] = mi;
+      if (rank < Ksel) { kept[rank] = mi; kslot[rank] = s2; }
     }
     nkept = Ksel;
+    have_pdot = true;
+    cur = nxt;
     __syncwarp();
   }
 
