@@ -459,10 +459,15 @@ def run_sweep(args, cfg, local):
                 torch.cuda.synchronize()
                 ts.append(a.elapsed_time(b))
             out[name] = statistics.median(ts)
+            kern, _, _ = profile_kernels(pisa, lambda: fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx),
+                                         max(1, args.steps), flush)
+            out[name + "_kernels"] = {k: round(v["avg_ms"], 4) for k, v in kern.items()}
         print(json.dumps({"workload": "selection sweep", "N": N, "B": c["B"], "Hq": c["Hq"], "Hkv": c["Hkv"],
                           "d": c["d"], "K": c["K"], "pyramid_select_ms": out["pyramid"],
                           "flat_select_ms": out["flat"], "flat_over_pyramid": out["flat"] / out["pyramid"],
-                          "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3)}), flush=True)
+                          "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3),
+                          "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"]}),
+              flush=True)
         del Q, Kt, pyr, idx, ws_p, ws_f
         torch.cuda.empty_cache()
 
