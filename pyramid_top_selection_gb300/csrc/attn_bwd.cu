@@ -7,20 +7,20 @@
 // With P = exp(s q.k - lse) (lse from the forward), D_i = dO_i . O_i and
 // dS = P (dO . v - D):  dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO.
 //
-// Block-major: the selected (leaf, query) pairs are grouped by leaf and one CTA owns one
-// leaf block of one KV head, so that block's dK/dV are complete inside the CTA (no atomics)
-// and summed over all rows = (query, head of the group) that selected it. Each of the 4
+// Block-major: the selected (leaf, query) pairs are grouped by (KV head, query chunk, leaf)
+// and cut into work items; one CTA takes one item (a leaf block of one KV head and a run of
+// the rows = (query, head of the group) that selected it) and adds its share of that
+// block's dK/dV into fp32 accumulators with vector reductions. Each of the 4
 // warps owns 16 of the 64 keys and keeps their dK/dV in registers across all row chunks;
 // rows come in chunks of 32, staged in shared memory row-major and transposed. dQ of a
 // (row, block) pair is a partial written to the workspace; a second kernel sums the <= K
 // partials of every row.
 #include "device.cuh"
+#include "group.h"
 #include "profile.h"
 
 namespace pisa {
 
-int launch_group(const Dims& s, const int32_t* cand, int W, int32_t* counts, int32_t* cursor,
-                 int32_t* list, cudaStream_t st);
 size_t align256(size_t x);
 
 namespace {
@@ -67,12 +67,12 @@ delta_kernel(int64_t rows, const __nv_bfloat16* __restrict__ O, const __nv_bfloa
 
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32)
-attn_bwd_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                 const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ dO,
                 const float* __restrict__ lse, const float* __restrict__ delta,
-                const int32_t* __restrict__ off, const int32_t* __restrict__ list,
-                __nv_bfloat16* __restrict__ part_dq, __nv_bfloat16* __restrict__ dK,
-                __nv_bfloat16* __restrict__ dV) {
+                const int32_t* __restrict__ list, const int4* __restrict__ items,
+                const int32_t* __restrict__ n_items, __nv_bfloat16* __restrict__ part_dq,
+                float* __restrict__ dk_acc, float* __restrict__ dv_acc) {
   using L = BwdSmem<D>;
   constexpr int KS = D / 16, ND = D / 8, QPC = kRows / G;
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -85,10 +85,12 @@ attn_bwd_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
   int* s_slot = s_i + kRows;
   int* s_h = s_slot + kRows;
 
-  const int t = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
-  const int64_t bin = head * s.n0 + t;
-  const int beg = off[bin], end = off[bin + 1];
+  if (static_cast<int>(blockIdx.x) >= *n_items) return;
+  const int4 item = items[blockIdx.x];
+  const int t = gp.leaf_of(item.x);
+  const int64_t head = gp.head_of(item.x);
+  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
+  const int beg = item.y, end = item.y + item.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
   const int kbase = t * 64;
@@ -255,7 +257,8 @@ attn_bwd_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
       }
     }
   }
-  // dK, dV of this leaf block (zero when no query selected it)
+  // this item's share of the leaf block's dK and dV (unscaled dK), added into fp32
+  // accumulators with vector reductions: items of one leaf run in different CTAs
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int64_t j = static_cast<int64_t>(kbase) + key0 + g + 8 * half;
@@ -263,10 +266,22 @@ attn_bwd_kernel(Dims s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
     const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D;
 #pragma unroll
     for (int nd = 0; nd < ND; ++nd) {
-      *reinterpret_cast<uint32_t*>(dK + o + nd * 8 + 2 * p) =
-          pack_bf16(s.scale * dk[nd][2 * half], s.scale * dk[nd][2 * half + 1]);
-      *reinterpret_cast<uint32_t*>(dV + o + nd * 8 + 2 * p) = pack_bf16(dv[nd][2 * half], dv[nd][2 * half + 1]);
+      atomicAdd(reinterpret_cast<float2*>(dk_acc + o + nd * 8 + 2 * p), make_float2(dk[nd][2 * half], dk[nd][2 * half + 1]));
+      atomicAdd(reinterpret_cast<float2*>(dv_acc + o + nd * 8 + 2 * p), make_float2(dv[nd][2 * half], dv[nd][2 * half + 1]));
     }
+  }
+}
+
+// dK = bf16(s * dK_acc), dV = bf16(dV_acc), 8 elements per thread.
+__global__ void dkdv_convert_kernel(int64_t n8, float scale, const float4* __restrict__ dk_acc,
+                                    const float4* __restrict__ dv_acc, uint4* __restrict__ dK,
+                                    uint4* __restrict__ dV) {
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = dk_acc[2 * q], c = dk_acc[2 * q + 1], e = dv_acc[2 * q], f = dv_acc[2 * q + 1];
+    dK[q] = make_uint4(pack_bf16(scale * a.x, scale * a.y), pack_bf16(scale * a.z, scale * a.w),
+                       pack_bf16(scale * c.x, scale * c.y), pack_bf16(scale * c.z, scale * c.w));
+    dV[q] = make_uint4(pack_bf16(e.x, e.y), pack_bf16(e.z, e.w), pack_bf16(f.x, f.y), pack_bf16(f.z, f.w));
   }
 }
 
@@ -298,45 +313,53 @@ dq_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* 
 }
 
 template <int D, int G>
-int bwd_launch(const Dims& s, const void* Q, const void* K, const void* V, const void* dO,
-               const float* lse, const float* delta, const int32_t* off, const int32_t* list,
-               __nv_bfloat16* pdq, void* dK, void* dV, cudaStream_t st) {
+int bwd_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+               const void* dO, const float* lse, const float* delta, const int32_t* list,
+               const int4* items, const int32_t* n_items, __nv_bfloat16* pdq, float* dk_acc,
+               float* dv_acc, cudaStream_t st) {
   const int smem = BwdSmem<D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope ps(st, "attn_bwd");
-  attn_bwd_kernel<D, G><<<dim3(s.n0, s.Hkv, s.B), kWarps * 32, smem, st>>>(
-      s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
-      static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(dO), lse, delta, off, list,
-      pdq, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
+  attn_bwd_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, smem, st>>>(
+      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+      static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(dO), lse, delta, list,
+      items, n_items, pdq, dk_acc, dv_acc);
   return cudaGetLastError();
 }
 
 template <int D>
-int bwd_dispatch(const Dims& s, const void* Q, const void* K, const void* V, const void* dO,
-                 const float* lse, const float* delta, const int32_t* off, const int32_t* list,
-                 __nv_bfloat16* pdq, void* dK, void* dV, cudaStream_t st) {
+int bwd_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                 const void* dO, const float* lse, const float* delta, const int32_t* list,
+                 const int4* items, const int32_t* n_items, __nv_bfloat16* pdq, float* dk_acc,
+                 float* dv_acc, cudaStream_t st) {
   switch (s.G) {
-    case 1: return bwd_launch<D, 1>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
-    case 2: return bwd_launch<D, 2>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
-    case 4: return bwd_launch<D, 4>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
-    default: return bwd_launch<D, 8>(s, Q, K, V, dO, lse, delta, off, list, pdq, dK, dV, st);
+    case 1: return bwd_launch<D, 1>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
+    case 2: return bwd_launch<D, 2>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
+    case 4: return bwd_launch<D, 4>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
+    default: return bwd_launch<D, 8>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
   }
+}
+
+// Query chunks of about 16 MiB of one head's Q and dO rows; about 2048 (query, head) rows
+// (at most 1024 queries) per work item.
+GroupPlan bwd_plan(const Dims& s) {
+  const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2 * 2;
+  const int cap = (2048 / s.G) < 1024 ? 2048 / s.G : 1024;
+  return make_group_plan(s, s.K, (int64_t(16) << 20) / per_query, cap);
 }
 
 }  // namespace
 
 AttnBwdWs attn_bwd_ws(const Dims& s) {
   AttnBwdWs w{};
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
-  const size_t bins = static_cast<size_t>(s.B) * s.Hkv * s.n0;
-  size_t o = 0;
-  w.counts = o;  o += align256((bins + 1) * 4);
-  w.cursor = o;  o += align256((bins + 1) * 4);
-  w.list = o;    o += align256(units * s.K * 4);
+  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
+  size_t o = group_ws(bwd_plan(s), 0).end;
   w.delta = o;   o += align256(rows * 4);
   w.part_dq = o; o += align256(rows * s.K * s.d * 2);
+  w.dk_acc = o;  o += align256(kvel * 4);
+  w.dv_acc = o;  o += align256(kvel * 4);
   w.total = o;
   return w;
 }
@@ -346,13 +369,18 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
                     void* dV, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnBwdWs w = attn_bwd_ws(s);
-  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
-  int32_t* cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
-  int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+  const GroupPlan gp = bwd_plan(s);
+  const GroupWs g = group_ws(gp, 0);
   float* delta = reinterpret_cast<float*>(ws + w.delta);
   __nv_bfloat16* pdq = reinterpret_cast<__nv_bfloat16*>(ws + w.part_dq);
-  int err = launch_group(s, idx, s.K, counts, cursor, list, st);
+  float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
+  float* dv_acc = reinterpret_cast<float*>(ws + w.dv_acc);
+  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
+  int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;
+  cudaError_t e = cudaMemsetAsync(dk_acc, 0, kvel * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dv_acc, 0, kvel * 4, st);
+  if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
   const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
   {
@@ -365,9 +393,20 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
                                                static_cast<const __nv_bfloat16*>(dO), delta);
   }
   if ((err = cudaGetLastError())) return err;
-  err = s.d == 128 ? bwd_dispatch<128>(s, Q, K, V, dO, lse, delta, counts, list, pdq, dK, dV, st)
-                   : bwd_dispatch<64>(s, Q, K, V, dO, lse, delta, counts, list, pdq, dK, dV, st);
+  const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
+  const int4* items = reinterpret_cast<const int4*>(ws + g.items);
+  const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
+  err = s.d == 128 ? bwd_dispatch<128>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st)
+                   : bwd_dispatch<64>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
   if (err) return err;
+  {
+    ProfScope ps(st, "attn_bwd_dkdv");
+    const int64_t n8 = static_cast<int64_t>(kvel / 8);
+    const int64_t nb = (n8 + 255) / 256;
+    dkdv_convert_kernel<<<static_cast<unsigned>(nb < 152 * 32 ? nb : 152 * 32), 256, 0, st>>>(
+        n8, s.scale, reinterpret_cast<const float4*>(dk_acc), reinterpret_cast<const float4*>(dv_acc),
+        static_cast<uint4*>(dK), static_cast<uint4*>(dV));
+  }
   {
     ProfScope ps(st, "attn_bwd_dq");
     if (s.d == 128)

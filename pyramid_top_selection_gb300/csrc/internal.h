@@ -49,7 +49,7 @@ struct AttnFwdWs {
   size_t part_o, part_lse, status, total;
 };
 struct AttnBwdWs {
-  size_t counts, cursor, list, delta, part_dq, total;
+  size_t delta, part_dq, dk_acc, dv_acc, total;
 };
 SelectWs select_ws(const Dims& s, const Geo& g);
 AttnFwdWs attn_fwd_ws(const Dims& s);
