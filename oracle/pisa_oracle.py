@@ -332,6 +332,36 @@ def selected_keys(idx_row: np.ndarray, i: int, C: int, N: int) -> np.ndarray:
     return np.asarray(js, dtype=np.int64)
 
 
+def selected_head_lse(Q, K, idx, C: int, scale: float | None = None, queries=None):
+    """Per-head LSE of every selected leaf: log sum_{j in leaf idx[b,kv,i,k], j <= i}
+    exp(s q_{i,h} . k_j) for h in KV head kv's group (the exact leaf score of the digest
+    page's "Method key points" before the GQA heads are summed).
+
+    Returns [B,Hq,N,K] f64: -inf for -1 slots, nan for queries not computed."""
+    Q, K = _as64(Q), _as64(K)
+    idx = np.asarray(idx)
+    B, N, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    G = Hq // Hkv
+    Ksel = idx.shape[-1]
+    s = default_scale(d) if scale is None else float(scale)
+    qs = range(N) if queries is None else [int(x) for x in queries]
+    out = np.full((B, Hq, N, Ksel), np.nan)
+    for b in range(B):
+        for kv in range(Hkv):
+            hs = slice(kv * G, (kv + 1) * G)
+            for i in qs:
+                for k in range(Ksel):
+                    t = int(idx[b, kv, i, k])
+                    if t < 0:
+                        out[b, hs, i, k] = -np.inf
+                        continue
+                    lo, hi = node_range(0, t, C, N)
+                    logits = s * (Q[b, i, hs, :] @ K[b, lo:min(hi, i + 1), kv, :].T)   # [G, n]
+                    out[b, hs, i, k] = _logsumexp(logits, axis=1)
+    return out
+
+
 def sparse_attn_fwd(Q, K, V, idx, C: int, scale: float | None = None, queries=None):
     """o_{i,h} = sum_{j in J_i} softmax_j(s q_{i,h} . k_j) v_j ; lse_{i,h} = log sum exp.
 

@@ -283,6 +283,64 @@ def test_attention_all_selected_equals_sdpa():
     np.testing.assert_allclose(lse, torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
 
 
+def _random_idx(B, Hkv, N, C, Ksel, seed):
+    """Random ascending leaf lists of visible leaves, -1 padded, some rows short."""
+    r = np.random.default_rng(seed)
+    idx = np.full((B, Hkv, N, Ksel), -1, dtype=np.int32)
+    for b in range(B):
+        for kv in range(Hkv):
+            for i in range(N):
+                vis = i // C + 1
+                n = min(vis, int(r.integers(1, Ksel + 1)))
+                idx[b, kv, i, :n] = np.sort(r.choice(vis, size=n, replace=False))
+    return idx
+
+
+def test_selected_head_lse_equals_masked_dense_logsumexp():
+    # Per-head block LSE against torch.logsumexp over dense logits with a block-and-causal mask.
+    B, N, Hq, Hkv, d, C, Ksel = 1, 45, 4, 2, 8, 8, 3
+    Q, K = _rand((B, N, Hq, d), 120), _rand((B, N, Hkv, d), 121)
+    s = 0.7
+    idx = _random_idx(B, Hkv, N, C, Ksel, 122)
+    got = po.selected_head_lse(Q, K, idx, C, scale=s)
+    q, k, _ = _sdpa_dense(Q, K, K, s)
+    logits = (q @ k.transpose(-1, -2)) * s                    # [B, Hq, N, N]
+    j = torch.arange(N)
+    for h in range(Hq):
+        for i in range(N):
+            for slot in range(Ksel):
+                t = int(idx[0, h // (Hq // Hkv), i, slot])
+                if t < 0:
+                    assert got[0, h, i, slot] == -np.inf
+                    continue
+                keep = (j // C == t) & (j <= i)
+                ref = torch.logsumexp(logits[0, h, i].masked_fill(~keep, float("-inf")), dim=0)
+                assert abs(got[0, h, i, slot] - ref.item()) < 1e-12
+
+
+def test_block_lses_combine_to_attention_lse():
+    # LSE over a disjoint union of key sets = LSE of the per-set LSEs.
+    B, N, Hq, Hkv, d, C, Ksel = 2, 40, 4, 1, 8, 8, 4
+    Q, K, V = _rand((B, N, Hq, d), 123), _rand((B, N, Hkv, d), 124), _rand((B, N, Hkv, d), 125)
+    idx = _random_idx(B, Hkv, N, C, Ksel, 126)
+    hl = po.selected_head_lse(Q, K, idx, C, scale=0.4)
+    _, lse = po.sparse_attn_fwd(Q, K, V, idx, C, scale=0.4)
+    np.testing.assert_allclose(torch.logsumexp(torch.from_numpy(hl), dim=-1).numpy(), lse, rtol=1e-12, atol=1e-12)
+
+
+def test_head_lse_of_the_selection_sums_to_its_scores():
+    # The selection's leaf score is the group sum of the per-head leaf LSEs.
+    B, N, Hq, Hkv, d, C, Ksel = 1, 96, 4, 2, 8, 8, 3
+    Q, K = _rand((B, N, Hq, d), 127), _rand((B, N, Hkv, d), 128)
+    o = po.select(Q, K, C, Ksel, scale=0.5)
+    hl = po.selected_head_lse(Q, K, o["idx"], C, scale=0.5)
+    G = Hq // Hkv
+    summed = hl.reshape(B, Hkv, G, N, Ksel).sum(axis=2)
+    ok = o["idx"] >= 0
+    np.testing.assert_allclose(summed[ok], o["score"][ok], rtol=1e-12, atol=1e-12)
+    assert np.all(np.isneginf(summed[~ok]))
+
+
 def test_attention_masks_unselected_blocks():
     # Only leaf 1 selected: the output must be the softmax over exactly its visible keys.
     B, N, Hq, Hkv, d, C = 1, 32, 2, 1, 4, 8
