@@ -195,14 +195,23 @@ def algorithmic(kernel, cfg, idx_host=None):
         units = B * Hkv * cands
         per = G * C * 2 * d
         return "tensor", units * per, "flops", units, per
-    if kernel in ("attn_fwd", "attn_fwd_tc", "attn_fwd_partial") and idx_host is not None:
+    if kernel == "attn_fwd_tc" and idx_host is not None:
         keys = selected_keys(idx_host, C, N)
         units = keys * G
         per = 4 * d
         return "tensor", units * per, "flops", units, per
-    if kernel == "attn_combine":
+    if kernel == "attn_lse_tc" and idx_host is not None:
+        keys = selected_keys(idx_host, C, N)
+        units = keys * G
+        per = 2 * d
+        return "tensor", units * per, "flops", units, per
+    if kernel == "attn_rows":   # K block LSEs + K indices read, lse written, accumulator cleared
         units = B * N * Hq
-        per = K * (2 * d + 4) + 2 * d + 4 + K * 4
+        per = K * 4 + K * 4 / G + 4 + d * 4
+        return "hbm", units * per, "bytes", units, per
+    if kernel == "attn_out":    # fp32 accumulator read, bf16 O written
+        units = B * N * Hq
+        per = d * 4 + d * 2
         return "hbm", units * per, "bytes", units, per
     return None
 
@@ -230,6 +239,7 @@ def run_ours(args, cfg, rank, world, local):
     pyr = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=dev)
     idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
     score = torch.empty(B, Hkv, N, K, dtype=torch.float32, device=dev)
+    hl = torch.empty(B, Hq, N, K, dtype=torch.float32, device=dev)
     O = torch.empty_like(Q)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
     ws_sel = pisa.workspace(shape, 0, dev)
@@ -238,8 +248,8 @@ def run_ours(args, cfg, rank, world, local):
 
     def step(Qs, Ks, Vs):
         pisa.build_pyramid(Ks, shape, out=pyr)
-        pisa.select(Qs, Ks, pyr, shape, ws=ws_sel, idx=idx, score=score)
-        pisa.sparse_attn_fwd(Qs, Ks, Vs, idx, shape, ws=ws_att, out=O, lse=lse)
+        pisa.select(Qs, Ks, pyr, shape, ws=ws_sel, idx=idx, score=score, head_lse=hl)
+        pisa.sparse_attn_fwd(Qs, Ks, Vs, idx, shape, ws=ws_att, out=O, lse=lse, head_lse=hl)
 
     def barrier():
         if world > 1:
@@ -573,6 +583,7 @@ def run_train(args, cfg, rank, world, local):
     _, _, nodes = pisa.pyramid_layout(shape)
     pyr = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=dev)
     idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    hl = torch.empty(B, Hq, N, K, dtype=torch.float32, device=dev)
     O = torch.empty_like(Q)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
     ws_sel, ws_f, ws_b = (pisa.workspace(shape, op, dev) for op in (0, 2, 3))
@@ -580,8 +591,8 @@ def run_train(args, cfg, rank, world, local):
 
     def step():
         pisa.build_pyramid(Kt, shape, out=pyr)
-        pisa.select(Q, Kt, pyr, shape, ws=ws_sel, want_score=False, idx=idx)
-        pisa.sparse_attn_fwd(Q, Kt, V, idx, shape, ws=ws_f, out=O, lse=lse)
+        pisa.select(Q, Kt, pyr, shape, ws=ws_sel, want_score=False, idx=idx, head_lse=hl)
+        pisa.sparse_attn_fwd(Q, Kt, V, idx, shape, ws=ws_f, out=O, lse=lse, head_lse=hl)
         pisa.sparse_attn_bwd(Q, Kt, V, O, lse, dO, idx, shape, ws=ws_b)
 
     for _ in range(args.warmup):

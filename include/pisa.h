@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PISA_VERSION 1
+#define PISA_VERSION 2
 #define PISA_MAX_LEVELS 32
 
 enum {
@@ -106,15 +106,20 @@ int pisa_build_pyramid(const pisa_shape_t* shape, const void* K, float* pyr_sum,
  *   idx   [B,Hkv,N,K] int32 (written): selected leaves ascending, -1 padded when fewer
  *         than K leaves are visible.
  *   score [B,Hkv,N,K] fp32 (written, may be NULL): leaf scores aligned with idx, -inf pad.
+ *   head_lse [B,Hq,N,K] fp32 (written, may be NULL): the per-head terms of the score,
+ *         head_lse[b,h,i,k] = log sum_{j in leaf idx[b,h/G,i,k], j <= i} exp(s q_{i,h}.k_j),
+ *         -inf pad; the G heads of a KV head sum to its score. pisa_sparse_attn_fwd takes
+ *         it to normalise the attention without a second pass over the keys.
  *   ws / ws_bytes: workspace of at least pisa_workspace_size(shape, PISA_OP_SELECT). */
 int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const float* pyr_sum,
-                int32_t* idx, float* score, void* ws, size_t ws_bytes, void* stream);
+                int32_t* idx, float* score, float* head_lse, void* ws, size_t ws_bytes,
+                void* stream);
 
 /* pisa_select without a caller workspace (the pages have no counterpart: this is an
  * integration aid). For callers that cannot hand the library device memory at call time,
  * for instance code running under an engine that owns a fixed device-memory arena and
  * forbids allocations on the serving path, or a plugin whose host exposes no allocator.
- * Same arguments, results and errors as pisa_select minus ws/ws_bytes; it allocates
+ * Same arguments, results and errors as pisa_select minus head_lse and ws/ws_bytes; it allocates
  * nothing and calls no allocating routine. Its scratch is one fixed 32 MiB array inside
  * the library's device image, held on every GPU that loads the library until the process
  * exits. Shapes whose pisa_workspace_size(shape, PISA_OP_SELECT) exceeds 32 MiB are
@@ -139,11 +144,17 @@ int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
  * "Reference value of the work"): o_{i,h} = sum_{j in J_i} softmax_j(s q_{i,h}.k_j) v_j,
  * J_i = keys j <= i inside the leaves idx[b, h/G, i, :] (-1 entries ignored).
  *   Q [B,N,Hq,d], K, V [B,N,Hkv,d] bf16; idx [B,Hkv,N,K] int32 (read).
- *   O [B,N,Hq,d] bf16 and lse [B,Hq,N] fp32 = log sum_{j in J_i} exp(s q.k_j) (written).
+ *   head_lse [B,Hq,N,K] fp32 (read, may be NULL): the per-block LSEs of these very idx,
+ *         as pisa_select writes them. Given, the softmax normaliser lse is known before
+ *         any key is visited; NULL, the call first computes them itself (one more pass of
+ *         Q.K^T over the selected blocks). Values that are not those LSEs give wrongly
+ *         normalised outputs; nothing checks them.
+ *   O [B,N,Hq,d] bf16 and lse [B,Hq,N] fp32 = log sum_{j in J_i} exp(s q.k_j) (written);
+ *         a row with no selected key gets O = 0 and lse = -inf.
  *   Workspace: PISA_OP_ATTN_FWD. */
 int pisa_sparse_attn_fwd(const pisa_shape_t* shape, const void* Q, const void* K, const void* V,
-                         const int32_t* idx, void* O, float* lse, void* ws, size_t ws_bytes,
-                         void* stream);
+                         const int32_t* idx, const float* head_lse, void* O, float* lse,
+                         void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of the selected attention only; the discrete selection takes no gradient
  * (digest page, "Reference value of the work"). With P = exp(s q.k - lse),

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpisa.so")
 PISA_OK, PISA_EINVAL, PISA_EUNSUPPORTED, PISA_EWORKSPACE, PISA_ECUDA, PISA_ETIMEOUT = range(6)
 OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD = range(4)
 MAX_LEVELS = 32
+ABI_VERSION = 2          # PISA_VERSION of the header these argument lists follow
 
 EXPORTS = (
     "pisa_version", "pisa_last_error", "pisa_pyramid_layout", "pisa_workspace_size",
@@ -62,13 +63,16 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         P = ctypes.POINTER
         L.pisa_version.restype = ctypes.c_int
+        if L.pisa_version() != ABI_VERSION:
+            raise ImportError(f"libpisa.so has ABI version {L.pisa_version()}, this binding needs {ABI_VERSION}: "
+                              "rebuild with pyramid_top_selection_gb300/build.py")
         L.pisa_last_error.restype = ctypes.c_char_p
         L.pisa_pyramid_layout.argtypes = [P(Shape), P(i32), P(i64), P(i64)]
         L.pisa_workspace_size.argtypes = [P(Shape), ctypes.c_int, P(sz)]
         L.pisa_build_pyramid.argtypes = [P(Shape), vp, vp, vp]
-        L.pisa_select.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
+        L.pisa_select.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_select_flat.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
-        L.pisa_sparse_attn_fwd.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.pisa_sparse_attn_fwd.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_sparse_attn_bwd.argtypes = [P(Shape)] + [vp] * 10 + [vp, sz, vp]
         L.pisa_decode_pyramid_layout.argtypes = [P(DecodeShape), P(i32), P(i64), P(i64)]
         L.pisa_decode_build_pyramid.argtypes = [P(DecodeShape), vp, vp, vp, vp]
@@ -146,44 +150,69 @@ def build_pyramid(Kt: torch.Tensor, shape: Shape, out: torch.Tensor | None = Non
     return pyr
 
 
-def _select_common(fn, op, Q, Kt, pyr, shape, ws, want_score, idx=None, score=None):
-    _need(Q, torch.bfloat16, "Q")
-    _need(Kt, torch.bfloat16, "K")
-    _need(pyr, torch.float32, "pyr_sum")
+def _select_out(Q, shape, want_score, idx, score):
     dev = Q.device
     if idx is None:
         idx = torch.empty(shape.B, shape.Hkv, shape.N, shape.K, dtype=torch.int32, device=dev)
     if score is None and want_score:
         score = torch.empty(shape.B, shape.Hkv, shape.N, shape.K, dtype=torch.float32, device=dev)
-    if ws is None:
-        ws = _workspace(shape, op, dev)
-    _check(fn(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
-              _ptr(ws), ws.numel(), _stream(dev)))
     return idx, score
 
 
-def select(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, score=None):
-    """Pyramid Top-K selection: idx [B,Hkv,N,K] int32 (ascending, -1 pad), score fp32."""
-    return _select_common(lib().pisa_select, OP_SELECT, Q, Kt, pyr, shape, ws, want_score, idx, score)
+def _select_in(Q, Kt, pyr):
+    _need(Q, torch.bfloat16, "Q")
+    _need(Kt, torch.bfloat16, "K")
+    _need(pyr, torch.float32, "pyr_sum")
+
+
+def select(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, score=None,
+           want_head_lse=False, head_lse=None):
+    """Pyramid Top-K selection: idx [B,Hkv,N,K] int32 (ascending, -1 pad), score fp32.
+
+    With want_head_lse (or a head_lse buffer) also returns the per-head leaf LSEs
+    [B,Hq,N,K] fp32 that sparse_attn_fwd takes to skip its normalisation pass."""
+    _select_in(Q, Kt, pyr)
+    dev = Q.device
+    idx, score = _select_out(Q, shape, want_score, idx, score)
+    if head_lse is None and want_head_lse:
+        head_lse = torch.empty(shape.B, shape.Hq, shape.N, shape.K, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _workspace(shape, OP_SELECT, dev)
+    _check(lib().pisa_select(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
+                             _ptr(head_lse), _ptr(ws), ws.numel(), _stream(dev)))
+    if head_lse is not None:
+        return idx, score, head_lse
+    return idx, score
 
 
 def select_flat(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, score=None):
     """Flat O(N^2/C) block selection (comparator)."""
-    return _select_common(lib().pisa_select_flat, OP_SELECT_FLAT, Q, Kt, pyr, shape, ws, want_score, idx, score)
+    _select_in(Q, Kt, pyr)
+    dev = Q.device
+    idx, score = _select_out(Q, shape, want_score, idx, score)
+    if ws is None:
+        ws = _workspace(shape, OP_SELECT_FLAT, dev)
+    _check(lib().pisa_select_flat(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
+                                  _ptr(ws), ws.numel(), _stream(dev)))
+    return idx, score
 
 
-def sparse_attn_fwd(Q, Kt, V, idx, shape: Shape, ws=None, out=None, lse=None):
-    """Causal attention over the selected leaves: O [B,N,Hq,d] bf16, lse [B,Hq,N] fp32."""
+def sparse_attn_fwd(Q, Kt, V, idx, shape: Shape, ws=None, out=None, lse=None, head_lse=None):
+    """Causal attention over the selected leaves: O [B,N,Hq,d] bf16, lse [B,Hq,N] fp32.
+
+    head_lse: the selection's per-head leaf LSEs for these idx (optional)."""
     for t, n in ((Q, "Q"), (Kt, "K"), (V, "V")):
         _need(t, torch.bfloat16, n)
     _need(idx, torch.int32, "idx")
+    if head_lse is not None:
+        _need(head_lse, torch.float32, "head_lse")
     dev = Q.device
     O = out if out is not None else torch.empty_like(Q)
     lse = lse if lse is not None else torch.empty(shape.B, shape.Hq, shape.N, dtype=torch.float32, device=dev)
     if ws is None:
         ws = _workspace(shape, OP_ATTN_FWD, dev)
     _check(lib().pisa_sparse_attn_fwd(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(V), _ptr(idx),
-                                      _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)))
+                                      _ptr(head_lse), _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)))
     return O, lse
 
 

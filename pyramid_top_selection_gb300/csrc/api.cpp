@@ -93,7 +93,7 @@ int layout_out(const pisa::Geo& g, int32_t* n_levels, int64_t* level_offset, int
 
 size_t ws_bytes_for(const pisa::Dims& d, const pisa::Geo& g, int op) {
   switch (op) {
-    case PISA_OP_SELECT: return pisa::select_ws(d, g).total;
+    case PISA_OP_SELECT: return pisa::select_ws(d, g).total_head;
     case PISA_OP_SELECT_FLAT: return pisa::flat_ws(d, g);
     case PISA_OP_ATTN_FWD: return pisa::attn_fwd_ws(d).total;
     case PISA_OP_ATTN_BWD: return pisa::attn_bwd_ws(d).total;
@@ -141,7 +141,7 @@ int pisa_build_pyramid(const pisa_shape_t* shape, const void* K, float* pyr_sum,
 }
 
 int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const float* pyr_sum,
-                int32_t* idx, float* score, void* ws, size_t ws_bytes, void* stream) {
+                int32_t* idx, float* score, float* head_lse, void* ws, size_t ws_bytes, void* stream) {
   PISA_CHECK(check_shape(shape));
   PISA_CHECK(check_ptr(Q, "Q"));
   PISA_CHECK(check_ptr(K, "K"));
@@ -150,8 +150,9 @@ int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const f
   PISA_CHECK(check_ptr(score, "score", true));
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  PISA_CHECK(check_ptr(head_lse, "head_lse", true));
   PISA_CHECK(check_ws(d, g, PISA_OP_SELECT, ws, ws_bytes));
-  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
+  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, head_lse, static_cast<char*>(ws), stream),
                  "pisa_select");
 }
 
@@ -172,7 +173,7 @@ int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
                 "use pisa_select with a caller workspace", need, pisa::noalloc_scratch_bytes());
   void* ws = nullptr;
   PISA_CHECK(cuda_rc(pisa::noalloc_scratch(&ws), "pisa_select_noalloc scratch set-up"));
-  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
+  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, nullptr, static_cast<char*>(ws), stream),
                  "pisa_select_noalloc");
 }
 
@@ -193,8 +194,8 @@ int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
 }
 
 int pisa_sparse_attn_fwd(const pisa_shape_t* shape, const void* Q, const void* K, const void* V,
-                         const int32_t* idx, void* O, float* lse, void* ws, size_t ws_bytes,
-                         void* stream) {
+                         const int32_t* idx, const float* head_lse, void* O, float* lse, void* ws,
+                         size_t ws_bytes, void* stream) {
   PISA_CHECK(check_shape(shape));
   PISA_CHECK(check_ptr(Q, "Q"));
   PISA_CHECK(check_ptr(K, "K"));
@@ -204,8 +205,9 @@ int pisa_sparse_attn_fwd(const pisa_shape_t* shape, const void* Q, const void* K
   PISA_CHECK(check_ptr(lse, "lse"));
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  PISA_CHECK(check_ptr(head_lse, "head_lse", true));
   PISA_CHECK(check_ws(d, g, PISA_OP_ATTN_FWD, ws, ws_bytes));
-  return cuda_rc(pisa::launch_attn_fwd(d, Q, K, V, idx, O, lse, static_cast<char*>(ws), stream),
+  return cuda_rc(pisa::launch_attn_fwd(d, Q, K, V, idx, head_lse, O, lse, static_cast<char*>(ws), stream),
                  "pisa_sparse_attn_fwd");
 }
 

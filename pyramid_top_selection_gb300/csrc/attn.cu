@@ -8,9 +8,10 @@
 //
 // Forward, block-major: the selected (leaf, query) pairs are grouped by (KV head, query
 // chunk, leaf) and cut into work items (group.cu); the tensor-core kernel (attn_tc.cu)
-// takes one item per CTA. Each (row, block) yields a normalised partial output and its
-// block LSE; a combine kernel then merges the <= K partials of every row:
-// lse = log sum_t exp(lse_t), o = sum_t exp(lse_t - lse) o_t.
+// takes one item per CTA. A row's softmax normaliser lse = log sum_t exp(lse_t) comes
+// from the per-block LSEs lse_t (the selection's per-head leaf terms, or a first S-only
+// pass), so each (row, block) adds its final share exp(s q.k - lse) v into an fp32
+// accumulator; a last kernel converts the accumulator to bf16.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -19,16 +20,18 @@ namespace pisa {
 
 int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
-                       __nv_bfloat16* po, float* pl, void* O, float* lse, int32_t* status, cudaStream_t st);
+                       const float* head_lse, float* block_lse_ws, float* o_acc, void* O, float* lse,
+                       int32_t* status, cudaStream_t st);
 
 namespace {
 
-// Query chunk so that one chunk's query rows stay in L2 while its leaves are swept; about
-// 2048 (query, head) rows (at most 1024 queries) per work item.
+// Query chunks of about 16 MiB of one KV head's fp32 accumulator rows (G heads x d), so the
+// rows that the running items add into stay in L2; about 2048 (query, head) rows (at most
+// 1024 queries) per work item.
 GroupPlan fwd_plan(const Dims& s) {
-  const int64_t per_query = static_cast<int64_t>(s.G) * s.K * s.d * 2;
+  const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 4;
   const int cap = (2048 / s.G) < 1024 ? 2048 / s.G : 1024;
-  return make_group_plan(s, s.K, (int64_t(64) << 20) / per_query, cap);
+  return make_group_plan(s, s.K, (int64_t(16) << 20) / per_query, cap);
 }
 
 }  // namespace
@@ -38,15 +41,15 @@ AttnFwdWs attn_fwd_ws(const Dims& s) {
   const GroupPlan gp = fwd_plan(s);
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
   size_t o = group_ws(gp, 0).end;
-  w.part_o = o;   o += align256(rows * s.K * s.d * 2);
-  w.part_lse = o; o += align256(rows * s.K * 4);
-  w.status = o;   o += 256;
+  w.block_lse = o; o += align256(rows * s.K * 4);
+  w.o_acc = o;     o += align256(rows * s.d * 4);
+  w.status = o;    o += 256;
   w.total = o;
   return w;
 }
 
-int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
-                    const int32_t* idx, void* O, float* lse, char* ws, void* stream) {
+int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V, const int32_t* idx,
+                    const float* head_lse, void* O, float* lse, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnFwdWs w = attn_fwd_ws(s);
   const GroupPlan gp = fwd_plan(s);
@@ -58,10 +61,9 @@ int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
   const int4* items = reinterpret_cast<const int4*>(ws + g.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
-  return launch_attn_fwd_tc(s, gp, Q, K, V, idx, list, items, n_items,
-                            reinterpret_cast<__nv_bfloat16*>(ws + w.part_o),
-                            reinterpret_cast<float*>(ws + w.part_lse), O, lse,
-                            reinterpret_cast<int32_t*>(ws + w.status), st);
+  return launch_attn_fwd_tc(s, gp, Q, K, V, idx, list, items, n_items, head_lse,
+                            reinterpret_cast<float*>(ws + w.block_lse), reinterpret_cast<float*>(ws + w.o_acc),
+                            O, lse, reinterpret_cast<int32_t*>(ws + w.status), st);
 }
 
 }  // namespace pisa

@@ -42,11 +42,12 @@ struct Dims {
 };
 
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.
+// total: without the per-head leaf terms; total_head: with them (head_lse requested).
 struct SelectWs {
-  size_t split, cand, cscore, group, total;
+  size_t split, cand, cscore, group, total, chead, total_head;
 };
 struct AttnFwdWs {
-  size_t part_o, part_lse, status, total;
+  size_t block_lse, o_acc, status, total;
 };
 struct AttnBwdWs {
   size_t delta, part_dq, dk_acc, dv_acc, total;
@@ -60,11 +61,11 @@ size_t flat_ws(const Dims& s, const Geo& g);
 int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32_t* len,
                          int64_t tokens_per_seq, float* pyr, void* stream);
 int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
-                  int32_t* idx, float* score, char* ws, void* stream);
+                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream);
 int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
                        const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
-int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V,
-                    const int32_t* idx, void* O, float* lse, char* ws, void* stream);
+int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V, const int32_t* idx,
+                    const float* head_lse, void* O, float* lse, char* ws, void* stream);
 int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, const void* O,
                     const float* lse, const void* dO, const int32_t* idx, void* dQ, void* dK,
                     void* dV, char* ws, void* stream);

@@ -336,73 +336,6 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   }
 }
 
-// ---------------------------------------------------------------------------- grouping
-__global__ void group_count_kernel(const int32_t* __restrict__ cand, int64_t total, int W, int N,
-                                   int n0, int32_t* __restrict__ counts) {
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = cand[e];
-    if (t >= 0) {
-      const int64_t bk = (e / W) / N;
-      atomicAdd(&counts[bk * n0 + t], 1);
-    }
-  }
-}
-
-// Exclusive scan of n counts into off[0..n] by one 1024-thread block.
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* counts, int n, int32_t* off) {
-  __shared__ int32_t warp_tot[32];
-  const int tid = threadIdx.x;
-  const int per = (n + 1023) / 1024;
-  const int s0 = min(tid * per, n), s1 = min(s0 + per, n);
-  int32_t local = 0;
-  for (int k = s0; k < s1; ++k) local += counts[k];
-  // inclusive scan of `local` over the block
-  const int lane = tid & 31, w = tid >> 5;
-  int32_t v = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) warp_tot[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int32_t t = warp_tot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    warp_tot[lane] = t;
-  }
-  __syncthreads();
-  int32_t run = v - local + (w > 0 ? warp_tot[w - 1] : 0);
-  for (int k = s0; k < s1; ++k) {   // in place is safe: each thread reads then writes its own chunk
-    const int32_t c = counts[k];
-    off[k] = run;
-    run += c;
-  }
-  if (tid == 1023) off[n] = run;
-}
-
-__global__ void group_scatter_kernel(const int32_t* __restrict__ cand, int64_t total, int W, int N,
-                                     int n0, const int32_t* __restrict__ off,
-                                     int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = cand[e];
-    if (t >= 0) {
-      const int64_t unit = e / W;
-      const int slot = static_cast<int>(e - unit * W);
-      const int i = static_cast<int>(unit % N);
-      const int64_t bin = (unit / N) * n0 + t;
-      const int32_t pos = off[bin] + atomicAdd(&cursor[bin], 1);
-      list[pos] = (i << 6) | slot;
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------- stage 2
 // One CTA per (leaf t, KV head, batch): exact leaf LSE for every (query, head) row whose
 // query has t among its candidates. Keys in smem (row stride D+16 bf16: conflict-free
@@ -412,7 +345,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 leaf_score_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
                   const __nv_bfloat16* __restrict__ K, const int32_t* __restrict__ list,
                   const int4* __restrict__ items, const int32_t* __restrict__ n_items, int W,
-                  float* __restrict__ pair_score) {
+                  float* __restrict__ pair_score, float* __restrict__ pair_head) {
   constexpr int KS = D / 16, KROW = D + 16, QPT = 16 / G;
   __shared__ __align__(16) __nv_bfloat16 sK[64 * KROW];
   if (static_cast<int>(blockIdx.x) >= *n_items) return;
@@ -487,6 +420,10 @@ leaf_score_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
     s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
     float l0 = ms0 + logf(s0), l1 = ms1 + logf(s1);
+    if (pair_head && p == 0) {   // per-head terms, [head, N, W, G]
+      if (ok0) pair_head[((head * s.N + i0) * W + (pk0 & 63)) * G + h0] = l0;
+      if (ok1) pair_head[((head * s.N + i1) * W + (pk1 & 63)) * G + h1] = l1;
+    }
 #pragma unroll
     for (int o = 4; o < 4 * G; o <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
@@ -502,8 +439,9 @@ leaf_score_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
 // ---------------------------------------------------------------------------- finish
 // One warp per (b, KV head, query): top K of the <= W candidate scores; ascending output.
 __global__ void __launch_bounds__(kWarps * 32)
-topk_kernel(int64_t units, int W, int Ksel, const int32_t* __restrict__ cand,
-            const float* __restrict__ csc, int32_t* __restrict__ idx, float* __restrict__ score) {
+topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restrict__ cand,
+            const float* __restrict__ csc, const float* __restrict__ chead, int32_t* __restrict__ idx,
+            float* __restrict__ score, float* __restrict__ head_lse) {
   __shared__ int s_i[kWarps][kMaxCand];
   __shared__ float s_s[kWarps][kMaxCand];
   __shared__ int s_k[kWarps][kMaxCand];
@@ -534,10 +472,15 @@ topk_kernel(int64_t units, int W, int Ksel, const int32_t* __restrict__ cand,
     for (int o = 0; o < W; ++o) pos += (s_k[warp][o] && s_i[warp][o] < mi) ? 1 : 0;
     idx[u * Ksel + pos] = mi;
     if (score) score[u * Ksel + pos] = s_s[warp][q];
+    if (head_lse)   // unit u = (b*Hkv + kv)*N + i -> rows (b*Hq + kv*G + h)*N + i
+      for (int h = 0; h < G; ++h)
+        head_lse[(((u / N) * G + h) * N + u % N) * Ksel + pos] = chead[(u * W + q) * G + h];
   }
   for (int q = nk + lane; q < Ksel; q += 32) {
     idx[u * Ksel + q] = -1;
     if (score) score[u * Ksel + q] = neg_inf();
+    if (head_lse)
+      for (int h = 0; h < G; ++h) head_lse[(((u / N) * G + h) * N + u % N) * Ksel + q] = neg_inf();
   }
 }
 
@@ -736,21 +679,23 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
 
 template <int D, int G>
 void leaf_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                 const int4* items, const int32_t* n_items, int W, float* pair_score, cudaStream_t st) {
+                 const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                 cudaStream_t st) {
   ProfScope ps(st, "leaf_score");
   leaf_score_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, 0, st>>>(
       s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), list, items,
-      n_items, W, pair_score);
+      n_items, W, pair_score, pair_head);
 }
 
 template <int D>
 void leaf_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                   const int4* items, const int32_t* n_items, int W, float* pair_score, cudaStream_t st) {
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                   cudaStream_t st) {
   switch (s.G) {
-    case 1: leaf_launch<D, 1>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
-    case 2: leaf_launch<D, 2>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
-    case 4: leaf_launch<D, 4>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
-    default: leaf_launch<D, 8>(s, gp, Q, K, list, items, n_items, W, pair_score, st); break;
+    case 1: leaf_launch<D, 1>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
+    case 2: leaf_launch<D, 2>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
+    case 4: leaf_launch<D, 4>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
+    default: leaf_launch<D, 8>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
   }
 }
 
@@ -780,39 +725,14 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   w.cscore = o; o += align256(units * W * 4);
   w.group = o;
   o = group_ws(leaf_plan(s), o).end;
-  w.total = o;
+  w.total = o;           // without the per-head terms
+  w.chead = o;  o += align256(units * W * s.G * 4);
+  w.total_head = o;      // with them (head_lse requested)
   return w;
 }
 
 size_t flat_ws(const Dims& s, const Geo& g) {
   return align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
-}
-
-// Groups the (leaf, query) pairs of cand [units, W] (-1 entries skipped) by leaf: after
-// the call, off[bin..bin+1] delimits list entries (i << 6 | slot) of bin = head*n0 + leaf.
-int launch_group(const Dims& s, const int32_t* cand, int W, int32_t* counts, int32_t* cursor,
-                 int32_t* list, cudaStream_t st) {
-  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
-  const int64_t total = units * W;
-  const int bins = s.B * s.Hkv * s.n0;
-  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (bins + 1), st);
-  if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * (bins + 1), st);
-  if (e != cudaSuccess) return e;
-  {
-    ProfScope ps(st, "group_count");
-    group_count_kernel<<<grid_for(total, 256), 256, 0, st>>>(cand, total, W, s.N, s.n0, counts);
-  }
-  {
-    ProfScope ps(st, "group_scan");
-    scan_kernel<<<1, 1024, 0, st>>>(counts, bins, counts);   // counts -> offsets, in place
-  }
-  {
-    ProfScope ps(st, "group_scatter");
-    group_scatter_kernel<<<grid_for(total, 256), 256, 0, st>>>(cand, total, W, s.N, s.n0, counts,
-                                                                cursor, list);
-  }
-  return cudaGetLastError();
 }
 
 int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
@@ -823,12 +743,13 @@ int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cuda
 }
 
 int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
-                  int32_t* idx, float* score, char* ws, void* stream) {
+                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const SelectWs w = select_ws(s, g);
   uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
   int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
+  float* chead = head_lse ? reinterpret_cast<float*>(ws + w.chead) : nullptr;
   const GroupPlan gp = leaf_plan(s);
   const GroupWs gw = group_ws(gp, w.group);
   int err = launch_split(s, g, pyr, spl, st);
@@ -849,14 +770,14 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + gw.list);
   const int4* items = reinterpret_cast<const int4*>(ws + gw.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + gw.icount) + gp.bins;
-  if (s.d == 128) leaf_dispatch<128>(s, gp, Q, K, list, items, n_items, W, cscore, st);
-  else leaf_dispatch<64>(s, gp, Q, K, list, items, n_items, W, cscore, st);
+  if (s.d == 128) leaf_dispatch<128>(s, gp, Q, K, list, items, n_items, W, cscore, chead, st);
+  else leaf_dispatch<64>(s, gp, Q, K, list, items, n_items, W, cscore, chead, st);
   if ((err = cudaGetLastError())) return err;
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
     ProfScope ps(st, "topk");
     topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, W, s.K, cand, cscore, idx, score);
+        units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse);
   }
   return cudaGetLastError();
 }

@@ -25,7 +25,8 @@ def test_library_exports_every_declared_symbol():
     for name in decl:
         assert hasattr(L, name), name
     assert set(decl) == set(_pisa.EXPORTS)
-    assert L.pisa_version() == 1
+    hdr = int(re.search(r"#define PISA_VERSION (\d+)", open(os.path.join(ROOT, "include", "pisa.h")).read()).group(1))
+    assert L.pisa_version() == hdr == _pisa.ABI_VERSION
 
 
 @pytest.mark.parametrize("N,C", [(4096, 64), (65536, 64), (262144, 64), (1, 64), (65, 64), (130, 64)])
@@ -58,17 +59,19 @@ def test_host_validation_before_any_cuda_call():
         (pisa.make_shape(1, 4096, 4, 1, 64, 64, 8, scale=-1.0), _pisa.PISA_EINVAL, "scale"),
     ]
     for shape, code, text in cases:
-        rc, msg = _rc(L.pisa_select, ctypes.byref(shape), A, A, A, A, None, A, 1 << 40, None)
+        rc, msg = _rc(L.pisa_select, ctypes.byref(shape), A, A, A, A, None, None, A, 1 << 40, None)
         assert rc == code and text in msg, (rc, msg)
-    rc, msg = _rc(L.pisa_select, ctypes.byref(good), None, A, A, A, None, A, ws, None)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), None, A, A, A, None, None, A, ws, None)
     assert rc == _pisa.PISA_EINVAL and "Q is NULL" in msg
-    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A + 8, A, A, A, None, A, ws, None)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A + 8, A, A, A, None, None, A, ws, None)
     assert rc == _pisa.PISA_EINVAL and "aligned" in msg
-    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, A, ws - 1, None)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, None, A, ws - 1, None)
     assert rc == _pisa.PISA_EWORKSPACE
-    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, None, ws, None)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, None, None, ws, None)
     assert rc == _pisa.PISA_EWORKSPACE
-    rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, A, A, A, 1 << 40, None)
+    rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, A + 4, A, ws, None)
+    assert rc == _pisa.PISA_EINVAL and "head_lse" in msg
+    rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, None, A, A, A, 1 << 40, None)
     assert rc == _pisa.PISA_EINVAL and "V is NULL" in msg
     rc, msg = _rc(L.pisa_build_pyramid, None, A, A, None)
     assert rc == _pisa.PISA_EINVAL

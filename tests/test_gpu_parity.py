@@ -31,6 +31,13 @@ def _inputs(B, N, Hq, Hkv, d, needles, seed=0):
     return (Q, K, V), (Q.cuda(), K.cuda(), V.cuda())
 
 
+def _check_head_lse(got, want, what="head_lse"):
+    """Per-head leaf LSEs: -inf exactly on the padded slots, SCORE_ATOL elsewhere."""
+    assert np.array_equal(np.isneginf(got), np.isneginf(want)), what
+    f = np.isfinite(want)
+    check_close(got[f], want[f], atol=SCORE_ATOL, rtol=0, what=what)
+
+
 def _pyr_levels(pyr, shape):
     _, off, _ = pisa.pyramid_layout(shape)
     return off
@@ -53,11 +60,13 @@ def test_pyramid_select_flat_attention_vs_oracle(case):
                 cnt = np.array([po.node_range(l, m, C, N)[1] - po.node_range(l, m, C, N)[0] for m in range(len(S))])
                 got = pg[b, kv, off[l]:off[l] + len(S)]
                 assert np.all(np.abs(got - S) <= 1e-6 * cnt[:, None] + 1e-6 * np.abs(S)), (b, kv, l)
-    # A2-A4 selection
-    idx, score = pisa.select(Qg, Kg, pyr, shape)
+    # A2-A4 selection (with the per-head leaf terms, as the prefill path runs it)
+    idx, score, hl = pisa.select(Qg, Kg, pyr, shape, want_head_lse=True)
     idx4, score4 = pisa.select(Qg, Kg, pyr, pisa.make_shape(B, N, Hq, Hkv, d, C, K, qtile=4))
     torch.cuda.synchronize()
     assert torch.equal(idx, idx4) and torch.equal(score, score4)      # qtile is scheduling only
+    gi = idx.cpu().numpy()
+    _check_head_lse(hl.cpu().numpy(), po.selected_head_lse(Q, Kt, gi, C))
     ora = po.select(Q, Kt, C, K)
     st = check_selection(idx.cpu().numpy(), score.cpu().numpy(), ora, range(N), C, K, N)
     assert st["strict"] + st["exempt"] == st["units"]
@@ -66,12 +75,17 @@ def test_pyramid_select_flat_attention_vs_oracle(case):
     fidx, fscore = pisa.select_flat(Qg, Kg, pyr, shape)
     fora = po.select_flat(Q, Kt, C, K)
     check_selection(fidx.cpu().numpy(), fscore.cpu().numpy(), fora, range(N), C, K, N)
-    # A5 attention over the oracle's selection
+    # A5 attention over the oracle's selection (block LSEs computed by the call itself)
     oidx = torch.from_numpy(ora["idx"]).cuda()
     O, lse = pisa.sparse_attn_fwd(Qg, Kg, Vg, oidx, shape)
     Oref, lref = po.sparse_attn_fwd(Q, Kt, V, ora["idx"], C)
     check_close(O.float().cpu().numpy(), Oref, what="O")
     check_close(lse.cpu().numpy(), lref, atol=1e-3, rtol=0, what="lse")
+    # ... and over the GPU's own selection, normalised by the selection's head_lse
+    O2, lse2 = pisa.sparse_attn_fwd(Qg, Kg, Vg, idx, shape, head_lse=hl)
+    Oref2, lref2 = po.sparse_attn_fwd(Q, Kt, V, gi, C)
+    check_close(O2.float().cpu().numpy(), Oref2, what="O (head_lse)")
+    check_close(lse2.cpu().numpy(), lref2, atol=1e-3, rtol=0, what="lse (head_lse)")
 
 
 def test_select_is_independent_of_pyramid_height():
@@ -106,6 +120,11 @@ def test_attention_random_selection_vs_oracle():
     Oref, lref = po.sparse_attn_fwd(Q, Kt, V, idx.numpy(), C)
     check_close(O.float().cpu().numpy(), Oref, what="O")
     check_close(lse.cpu().numpy(), lref, atol=1e-3, rtol=0, what="lse")
+    # the same selection with caller-supplied block LSEs (the oracle's, rounded to fp32)
+    hl = torch.from_numpy(po.selected_head_lse(Q, Kt, idx.numpy(), C)).float().cuda()
+    O2, lse2 = pisa.sparse_attn_fwd(Qg, Kg, Vg, idx.cuda(), shape, head_lse=hl)
+    check_close(O2.float().cpu().numpy(), Oref, what="O (head_lse)")
+    check_close(lse2.cpu().numpy(), lref, atol=1e-3, rtol=0, what="lse (head_lse)")
 
 
 @pytest.mark.parametrize("name,Hq,Hkv,N", [("prefill_64k_gqa8", 16, 2, 65536), ("sweep_64k_gqa4", 32, 8, 65536)])
@@ -117,22 +136,26 @@ def test_full_size_sampled_vs_oracle(name, Hq, Hkv, N):
     (Q, Kt, V), (Qg, Kg, Vg) = _inputs(B, N, Hq, Hkv, d, True)
     shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, qtile=4)
     pyr = pisa.build_pyramid(Kg, shape)
-    idx, score = pisa.select(Qg, Kg, pyr, shape)
+    idx, score, hl = pisa.select(Qg, Kg, pyr, shape, want_head_lse=True)
     fidx, fscore = pisa.select_flat(Qg, Kg, pyr, shape)
-    O, lse = pisa.sparse_attn_fwd(Qg, Kg, Vg, idx, shape)
+    O, lse = pisa.sparse_attn_fwd(Qg, Kg, Vg, idx, shape, head_lse=hl)
+    O_own, lse_own = pisa.sparse_attn_fwd(Qg, Kg, Vg, idx, shape)     # block LSEs recomputed
     torch.cuda.synchronize()
     qs = sorted(set(range(0, N, 4099)) | {0, 1, 63, 64, 4095, 4096, N - 2, N - 1})
     ora = po.select(Q, Kt, C, K, queries=qs)
     gi = idx.cpu().numpy()
     check_selection(gi, score.cpu().numpy(), ora, qs, C, K, N)
+    hl_ref = po.selected_head_lse(Q, Kt, gi, C, queries=qs)
+    _check_head_lse(hl.cpu().numpy()[:, :, qs], hl_ref[:, :, qs])
     fora = po.select_flat(Q, Kt, C, K, queries=qs)
     check_selection(fidx.cpu().numpy(), fscore.cpu().numpy(), fora, qs, C, K, N)
     # attention of the GPU path's own selection, re-derived by the oracle from the oracle's
     # idx where they agree (exempt units are skipped)
     same = [i for i in qs if np.array_equal(gi[:, :, i], ora["idx"][:, :, i])]
     Oref, lref = po.sparse_attn_fwd(Q, Kt, V, ora["idx"], C, queries=same)
-    check_close(O.float().cpu().numpy()[:, same], Oref[:, same], what="O")
-    check_close(lse.cpu().numpy()[:, :, same], lref[:, :, same], atol=1e-3, rtol=0, what="lse")
+    for Og, lg, tag in ((O, lse, "head_lse"), (O_own, lse_own, "own LSE pass")):
+        check_close(Og.float().cpu().numpy()[:, same], Oref[:, same], what=f"O ({tag})")
+        check_close(lg.cpu().numpy()[:, :, same], lref[:, :, same], atol=1e-3, rtol=0, what=f"lse ({tag})")
 
 
 # ------------------------------------------------------------------------------- decode
