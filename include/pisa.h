@@ -28,7 +28,8 @@
  *    PISA_EWORKSPACE and enqueues nothing. A launch failure returns PISA_ECUDA. The text
  *    of the last error of the calling thread is returned by pisa_last_error().
  *  - Supported in this build: d in {64,128}, C = 64, g = 2, 1 <= K <= 32,
- *    G in {1,2,4,8}, 1 <= N <= 2^24. Anything else returns PISA_EUNSUPPORTED.
+ *    G in {1,2,4,8}, 1 <= N <= 2^24, B*Hkv*N*2K < 2^31 and B*N*Hq < 2^31. Anything else
+ *    returns PISA_EUNSUPPORTED.
  */
 #ifndef PISA_H_
 #define PISA_H_

@@ -49,6 +49,9 @@ int check_common(int B, int N, int Hq, int Hkv, int d, int C, int K, int g) {
   const int64_t pairs = static_cast<int64_t>(B) * Hkv * N * 2 * K;
   if (pairs >= (int64_t(1) << 31))
     return fail(PISA_EUNSUPPORTED, "B*Hkv*N*2K=%lld exceeds 2^31", static_cast<long long>(pairs));
+  const int64_t rows = static_cast<int64_t>(B) * N * Hq;   // TMA row coordinates are int32
+  if (rows >= (int64_t(1) << 31))
+    return fail(PISA_EUNSUPPORTED, "B*N*Hq=%lld exceeds 2^31", static_cast<long long>(rows));
   return PISA_OK;
 }
 

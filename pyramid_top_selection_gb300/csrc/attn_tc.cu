@@ -1,247 +1,335 @@
-// Causal block-sparse attention forward on the fifth-generation tensor cores (tcgen05).
+// Block-major tensor-core kernels (tcgen05) over grouped (leaf block, query) pairs: the
+// sparse attention forward, its block-LSE pass, and the stage-2 exact leaf scoring.
 //
 // "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference value
-// of the work": queries that use the same leaf key block are grouped into tiles so the
-// block's keys are read once per tile, and attention runs only over the selected blocks.
+// of the work" and "Method key points": queries that use the same leaf key block are
+// grouped into tiles so the block's keys are read once per tile; leaves are scored by the
+// exact LSE over their raw keys (the G heads of a KV head sum their LSEs), and attention
+// runs only over the selected blocks.
 //
-// The softmax normaliser of row (query i, head h) is lse = log sum_k exp(lse_k) over the
-// LSEs lse_k of its selected blocks, which the selection already computed exactly (they
-// are the per-head terms of its leaf scores). With lse known before any key is visited,
-// every block's contribution exp(s q.k - lse) v is already final: the blocks of a row are
-// summed, not merged, so they can be added straight into an fp32 accumulator in any order.
+// Attention normaliser. Row (query i, head h) has lse = log sum_k exp(lse_k) over the LSEs
+// lse_k of its selected blocks, which the selection already computed exactly (the per-head
+// terms of its leaf scores). With lse known before any key is visited, every block's
+// contribution exp(s q.k - lse) v is final: the blocks of a row are summed, not merged, and
+// go straight into an fp32 accumulator in any order.
 //
-// One CTA takes one work item (a leaf block of one KV head and up to 2048 (query, head)
-// rows that selected it) in tiles of 128 rows:
-//   * the item's pair list is staged in shared memory; the leaf's K (64 x d) and V^T
-//     (d x 64) are staged once in the K-major 128-byte-swizzled layout;
-//   * the next tile's 128 query rows are gathered with cp.async into the other half of a
-//     double-buffered Q tile while the current tile computes;
-//   * S = Q K^T (M=128, N=64) and O = P V (M=128, N=d) run as tcgen05.mma issued by one
-//     thread, accumulating in TMEM; completion is tracked with mbarriers;
-//   * each thread owns one row: it reads its S row from TMEM, applies the causal mask,
-//     P = exp(s S - lse) (bf16) goes into the first K-block of the current Q buffer (Q is
-//     no longer needed once S is done); after P V, the thread copies its O row, 64 columns
-//     at a time, into a padded staging row in that same buffer and hands it to the TMA
-//     unit as one bulk fp32 reduce-add into the accumulator (coalesced 256-byte requests
-//     instead of 32 rows per warp store; the accumulator rows of a query chunk stay in L2).
-// The LSE mode runs the same tiles through S only and writes every (row, block) LSE, for
-// callers that do not pass the selection's. Every mbarrier wait is bounded: if one gives
-// up, the kernel records PISA_ETIMEOUT in the status word, lets its outstanding copies
-// finish, frees its TMEM and returns.
+// One CTA (8 warps) takes one work item: a leaf block of one KV head and up to 2048
+// (query, head) rows that chose it, in tiles of 128 rows (row = TMEM lane; the two
+// warpgroups split the columns of every tile):
+//   * the leaf's K (64 x d) arrives by TMA tile load, V^T (d x 64) is transposed by the
+//     threads once per item, both in the K-major 128-byte-swizzled layout;
+//   * the tiles' query rows are gathered with cp.async (each thread copies half a row) into
+//     a double-buffered Q tile; a thread confirms its copies of a tile one tile later
+//     (wait, proxy fence, mbarrier arrival), so the MMA issuer never waits on a fresh copy;
+//   * S = Q K^T (M=128, N=64) into one of two TMEM buffers, issued for the next tile as soon
+//     as its rows have landed, so it overlaps this tile's softmax; O = P V (M=128, N=d);
+//   * output mode: P = 2^(s log2(e) S - log2(e) lse) on the visible keys (bf16, into the
+//     free first K-block of the tile's Q buffer); after P V, each warpgroup moves its half
+//     of O through a swizzled staging tile in the same buffer, and one lane per query adds
+//     its G heads x 32 columns into the accumulator with a single TMA tensor reduce-add;
+//   * LSE and leaf modes stop after S: each warpgroup reduces its 32 columns to a (max,
+//     sum) pair, the halves merge in shared memory, and the row LSE is written per (row,
+//     block) or, summed over the G heads of its query (adjacent lanes), per (query, leaf).
+// Every mbarrier wait is bounded: if one gives up, the kernel records PISA_ETIMEOUT in the
+// status word, lets its outstanding copies finish, frees its TMEM and returns.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace pisa {
 
 namespace {
 
+constexpr int kThreads = 256;
 constexpr int kRows = 128;
 constexpr int kMaxItem = 1024;       // entries per work item (queries)
-constexpr int kModeLse = 0, kModeOut = 1;
+constexpr int kModeLse = 0, kModeOut = 1, kModeLeaf = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int round1024(int x) { return (x + 1023) / 1024 * 1024; }
 constexpr int imax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int MODE>
-struct TcFwdSmem {
+struct TcSmem {
   static constexpr int KB = D / 64;                 // K-blocks along the head dim
   static constexpr int Q_BYTES = KB * kRows * 128;  // one Q tile
-  static constexpr int STG_ROW = 64 * 4 + 16;       // 64 fp32 of an O row + 16 B (no bank conflicts)
-  static constexpr int BUF = MODE == kModeOut ? round1024(imax(Q_BYTES, kRows * STG_ROW)) : Q_BYTES;
+  static constexpr int STAGE = kRows * 128;         // one warpgroup's 32-column fp32 staging tile
+  static constexpr int BUF = MODE == kModeOut ? imax(Q_BYTES, 2 * STAGE) : Q_BYTES;
   static constexpr int K_BYTES = KB * 64 * 128;
   static constexpr int V_BYTES = MODE == kModeOut ? D * 128 : 0;   // V^T: D rows of 64 keys
   static constexpr int oQ0 = 0, oK = 2 * BUF, oV = oK + K_BYTES;
   static constexpr int bytes = oV + V_BYTES + 1024; // + alignment slack
-  static constexpr int tmem_cols = MODE == kModeOut ? ((64 + D) <= 128 ? 128 : 256) : 64;
+  // TMEM: S0 | S1 (64 columns each) | O (D columns)
+  static constexpr int tmem_cols = MODE == kModeOut ? 256 : 128;
+};
+
+struct TcArgs {
+  Dims s;
+  GroupPlan gp;
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* V;
+  const int32_t* list;
+  const int4* items;
+  const int32_t* n_items;
+  const float* lse_rows;   // output mode: [B,Hq,N]
+  float* out;              // LSE mode: block LSE [B,Hq,N,K]; leaf mode: scores [heads,N,W]
+  float* out_head;         // leaf mode: per-head terms [heads,N,W,G] (may be NULL)
+  int W;                   // slots per query unit (K, or 2K for the leaf candidates)
+  int32_t* status;
 };
 
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kRows, 1)
-attn_fwd_tc_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
-                   const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-                   const int32_t* __restrict__ list, const int4* __restrict__ items,
-                   const int32_t* __restrict__ n_items, const float* __restrict__ lse_rows,
-                   float* __restrict__ block_lse, float* __restrict__ o_acc, int32_t* status) {
-  using L = TcFwdSmem<D, MODE>;
+__global__ void __launch_bounds__(kThreads, 2)
+block_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap) {
+  using L = TcSmem<D, MODE>;
   constexpr int EPT = kRows / G;          // entries (queries) per tile
-  constexpr int CH = D / 8;               // 16-byte chunks per row
+  constexpr int KB = L::KB;
+  constexpr int HC = D / 16;              // 16-byte chunks per half row
   extern __shared__ unsigned char smraw[];
-  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_k, bar_o;
   __shared__ uint32_t tmem_base;
   __shared__ int s_list[kMaxItem];        // the item's (query << 6 | slot) entries
-  __shared__ int s_abort;
+  __shared__ float2 s_ml[2][kRows];       // LSE/leaf: the second warpgroup's (max, sum) per row
 
-  if (static_cast<int>(blockIdx.x) >= *n_items) return;
-  const int4 item = items[blockIdx.x];
+  const Dims& s = a.s;
+  if (static_cast<int>(blockIdx.x) >= *a.n_items) return;
+  const int4 item = a.items[blockIdx.x];
   const int beg = item.y, n_ent = item.z;
-  const int t = gp.leaf_of(item.x);
-  const int64_t head = gp.head_of(item.x);
+  const int t = a.gp.leaf_of(item.x);
+  const int64_t head = a.gp.head_of(item.x);
   const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;                       // column half of every tile
+  const int r = (warp & 3) * 32 + lane;           // tile row = TMEM lane
+  const int h = r % G;
   const int kbase = t * 64;
   const int n_tiles = (n_ent + EPT - 1) / EPT;
 
   unsigned char* sm = smraw + ((1024 - (tc::su32(smraw) & 1023)) & 1023);
-  const uint32_t aQ0 = tc::su32(sm + L::oQ0);     // Q buffer `buf` starts at aQ0 + buf * BUF
+  const uint32_t aQ0 = tc::su32(sm + L::oQ0);     // Q buffer `bf` starts at aQ0 + bf * BUF
   const uint32_t aK = tc::su32(sm + L::oK), aV = tc::su32(sm + L::oV);
   constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
 
   if (tid == 0) {
-    tc::bar_init(&bar[0], 1);
-    tc::bar_init(&bar[1], 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::bar_init(&bar_q[k], kThreads);   // every thread confirms its copies
+      tc::bar_init(&bar_s[k], 1);
+    }
+    tc::bar_init(&bar_k, 1);
+    tc::bar_init(&bar_o, 1);
     tc::fence_bar_init();
-    s_abort = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, L::tmem_cols);
-  for (int e = tid; e < n_ent; e += kRows) s_list[e] = list[beg + e];
-  // entry e of tile j: query s_list[j*EPT + e] >> 6, slot & 63 (query -1 past the end)
-  auto entry_query = [&](int j, int e) {
-    const int ge = j * EPT + e;
-    return ge < n_ent ? (s_list[ge] >> 6) : -1;
-  };
-  auto gather_q = [&](int j, int buf) {
-    const uint32_t dstb = aQ0 + buf * L::BUF;
-    for (int lin = tid; lin < kRows * CH; lin += kRows) {
-      const int r = lin / CH, c = lin % CH;
-      const int i = entry_query(j, r / G);
-      const __nv_bfloat16* src =
-          Q + ((static_cast<int64_t>(b) * s.N + (i < 0 ? 0 : i)) * s.Hq + kv * G + (r % G)) * D + c * 8;
-      tc::cp_async16(dstb + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8), src, i >= 0);
-    }
-  };
-  __syncthreads();
-  gather_q(0, 0);
-  // leaf K tile (async) and V^T, transposed by the threads (lanes walk keys: no bank conflicts)
-  for (int lin = tid; lin < 64 * CH; lin += kRows) {
-    const int r = lin / CH, c = lin % CH;
-    const int64_t j = static_cast<int64_t>(kbase) + r;
-    const bool ok = j < s.N;
-    const __nv_bfloat16* src = K + ((static_cast<int64_t>(b) * s.N + (ok ? j : 0)) * s.Hkv + kv) * D + c * 8;
-    tc::cp_async16(aK + (c >> 3) * (64 * 128) + tc::sw128(r, (c & 7) * 8), src, ok);
-  }
-  tc::cp_async_commit();
-  if constexpr (MODE == kModeOut) {
-    for (int lin = tid; lin < 64 * CH; lin += kRows) {
-      const int r = lin % 64, c = lin / 64;   // key r, dims c*8 .. c*8+7
-      const int64_t j = static_cast<int64_t>(kbase) + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (j < s.N) v = ldg_u4(V + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<__nv_bfloat16*>(sm + L::oV + tc::sw128(c * 8 + u, r)) = e[u];
-    }
-  }
+  for (int e = tid; e < n_ent; e += kThreads) s_list[e] = a.list[beg + e];
   tc::before_sync();
   __syncthreads();
   tc::after_sync();
-  const uint32_t tS = tmem_base, tO = tmem_base + 64;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const int r = tid, h = r % G;
 
-  for (int jt = 0; jt < n_tiles; ++jt) {
-    const int buf = jt & 1;
-    const uint32_t aQb = aQ0 + buf * L::BUF;
-    // prefetch the next tile's rows into the other buffer (its last readers, the previous
-    // tile's MMAs and bulk reductions, have completed)
-    if (jt + 1 < n_tiles) gather_q(jt + 1, buf ^ 1);
+  // query of row rr of tile j (-1 past the end of the item)
+  auto query_of = [&](int j, int rr) {
+    const int e = j * EPT + rr / G;
+    return e < n_ent ? (s_list[e] >> 6) : -1;
+  };
+  bool bad = false;                 // this thread saw a bounded wait give up
+  // all threads: cp.async of tile j's 128 query rows into Q buffer bf, one commit group;
+  // thread t copies half row t >> 1 (zero-filled past the end of the item)
+  auto gather = [&](int j, int bf) {
+    const int rr = tid >> 1, qi = query_of(j, rr);
+    const __nv_bfloat16* src =
+        a.Q + ((static_cast<int64_t>(b) * s.N + (qi < 0 ? 0 : qi)) * s.Hq + kv * G + rr % G) * D;
+    const uint32_t dst = aQ0 + bf * L::BUF;
+#pragma unroll
+    for (int u = 0; u < HC; ++u) {
+      const int c = (tid & 1) * HC + u;
+      tc::cp_async16(dst + (c >> 3) * (kRows * 128) + tc::sw128(rr, (c & 7) * 8), src + c * 8, qi >= 0);
+    }
     tc::cp_async_commit();
-    tc::cp_async_wait<1>();              // this tile's rows (and the K tile) have landed
+  };
+  // this thread's copies of the tile in buffer bf have landed (all but `newer` groups):
+  // make them visible to the tensor cores and arrive on the buffer's barrier
+  auto confirm = [&](int bf, bool newer) {
+    if (newer) tc::cp_async_wait<1>(); else tc::cp_async_wait<0>();
+    tc::fence_async_smem();
+    tc::bar_arrive(&bar_q[bf]);
+  };
+  // thread 0: S(j) = Q(j) K^T into TMEM buffer j & 1, once tile j's rows (and K) have landed
+  auto issue_s = [&](int j) {
+    const int bf = j & 1;
+    bool ok = tc::bar_wait(&bar_q[bf], (j >> 1) & 1);
+    if (j == 0) ok = tc::bar_wait(&bar_k, 0) && ok;
+    if (!ok) bad = true;
+    tc::after_sync();
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+      tc::mma(tmem_base + 64 * bf, tc::desc(aQ0 + bf * L::BUF + (ks >> 2) * (kRows * 128) + (ks & 3) * 32),
+              tc::desc(aK + (ks >> 2) * (64 * 128) + (ks & 3) * 32), idS, ks > 0);
+    tc::commit(&bar_s[bf]);
+  };
+
+  if (tid == 0) {
+    tc::bar_expect_tx(&bar_k, L::K_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) tc::tma_load4(aK + kb * (64 * 128), &kmap, kb * 64, kv, kbase, b, &bar_k);
+  }
+  gather(0, 0);
+  if (n_tiles > 1) gather(1, 1);
+  confirm(0, n_tiles > 1);
+  if constexpr (MODE == kModeOut) {
+    // V^T, transposed by the threads (lanes walk keys: no bank conflicts); rows past N are 0
+    for (int lin = tid; lin < 64 * (D / 8); lin += kThreads) {
+      const int key = lin % 64, c = lin / 64;   // dims c*8 .. c*8+7
+      const int64_t j = static_cast<int64_t>(kbase) + key;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (j < s.N) v = ldg_u4(a.V + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<__nv_bfloat16*>(sm + L::oV + tc::sw128(c * 8 + u, key)) = e[u];
+    }
     tc::fence_async_smem();
     tc::before_sync();
     __syncthreads();
-    if (tid == 0) {
-      tc::after_sync();
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        tc::mma(tS, tc::desc(aQb + (ks >> 2) * (kRows * 128) + (ks & 3) * 32),
-                tc::desc(aK + (ks >> 2) * (64 * 128) + (ks & 3) * 32), idS, ks > 0);
-      tc::commit(&bar[0]);
-    }
-    const int qi = entry_query(jt, r / G);
-    const int64_t lrow_at = (static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + (qi < 0 ? 0 : qi);
-    float lrow = 0.f;
-    if (MODE == kModeOut && qi >= 0) lrow = lse_rows[lrow_at];   // in flight during the MMA
-    if (!tc::bar_wait(&bar[0], jt & 1)) atomicOr(&s_abort, 1);
+  }
+  if (tid == 0) issue_s(0);
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const float c1 = s.scale * kLog2e;              // logits in base-2 units
+
+  for (int jt = 0; jt < n_tiles; ++jt) {
+    const int bf = jt & 1;
+    const int qi = query_of(jt, r);
+    const int lim = qi - kbase - 32 * wg;        // this half's column c is visible iff c <= lim
+    const int slot = qi >= 0 ? (s_list[jt * EPT + r / G] & 63) : 0;
+    float lrow2 = 0.f;
+    if (MODE == kModeOut && qi >= 0)               // in flight during the MMA wait
+      lrow2 = a.lse_rows[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + qi] * kLog2e;
+    if (!tc::bar_wait(&bar_s[bf], (jt >> 1) & 1)) bad = true;
     tc::after_sync();
-    float sv[64];
-    tc::tmem_ld64(tS + lane_off, sv);
-    if constexpr (MODE == kModeLse) {
-      float mx = neg_inf(), l = 0.f;
+
+    if constexpr (MODE != kModeOut) {
+      // Q[bf] is free (S(jt) is done): tile jt+2's rows go there; tile jt+1's rows (copied
+      // one tile ago) are confirmed and S(jt+1) starts now
+      if (jt + 2 < n_tiles) gather(jt + 2, bf);
+      if (jt + 1 < n_tiles) confirm(bf ^ 1, jt + 2 < n_tiles);
+      if (tid == 0 && jt + 1 < n_tiles) issue_s(jt + 1);
+      float sv[32];
+      tc::tmem_ld32(tmem_base + 64 * bf + 32 * wg + lane_off, sv);
+      float mx = -INFINITY;
+      if (lim >= 31) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        sv[c] = (kbase + c <= qi) ? s.scale * sv[c] : neg_inf();
-        mx = fmaxf(mx, sv[c]);
-      }
-      const float m = mx == neg_inf() ? 0.f : mx;
+        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, sv[c]);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) l += expf(sv[c] - m);
-      if (qi >= 0)
-        block_lse[lrow_at * s.K + (s_list[jt * EPT + r / G] & 63)] = l > 0.f ? m + logf(l) : neg_inf();
-      tc::before_sync();
-      __syncthreads();
-      if (s_abort) break;
-    } else {
-      // P = exp(s S - lse) on the visible keys; into the (now free) first K-block of Q[buf]
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float pv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = cc * 8 + u;
-          pv[u] = (kbase + c <= qi) ? expf(fmaf(s.scale, sv[c], -lrow)) : 0.f;
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = c <= lim ? sv[c] : -INFINITY;
+          mx = fmaxf(mx, sv[c]);
         }
-        uint4 pk;
-        pk.x = pack_bf16(pv[0], pv[1]);
-        pk.y = pack_bf16(pv[2], pv[3]);
-        pk.z = pack_bf16(pv[4], pv[5]);
-        pk.w = pack_bf16(pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(sm + L::oQ0 + buf * L::BUF + tc::sw128(r, cc * 8)) = pk;
       }
+      float l = 0.f, m2 = -INFINITY;
+      if (mx != -INFINITY) {
+        m2 = mx * c1;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) l += tc::ex2(fmaf(sv[c], c1, -m2));
+      }
+      if (wg == 1) s_ml[bf][r] = make_float2(m2, l);
+      tc::before_sync();
+      const bool stop = __syncthreads_or(bad);
+      if (wg == 0 && !stop) {
+        const float2 o = s_ml[bf][r];
+        const float M = fmaxf(m2, o.x);
+        float lse = -INFINITY;
+        if (M != -INFINITY) {
+          const float Lsum = l * tc::ex2(m2 - M) + o.y * tc::ex2(o.x - M);
+          lse = (M + tc::lg2(Lsum)) * kLn2;
+        }
+        if constexpr (MODE == kModeLse) {
+          if (qi >= 0)
+            a.out[((static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + qi) * s.K + slot] = lse;
+        } else {
+          // sum over the G heads of the query: G adjacent lanes (padding entries are whole)
+          float sum = lse;
+#pragma unroll
+          for (int o2 = 1; o2 < G; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+          if (qi >= 0) {
+            const int64_t at = (head * s.N + qi) * a.W + slot;
+            if (h == 0) a.out[at] = sum;
+            if (a.out_head) a.out_head[at * G + h] = lse;
+          }
+        }
+      }
+      if (stop) break;
+    } else {
+      // P = 2^(c1 S - log2e lse) on the visible keys, this half's 32 keys of the row, into
+      // the first K-block of Q[bf]
+      float sv[32];
+      tc::tmem_ld32(tmem_base + 64 * bf + 32 * wg + lane_off, sv);
+      if (lim >= 31) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = tc::ex2(fmaf(sv[c], c1, -lrow2));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = c <= lim ? tc::ex2(fmaf(sv[c], c1, -lrow2)) : 0.f;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint4 pk;
+        pk.x = pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]);
+        pk.y = pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]);
+        pk.z = pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]);
+        pk.w = pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]);
+        *reinterpret_cast<uint4*>(sm + L::oQ0 + bf * L::BUF + tc::sw128(r, 32 * wg + cc * 8)) = pk;
+      }
+      if (jt + 1 < n_tiles) confirm(bf ^ 1, false);   // tile jt+1's rows, copied last tile
       tc::fence_async_smem();
       tc::before_sync();
-      __syncthreads();
-      if (s_abort) break;
+      if (__syncthreads_or(bad)) break;
       if (tid == 0) {
         tc::after_sync();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma(tO, tc::desc(aQb + kk * 32), tc::desc(aV + kk * 32), idO, kk > 0);
-        tc::commit(&bar[1]);
+          tc::mma(tmem_base + 128, tc::desc(aQ0 + bf * L::BUF + kk * 32), tc::desc(aV + kk * 32), idO, kk > 0);
+        tc::commit(&bar_o);
+        if (jt + 1 < n_tiles) issue_s(jt + 1);   // overlaps this tile's epilogue
       }
-      if (!tc::bar_wait(&bar[1], jt & 1)) atomicOr(&s_abort, 1);
+      if (!tc::bar_wait(&bar_o, jt & 1)) bad = true;
       tc::after_sync();
-      // epilogue: the O row, 64 columns at a time, through this thread's staging row in the
-      // now free Q[buf] and one bulk reduce-add each into the accumulator row
-      const int64_t row = (static_cast<int64_t>(b) * s.N + (qi < 0 ? 0 : qi)) * s.Hq + kv * G + h;
-      float4* stg = reinterpret_cast<float4*>(sm + L::oQ0 + buf * L::BUF + r * L::STG_ROW);
-      const uint32_t a_stg = tc::su32(stg);
+      // epilogue: this warpgroup's D/2 columns in rounds of 32 through its staging tile
+      // (row r at +128 r, 16-byte chunks swizzled by r & 7); the lane holding a query's
+      // first head adds the query's G x 32 box into the accumulator
+      const uint32_t stg = aQ0 + bf * L::BUF + wg * L::STAGE;
+      unsigned char* stg_p = sm + L::oQ0 + bf * L::BUF + wg * L::STAGE;
+      const bool issuer = h == 0 && qi >= 0;
+      const int unit = (b * s.N + (qi < 0 ? 0 : qi)) * s.Hkv + kv;
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        float ov[64];
-        tc::tmem_ld64(tO + lane_off + half * 64, ov);
-        if (half > 0) tc::bulk_wait_read<0>();      // the staging row was read out
+      for (int rd = 0; rd < D / 64; ++rd) {
+        const int c0 = wg * (D / 2) + 32 * rd;
+        float ov[32];
+        tc::tmem_ld32(tmem_base + 128 + c0 + lane_off, ov);
+        if (rd > 0) {
+          if (issuer) tc::bulk_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) stg[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(stg_p + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
         tc::fence_async_smem();
-        if (qi >= 0) {
-          tc::bulk_reduce_add_f32(o_acc + row * D + half * 64, a_stg, 256);
+        __syncwarp();
+        if (issuer) {
+          tc::tma_reduce_add3(&omap, c0, 0, unit, stg + r * 128);
           tc::bulk_commit();
         }
       }
-      tc::bulk_wait_read<0>();                     // Q[buf] is gathered into again next tile
+      if (issuer) tc::bulk_wait_read<0>();          // Q[bf] is gathered into again below
       tc::before_sync();
-      __syncthreads();
-      if (s_abort) break;
+      if (__syncthreads_or(bad)) break;
+      if (jt + 2 < n_tiles) gather(jt + 2, bf);
     }
   }
-  tc::cp_async_wait<0>();
+  tc::cp_async_wait<0>();                          // copies still in flight after an abort
   tc::bulk_wait<0>();                              // reductions complete before exit
   tc::before_sync();
-  __syncthreads();
-  if (s_abort && tid == 0) atomicOr(status, PISA_ETIMEOUT);
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, PISA_ETIMEOUT);
   if (warp == 0) tc::tmem_free(tmem_base, L::tmem_cols);
 }
 
@@ -280,48 +368,80 @@ attn_out_kernel(int64_t n8, const float4* __restrict__ o_acc, uint4* __restrict_
   }
 }
 
+// Tensor maps: K as 4-D [B, N, Hkv, d] (boxes of 64 tokens x 64 of one KV head), the
+// accumulator as 3-D [B*N*Hkv, G, d] fp32 (boxes of one query's G heads x 32 columns).
+int make_maps(const Dims& s, const void* K, const float* o_acc, CUtensorMap* km, CUtensorMap* om) {
+  const uint64_t d = static_cast<uint64_t>(s.d);
+  {
+    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv), static_cast<uint64_t>(s.N),
+                              static_cast<uint64_t>(s.B)};
+    const uint64_t st[3] = {d * 2, d * 2 * s.Hkv, d * 2 * s.Hkv * s.N};
+    const uint32_t box[4] = {64, 1, 64, 1};
+    if (int e = encode_tmap(km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, st, box)) return e;
+  }
+  if (o_acc) {
+    const uint64_t dims[3] = {d, static_cast<uint64_t>(s.G), static_cast<uint64_t>(s.B) * s.N * s.Hkv};
+    const uint64_t st[2] = {d * 4, d * 4 * s.G};
+    const uint32_t box[3] = {32, static_cast<uint32_t>(s.G), 1};
+    if (int e = encode_tmap(om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o_acc, dims, st, box)) return e;
+  } else {
+    *om = *km;                                      // not read outside the output mode
+  }
+  return 0;
+}
+
 template <int D, int G, int MODE>
-int tc_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
-              const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
-              float* block_lse, float* o_acc, int32_t* status, cudaStream_t st) {
-  const int smem = TcFwdSmem<D, MODE>::bytes;
+int tc_launch(const TcArgs& a, const CUtensorMap& km, const CUtensorMap& om, const char* name, cudaStream_t st) {
+  const int smem = TcSmem<D, MODE>::bytes;
   cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_tc_kernel<D, G, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(block_tc_kernel<D, G, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  ProfScope ps(st, MODE == kModeOut ? "attn_fwd_tc" : "attn_lse_tc");
-  attn_fwd_tc_kernel<D, G, MODE><<<static_cast<unsigned>(gp.max_items), kRows, smem, st>>>(
-      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
-      static_cast<const __nv_bfloat16*>(V), list, items, n_items, lse_rows, block_lse, o_acc, status);
+  ProfScope ps(st, name);
+  block_tc_kernel<D, G, MODE><<<static_cast<unsigned>(a.gp.max_items), kThreads, smem, st>>>(a, km, om);
   return cudaGetLastError();
 }
 
 template <int MODE>
-int tc_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
-                const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
-                float* block_lse, float* o_acc, int32_t* status, cudaStream_t st) {
-#define PISA_TC_CASE(DD, GG)                                                                          \
-  if (s.d == DD && s.G == GG)                                                                         \
-    return tc_launch<DD, GG, MODE>(s, gp, Q, K, V, list, items, n_items, lse_rows, block_lse, o_acc, \
-                                   status, st);
+int tc_dispatch(const TcArgs& a, const CUtensorMap& km, const CUtensorMap& om, const char* name, cudaStream_t st) {
+#define PISA_TC_CASE(DD, GG) \
+  if (a.s.d == DD && a.s.G == GG) return tc_launch<DD, GG, MODE>(a, km, om, name, st);
   PISA_TC_CASE(128, 1) PISA_TC_CASE(128, 2) PISA_TC_CASE(128, 4) PISA_TC_CASE(128, 8)
   PISA_TC_CASE(64, 1) PISA_TC_CASE(64, 2) PISA_TC_CASE(64, 4) PISA_TC_CASE(64, 8)
 #undef PISA_TC_CASE
   return static_cast<int>(cudaErrorNotSupported);
 }
 
+TcArgs base_args(const Dims& s, const GroupPlan& gp, const void* Q, const int32_t* list, const int4* items,
+                 const int32_t* n_items, int32_t* status) {
+  TcArgs a{};
+  a.s = s;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.gp = gp;
+  a.list = list;
+  a.items = items;
+  a.n_items = n_items;
+  a.status = status;
+  a.W = s.K;
+  return a;
+}
+
 }  // namespace
 
-// Tensor-core forward for d in {64, 128} and G in {1, 2, 4, 8}: [block LSE pass when
+// Attention forward for d in {64, 128} and G in {1, 2, 4, 8}: [block LSE pass when
 // head_lse is NULL] -> row LSE + accumulator clear -> output pass -> bf16 conversion.
 int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
                        const float* head_lse, float* block_lse_ws, float* o_acc, void* O, float* lse,
                        int32_t* status, cudaStream_t st) {
+  CUtensorMap km, om;
+  int err = make_maps(s, K, o_acc, &km, &om);
+  if (err) return err;
+  TcArgs a = base_args(s, gp, Q, list, items, n_items, status);
+  a.V = static_cast<const __nv_bfloat16*>(V);
   const float* hl = head_lse;
-  int err;
   if (!hl) {
-    err = tc_dispatch<kModeLse>(s, gp, Q, K, V, list, items, n_items, nullptr, block_lse_ws, nullptr, status, st);
-    if (err) return err;
+    a.out = block_lse_ws;
+    if ((err = tc_dispatch<kModeLse>(a, km, om, "attn_lse_tc", st))) return err;
     hl = block_lse_ws;
   }
   const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
@@ -335,8 +455,9 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
           s, idx, hl, lse, reinterpret_cast<float4*>(o_acc));
   }
   if ((err = cudaGetLastError())) return err;
-  err = tc_dispatch<kModeOut>(s, gp, Q, K, V, list, items, n_items, lse, nullptr, o_acc, status, st);
-  if (err) return err;
+  a.lse_rows = lse;
+  a.out = nullptr;
+  if ((err = tc_dispatch<kModeOut>(a, km, om, "attn_fwd_tc", st))) return err;
   {
     ProfScope ps(st, "attn_out");
     const int64_t n8 = rows * s.d / 8;
@@ -345,6 +466,21 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
         n8, reinterpret_cast<const float4*>(o_acc), static_cast<uint4*>(O));
   }
   return cudaGetLastError();
+}
+
+// Stage-2 exact leaf scores of the grouped (candidate leaf, query) pairs: score[unit, slot]
+// = sum over the G heads of the leaf's LSE; per-head terms into pair_head when given.
+int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                   int32_t* status, cudaStream_t st) {
+  CUtensorMap km, om;
+  int err = make_maps(s, K, nullptr, &km, &om);
+  if (err) return err;
+  TcArgs a = base_args(s, gp, Q, list, items, n_items, status);
+  a.out = pair_score;
+  a.out_head = pair_head;
+  a.W = W;
+  return tc_dispatch<kModeLeaf>(a, km, om, "leaf_score", st);
 }
 
 }  // namespace pisa
