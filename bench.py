@@ -205,9 +205,9 @@ def algorithmic(kernel, cfg, idx_host=None):
         units = keys * G
         per = 2 * d
         return "tensor", units * per, "flops", units, per
-    if kernel == "attn_rows":   # K block LSEs + K indices read, lse written, accumulator cleared
+    if kernel == "attn_rows":   # K block LSEs + K indices read, lse written
         units = B * N * Hq
-        per = K * 4 + K * 4 / G + 4 + d * 4
+        per = K * 4 + K * 4 / G + 4
         return "hbm", units * per, "bytes", units, per
     if kernel == "attn_out":    # fp32 accumulator read, bf16 O written
         units = B * N * Hq

@@ -1,11 +1,9 @@
-// Block-major tensor-core kernels (tcgen05) over grouped (leaf block, query) pairs: the
-// sparse attention forward, its block-LSE pass, and the stage-2 exact leaf scoring.
+// Causal block-sparse attention forward on the fifth-generation tensor cores (tcgen05), and
+// its block-LSE pass.
 //
 // "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference value
-// of the work" and "Method key points": queries that use the same leaf key block are
-// grouped into tiles so the block's keys are read once per tile; leaves are scored by the
-// exact LSE over their raw keys (the G heads of a KV head sum their LSEs), and attention
-// runs only over the selected blocks.
+// of the work": queries that use the same leaf key block are grouped into tiles so the
+// block's keys are read once per tile, and attention runs only over the selected blocks.
 //
 // Attention normaliser. Row (query i, head h) has lse = log sum_k exp(lse_k) over the LSEs
 // lse_k of its selected blocks, which the selection already computed exactly (the per-head
@@ -27,9 +25,9 @@
 //     free first K-block of the tile's Q buffer); after P V, each warpgroup moves its half
 //     of O through a swizzled staging tile in the same buffer, and one lane per query adds
 //     its G heads x 32 columns into the accumulator with a single TMA tensor reduce-add;
-//   * LSE and leaf modes stop after S: each warpgroup reduces its 32 columns to a (max,
-//     sum) pair, the halves merge in shared memory, and the row LSE is written per (row,
-//     block) or, summed over the G heads of its query (adjacent lanes), per (query, leaf).
+//   * the LSE mode (for callers without the selection's LSEs) stops after S: each
+//     warpgroup reduces its 32 columns to a (max, sum) pair, the halves merge in shared
+//     memory, and the row LSE is written per (row, block).
 // Every mbarrier wait is bounded: if one gives up, the kernel records PISA_ETIMEOUT in the
 // status word, lets its outstanding copies finish, frees its TMEM and returns.
 #include "device.cuh"
@@ -45,7 +43,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 128;
 constexpr int kMaxItem = 1024;       // entries per work item (queries)
-constexpr int kModeLse = 0, kModeOut = 1, kModeLeaf = 2;
+constexpr int kModeLse = 0, kModeOut = 1;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -74,9 +72,7 @@ struct TcArgs {
   const int4* items;
   const int32_t* n_items;
   const float* lse_rows;   // output mode: [B,Hq,N]
-  float* out;              // LSE mode: block LSE [B,Hq,N,K]; leaf mode: scores [heads,N,W]
-  float* out_head;         // leaf mode: per-head terms [heads,N,W,G] (may be NULL)
-  int W;                   // slots per query unit (K, or 2K for the leaf candidates)
+  float* out;              // LSE mode: block LSE [B,Hq,N,K]
   int32_t* status;
 };
 
@@ -91,7 +87,7 @@ block_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const 
   __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_k, bar_o;
   __shared__ uint32_t tmem_base;
   __shared__ int s_list[kMaxItem];        // the item's (query << 6 | slot) entries
-  __shared__ float2 s_ml[2][kRows];       // LSE/leaf: the second warpgroup's (max, sum) per row
+  __shared__ float2 s_ml[2][kRows];       // LSE mode: the second warpgroup's (max, sum) per row
 
   const Dims& s = a.s;
   if (static_cast<int>(blockIdx.x) >= *a.n_items) return;
@@ -206,7 +202,7 @@ block_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const 
     if (!tc::bar_wait(&bar_s[bf], (jt >> 1) & 1)) bad = true;
     tc::after_sync();
 
-    if constexpr (MODE != kModeOut) {
+    if constexpr (MODE == kModeLse) {
       // Q[bf] is free (S(jt) is done): tile jt+2's rows go there; tile jt+1's rows (copied
       // one tile ago) are confirmed and S(jt+1) starts now
       if (jt + 2 < n_tiles) gather(jt + 2, bf);
@@ -242,20 +238,7 @@ block_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const 
           const float Lsum = l * tc::ex2(m2 - M) + o.y * tc::ex2(o.x - M);
           lse = (M + tc::lg2(Lsum)) * kLn2;
         }
-        if constexpr (MODE == kModeLse) {
-          if (qi >= 0)
-            a.out[((static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + qi) * s.K + slot] = lse;
-        } else {
-          // sum over the G heads of the query: G adjacent lanes (padding entries are whole)
-          float sum = lse;
-#pragma unroll
-          for (int o2 = 1; o2 < G; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-          if (qi >= 0) {
-            const int64_t at = (head * s.N + qi) * a.W + slot;
-            if (h == 0) a.out[at] = sum;
-            if (a.out_head) a.out_head[at * G + h] = lse;
-          }
-        }
+        if (qi >= 0) a.out[((static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + qi) * s.K + slot] = lse;
       }
       if (stop) break;
     } else {
@@ -333,29 +316,27 @@ block_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const 
   if (warp == 0) tc::tmem_free(tmem_base, L::tmem_cols);
 }
 
-// One warp per (b, query, head) row: lse = log sum_k exp(block_lse_k) over the row's valid
-// slots (lane k < K holds slot k), written to the caller's lse; the row's accumulator is
-// cleared for the reduce-adds.
-template <int D>
+// lse = log sum_k exp(block_lse_k) over each row's valid slots, written to the caller's lse
+// ([B,Hq,N]); one thread per row, rows in lse order (consecutive threads read consecutive
+// rows of block_lse and idx).
 __global__ void __launch_bounds__(256)
 attn_rows_kernel(Dims s, const int32_t* __restrict__ idx, const float* __restrict__ block_lse,
-                 float* __restrict__ lse_out, float4* __restrict__ o_acc) {
-  const int64_t row = blockIdx.x * 8LL + (threadIdx.x >> 5);       // (b*N + i)*Hq + h
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<int64_t>(s.B) * s.N * s.Hq) return;
-  const int h = static_cast<int>(row % s.Hq);
-  const int64_t bi = row / s.Hq;
-  const int i = static_cast<int>(bi % s.N), b = static_cast<int>(bi / s.N);
-  const int64_t unit = (static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i;
-  const int64_t lrow = (static_cast<int64_t>(b) * s.Hq + h) * s.N + i;
-  const bool valid = lane < s.K && idx[unit * s.K + lane] >= 0;
-  const float my = valid ? block_lse[lrow * s.K + lane] : neg_inf();
-  float m = my;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const float den = warp_sum((valid && m != neg_inf()) ? expf(my - m) : 0.f);
-  if (lane == 0) lse_out[lrow] = den > 0.f ? m + logf(den) : neg_inf();
-  for (int c = lane; c < D / 4; c += 32) o_acc[row * (D / 4) + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                 float* __restrict__ lse_out) {
+  const int64_t lrow = blockIdx.x * 256LL + threadIdx.x;            // (b*Hq + h)*N + i
+  if (lrow >= static_cast<int64_t>(s.B) * s.N * s.Hq) return;
+  const int i = static_cast<int>(lrow % s.N);
+  const int64_t bh = lrow / s.N;
+  const int h = static_cast<int>(bh % s.Hq), b = static_cast<int>(bh / s.Hq);
+  const int32_t* id = idx + ((static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i) * s.K;
+  const float* bl = block_lse + lrow * s.K;
+  float m = neg_inf();
+  for (int k = 0; k < s.K; ++k)
+    if (id[k] >= 0) m = fmaxf(m, bl[k]);
+  float den = 0.f;
+  if (m != neg_inf())
+    for (int k = 0; k < s.K; ++k)
+      if (id[k] >= 0) den += expf(bl[k] - m);
+  lse_out[lrow] = den > 0.f ? m + logf(den) : neg_inf();
 }
 
 // O = bf16(accumulator), 8 elements per thread.
@@ -421,14 +402,13 @@ TcArgs base_args(const Dims& s, const GroupPlan& gp, const void* Q, const int32_
   a.items = items;
   a.n_items = n_items;
   a.status = status;
-  a.W = s.K;
   return a;
 }
 
 }  // namespace
 
 // Attention forward for d in {64, 128} and G in {1, 2, 4, 8}: [block LSE pass when
-// head_lse is NULL] -> row LSE + accumulator clear -> output pass -> bf16 conversion.
+// head_lse is NULL] -> accumulator clear, row LSE -> output pass -> bf16 conversion.
 int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
                        const float* head_lse, float* block_lse_ws, float* o_acc, void* O, float* lse,
@@ -446,13 +426,12 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
   }
   const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
   {
+    ProfScope ps(st, "attn_clear");
+    if ((err = cudaMemsetAsync(o_acc, 0, static_cast<size_t>(rows) * s.d * 4, st))) return err;
+  }
+  {
     ProfScope ps(st, "attn_rows");
-    if (s.d == 128)
-      attn_rows_kernel<128><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-          s, idx, hl, lse, reinterpret_cast<float4*>(o_acc));
-    else
-      attn_rows_kernel<64><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-          s, idx, hl, lse, reinterpret_cast<float4*>(o_acc));
+    attn_rows_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(s, idx, hl, lse);
   }
   if ((err = cudaGetLastError())) return err;
   a.lse_rows = lse;
@@ -466,21 +445,6 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
         n8, reinterpret_cast<const float4*>(o_acc), static_cast<uint4*>(O));
   }
   return cudaGetLastError();
-}
-
-// Stage-2 exact leaf scores of the grouped (candidate leaf, query) pairs: score[unit, slot]
-// = sum over the G heads of the leaf's LSE; per-head terms into pair_head when given.
-int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
-                   int32_t* status, cudaStream_t st) {
-  CUtensorMap km, om;
-  int err = make_maps(s, K, nullptr, &km, &om);
-  if (err) return err;
-  TcArgs a = base_args(s, gp, Q, list, items, n_items, status);
-  a.out = pair_score;
-  a.out_head = pair_head;
-  a.W = W;
-  return tc_dispatch<kModeLeaf>(a, km, om, "leaf_score", st);
 }
 
 }  // namespace pisa

@@ -163,7 +163,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
           tot += mx + logf(expf(x0 - mx) + expf(x1 - mx));
         }
       }
-      s_sc[tid] = tot;
+      s_sc[tid] = no_nan(tot);
     }
     __syncthreads();
     if (tid < nc) {
@@ -241,7 +241,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   if (tid < nlc) {
     float tot = 0.f;
     for (int h = 0; h < G; ++h) tot += lh[tid * G + h];
-    s_sc[tid] = tot;
+    s_sc[tid] = no_nan(tot);
   }
   __syncthreads();
   // 5. top K leaves, ascending

@@ -54,7 +54,12 @@ __device__ __forceinline__ uint4 ldg_u4(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// Strict "a beats b" order of the selection: higher score, then lower node index.
+// A score that enters a top-K: NaN (only non-finite inputs make one) becomes -inf, so the
+// order below stays total and a rank-based top-K never keeps more than K.
+__device__ __forceinline__ float no_nan(float x) { return x != x ? neg_inf() : x; }
+
+// Strict "a beats b" order of the selection: higher score, then lower node index (scores
+// pass through no_nan first).
 __device__ __forceinline__ bool beats(float sa, int ia, float sb, int ib) {
   return sa > sb || (sa == sb && ia < ib);
 }
