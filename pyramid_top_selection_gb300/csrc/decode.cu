@@ -132,24 +132,40 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
       continue;
     }
     const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
-    for (int it = tid; it < nc * 2 * G; it += kThreads) {
-      const int cs = it / (2 * G), e = (it / G) & 1, h = it % G;
-      const int64_t ch = 2LL * s_cand[cs] + e;
-      const int64_t st = ch * cspan;
-      if (st > p) { dots[it] = neg_inf(); continue; }
-      const float4* row = reinterpret_cast<const float4*>(pyr_h + (geo.off[lam - 1] + ch) * D);
-      const float4* qq = reinterpret_cast<const float4*>(q32 + h * D);
-      float acc = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < D / 4; ++k) {
-        const float4 x = row[k], y = qq[k];
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-        acc = fmaf(x.z, y.z, acc);
-        acc = fmaf(x.w, y.w, acc);
+    {
+      // child rows (candidate cs, child e) -> row 2cs+e, 64 rows per pass; thread = (row,
+      // quarter of the dims): its D/4 dims of the row load at once, each head's partial dot
+      // is combined over the 4 quarters (adjacent lanes) with two shuffles
+      constexpr int QD = D / 4, NV = QD / 4;
+      const int rq = tid >> 2, qt = tid & 3;
+      for (int base = 0; base < 2 * nc; base += kThreads / 4) {
+        const int row = base + rq;
+        const int64_t ch = row < 2 * nc ? 2LL * s_cand[row >> 1] + (row & 1) : 0;
+        const int64_t st = ch * cspan;
+        const bool vis = row < 2 * nc && st <= p;
+        float4 xr[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          xr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (vis) xr[u] = reinterpret_cast<const float4*>(pyr_h + (geo.off[lam - 1] + ch) * D + qt * QD)[u];
+        }
+        const float cnt = vis ? static_cast<float>(min(st + cspan, static_cast<int64_t>(p) + 1) - st) : 1.f;
+        for (int h = 0; h < G; ++h) {
+          const float4* qq = reinterpret_cast<const float4*>(q32 + h * D + qt * QD);
+          float part = 0.f;
+#pragma unroll
+          for (int u = 0; u < NV; ++u) {
+            const float4 y = qq[u];
+            part = fmaf(xr[u].x, y.x, part);
+            part = fmaf(xr[u].y, y.y, part);
+            part = fmaf(xr[u].z, y.z, part);
+            part = fmaf(xr[u].w, y.w, part);
+          }
+          part += __shfl_xor_sync(0xffffffffu, part, 1);
+          part += __shfl_xor_sync(0xffffffffu, part, 2);
+          if (qt == 0 && row < 2 * nc) dots[row * G + h] = vis ? s.scale * part / cnt : neg_inf();
+        }
       }
-      const float cnt = static_cast<float>(min(st + cspan, static_cast<int64_t>(p) + 1) - st);
-      dots[it] = s.scale * acc / cnt;
     }
     __syncthreads();
     if (tid < nc) {
@@ -275,37 +291,53 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
     s_lse[tid] = mx + logf(sum);
   }
   __syncthreads();
+  // P = exp(S - lse) of the selected leaves, in place (one pass, all threads)
+  for (int it = tid; it < nsel * 64 * G; it += kThreads) {
+    const int k = it / (64 * G), rem = it % (64 * G);
+    float* Sr = Sb + static_cast<int64_t>(s_sel[k]) * 64 * G;
+    Sr[rem] = expf(Sr[rem] - s_lse[rem % G]);
+  }
+  __syncthreads();
   {
+    // o_h = sum over the selected keys of P[key][h] v_key: the keys of all selected leaves
+    // are one flat list; each warp takes kKeyBatch consecutive keys at a time with all of
+    // their V rows (lane: dims lane*PER ..) in flight before any is used
     constexpr int PER = D / 32;
+    constexpr int kKeyBatch = 16;
     float acc[8][PER];
 #pragma unroll
     for (int h = 0; h < 8; ++h)
 #pragma unroll
       for (int u = 0; u < PER; ++u) acc[h][u] = 0.f;
-    for (int k = warp; k < nsel; k += kWarps) {
-      const int cs = s_sel[k];
-      const int64_t t0 = static_cast<int64_t>(s_cand[cs]) * C;
-      const float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
-      for (int key = 0; key < 64 && t0 + key <= p; ++key) {
-        const __nv_bfloat16* vr = vrow(t0 + key) + lane * PER;
-        float vv[PER];
-        if (PER == 4) {
-          const uint2 x = *reinterpret_cast<const uint2*>(vr);
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x);
+    const int nkeys = nsel * 64;
+    for (int base = warp * kKeyBatch; base < nkeys; base += kWarps * kKeyBatch) {
+      uint2 x[kKeyBatch];
 #pragma unroll
-          for (int u = 0; u < PER; ++u) vv[u] = __bfloat162float(e[u]);
-        } else {
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(vr);
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x);
-#pragma unroll
-          for (int u = 0; u < PER; ++u) vv[u] = __bfloat162float(e[u]);
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int kk = base + u;
+        const int64_t j = kk < nkeys ? static_cast<int64_t>(s_cand[s_sel[kk >> 6]]) * C + (kk & 63) : p + 1;
+        x[u] = make_uint2(0, 0);
+        if (j <= p) {
+          const __nv_bfloat16* vr = vrow(j) + lane * PER;
+          if (PER == 4) x[u] = *reinterpret_cast<const uint2*>(vr);
+          else x[u].x = *reinterpret_cast<const uint32_t*>(vr);
         }
+      }
+#pragma unroll
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int kk = base + u;
+        if (kk >= nkeys) break;
+        const float* Pr = Sb + static_cast<int64_t>(s_sel[kk >> 6]) * 64 * G + (kk & 63) * G;
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x[u]);
+        float vv[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) vv[q] = __bfloat162float(e[q]);
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
           if (h < G) {
-            const float pw = expf(Sr[key * G + h] - s_lse[h]);
+            const float pw = Pr[h];
 #pragma unroll
-            for (int u = 0; u < PER; ++u) acc[h][u] = fmaf(pw, vv[u], acc[h][u]);
+            for (int q = 0; q < PER; ++q) acc[h][q] = fmaf(pw, vv[q], acc[h][q]);
           }
         }
       }
