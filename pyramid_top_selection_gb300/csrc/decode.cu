@@ -32,8 +32,8 @@ struct DecodeSmem {
 __host__ __device__ inline DecodeSmem decode_smem(int G, int D, int K) {
   DecodeSmem m{};
   int o = 0;
-  m.q32 = o;  o += G * D;
-  m.S = o;    o += 2 * K * 64 * G;
+  m.q32 = o;  o += G * (D + 16);   // per head: 4 quarters of D/4 floats, each padded by 4
+  m.S = o;    o += 2 * K * (64 * G + 4);   // per candidate leaf: 64 keys x G heads + 4 pad
   m.lh = o;   o += 2 * K * G;
   m.red = o;  o += kWarps * G * D;
   m.dots = o; o += kMaxCand * 2 * G;
@@ -84,7 +84,9 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
     reinterpret_cast<uint4*>(vrow(p))[tid] = ldg_u4(vn + head * D + tid * 8);
   }
   const __nv_bfloat16* qg = qn + (static_cast<int64_t>(b) * s.Hq + kv * G) * D;
-  for (int it = tid; it < G * D; it += kThreads) q32[it] = __bfloat162float(qg[it]);
+  // quarters 16 bytes apart in bank terms, so the level dots' 4 quarter readers never collide
+  for (int it = tid; it < G * D; it += kThreads)
+    q32[(it / D) * (D + 16) + (it % D) / (D / 4) * (D / 4 + 4) + it % (D / 4)] = __bfloat162float(qg[it]);
   __syncthreads();
 
   // 2. leaf recompute (token order) and ancestor path (left + right)
@@ -107,31 +109,51 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   }
   __syncthreads();
 
-  // 3. intermediate levels
-  if (tid == 0) { s_kept[0] = 0; s_n[0] = 1; }
-  __syncthreads();
+  // 3. intermediate levels. Warp 0 drives the descent: it expands the kept nodes into
+  // candidates (ballot compaction) and keeps them all while there are at most K, with no
+  // CTA barrier; a level with more candidates is published for the CTA-wide dot phase (two
+  // barriers), then warp 0 scores the candidates and keeps the top K by shuffle ranks.
+  __shared__ int s_lam;
   const int Lv = geo.n_levels;
-  for (int lam = Lv - 2; lam >= 1; --lam) {
-    const int64_t span = static_cast<int64_t>(C) << lam;
-    if (tid == 0) {
+  int lam = Lv - 2;          // warp 0: the level whose candidates come next
+  int n_kept = 1;            // warp 0: kept nodes (in s_kept) at level lam + 1
+  if (tid == 0) s_kept[0] = 0;
+  __syncwarp();
+  while (true) {
+    if (warp == 0) {
       int nc = 0;
-      for (int k = 0; k < s_n[0]; ++k) {
-        const int a = s_kept[k];
-        s_cand[nc++] = 2 * a;
-        if (static_cast<int64_t>(2 * a + 1) * span <= p) s_cand[nc++] = 2 * a + 1;
+      for (; lam >= 1; --lam) {
+        const int64_t span = static_cast<int64_t>(C) << lam;
+        int a = 0;
+        bool c1 = false;
+        if (lane < n_kept) {
+          a = s_kept[lane];
+          c1 = static_cast<int64_t>(2 * a + 1) * span <= p;
+        }
+        const unsigned m1 = __ballot_sync(0xffffffffu, c1);
+        const int pos = lane + __popc(m1 & lanemask_lt());
+        if (lane < n_kept) {
+          s_cand[pos] = 2 * a;
+          if (c1) s_cand[pos + 1] = 2 * a + 1;
+        }
+        nc = n_kept + __popc(m1);
+        __syncwarp();
+        if (nc > Ksel) break;
+        if (lane < nc) s_kept[lane] = s_cand[lane];
+        n_kept = nc;
+        __syncwarp();
       }
-      s_n[1] = nc;
+      if (lane == 0) {
+        s_lam = lam;
+        s_n[0] = n_kept;
+        s_n[1] = nc;
+      }
     }
     __syncthreads();
+    const int lv = s_lam;
+    if (lv < 1) break;
     const int nc = s_n[1];
-    if (nc <= Ksel) {
-      if (tid < nc) s_kept[tid] = s_cand[tid];
-      __syncthreads();
-      if (tid == 0) s_n[0] = nc;
-      __syncthreads();
-      continue;
-    }
-    const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
+    const int64_t cspan = static_cast<int64_t>(C) << (lv - 1);
     {
       // child rows (candidate cs, child e) -> row 2cs+e, 64 rows per pass; thread = (row,
       // quarter of the dims): its D/4 dims of the row load at once, each head's partial dot
@@ -147,11 +169,11 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
           xr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (vis) xr[u] = reinterpret_cast<const float4*>(pyr_h + (geo.off[lam - 1] + ch) * D + qt * QD)[u];
+          if (vis) xr[u] = reinterpret_cast<const float4*>(pyr_h + (geo.off[lv - 1] + ch) * D + qt * QD)[u];
         }
         const float cnt = vis ? static_cast<float>(min(st + cspan, static_cast<int64_t>(p) + 1) - st) : 1.f;
         for (int h = 0; h < G; ++h) {
-          const float4* qq = reinterpret_cast<const float4*>(q32 + h * D + qt * QD);
+          const float4* qq = reinterpret_cast<const float4*>(q32 + h * (D + 16) + qt * (QD + 4));
           float part = 0.f;
 #pragma unroll
           for (int u = 0; u < NV; ++u) {
@@ -168,30 +190,48 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
       }
     }
     __syncthreads();
-    if (tid < nc) {
-      float tot = 0.f;
-      for (int h = 0; h < G; ++h) {
-        const float x0 = dots[(tid * 2) * G + h], x1 = dots[(tid * 2 + 1) * G + h];
-        if (x1 == neg_inf()) {
-          tot += x0;
-        } else {
-          const float mx = fmaxf(x0, x1);
-          tot += mx + logf(expf(x0 - mx) + expf(x1 - mx));
+    if (warp == 0) {
+      // scores of candidates lane and lane + 32, then each one's rank among all of them
+      float sc[2];
+      int ci[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = lane + 32 * u;
+        sc[u] = neg_inf();
+        ci[u] = 0;
+        if (c < nc) {
+          float tot = 0.f;
+          for (int h = 0; h < G; ++h) {
+            const float x0 = dots[(2 * c) * G + h], x1 = dots[(2 * c + 1) * G + h];
+            if (x1 == neg_inf()) {
+              tot += x0;
+            } else {
+              const float mx = fmaxf(x0, x1);
+              tot += mx + logf(expf(x0 - mx) + expf(x1 - mx));
+            }
+          }
+          sc[u] = no_nan(tot);
+          ci[u] = s_cand[c];
         }
       }
-      s_sc[tid] = no_nan(tot);
+      int rk[2] = {0, 0};
+      const int nv = nc > 32 ? 2 : 1;
+      for (int v = 0; v < nv; ++v)
+        for (int o = 0; o < 32; ++o) {
+          const float so = __shfl_sync(0xffffffffu, sc[v], o);
+          const int io = __shfl_sync(0xffffffffu, ci[v], o);
+          if (o + 32 * v < nc) {
+            rk[0] += beats(so, io, sc[0], ci[0]) ? 1 : 0;
+            rk[1] += beats(so, io, sc[1], ci[1]) ? 1 : 0;
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (lane + 32 * u < nc && rk[u] < Ksel) s_kept[rk[u]] = ci[u];
+      n_kept = Ksel;
+      --lam;
+      __syncwarp();
     }
-    __syncthreads();
-    if (tid < nc) {
-      const float my = s_sc[tid];
-      const int mi = s_cand[tid];
-      int rank = 0;
-      for (int o = 0; o < nc; ++o) rank += beats(s_sc[o], s_cand[o], my, mi) ? 1 : 0;
-      if (rank < Ksel) s_kept[rank] = mi;
-    }
-    __syncthreads();
-    if (tid == 0) s_n[0] = Ksel;
-    __syncthreads();
   }
 
   // 4. leaf candidates and exact leaf LSE (MMA: rows = keys, columns = heads)
@@ -231,7 +271,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
           const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
           mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
         }
-        float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
+        float* Sr = Sb + static_cast<int64_t>(cs) * (64 * G + 4);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int h = 2 * pq + e;
@@ -246,7 +286,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   __syncthreads();
   for (int it = tid; it < nlc * G; it += kThreads) {
     const int cs = it / G, h = it % G;
-    const float* Sr = Sb + static_cast<int64_t>(cs) * 64 * G;
+    const float* Sr = Sb + static_cast<int64_t>(cs) * (64 * G + 4);
     float mx = neg_inf();
     for (int k = 0; k < 64; ++k) mx = fmaxf(mx, Sr[k * G + h]);
     float sum = 0.f;
@@ -294,7 +334,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   // P = exp(S - lse) of the selected leaves, in place (one pass, all threads)
   for (int it = tid; it < nsel * 64 * G; it += kThreads) {
     const int k = it / (64 * G), rem = it % (64 * G);
-    float* Sr = Sb + static_cast<int64_t>(s_sel[k]) * 64 * G;
+    float* Sr = Sb + static_cast<int64_t>(s_sel[k]) * (64 * G + 4);
     Sr[rem] = expf(Sr[rem] - s_lse[rem % G]);
   }
   __syncthreads();
@@ -327,7 +367,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
       for (int u = 0; u < kKeyBatch; ++u) {
         const int kk = base + u;
         if (kk >= nkeys) break;
-        const float* Pr = Sb + static_cast<int64_t>(s_sel[kk >> 6]) * 64 * G + (kk & 63) * G;
+        const float* Pr = Sb + static_cast<int64_t>(s_sel[kk >> 6]) * (64 * G + 4) + (kk & 63) * G;
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x[u]);
         float vv[PER];
 #pragma unroll

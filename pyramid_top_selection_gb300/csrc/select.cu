@@ -34,11 +34,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kMaxCand = 64;   // 2K for K <= 32
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
 
 // fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}.
 __global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4) {
