@@ -44,7 +44,7 @@ struct Dims {
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.
 // total: without the per-head leaf terms; total_head: with them (head_lse requested).
 struct SelectWs {
-  size_t split, cand, cscore, group, total, chead, total_head;
+  size_t split, cand, cscore, status, group, total, chead, total_head;
 };
 struct AttnFwdWs {
   size_t block_lse, o_acc, status, total;

@@ -1,0 +1,370 @@
+// Stage-2 exact leaf scoring on the fifth-generation tensor cores: a persistent,
+// warp-specialised kernel.
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Method key
+// points": leaves are scored by the exact LSE over their raw keys and the G query heads of a
+// KV head sum their LSEs; "Reference value of the work": the queries that use the same leaf
+// block are grouped into tiles so the block's keys are read once per tile.
+//
+// One CTA per SM walks the work items (a candidate leaf of one KV head and the (query,
+// head) rows that have it among their candidates) with a static stride, in tiles of 128
+// rows. Roles, connected by mbarrier rings so that no role waits on another's latency:
+//   * producers (warps 8-11, 32 tile rows per warp): gather the query vectors with cp.async
+//     into a 4-stage ring of swizzled Q tiles, each warp instruction copying whole rows
+//     (full 32-byte sectors); a thread confirms a tile's copies (wait, proxy fence,
+//     arrival) once it has issued the next tile;
+//   * control (warp 12, one thread): loads each item's 64 keys by TMA into a 2-stage ring
+//     (the next item's while the current one runs) and issues S = Q K^T (M=128, N=64) as
+//     tcgen05.mma into a 4-stage ring of TMEM accumulators;
+//   * softmax (two warpgroups, warps 0-3 and 4-7, on alternate tiles; thread = TMEM lane =
+//     tile row): reads its S row, frees the TMEM stage, and reduces the row to its LSE over
+//     the visible keys; the G rows of a query (adjacent lanes) sum their LSEs into the
+//     candidate's score.
+// Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
+// its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
+#include "device.cuh"
+#include "group.h"
+#include "profile.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kNQ = 4;            // Q tile stages
+constexpr int kNS = 4;            // TMEM S stages (64 columns each)
+constexpr int kNK = 2;            // K tile stages
+constexpr int kThreads = 416;     // softmax 0-255 (two warpgroups), producers 256-383, control 384-415
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct LeafSmem {
+  static constexpr int KB = D / 64;
+  static constexpr int Q_BYTES = KB * kRows * 128;
+  static constexpr int K_BYTES = KB * 64 * 128;
+  static constexpr int oQ = 0, oK = kNQ * Q_BYTES;
+  static constexpr int bytes = oK + kNK * K_BYTES + 1024;
+};
+
+struct LeafArgs {
+  Dims s;
+  GroupPlan gp;
+  const __nv_bfloat16* Q;
+  const int32_t* list;
+  const int4* items;
+  const int32_t* n_items;
+  int W;
+  float* pair_score;   // [heads, N, W]
+  float* pair_head;    // [heads, N, W, G] or NULL
+  int32_t* status;
+};
+
+// One item's fields, as every role decodes them.
+struct ItemView {
+  int beg, n_ent, kbase, b, kv;
+  int64_t head;
+};
+
+__device__ __forceinline__ ItemView view_item(const LeafArgs& a, int it) {
+  const int4 item = a.items[it];
+  ItemView v;
+  v.beg = item.y;
+  v.n_ent = item.z;
+  v.kbase = a.gp.leaf_of(item.x) * 64;
+  v.head = a.gp.head_of(item.x);
+  v.b = static_cast<int>(v.head / a.s.Hkv);
+  v.kv = static_cast<int>(v.head % a.s.Hkv);
+  return v;
+}
+
+// Position in this CTA's tile sequence: items blockIdx.x, blockIdx.x + gridDim.x, ..., each
+// cut into tiles of `ept` entries.
+struct TileCursor {
+  int it, j, n_tiles;
+  ItemView v;
+};
+
+__device__ __forceinline__ bool first_tile(const LeafArgs& a, int n_items, int ept, TileCursor& c) {
+  c.it = blockIdx.x;
+  c.j = 0;
+  if (c.it >= n_items) return false;
+  c.v = view_item(a, c.it);
+  c.n_tiles = (c.v.n_ent + ept - 1) / ept;
+  return true;
+}
+
+__device__ __forceinline__ bool next_tile(const LeafArgs& a, int n_items, int ept, TileCursor& c) {
+  if (++c.j < c.n_tiles) return true;
+  c.it += gridDim.x;
+  c.j = 0;
+  if (c.it >= n_items) return false;
+  c.v = view_item(a, c.it);
+  c.n_tiles = (c.v.n_ent + ept - 1) / ept;
+  return true;
+}
+
+// List entry (query << 6 | slot) of tile row r, -1 past the end of the item.
+__device__ __forceinline__ int row_entry(const LeafArgs& a, const TileCursor& c, int ept, int G, int r) {
+  const int e = c.j * ept + r / G;
+  return e < c.v.n_ent ? a.list[c.v.beg + e] : -1;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
+  using L = LeafSmem<D>;
+  constexpr int EPT = kRows / G;          // entries (queries) per tile
+  constexpr int CH = D / 8;               // 16-byte chunks per row
+  extern __shared__ unsigned char smraw[];
+  __shared__ __align__(8) uint64_t q_full[kNQ], q_empty[kNQ], s_full[kNS], s_empty[kNS], k_full[kNK],
+      k_empty[kNK];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+
+  const Dims& s = a.s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* sm = smraw + ((1024 - (tc::su32(smraw) & 1023)) & 1023);
+  const uint32_t aQ = tc::su32(sm + L::oQ), aK = tc::su32(sm + L::oK);
+  const int n_items = *a.n_items;
+
+  if (tid == 0) {
+    for (int k = 0; k < kNQ; ++k) {
+      tc::bar_init(&q_full[k], kRows);
+      tc::bar_init(&q_empty[k], 1);
+    }
+    for (int k = 0; k < kNS; ++k) {
+      tc::bar_init(&s_full[k], 1);
+      tc::bar_init(&s_empty[k], kRows);
+    }
+    for (int k = 0; k < kNK; ++k) {
+      tc::bar_init(&k_full[k], 1);
+      tc::bar_init(&k_empty[k], 1);
+    }
+    tc::fence_bar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kNS * 64);
+  tc::before_sync();
+  __syncthreads();
+  tc::after_sync();
+  auto give_up = [&]() { atomicOr(&s_abort, 1); };
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+
+  if (warp >= 8 && warp < 12) {
+    // ---------------------------------------------------------------- producers
+    // the next tile's list entries (and item) load while this tile's copies are issued; lane
+    // l holds the entry of the warp's row l, and instruction k copies rows k*RPI .. of the
+    // warp's 32, chunk (lane % CH) of row (lane / CH)
+    constexpr int RPI = 32 / CH;                      // rows per warp instruction
+    const int wr = (warp - 8) * 32;                   // the warp's first tile row
+    TileCursor cur;
+    bool have = first_tile(a, n_items, EPT, cur);
+    int pk = have ? row_entry(a, cur, EPT, G, wr + lane) : -1;
+    int T = 0;
+    while (have && !aborted()) {
+      TileCursor nxt = cur;
+      const bool have_n = next_tile(a, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a, nxt, EPT, G, wr + lane) : -1;
+      const int st = T % kNQ;
+      if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
+      const uint32_t dst = aQ + st * L::Q_BYTES;
+      const int c = lane % CH;
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        const int rl = k * RPI + lane / CH;           // row within the warp's 32
+        const int qi = __shfl_sync(0xffffffffu, pk, rl) >> 6;
+        const int r = wr + rl;
+        const __nv_bfloat16* src =
+            a.Q + ((static_cast<int64_t>(cur.v.b) * s.N + (qi < 0 ? 0 : qi)) * s.Hq + cur.v.kv * G + r % G) * D;
+        tc::cp_async16(dst + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8), src + c * 8, qi >= 0);
+      }
+      tc::cp_async_commit();
+      if (T > 0) {             // the previous tile's copies have had a tile's time to land
+        tc::cp_async_wait<1>();
+        tc::fence_async_smem();
+        tc::bar_arrive(&q_full[(T - 1) % kNQ]);
+      }
+      cur = nxt;
+      have = have_n;
+      pk = pk_n;
+      ++T;
+    }
+    tc::cp_async_wait<0>();
+    if (T > 0) {
+      tc::fence_async_smem();
+      tc::bar_arrive(&q_full[(T - 1) % kNQ]);
+    }
+  } else if (warp == 12) {
+    // ---------------------------------------------------------------- control
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
+      auto load_k = [&](int I, int it) {
+        const int ks = I % kNK;
+        if (!tc::bar_wait(&k_empty[ks], ((I / kNK) & 1) ^ 1)) { give_up(); return; }
+        const ItemView v = view_item(a, it);
+        tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+      };
+      int T = 0, I = 0;
+      if (static_cast<int>(blockIdx.x) < n_items) load_k(0, blockIdx.x);
+      for (int it = blockIdx.x; it < n_items && !aborted(); it += gridDim.x, ++I) {
+        if (it + static_cast<int>(gridDim.x) < n_items) load_k(I + 1, it + gridDim.x);
+        const int ks = I % kNK;
+        if (!tc::bar_wait(&k_full[ks], (I / kNK) & 1)) { give_up(); break; }
+        const ItemView v = view_item(a, it);
+        const int n_tiles = (v.n_ent + EPT - 1) / EPT;
+        for (int j = 0; j < n_tiles; ++j, ++T) {
+          const int st = T % kNQ, ss = T % kNS;
+          if (!tc::bar_wait(&q_full[st], (T / kNQ) & 1) || !tc::bar_wait(&s_empty[ss], ((T / kNS) & 1) ^ 1)) {
+            give_up();
+            break;
+          }
+          tc::after_sync();
+#pragma unroll
+          for (int ks2 = 0; ks2 < D / 16; ++ks2)
+            tc::mma(tmem_base + 64 * ss,
+                    tc::desc(aQ + st * L::Q_BYTES + (ks2 >> 2) * (kRows * 128) + (ks2 & 3) * 32),
+                    tc::desc(aK + ks * L::K_BYTES + (ks2 >> 2) * (64 * 128) + (ks2 & 3) * 32), idS, ks2 > 0);
+          tc::commit(&s_full[ss]);
+          tc::commit(&q_empty[st]);
+        }
+        tc::commit(&k_empty[ks]);
+      }
+    }
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax
+    // warpgroup sg takes the tiles T with T % 2 == sg; its entries for the next such tile
+    // load while the current one is reduced
+    const int sg = warp >> 2;
+    const int r = tid & (kRows - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c1 = s.scale * kLog2e;
+    const int h = r % G;
+    TileCursor cur;
+    bool have = first_tile(a, n_items, EPT, cur);
+    int T = 0;
+    if (have && sg == 1) {
+      have = next_tile(a, n_items, EPT, cur);
+      T = 1;
+    }
+    int pk = have ? row_entry(a, cur, EPT, G, r) : -1;
+    while (have && !aborted()) {
+      TileCursor nxt = cur;
+      bool have_n = next_tile(a, n_items, EPT, nxt);
+      if (have_n) have_n = next_tile(a, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a, nxt, EPT, G, r) : -1;   // in flight during this tile
+      const int ss = T % kNS;
+      const bool ok = tc::bar_wait(&s_full[ss], (T / kNS) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }   // warp-uniform exit
+      tc::after_sync();
+      float sv[64];
+      tc::tmem_ld64(tmem_base + 64 * ss + lane_off, sv);
+      tc::before_sync();
+      tc::bar_arrive(&s_empty[ss]);
+      const int qi = pk >> 6;                                  // -1 on padding rows
+      const int lim = qi - cur.v.kbase;                        // key c is visible iff c <= lim
+      if (lim < 63) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
+      }
+      // four partial chains for the max and the sum (independent instructions in flight)
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      float lse = -INFINITY;
+      if (mx != -INFINITY) {
+        const float m2 = mx * c1;
+        float lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) lq[c & 3] += tc::ex2(fmaf(sv[c], c1, -m2));
+        lse = (m2 + tc::lg2((lq[0] + lq[1]) + (lq[2] + lq[3]))) * kLn2;
+      }
+      // G adjacent lanes hold the heads of one query (a padding entry is whole)
+      float sum = lse;
+#pragma unroll
+      for (int o = 1; o < G; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (pk >= 0) {
+        const int64_t at = (cur.v.head * s.N + qi) * a.W + (pk & 63);
+        if (h == 0) a.pair_score[at] = sum;
+        if (a.pair_head) a.pair_head[at * G + h] = lse;
+      }
+      cur = nxt;
+      have = have_n;
+      pk = pk_n;
+      T += 2;
+    }
+  }
+  tc::before_sync();
+  __syncthreads();
+  if (tid == 0 && s_abort) atomicOr(a.status, PISA_ETIMEOUT);
+  if (warp == 0) {
+    tc::after_sync();
+    tc::tmem_free(tmem_base, kNS * 64);
+  }
+}
+
+template <int D, int G>
+int leaf_tc_launch(const LeafArgs& a, const CUtensorMap& km, int grid, cudaStream_t st) {
+  const int smem = LeafSmem<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(leaf_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ProfScope ps(st, "leaf_score");
+  leaf_tc_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km);
+  return cudaGetLastError();
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
+}  // namespace
+
+// Exact leaf scores of the grouped (candidate leaf, query) pairs: pair_score[unit, slot] =
+// sum over the G heads of the leaf's LSE; per-head terms into pair_head when it is given.
+int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                   int32_t* status, cudaStream_t st) {
+  CUtensorMap km;
+  {
+    const uint64_t d = static_cast<uint64_t>(s.d);
+    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv), static_cast<uint64_t>(s.N),
+                              static_cast<uint64_t>(s.B)};
+    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv, d * 2 * s.Hkv * s.N};
+    const uint32_t box[4] = {64, 1, 64, 1};
+    if (int e = encode_tmap(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, strides, box)) return e;
+  }
+  LeafArgs a{};
+  a.s = s;
+  a.gp = gp;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.list = list;
+  a.items = items;
+  a.n_items = n_items;
+  a.W = W;
+  a.pair_score = pair_score;
+  a.pair_head = pair_head;
+  a.status = status;
+  const int64_t mi = gp.max_items;
+  const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
+#define PISA_LEAF_CASE(DD, GG) \
+  if (s.d == DD && s.G == GG) return leaf_tc_launch<DD, GG>(a, km, grid, st);
+  PISA_LEAF_CASE(128, 1) PISA_LEAF_CASE(128, 2) PISA_LEAF_CASE(128, 4) PISA_LEAF_CASE(128, 8)
+  PISA_LEAF_CASE(64, 1) PISA_LEAF_CASE(64, 2) PISA_LEAF_CASE(64, 4) PISA_LEAF_CASE(64, 8)
+#undef PISA_LEAF_CASE
+  return static_cast<int>(cudaErrorNotSupported);
+}
+
+}  // namespace pisa

@@ -19,14 +19,18 @@
 //   ancestor path. Output: <= 2K leaf candidates per query.
 // Grouping: counting sort of (leaf, query) pairs into (KV head, query chunk, leaf) bins,
 //   cut into work items (group.cu).
-// Stage 2 (leaf_score_kernel): one CTA per work item; the leaf's 64 keys sit in shared
-//   memory and every (query, head) row of the item is scored against them with MMAs.
+// Stage 2 (leaf_tc.cu): a persistent warp-specialised tcgen05 kernel walks the work items;
+//   each item's 64 keys arrive by TMA and every (query, head) row is scored against them.
 // Finish (topk_kernel): top K of the <= 2K exact leaf scores, output ascending.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
 
 namespace pisa {
+
+int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                   int32_t* status, cudaStream_t st);
 
 
 namespace {
@@ -332,106 +336,6 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   }
 }
 
-// ---------------------------------------------------------------------------- stage 2
-// One CTA per (leaf t, KV head, batch): exact leaf LSE for every (query, head) row whose
-// query has t among its candidates. Keys in smem (row stride D+16 bf16: conflict-free
-// 8-byte fragment loads); rows = (list entry, head), 16 per MMA tile.
-template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32)
-leaf_score_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q,
-                  const __nv_bfloat16* __restrict__ K, const int32_t* __restrict__ list,
-                  const int4* __restrict__ items, const int32_t* __restrict__ n_items, int W,
-                  float* __restrict__ pair_score, float* __restrict__ pair_head) {
-  constexpr int KS = D / 16, KROW = D + 16, QPT = 16 / G;
-  __shared__ __align__(16) __nv_bfloat16 sK[64 * KROW];
-  if (static_cast<int>(blockIdx.x) >= *n_items) return;
-  const int4 item = items[blockIdx.x];
-  const int beg = item.y;
-  const int t = gp.leaf_of(item.x);
-  const int64_t head = gp.head_of(item.x);
-  const int b = static_cast<int>(head / s.Hkv), kv = static_cast<int>(head % s.Hkv);
-  for (int it = threadIdx.x; it < 64 * (D / 8); it += blockDim.x) {
-    const int r = it / (D / 8), c = it % (D / 8);
-    const int64_t j = static_cast<int64_t>(t) * 64 + r;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (j < s.N) v = ldg_u4(K + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8);
-    *reinterpret_cast<uint4*>(&sK[r * KROW + c * 8]) = v;
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, p = lane & 3;
-  const int n_ent = item.z;
-  const int n_mt = (n_ent + QPT - 1) / QPT;
-  const int kbase = t * 64;
-  for (int mt = warp; mt < n_mt; mt += kWarps) {
-    const int e0 = mt * QPT + g / G, h0 = g % G;
-    const int e1 = mt * QPT + (g + 8) / G, h1 = (g + 8) % G;
-    const bool ok0 = e0 < n_ent, ok1 = e1 < n_ent;
-    const int pk0 = ok0 ? list[beg + e0] : 0, pk1 = ok1 ? list[beg + e1] : 0;
-    const int i0 = pk0 >> 6, i1 = pk1 >> 6;
-    const __nv_bfloat16* q0 = Q + ((static_cast<int64_t>(b) * s.N + i0) * s.Hq + kv * G + h0) * D;
-    const __nv_bfloat16* q1 = Q + ((static_cast<int64_t>(b) * s.N + i1) * s.Hq + kv * G + h1) * D;
-    float acc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint2 x0 = ok0 ? ldg_u2(q0 + 16 * ks + 4 * p) : make_uint2(0, 0);
-      const uint2 x1 = ok1 ? ldg_u2(q1 + 16 * ks + 4 * p) : make_uint2(0, 0);
-      const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const uint2 bb = *reinterpret_cast<const uint2*>(&sK[(nt * 8 + g) * KROW + 16 * ks + 4 * p]);
-        mma_bf16(acc[nt], a, bb.x, bb.y);
-      }
-    }
-    float m0 = neg_inf(), m1 = neg_inf();
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kbase + nt * 8 + 2 * p + e;
-        acc[nt][e] = key <= i0 ? s.scale * acc[nt][e] : neg_inf();
-        acc[nt][2 + e] = key <= i1 ? s.scale * acc[nt][2 + e] : neg_inf();
-        m0 = fmaxf(m0, acc[nt][e]);
-        m1 = fmaxf(m1, acc[nt][2 + e]);
-      }
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-    const float ms0 = m0 == neg_inf() ? 0.f : m0, ms1 = m1 == neg_inf() ? 0.f : m1;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s0 += expf(acc[nt][e] - ms0);
-        s1 += expf(acc[nt][2 + e] - ms1);
-      }
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-    float l0 = ms0 + logf(s0), l1 = ms1 + logf(s1);
-    if (pair_head && p == 0) {   // per-head terms, [head, N, W, G]
-      if (ok0) pair_head[((head * s.N + i0) * W + (pk0 & 63)) * G + h0] = l0;
-      if (ok1) pair_head[((head * s.N + i1) * W + (pk1 & 63)) * G + h1] = l1;
-    }
-#pragma unroll
-    for (int o = 4; o < 4 * G; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    if (p == 0 && h0 == 0 && ok0)
-      pair_score[(head * s.N + i0) * W + (pk0 & 63)] = l0;
-    if (p == 0 && h1 == 0 && ok1)
-      pair_score[(head * s.N + i1) * W + (pk1 & 63)] = l1;
-  }
-}
-
 // ---------------------------------------------------------------------------- finish
 // One warp per (b, KV head, query): top K of the <= W candidate scores; ascending output.
 __global__ void __launch_bounds__(kWarps * 32)
@@ -674,28 +578,6 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
   }
 }
 
-template <int D, int G>
-void leaf_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                 const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
-                 cudaStream_t st) {
-  ProfScope ps(st, "leaf_score");
-  leaf_score_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, 0, st>>>(
-      s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), list, items,
-      n_items, W, pair_score, pair_head);
-}
-
-template <int D>
-void leaf_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
-                   cudaStream_t st) {
-  switch (s.G) {
-    case 1: leaf_launch<D, 1>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
-    case 2: leaf_launch<D, 2>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
-    case 4: leaf_launch<D, 4>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
-    default: leaf_launch<D, 8>(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, st); break;
-  }
-}
-
 // Stage-2 grouping: query chunks of about 16 MiB of one head's query rows; about 1024
 // (query, head) rows per work item.
 GroupPlan leaf_plan(const Dims& s) {
@@ -720,6 +602,7 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
+  w.status = o; o += 256;
   w.group = o;
   o = group_ws(leaf_plan(s), o).end;
   w.total = o;           // without the per-head terms
@@ -751,6 +634,7 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const GroupWs gw = group_ws(gp, w.group);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
+  if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
   ProfScope ps(st, "route");
@@ -767,9 +651,9 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + gw.list);
   const int4* items = reinterpret_cast<const int4*>(ws + gw.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + gw.icount) + gp.bins;
-  if (s.d == 128) leaf_dispatch<128>(s, gp, Q, K, list, items, n_items, W, cscore, chead, st);
-  else leaf_dispatch<64>(s, gp, Q, K, list, items, n_items, W, cscore, chead, st);
-  if ((err = cudaGetLastError())) return err;
+  if ((err = launch_leaf_tc(s, gp, Q, K, list, items, n_items, W, cscore, chead,
+                            reinterpret_cast<int32_t*>(ws + w.status), st)))
+    return err;
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
     ProfScope ps(st, "topk");
