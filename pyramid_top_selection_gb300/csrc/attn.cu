@@ -25,13 +25,12 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
 
 namespace {
 
-// Query chunks of about 16 MiB of one KV head's fp32 accumulator rows (G heads x d), so the
-// rows that the running items add into stay in L2; about 2048 (query, head) rows (at most
-// 1024 queries) per work item.
+// Query chunks of about 64 MiB of one KV head's fp32 accumulator rows (G heads x d): the
+// rows that the running items add into stay in L2, and items are long enough that the
+// per-item start (keys, V^T) is paid rarely; at most 1024 queries per work item.
 GroupPlan fwd_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 4;
-  const int cap = (2048 / s.G) < 1024 ? 2048 / s.G : 1024;
-  return make_group_plan(s, s.K, (int64_t(16) << 20) / per_query, cap);
+  return make_group_plan(s, s.K, (int64_t(64) << 20) / per_query, 1024);
 }
 
 }  // namespace

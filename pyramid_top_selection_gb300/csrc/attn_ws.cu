@@ -1,0 +1,456 @@
+// Causal block-sparse attention forward on the fifth-generation tensor cores: a persistent,
+// warp-specialised kernel.
+//
+// "Block Sparse Attention with Log-Linear Complexity", daily digest page, "Reference value
+// of the work": queries that use the same leaf key block are grouped into tiles so the
+// block's keys are read once per tile, and attention runs only over the selected blocks.
+//
+// Normaliser. Row (query i, head h) has lse = log sum_k exp(lse_k) over the LSEs of its
+// selected blocks (the selection's per-head leaf terms, or the LSE pass), known before any
+// key is visited; so every block's contribution exp(s q.k - lse) v is final and the blocks
+// of a row are summed straight into an fp32 accumulator, in any order.
+//
+// One CTA per SM walks the work items (a selected leaf of one KV head and the (query, head)
+// rows that chose it) with a static stride, in tiles of 128 rows. Roles, connected by
+// mbarrier rings:
+//   * producers (warps 12-15): per item, V^T (d x 64) transposed into a 2-stage ring; per
+//     tile, the query rows gathered with cp.async (whole rows per warp instruction) into a
+//     2-stage ring of swizzled Q tiles, confirmed one tile later (the next item's V rows
+//     load into registers meanwhile);
+//   * control (warp 16, one thread): each item's keys by TMA into a 2-stage ring; S = Q K^T
+//     (M=128, N=64) into one of 2 TMEM stages and O = P V (M=128, N=d) into one of 2 TMEM
+//     stages, issuing the next tile's S before this tile's P V;
+//   * softmax (two warpgroups, warps 0-3 and 4-7, alternate tiles): S row -> P = 2^(s log2e S
+//     - log2e lse) on the visible keys, bf16, into a 2-stage ring of swizzled P tiles;
+//   * epilogue (warps 8-11): O row from TMEM, 32 columns at a time, through two swizzled
+//     staging tiles; the lane holding a query's first head adds the query's G heads x 32
+//     columns into the accumulator with one TMA tensor reduce-add.
+// Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
+// its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
+#include "device.cuh"
+#include "group.h"
+#include "profile.h"
+#include "tc.cuh"
+#include "tiles.cuh"
+#include "tmap.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kNQ = 2, kNP = 2, kNKV = 2;   // Q, P, K/V stages; S and O have 2 TMEM stages
+constexpr int kThreads = 544;               // softmax 0-255, epilogue 256-383, producers 384-511, control 512-543
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct AttnSmem {
+  static constexpr int KB = D / 64;
+  static constexpr int Q_BYTES = KB * kRows * 128;
+  static constexpr int P_BYTES = kRows * 128;       // 128 rows x 64 keys bf16
+  static constexpr int K_BYTES = KB * 64 * 128;
+  static constexpr int V_BYTES = D * 128;           // V^T: D rows of 64 keys
+  static constexpr int STG = kRows * 128;           // 128 rows x 32 fp32
+  static constexpr int oQ = 0, oP = oQ + kNQ * Q_BYTES, oK = oP + kNP * P_BYTES, oV = oK + kNKV * K_BYTES,
+                       oS = oV + kNKV * V_BYTES;
+  static constexpr int bytes = oS + 2 * STG + 1024;
+  static constexpr int tmem_o = 128;                // O stage k at column 128 + k * D
+};
+
+struct AttnArgs {
+  Dims s;
+  ItemSource src;
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* V;
+  const int32_t* n_items;
+  const float* lse_rows;   // [B, Hq, N]
+  int32_t* status;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap) {
+  using L = AttnSmem<D>;
+  constexpr int EPT = kRows / G;
+  constexpr int CH = D / 8;               // 16-byte chunks per Q / V row
+  extern __shared__ unsigned char smraw[];
+  __shared__ __align__(8) uint64_t q_full[kNQ], q_empty[kNQ], s_full[2], s_empty[2], p_full[kNP], p_empty[kNP],
+      o_full[2], o_empty[2], k_full[kNKV], k_empty[kNKV], v_full[kNKV], v_empty[kNKV];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+
+  const Dims& s = a.s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* sm = smraw + ((1024 - (tc::su32(smraw) & 1023)) & 1023);
+  const uint32_t aQ = tc::su32(sm + L::oQ), aP = tc::su32(sm + L::oP), aK = tc::su32(sm + L::oK),
+                 aV = tc::su32(sm + L::oV), aS = tc::su32(sm + L::oS);
+  const int n_items = *a.n_items;
+
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) {
+      tc::bar_init(&q_full[k], kRows);
+      tc::bar_init(&q_empty[k], 1);
+      tc::bar_init(&s_full[k], 1);
+      tc::bar_init(&s_empty[k], kRows);
+      tc::bar_init(&p_full[k], kRows);
+      tc::bar_init(&p_empty[k], 1);
+      tc::bar_init(&o_full[k], 1);
+      tc::bar_init(&o_empty[k], kRows);
+      tc::bar_init(&k_full[k], 1);
+      tc::bar_init(&k_empty[k], 1);
+      tc::bar_init(&v_full[k], kRows);
+      tc::bar_init(&v_empty[k], 1);
+    }
+    tc::fence_bar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
+  tc::before_sync();
+  __syncthreads();
+  tc::after_sync();
+  auto give_up = [&]() { atomicOr(&s_abort, 1); };
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+
+  if (warp >= 12 && warp < 16) {
+    // ---------------------------------------------------------------- producers
+    constexpr int RPI = 32 / CH;                      // Q rows per warp instruction
+    const int pt = tid - 384;                         // 0..127
+    const int wr = (warp - 12) * 32;
+    TileCursor cur;
+    bool have = first_tile(a.src, n_items, EPT, cur);
+    int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
+    int T = 0, I = 0;
+    bool pending = false;                             // tile T-1 issued, not yet confirmed
+    auto confirm_last = [&](bool newer_outstanding) {
+      if (newer_outstanding) tc::cp_async_wait<1>(); else tc::cp_async_wait<0>();
+      tc::fence_async_smem();
+      tc::bar_arrive(&q_full[(T - 1) % kNQ]);
+    };
+    // V rows of an item: thread pt holds chunks (key, c) = (lin % 64, lin / 64) for
+    // lin = pt + 128 u; loaded one item ahead, transposed into the V stage at the item start
+    constexpr int VU = 64 * CH / kRows;
+    uint4 vreg[VU];
+    auto load_v = [&](const ItemView& v) {
+#pragma unroll
+      for (int u = 0; u < VU; ++u) {
+        const int lin = pt + kRows * u, key = lin % 64, c = lin / 64;
+        const int64_t j = static_cast<int64_t>(v.kbase) + key;
+        vreg[u] = make_uint4(0, 0, 0, 0);
+        if (j < s.N) vreg[u] = ldg_u4(a.V + ((static_cast<int64_t>(v.b) * s.N + j) * s.Hkv + v.kv) * D + c * 8);
+      }
+    };
+    if (have) load_v(cur.v);
+    while (have && !aborted()) {
+      if (cur.j == 0) {
+        // the control thread may need the pending tile before it can free a V stage
+        if (pending) {
+          confirm_last(false);
+          pending = false;
+        }
+        // V^T of the item (lanes walk keys: no bank conflicts); keys past N are zero
+        const int vs = I % kNKV;
+        if (!tc::bar_wait(&v_empty[vs], ((I / kNKV) & 1) ^ 1)) { give_up(); break; }
+        unsigned char* vt = sm + L::oV + vs * L::V_BYTES;
+#pragma unroll
+        for (int u = 0; u < VU; ++u) {
+          const int lin = pt + kRows * u, key = lin % 64, c = lin / 64;
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&vreg[u]);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) *reinterpret_cast<__nv_bfloat16*>(vt + tc::sw128(c * 8 + q, key)) = e[q];
+        }
+        tc::fence_async_smem();
+        tc::bar_arrive(&v_full[vs]);
+        ++I;
+        // the next item's V rows load while this item's tiles are gathered
+        const int it_n = cur.it + static_cast<int>(gridDim.x);
+        if (it_n < n_items) load_v(view_item(a.src, it_n));
+      }
+      TileCursor nxt = cur;
+      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
+      const int st = T % kNQ;
+      if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
+      const uint32_t dst = aQ + st * L::Q_BYTES;
+      const int c = lane % CH;
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        const int rl = k * RPI + lane / CH;
+        const int qi = __shfl_sync(0xffffffffu, pk, rl) >> 6;
+        const int r = wr + rl;
+        const __nv_bfloat16* src =
+            a.Q + ((static_cast<int64_t>(cur.v.b) * s.N + (qi < 0 ? 0 : qi)) * s.Hq + cur.v.kv * G + r % G) * D;
+        tc::cp_async16(dst + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8), src + c * 8, qi >= 0);
+      }
+      tc::cp_async_commit();
+      if (pending) confirm_last(true);                // tile T-1, a tile's time after its copies
+      pending = true;
+      cur = nxt;
+      have = have_n;
+      pk = pk_n;
+      ++T;
+    }
+    if (pending) confirm_last(false);
+    tc::cp_async_wait<0>();
+  } else if (warp == 16) {
+    // ---------------------------------------------------------------- control
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
+      // K of item number I (this CTA's I-th item, index it) into stage I % 2
+      auto load_k = [&](int I, int it) {
+        const int ks = I % kNKV;
+        if (!tc::bar_wait(&k_empty[ks], ((I / kNKV) & 1) ^ 1)) { give_up(); return; }
+        const ItemView v = view_item(a.src, it);
+        tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+      };
+      // S of tile T (cursor c, item number I)
+      auto issue_s = [&](const TileCursor& c, int T, int I) -> bool {
+        const int ks = I % kNKV, st = T % kNQ, ss = T & 1;
+        if (c.j == 0) {
+          if (c.it + static_cast<int>(gridDim.x) < n_items) load_k(I + 1, c.it + gridDim.x);
+          if (!tc::bar_wait(&k_full[ks], (I / kNKV) & 1)) return false;
+        }
+        if (!tc::bar_wait(&q_full[st], (T / kNQ) & 1) || !tc::bar_wait(&s_empty[ss], ((T >> 1) & 1) ^ 1))
+          return false;
+        tc::after_sync();
+#pragma unroll
+        for (int k2 = 0; k2 < D / 16; ++k2)
+          tc::mma(tmem_base + 64 * ss, tc::desc(aQ + st * L::Q_BYTES + (k2 >> 2) * (kRows * 128) + (k2 & 3) * 32),
+                  tc::desc(aK + ks * L::K_BYTES + (k2 >> 2) * (64 * 128) + (k2 & 3) * 32), idS, k2 > 0);
+        tc::commit(&s_full[ss]);
+        tc::commit(&q_empty[st]);
+        if (c.j + 1 == c.n_tiles) tc::commit(&k_empty[ks]);   // the item's last S
+        return true;
+      };
+      // P V of tile T
+      auto issue_pv = [&](const TileCursor& c, int T, int I) -> bool {
+        const int vs = I % kNKV, ps = T % kNP, os = T & 1;
+        if (c.j == 0 && !tc::bar_wait(&v_full[vs], (I / kNKV) & 1)) return false;
+        if (!tc::bar_wait(&p_full[ps], (T / kNP) & 1) || !tc::bar_wait(&o_empty[os], ((T >> 1) & 1) ^ 1))
+          return false;
+        tc::after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma(tmem_base + L::tmem_o + os * D, tc::desc(aP + ps * L::P_BYTES + kk * 32),
+                  tc::desc(aV + vs * L::V_BYTES + kk * 32), idO, kk > 0);
+        tc::commit(&o_full[os]);
+        tc::commit(&p_empty[ps]);
+        if (c.j + 1 == c.n_tiles) tc::commit(&v_empty[vs]);   // the item's last P V
+        return true;
+      };
+      TileCursor cs, cp;
+      bool have_s = first_tile(a.src, n_items, EPT, cs);
+      bool have_p = have_s;
+      cp = cs;
+      int Ts = 0, Is = 0, Tp = 0, Ip = 0;
+      if (have_s) {
+        load_k(0, cs.it);
+        if (!issue_s(cs, 0, 0)) give_up();
+        Ts = 1;
+        have_s = next_tile(a.src, n_items, EPT, cs);
+        if (have_s && cs.j == 0) Is = 1;
+      }
+      while (have_p && !aborted()) {
+        if (have_s) {                                        // S of the next tile first
+          if (!issue_s(cs, Ts, Is)) { give_up(); break; }
+          ++Ts;
+          have_s = next_tile(a.src, n_items, EPT, cs);
+          if (have_s && cs.j == 0) ++Is;
+        }
+        if (!issue_pv(cp, Tp, Ip)) { give_up(); break; }
+        ++Tp;
+        have_p = next_tile(a.src, n_items, EPT, cp);
+        if (have_p && cp.j == 0) ++Ip;
+      }
+    }
+  }
+  else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax
+    const int sg = warp >> 2;                         // tiles T with T % 2 == sg
+    const int r = tid & (kRows - 1);
+    const int h = r % G;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c1 = s.scale * kLog2e;
+    auto row_lse2 = [&](const TileCursor& c, int pkv) {
+      if (pkv < 0) return 0.f;
+      return a.lse_rows[(static_cast<int64_t>(c.v.b) * s.Hq + c.v.kv * G + h) * s.N + (pkv >> 6)] * kLog2e;
+    };
+    TileCursor cur;
+    bool have = first_tile(a.src, n_items, EPT, cur);
+    int T = 0;
+    if (have && sg == 1) {
+      have = next_tile(a.src, n_items, EPT, cur);
+      T = 1;
+    }
+    int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
+    float l2 = have ? row_lse2(cur, pk) : 0.f;
+    while (have && !aborted()) {
+      TileCursor nxt = cur;
+      bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      if (have_n) have_n = next_tile(a.src, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
+      const bool ok = tc::bar_wait(&s_full[sg], (T >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
+      tc::after_sync();
+      const float l2_n = have_n ? row_lse2(nxt, pk_n) : 0.f;   // in flight during the math
+      const int lim = pk < 0 ? -1 : (pk >> 6) - cur.v.kbase;    // key c is visible iff c <= lim
+      const int ps = T % kNP;
+      unsigned char* pt = sm + L::oP + ps * L::P_BYTES;
+      // the row's 64 keys in two halves of 32 (fewer live registers)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float sv[32];
+        tc::tmem_ld32(tmem_base + 64 * sg + 32 * half + lane_off, sv);
+        if (half == 1) {                                       // the S stage is free for S(T + 2)
+          tc::before_sync();
+          tc::bar_arrive(&s_empty[sg]);
+        }
+        const int lh = lim - 32 * half;
+        if (lh >= 31) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = tc::ex2(fmaf(sv[c], c1, -l2));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = c <= lh ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
+        }
+        if (half == 0) {
+          const bool ok2 = tc::bar_wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
+          if (!__all_sync(0xffffffffu, ok2)) {
+            give_up();
+            break;
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint4 pkd;
+          pkd.x = pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]);
+          pkd.y = pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]);
+          pkd.z = pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]);
+          pkd.w = pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]);
+          *reinterpret_cast<uint4*>(pt + tc::sw128(r, 32 * half + cc * 8)) = pkd;
+        }
+      }
+      if (aborted()) break;
+      tc::fence_async_smem();
+      tc::bar_arrive(&p_full[ps]);
+      cur = nxt;
+      have = have_n;
+      pk = pk_n;
+      l2 = l2_n;
+      T += 2;
+    }
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- epilogue
+    // row r's O, 32 columns per round, into staging tile (round & 1) at +128 r with 16-byte
+    // chunks swizzled by r & 7; every lane commits one bulk group per round (empty unless it
+    // issued), so "all but the newest group read out" means the other tile is free again
+    const int r = tid - 256;
+    const int h = r % G;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    TileCursor cur;
+    bool have = first_tile(a.src, n_items, EPT, cur);
+    int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
+    int T = 0, rd_all = 0;
+    while (have && !aborted()) {
+      TileCursor nxt = cur;
+      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
+      const int os = T & 1;
+      const bool ok = tc::bar_wait(&o_full[os], (T >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
+      tc::after_sync();
+      const bool issuer = h == 0 && pk >= 0;
+      const int unit = (cur.v.b * s.N + (pk < 0 ? 0 : (pk >> 6))) * s.Hkv + cur.v.kv;
+#pragma unroll
+      for (int rd = 0; rd < D / 32; ++rd, ++rd_all) {
+        float ov[32];
+        tc::tmem_ld32(tmem_base + L::tmem_o + os * D + 32 * rd + lane_off, ov);
+        if (rd == D / 32 - 1) {                        // the O stage is free for P V of T + 2
+          tc::before_sync();
+          tc::bar_arrive(&o_empty[os]);
+        }
+        const int sb = rd_all & 1;
+        tc::bulk_wait_read<1>();
+        __syncwarp();
+        unsigned char* stg = sm + L::oS + sb * L::STG;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+        tc::fence_async_smem();
+        __syncwarp();
+        if (issuer) tc::tma_reduce_add3(&omap, 32 * rd, 0, unit, aS + sb * L::STG + r * 128);
+        tc::bulk_commit();
+      }
+      cur = nxt;
+      have = have_n;
+      pk = pk_n;
+      ++T;
+    }
+    tc::bulk_wait<0>();
+  }
+  tc::before_sync();
+  __syncthreads();
+  if (tid == 0 && s_abort) atomicOr(a.status, PISA_ETIMEOUT);
+  if (warp == 0) {
+    tc::after_sync();
+    tc::tmem_free(tmem_base, 512);
+  }
+}
+
+template <int D, int G>
+int attn_ws_launch(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& om, int grid, cudaStream_t st) {
+  const int smem = AttnSmem<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_ws_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ProfScope ps(st, "attn_fwd_tc");
+  attn_ws_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km, om);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Attention output pass over the grouped (selected leaf, query) pairs: adds every row's
+// normalised block contributions into the fp32 accumulator o_acc [B, N, Hq, d].
+int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                       const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
+                       float* o_acc, int32_t* status, cudaStream_t st) {
+  CUtensorMap km, om;
+  const uint64_t d = static_cast<uint64_t>(s.d);
+  {
+    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv), static_cast<uint64_t>(s.N),
+                              static_cast<uint64_t>(s.B)};
+    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv, d * 2 * s.Hkv * s.N};
+    const uint32_t box[4] = {64, 1, 64, 1};
+    if (int e = encode_tmap(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, strides, box)) return e;
+  }
+  {
+    const uint64_t dims[3] = {d, static_cast<uint64_t>(s.G), static_cast<uint64_t>(s.B) * s.N * s.Hkv};
+    const uint64_t strides[2] = {d * 4, d * 4 * s.G};
+    const uint32_t box[3] = {32, static_cast<uint32_t>(s.G), 1};
+    if (int e = encode_tmap(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o_acc, dims, strides, box)) return e;
+  }
+  AttnArgs a{};
+  a.s = s;
+  a.src.gp = gp;
+  a.src.items = items;
+  a.src.list = list;
+  a.src.Hkv = s.Hkv;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.V = static_cast<const __nv_bfloat16*>(V);
+  a.n_items = n_items;
+  a.lse_rows = lse_rows;
+  a.status = status;
+  const int64_t mi = gp.max_items;
+  const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
+#define PISA_ATTN_CASE(DD, GG) \
+  if (s.d == DD && s.G == GG) return attn_ws_launch<DD, GG>(a, km, om, grid, st);
+  PISA_ATTN_CASE(128, 1) PISA_ATTN_CASE(128, 2) PISA_ATTN_CASE(128, 4) PISA_ATTN_CASE(128, 8)
+  PISA_ATTN_CASE(64, 1) PISA_ATTN_CASE(64, 2) PISA_ATTN_CASE(64, 4) PISA_ATTN_CASE(64, 8)
+#undef PISA_ATTN_CASE
+  return static_cast<int>(cudaErrorNotSupported);
+}
+
+}  // namespace pisa

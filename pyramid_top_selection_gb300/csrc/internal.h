@@ -52,6 +52,7 @@ struct AttnFwdWs {
 struct AttnBwdWs {
   size_t delta, part_dq, dk_acc, dv_acc, total;
 };
+int sm_count();
 SelectWs select_ws(const Dims& s, const Geo& g);
 AttnFwdWs attn_fwd_ws(const Dims& s);
 AttnBwdWs attn_bwd_ws(const Dims& s);

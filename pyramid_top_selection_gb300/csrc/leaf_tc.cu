@@ -26,6 +26,7 @@
 #include "group.h"
 #include "profile.h"
 #include "tc.cuh"
+#include "tiles.cuh"
 #include "tmap.h"
 
 namespace pisa {
@@ -51,66 +52,15 @@ struct LeafSmem {
 
 struct LeafArgs {
   Dims s;
-  GroupPlan gp;
+  ItemSource src;
   const __nv_bfloat16* Q;
-  const int32_t* list;
-  const int4* items;
   const int32_t* n_items;
   int W;
   float* pair_score;   // [heads, N, W]
   float* pair_head;    // [heads, N, W, G] or NULL
+  float* block_lse;    // when set: per-row LSE [B, Hq, N, W] instead of the scores
   int32_t* status;
 };
-
-// One item's fields, as every role decodes them.
-struct ItemView {
-  int beg, n_ent, kbase, b, kv;
-  int64_t head;
-};
-
-__device__ __forceinline__ ItemView view_item(const LeafArgs& a, int it) {
-  const int4 item = a.items[it];
-  ItemView v;
-  v.beg = item.y;
-  v.n_ent = item.z;
-  v.kbase = a.gp.leaf_of(item.x) * 64;
-  v.head = a.gp.head_of(item.x);
-  v.b = static_cast<int>(v.head / a.s.Hkv);
-  v.kv = static_cast<int>(v.head % a.s.Hkv);
-  return v;
-}
-
-// Position in this CTA's tile sequence: items blockIdx.x, blockIdx.x + gridDim.x, ..., each
-// cut into tiles of `ept` entries.
-struct TileCursor {
-  int it, j, n_tiles;
-  ItemView v;
-};
-
-__device__ __forceinline__ bool first_tile(const LeafArgs& a, int n_items, int ept, TileCursor& c) {
-  c.it = blockIdx.x;
-  c.j = 0;
-  if (c.it >= n_items) return false;
-  c.v = view_item(a, c.it);
-  c.n_tiles = (c.v.n_ent + ept - 1) / ept;
-  return true;
-}
-
-__device__ __forceinline__ bool next_tile(const LeafArgs& a, int n_items, int ept, TileCursor& c) {
-  if (++c.j < c.n_tiles) return true;
-  c.it += gridDim.x;
-  c.j = 0;
-  if (c.it >= n_items) return false;
-  c.v = view_item(a, c.it);
-  c.n_tiles = (c.v.n_ent + ept - 1) / ept;
-  return true;
-}
-
-// List entry (query << 6 | slot) of tile row r, -1 past the end of the item.
-__device__ __forceinline__ int row_entry(const LeafArgs& a, const TileCursor& c, int ept, int G, int r) {
-  const int e = c.j * ept + r / G;
-  return e < c.v.n_ent ? a.list[c.v.beg + e] : -1;
-}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -161,13 +111,13 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     constexpr int RPI = 32 / CH;                      // rows per warp instruction
     const int wr = (warp - 8) * 32;                   // the warp's first tile row
     TileCursor cur;
-    bool have = first_tile(a, n_items, EPT, cur);
-    int pk = have ? row_entry(a, cur, EPT, G, wr + lane) : -1;
+    bool have = first_tile(a.src, n_items, EPT, cur);
+    int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
     int T = 0;
     while (have && !aborted()) {
       TileCursor nxt = cur;
-      const bool have_n = next_tile(a, n_items, EPT, nxt);
-      const int pk_n = have_n ? row_entry(a, nxt, EPT, G, wr + lane) : -1;
+      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
       const int st = T % kNQ;
       if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
       const uint32_t dst = aQ + st * L::Q_BYTES;
@@ -204,7 +154,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       auto load_k = [&](int I, int it) {
         const int ks = I % kNK;
         if (!tc::bar_wait(&k_empty[ks], ((I / kNK) & 1) ^ 1)) { give_up(); return; }
-        const ItemView v = view_item(a, it);
+        const ItemView v = view_item(a.src, it);
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
@@ -216,7 +166,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
         if (it + static_cast<int>(gridDim.x) < n_items) load_k(I + 1, it + gridDim.x);
         const int ks = I % kNK;
         if (!tc::bar_wait(&k_full[ks], (I / kNK) & 1)) { give_up(); break; }
-        const ItemView v = view_item(a, it);
+        const ItemView v = view_item(a.src, it);
         const int n_tiles = (v.n_ent + EPT - 1) / EPT;
         for (int j = 0; j < n_tiles; ++j, ++T) {
           const int st = T % kNQ, ss = T % kNS;
@@ -246,18 +196,18 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     const float c1 = s.scale * kLog2e;
     const int h = r % G;
     TileCursor cur;
-    bool have = first_tile(a, n_items, EPT, cur);
+    bool have = first_tile(a.src, n_items, EPT, cur);
     int T = 0;
     if (have && sg == 1) {
-      have = next_tile(a, n_items, EPT, cur);
+      have = next_tile(a.src, n_items, EPT, cur);
       T = 1;
     }
-    int pk = have ? row_entry(a, cur, EPT, G, r) : -1;
+    int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     while (have && !aborted()) {
       TileCursor nxt = cur;
-      bool have_n = next_tile(a, n_items, EPT, nxt);
-      if (have_n) have_n = next_tile(a, n_items, EPT, nxt);
-      const int pk_n = have_n ? row_entry(a, nxt, EPT, G, r) : -1;   // in flight during this tile
+      bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      if (have_n) have_n = next_tile(a.src, n_items, EPT, nxt);
+      const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;   // in flight during this tile
       const int ss = T % kNS;
       const bool ok = tc::bar_wait(&s_full[ss], (T / kNS) & 1);
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }   // warp-uniform exit
@@ -284,6 +234,15 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) lq[c & 3] += tc::ex2(fmaf(sv[c], c1, -m2));
         lse = (m2 + tc::lg2((lq[0] + lq[1]) + (lq[2] + lq[3]))) * kLn2;
+      }
+      if (a.block_lse) {
+        if (pk >= 0)
+          a.block_lse[((static_cast<int64_t>(cur.v.b) * s.Hq + cur.v.kv * G + h) * s.N + qi) * a.W + (pk & 63)] = lse;
+        cur = nxt;
+        have = have_n;
+        pk = pk_n;
+        T += 2;
+        continue;
       }
       // G adjacent lanes hold the heads of one query (a padding entry is whole)
       float sum = lse;
@@ -314,11 +273,14 @@ int leaf_tc_launch(const LeafArgs& a, const CUtensorMap& km, int grid, cudaStrea
   const int smem = LeafSmem<D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(leaf_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  ProfScope ps(st, "leaf_score");
+  ProfScope ps(st, a.block_lse ? "attn_lse_tc" : "leaf_score");
   leaf_tc_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km);
   return cudaGetLastError();
 }
 
+}  // namespace
+
+// Streaming multiprocessors of the current device (persistent grids: one CTA per SM).
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -330,13 +292,11 @@ int sm_count() {
   return n;
 }
 
-}  // namespace
+namespace {
 
-// Exact leaf scores of the grouped (candidate leaf, query) pairs: pair_score[unit, slot] =
-// sum over the G heads of the leaf's LSE; per-head terms into pair_head when it is given.
-int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
-                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
-                   int32_t* status, cudaStream_t st) {
+int leaf_tc_run(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                float* block_lse, int32_t* status, cudaStream_t st) {
   CUtensorMap km;
   {
     const uint64_t d = static_cast<uint64_t>(s.d);
@@ -348,14 +308,16 @@ int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void
   }
   LeafArgs a{};
   a.s = s;
-  a.gp = gp;
+  a.src.gp = gp;
+  a.src.items = items;
+  a.src.list = list;
+  a.src.Hkv = s.Hkv;
   a.Q = static_cast<const __nv_bfloat16*>(Q);
-  a.list = list;
-  a.items = items;
   a.n_items = n_items;
   a.W = W;
   a.pair_score = pair_score;
   a.pair_head = pair_head;
+  a.block_lse = block_lse;
   a.status = status;
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
@@ -365,6 +327,24 @@ int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void
   PISA_LEAF_CASE(64, 1) PISA_LEAF_CASE(64, 2) PISA_LEAF_CASE(64, 4) PISA_LEAF_CASE(64, 8)
 #undef PISA_LEAF_CASE
   return static_cast<int>(cudaErrorNotSupported);
+}
+
+}  // namespace
+
+// Exact leaf scores of the grouped (candidate leaf, query) pairs: pair_score[unit, slot] =
+// sum over the G heads of the leaf's LSE; per-head terms into pair_head when it is given.
+int launch_leaf_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                   const int4* items, const int32_t* n_items, int W, float* pair_score, float* pair_head,
+                   int32_t* status, cudaStream_t st) {
+  return leaf_tc_run(s, gp, Q, K, list, items, n_items, W, pair_score, pair_head, nullptr, status, st);
+}
+
+// Per-(row, block) LSEs of the grouped (selected leaf, query) pairs of an attention call:
+// block_lse[b, h, i, slot] = log sum_{j in the leaf, j <= i} exp(s q_{i,h} . k_j).
+int launch_block_lse_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const int32_t* list,
+                        const int4* items, const int32_t* n_items, float* block_lse, int32_t* status,
+                        cudaStream_t st) {
+  return leaf_tc_run(s, gp, Q, K, list, items, n_items, s.K, nullptr, nullptr, block_lse, status, st);
 }
 
 }  // namespace pisa
