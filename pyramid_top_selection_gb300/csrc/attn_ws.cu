@@ -10,9 +10,9 @@
 // key is visited; so every block's contribution exp(s q.k - lse) v is final and the blocks
 // of a row are summed straight into an fp32 accumulator, in any order.
 //
-// One CTA per SM walks the work items (a selected leaf of one KV head and the (query, head)
-// rows that chose it) with a static stride, in tiles of 128 rows. Roles, connected by
-// mbarrier rings:
+// One CTA per SM takes work items (a selected leaf of one KV head and the (query, head) rows
+// that chose it) from a global counter through its item queue (tiles.cuh) and walks them in
+// tiles of 128 rows. Roles, connected by mbarrier rings:
 //   * producers (warps 12-15): per item, V^T (d x 64) transposed into a 2-stage ring; per
 //     tile, the query rows gathered with cp.async (whole rows per warp instruction) into a
 //     2-stage ring of swizzled Q tiles, confirmed one tile later (the next item's V rows
@@ -24,7 +24,8 @@
 //     - log2e lse) on the visible keys, bf16, into a 2-stage ring of swizzled P tiles;
 //   * epilogue (warps 8-11): O row from TMEM, 32 columns at a time, through two swizzled
 //     staging tiles; the lane holding a query's first head adds the query's G heads x 32
-//     columns into the accumulator with one TMA tensor reduce-add.
+//     columns into the accumulator with one TMA tensor reduce-add;
+//   * scheduler (warp 17, one thread): fills the item queue.
 // Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
 // its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
 #include "device.cuh"
@@ -40,7 +41,8 @@ namespace {
 
 constexpr int kRows = 128;
 constexpr int kNQ = 2, kNP = 2, kNKV = 2;   // Q, P, K/V stages; S and O have 2 TMEM stages
-constexpr int kThreads = 544;               // softmax 0-255, epilogue 256-383, producers 384-511, control 512-543
+constexpr int kThreads = 576;               // softmax 0-255, epilogue 256-383, producers 384-511, control, scheduler
+constexpr int kConsumerWarps = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -65,6 +67,7 @@ struct AttnArgs {
   const int32_t* n_items;
   const float* lse_rows;   // [B, Hq, N]
   int32_t* status;
+  int32_t* next_item;      // zeroed item counter
 };
 
 template <int D, int G>
@@ -78,6 +81,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       o_full[2], o_empty[2], k_full[kNKV], k_empty[kNKV], v_full[kNKV], v_empty[kNKV];
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
+  __shared__ ItemQueue s_q;
 
   const Dims& s = a.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -101,6 +105,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::bar_init(&v_full[k], kRows);
       tc::bar_init(&v_empty[k], 1);
     }
+    queue_init(s_q, kConsumerWarps);
     tc::fence_bar_init();
     s_abort = 0;
   }
@@ -116,8 +121,9 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     constexpr int RPI = 32 / CH;                      // Q rows per warp instruction
     const int pt = tid - 384;                         // 0..127
     const int wr = (warp - 12) * 32;
-    TileCursor cur;
-    bool have = first_tile(a.src, n_items, EPT, cur);
+    DynCursor cur;
+    const bool lead = warp == 12;                     // marks the queue positions demanded
+    bool have = dyn_first(s_q, EPT, &s_abort, cur, true, lead);
     int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
     int T = 0, I = 0;
     bool pending = false;                             // tile T-1 issued, not yet confirmed
@@ -162,11 +168,11 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::bar_arrive(&v_full[vs]);
         ++I;
         // the next item's V rows load while this item's tiles are gathered
-        const int it_n = cur.it + static_cast<int>(gridDim.x);
-        if (it_n < n_items) load_v(view_item(a.src, it_n));
+        const ItemView v_n = queue_peek(s_q, cur.k + 1, &s_abort);
+        if (v_n.n_ent >= 0) load_v(v_n);
       }
-      TileCursor nxt = cur;
-      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      DynCursor nxt = cur;
+      const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true, lead);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
       const int st = T % kNQ;
       if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
@@ -195,21 +201,21 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     // ---------------------------------------------------------------- control
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
-      // K of item number I (this CTA's I-th item, index it) into stage I % 2
-      auto load_k = [&](int I, int it) {
+      // K of the CTA's item number I into stage I % 2
+      auto load_k = [&](int I, const ItemView& v) {
         const int ks = I % kNKV;
         if (!tc::bar_wait(&k_empty[ks], ((I / kNKV) & 1) ^ 1)) { give_up(); return; }
-        const ItemView v = view_item(a.src, it);
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
       };
       // S of tile T (cursor c, item number I)
-      auto issue_s = [&](const TileCursor& c, int T, int I) -> bool {
+      auto issue_s = [&](const DynCursor& c, int T, int I) -> bool {
         const int ks = I % kNKV, st = T % kNQ, ss = T & 1;
         if (c.j == 0) {
-          if (c.it + static_cast<int>(gridDim.x) < n_items) load_k(I + 1, c.it + gridDim.x);
+          const ItemView v_n = queue_peek(s_q, c.k + 1, &s_abort);
+          if (v_n.n_ent >= 0) load_k(I + 1, v_n);
           if (!tc::bar_wait(&k_full[ks], (I / kNKV) & 1)) return false;
         }
         if (!tc::bar_wait(&q_full[st], (T / kNQ) & 1) || !tc::bar_wait(&s_empty[ss], ((T >> 1) & 1) ^ 1))
@@ -225,7 +231,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         return true;
       };
       // P V of tile T
-      auto issue_pv = [&](const TileCursor& c, int T, int I) -> bool {
+      auto issue_pv = [&](const DynCursor& c, int T, int I) -> bool {
         const int vs = I % kNKV, ps = T % kNP, os = T & 1;
         if (c.j == 0 && !tc::bar_wait(&v_full[vs], (I / kNKV) & 1)) return false;
         if (!tc::bar_wait(&p_full[ps], (T / kNP) & 1) || !tc::bar_wait(&o_empty[os], ((T >> 1) & 1) ^ 1))
@@ -240,28 +246,28 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         if (c.j + 1 == c.n_tiles) tc::commit(&v_empty[vs]);   // the item's last P V
         return true;
       };
-      TileCursor cs, cp;
-      bool have_s = first_tile(a.src, n_items, EPT, cs);
-      bool have_p = have_s;
-      cp = cs;
+      // cs (S, one tile ahead) only looks; cp (P V) frees the positions it leaves
+      DynCursor cs, cp;
+      bool have_s = dyn_first(s_q, EPT, &s_abort, cs, false, false, 1u);
+      bool have_p = dyn_first(s_q, EPT, &s_abort, cp, true, false, 1u);
       int Ts = 0, Is = 0, Tp = 0, Ip = 0;
       if (have_s) {
-        load_k(0, cs.it);
+        load_k(0, cs.v);
         if (!issue_s(cs, 0, 0)) give_up();
         Ts = 1;
-        have_s = next_tile(a.src, n_items, EPT, cs);
+        have_s = dyn_next(s_q, EPT, &s_abort, cs, false, false, 1u);
         if (have_s && cs.j == 0) Is = 1;
       }
       while (have_p && !aborted()) {
         if (have_s) {                                        // S of the next tile first
           if (!issue_s(cs, Ts, Is)) { give_up(); break; }
           ++Ts;
-          have_s = next_tile(a.src, n_items, EPT, cs);
+          have_s = dyn_next(s_q, EPT, &s_abort, cs, false, false, 1u);
           if (have_s && cs.j == 0) ++Is;
         }
         if (!issue_pv(cp, Tp, Ip)) { give_up(); break; }
         ++Tp;
-        have_p = next_tile(a.src, n_items, EPT, cp);
+        have_p = dyn_next(s_q, EPT, &s_abort, cp, true, false, 1u);
         if (have_p && cp.j == 0) ++Ip;
       }
     }
@@ -273,23 +279,23 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     const int h = r % G;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c1 = s.scale * kLog2e;
-    auto row_lse2 = [&](const TileCursor& c, int pkv) {
+    auto row_lse2 = [&](const DynCursor& c, int pkv) {
       if (pkv < 0) return 0.f;
       return a.lse_rows[(static_cast<int64_t>(c.v.b) * s.Hq + c.v.kv * G + h) * s.N + (pkv >> 6)] * kLog2e;
     };
-    TileCursor cur;
-    bool have = first_tile(a.src, n_items, EPT, cur);
+    DynCursor cur;
+    bool have = dyn_first(s_q, EPT, &s_abort, cur, true);
     int T = 0;
     if (have && sg == 1) {
-      have = next_tile(a.src, n_items, EPT, cur);
+      have = dyn_next(s_q, EPT, &s_abort, cur, true);
       T = 1;
     }
     int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     float l2 = have ? row_lse2(cur, pk) : 0.f;
     while (have && !aborted()) {
-      TileCursor nxt = cur;
-      bool have_n = next_tile(a.src, n_items, EPT, nxt);
-      if (have_n) have_n = next_tile(a.src, n_items, EPT, nxt);
+      DynCursor nxt = cur;
+      bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
+      if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
       const bool ok = tc::bar_wait(&s_full[sg], (T >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
@@ -349,13 +355,13 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     const int r = tid - 256;
     const int h = r % G;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    TileCursor cur;
-    bool have = first_tile(a.src, n_items, EPT, cur);
+    DynCursor cur;
+    bool have = dyn_first(s_q, EPT, &s_abort, cur, true);
     int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     int T = 0, rd_all = 0;
     while (have && !aborted()) {
-      TileCursor nxt = cur;
-      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      DynCursor nxt = cur;
+      const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
       const int os = T & 1;
       const bool ok = tc::bar_wait(&o_full[os], (T >> 1) & 1);
@@ -390,6 +396,9 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       ++T;
     }
     tc::bulk_wait<0>();
+  } else if (warp == 17) {
+    // ---------------------------------------------------------------- scheduler
+    if (lane == 0) queue_fill(s_q, a.src, a.next_item, n_items, &s_abort);
   }
   tc::before_sync();
   __syncthreads();
@@ -443,6 +452,7 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   a.n_items = n_items;
   a.lse_rows = lse_rows;
   a.status = status;
+  a.next_item = status + 32;
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
 #define PISA_ATTN_CASE(DD, GG) \

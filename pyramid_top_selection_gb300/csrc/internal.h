@@ -43,6 +43,8 @@ struct Dims {
 
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.
 // total: without the per-head leaf terms; total_head: with them (head_lse requested).
+// status: 256 bytes zeroed before the op's kernels; word 0 collects error bits, words 16
+// and 32 are the item counters of the persistent leaf-scoring and attention kernels.
 struct SelectWs {
   size_t split, cand, cscore, status, group, total, chead, total_head;
 };

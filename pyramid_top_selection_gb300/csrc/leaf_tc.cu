@@ -6,9 +6,10 @@
 // KV head sum their LSEs; "Reference value of the work": the queries that use the same leaf
 // block are grouped into tiles so the block's keys are read once per tile.
 //
-// One CTA per SM walks the work items (a candidate leaf of one KV head and the (query,
-// head) rows that have it among their candidates) with a static stride, in tiles of 128
-// rows. Roles, connected by mbarrier rings so that no role waits on another's latency:
+// One CTA per SM takes work items (a candidate leaf of one KV head and the (query, head)
+// rows that have it among their candidates) from a global counter through its item queue
+// (tiles.cuh) and walks them in tiles of 128 rows. Roles, connected by mbarrier rings so
+// that no role waits on another's latency:
 //   * producers (warps 8-11, 32 tile rows per warp): gather the query vectors with cp.async
 //     into a 4-stage ring of swizzled Q tiles, each warp instruction copying whole rows
 //     (full 32-byte sectors); a thread confirms a tile's copies (wait, proxy fence,
@@ -19,7 +20,8 @@
 //   * softmax (two warpgroups, warps 0-3 and 4-7, on alternate tiles; thread = TMEM lane =
 //     tile row): reads its S row, frees the TMEM stage, and reduces the row to its LSE over
 //     the visible keys; the G rows of a query (adjacent lanes) sum their LSEs into the
-//     candidate's score.
+//     candidate's score;
+//   * scheduler (warp 13, one thread): fills the item queue.
 // Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
 // its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
 #include "device.cuh"
@@ -37,7 +39,8 @@ constexpr int kRows = 128;
 constexpr int kNQ = 4;            // Q tile stages
 constexpr int kNS = 4;            // TMEM S stages (64 columns each)
 constexpr int kNK = 2;            // K tile stages
-constexpr int kThreads = 416;     // softmax 0-255 (two warpgroups), producers 256-383, control 384-415
+constexpr int kThreads = 448;     // softmax 0-255 (two warpgroups), producers 256-383, control, scheduler
+constexpr int kConsumerWarps = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -60,6 +63,7 @@ struct LeafArgs {
   float* pair_head;    // [heads, N, W, G] or NULL
   float* block_lse;    // when set: per-row LSE [B, Hq, N, W] instead of the scores
   int32_t* status;
+  int32_t* next_item;  // zeroed item counter
 };
 
 template <int D, int G>
@@ -73,6 +77,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       k_empty[kNK];
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
+  __shared__ ItemQueue s_q;
 
   const Dims& s = a.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -93,6 +98,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       tc::bar_init(&k_full[k], 1);
       tc::bar_init(&k_empty[k], 1);
     }
+    queue_init(s_q, kConsumerWarps);
     tc::fence_bar_init();
     s_abort = 0;
   }
@@ -110,13 +116,14 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     // warp's 32, chunk (lane % CH) of row (lane / CH)
     constexpr int RPI = 32 / CH;                      // rows per warp instruction
     const int wr = (warp - 8) * 32;                   // the warp's first tile row
-    TileCursor cur;
-    bool have = first_tile(a.src, n_items, EPT, cur);
+    DynCursor cur;
+    const bool lead = warp == 8;                      // marks the queue positions demanded
+    bool have = dyn_first(s_q, EPT, &s_abort, cur, true, lead);
     int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
     int T = 0;
     while (have && !aborted()) {
-      TileCursor nxt = cur;
-      const bool have_n = next_tile(a.src, n_items, EPT, nxt);
+      DynCursor nxt = cur;
+      const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true, lead);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
       const int st = T % kNQ;
       if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
@@ -151,22 +158,22 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     // ---------------------------------------------------------------- control
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
-      auto load_k = [&](int I, int it) {
+      auto load_k = [&](int I, const ItemView& v) {
         const int ks = I % kNK;
         if (!tc::bar_wait(&k_empty[ks], ((I / kNK) & 1) ^ 1)) { give_up(); return; }
-        const ItemView v = view_item(a.src, it);
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
       };
       int T = 0, I = 0;
-      if (static_cast<int>(blockIdx.x) < n_items) load_k(0, blockIdx.x);
-      for (int it = blockIdx.x; it < n_items && !aborted(); it += gridDim.x, ++I) {
-        if (it + static_cast<int>(gridDim.x) < n_items) load_k(I + 1, it + gridDim.x);
+      ItemView v = queue_take(s_q, 0, &s_abort);
+      if (v.n_ent >= 0) load_k(0, v);
+      for (; v.n_ent >= 0 && !aborted(); ++I) {
+        const ItemView v_n = queue_take(s_q, I + 1, &s_abort);
+        if (v_n.n_ent >= 0) load_k(I + 1, v_n);
         const int ks = I % kNK;
         if (!tc::bar_wait(&k_full[ks], (I / kNK) & 1)) { give_up(); break; }
-        const ItemView v = view_item(a.src, it);
         const int n_tiles = (v.n_ent + EPT - 1) / EPT;
         for (int j = 0; j < n_tiles; ++j, ++T) {
           const int st = T % kNQ, ss = T % kNS;
@@ -184,6 +191,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
           tc::commit(&q_empty[st]);
         }
         tc::commit(&k_empty[ks]);
+        v = v_n;
       }
     }
   } else if (warp < 8) {
@@ -195,18 +203,18 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c1 = s.scale * kLog2e;
     const int h = r % G;
-    TileCursor cur;
-    bool have = first_tile(a.src, n_items, EPT, cur);
+    DynCursor cur;
+    bool have = dyn_first(s_q, EPT, &s_abort, cur, true);
     int T = 0;
     if (have && sg == 1) {
-      have = next_tile(a.src, n_items, EPT, cur);
+      have = dyn_next(s_q, EPT, &s_abort, cur, true);
       T = 1;
     }
     int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     while (have && !aborted()) {
-      TileCursor nxt = cur;
-      bool have_n = next_tile(a.src, n_items, EPT, nxt);
-      if (have_n) have_n = next_tile(a.src, n_items, EPT, nxt);
+      DynCursor nxt = cur;
+      bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
+      if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;   // in flight during this tile
       const int ss = T % kNS;
       const bool ok = tc::bar_wait(&s_full[ss], (T / kNS) & 1);
@@ -258,6 +266,9 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       pk = pk_n;
       T += 2;
     }
+  } else if (warp == 13) {
+    // ---------------------------------------------------------------- scheduler
+    if (lane == 0) queue_fill(s_q, a.src, a.next_item, n_items, &s_abort);
   }
   tc::before_sync();
   __syncthreads();
@@ -319,6 +330,7 @@ int leaf_tc_run(const Dims& s, const GroupPlan& gp, const void* Q, const void* K
   a.pair_head = pair_head;
   a.block_lse = block_lse;
   a.status = status;
+  a.next_item = status + 16;
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
 #define PISA_LEAF_CASE(DD, GG) \
