@@ -16,15 +16,74 @@ namespace pisa {
 
 namespace {
 
-__global__ void gcount_kernel(GroupPlan gp, const int32_t* __restrict__ sel, int32_t* __restrict__ counts) {
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < gp.total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = sel[e];
-    if (t >= 0) {
-      const int64_t unit = e / gp.W;
-      const int i = static_cast<int>(unit % gp.N);
-      atomicAdd(&counts[gp.bin(unit / gp.N, i, t)], 1);
-    }
+// Pairs are binned per block of kGQ consecutive units (head * N + query): their bins lie in
+// at most two consecutive (head, chunk) groups in every block but a rare one at a short last
+// chunk, so a block counts them in a shared-memory histogram of 2 * n0 leaves and touches
+// each global counter once per block instead of once per pair. A block whose range spans
+// more groups (or any block when the histogram does not fit) falls back to global atomics.
+constexpr int kGQ = 256;          // units per block
+constexpr int kGThreads = 512;
+
+struct BinRange {
+  int64_t e0, g0, h0;
+  int n, i0;       // pairs in the block; query of its first unit
+  bool local;
+};
+
+__device__ __forceinline__ int64_t group_of(const GroupPlan& gp, int64_t unit) {
+  return (unit / gp.N) * gp.nch + (unit % gp.N) / gp.Nq;
+}
+
+__device__ __forceinline__ BinRange bin_range(const GroupPlan& gp, bool local_ok) {
+  const int64_t units = gp.total / gp.W;
+  const int64_t u0 = blockIdx.x * static_cast<int64_t>(kGQ);
+  const int64_t u1 = min(u0 + kGQ, units);
+  BinRange r;
+  r.e0 = u0 * gp.W;
+  r.n = static_cast<int>((u1 - u0) * gp.W);
+  r.g0 = group_of(gp, u0);
+  r.h0 = u0 / gp.N;
+  r.i0 = static_cast<int>(u0 % gp.N);
+  r.local = local_ok && group_of(gp, u1 - 1) - r.g0 <= 1;
+  return r;
+}
+
+// Pair k of the block (32-bit arithmetic): its query i, slot and (head, chunk) group.
+__device__ __forceinline__ void pair_at(const GroupPlan& gp, const BinRange& r, int k, int& i, int& slot,
+                                        int64_t& g) {
+  const int lu = k / gp.W;
+  slot = k - lu * gp.W;
+  i = r.i0 + lu;
+  int64_t h = r.h0;
+  while (i >= gp.N) {
+    i -= gp.N;
+    ++h;
+  }
+  g = h * gp.nch + i / gp.Nq;
+}
+
+__global__ void __launch_bounds__(kGThreads)
+gcount_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, int32_t* __restrict__ counts) {
+  extern __shared__ int32_t hist[];                 // [2 * n0]
+  const BinRange r = bin_range(gp, local_ok);
+  if (r.local) {
+    for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) hist[k] = 0;
+    __syncthreads();
+  }
+  for (int k = threadIdx.x; k < r.n; k += kGThreads) {
+    const int t = sel[r.e0 + k];
+    if (t < 0 || t >= gp.n0) continue;
+    int i, slot;
+    int64_t g;
+    pair_at(gp, r, k, i, slot, g);
+    if (r.local) atomicAdd(&hist[(g - r.g0) * gp.n0 + t], 1);
+    else atomicAdd(&counts[g * gp.n0 + t], 1);
+  }
+  if (!r.local) return;
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) {
+    const int c = hist[k];
+    if (c) atomicAdd(&counts[r.g0 * gp.n0 + k], c);
   }
 }
 
@@ -64,18 +123,48 @@ __global__ void __launch_bounds__(1024) gscan_kernel(int32_t* counts, int64_t n)
   if (tid == 1023) counts[n] = run;
 }
 
-__global__ void gscatter_kernel(GroupPlan gp, const int32_t* __restrict__ sel, const int32_t* __restrict__ off,
-                                int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < gp.total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = sel[e];
-    if (t >= 0) {
-      const int64_t unit = e / gp.W;
-      const int slot = static_cast<int>(e - unit * gp.W);
-      const int i = static_cast<int>(unit % gp.N);
-      const int64_t bin = gp.bin(unit / gp.N, i, t);
+// Scatter: a local block ranks its pairs within each bin in shared memory, reserves each
+// bin's range with one global atomic, then writes list[off + base + rank] = (i << 6) | slot.
+__global__ void __launch_bounds__(kGThreads)
+gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, const int32_t* __restrict__ off,
+                int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
+  extern __shared__ int32_t hist[];                 // [2 * n0] counts, then bases; ranks [kGQ * W]
+  int32_t* rank = hist + 2 * gp.n0;
+  const BinRange r = bin_range(gp, local_ok);
+  if (r.local) {
+    for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) hist[k] = 0;
+    __syncthreads();
+  }
+  for (int k = threadIdx.x; k < r.n; k += kGThreads) {
+    const int t = sel[r.e0 + k];
+    if (t < 0 || t >= gp.n0) continue;
+    int i, slot;
+    int64_t g;
+    pair_at(gp, r, k, i, slot, g);
+    if (r.local) {
+      rank[k] = atomicAdd(&hist[(g - r.g0) * gp.n0 + t], 1);
+    } else {
+      const int64_t bin = g * gp.n0 + t;
       list[off[bin] + atomicAdd(&cursor[bin], 1)] = (i << 6) | slot;
     }
+  }
+  if (!r.local) return;
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) {
+    const int c = hist[k];
+    if (c) {
+      const int64_t bin = r.g0 * gp.n0 + k;
+      hist[k] = off[bin] + atomicAdd(&cursor[bin], c);
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < r.n; k += kGThreads) {
+    const int t = sel[r.e0 + k];
+    if (t < 0 || t >= gp.n0) continue;
+    int i, slot;
+    int64_t g;
+    pair_at(gp, r, k, i, slot, g);
+    list[hist[(g - r.g0) * gp.n0 + t] + rank[k]] = (i << 6) | slot;
   }
 }
 
@@ -145,17 +234,37 @@ int launch_group_items(const GroupPlan& gp, const int32_t* sel, char* ws, const 
   cudaError_t e = cudaMemsetAsync(off, 0, sizeof(int32_t) * (gp.bins + 1), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * (gp.bins + 1), st);
   if (e != cudaSuccess) return e;
-  {
-    ProfScope ps(st, "group_count");
-    gcount_kernel<<<grid_for(gp.total, 256), 256, 0, st>>>(gp, sel, off);
-  }
-  {
+  // shared-memory binning when the histogram and the ranks fit (n0 up to ~20K leaves)
+  const int64_t blocks = (gp.total / gp.W + kGQ - 1) / kGQ;
+  const size_t hist_bytes = static_cast<size_t>(2) * gp.n0 * 4;
+  const size_t rank_bytes = static_cast<size_t>(kGQ) * gp.W * 4;
+  const bool local_ok = hist_bytes + rank_bytes <= 200 * 1024;
+  const size_t sm_count = local_ok ? hist_bytes : 0, sm_scatter = local_ok ? hist_bytes + rank_bytes : 0;
+  if (blocks > 0) {
+    if (sm_scatter > 48 * 1024) {
+      e = cudaFuncSetAttribute(gscatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sm_scatter));
+      if (e == cudaSuccess && sm_count > 48 * 1024)
+        e = cudaFuncSetAttribute(gcount_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sm_count));
+      if (e != cudaSuccess) return e;
+    }
+    {
+      ProfScope ps(st, "group_count");
+      gcount_kernel<<<static_cast<unsigned>(blocks), kGThreads, sm_count, st>>>(gp, local_ok, sel, off);
+    }
+    {
+      ProfScope ps(st, "group_scan");
+      gscan_kernel<<<1, 1024, 0, st>>>(off, gp.bins);
+    }
+    {
+      ProfScope ps(st, "group_scatter");
+      gscatter_kernel<<<static_cast<unsigned>(blocks), kGThreads, sm_scatter, st>>>(gp, local_ok, sel, off,
+                                                                                     cursor, list);
+    }
+  } else {
     ProfScope ps(st, "group_scan");
     gscan_kernel<<<1, 1024, 0, st>>>(off, gp.bins);
-  }
-  {
-    ProfScope ps(st, "group_scatter");
-    gscatter_kernel<<<grid_for(gp.total, 256), 256, 0, st>>>(gp, sel, off, cursor, list);
   }
   {
     ProfScope ps(st, "group_items");
