@@ -337,50 +337,63 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
 }
 
 // ---------------------------------------------------------------------------- finish
-// One warp per (b, KV head, query): top K of the <= W candidate scores; ascending output.
+// One warp per (b, KV head, query): top K of the <= W (<= 64) candidate scores, output
+// ascending. Lane l holds candidates l and l + 32 in registers; ranks and output positions
+// come from warp shuffles.
 __global__ void __launch_bounds__(kWarps * 32)
 topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restrict__ cand,
             const float* __restrict__ csc, const float* __restrict__ chead, int32_t* __restrict__ idx,
             float* __restrict__ score, float* __restrict__ head_lse) {
-  __shared__ int s_i[kWarps][kMaxCand];
-  __shared__ float s_s[kWarps][kMaxCand];
-  __shared__ int s_k[kWarps][kMaxCand];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = blockIdx.x * static_cast<int64_t>(kWarps) + warp;
   if (u >= units) return;
-  for (int q = lane; q < W; q += 32) {
-    const int c = cand[u * W + q];
-    s_i[warp][q] = c;
-    s_s[warp][q] = c >= 0 ? no_nan(csc[u * W + q]) : neg_inf();
+  const int J = W > 32 ? 2 : 1;
+  int ci[2] = {-1, -1};
+  float cs[2] = {neg_inf(), neg_inf()};
+  for (int j = 0; j < J; ++j) {
+    const int q = lane + 32 * j;
+    if (q < W) {
+      ci[j] = cand[u * W + q];
+      if (ci[j] >= 0) cs[j] = no_nan(csc[u * W + q]);
+    }
   }
-  __syncwarp();
-  for (int q = lane; q < W; q += 32) {
-    const int mi = s_i[warp][q];
-    int rank = 0;
-    if (mi >= 0)
-      for (int o = 0; o < W; ++o)
-        rank += (s_i[warp][o] >= 0 && beats(s_s[warp][o], s_i[warp][o], s_s[warp][q], mi)) ? 1 : 0;
-    s_k[warp][q] = (mi >= 0 && rank < Ksel) ? 1 : 0;
-  }
-  __syncwarp();
-  int nk = 0;
-  for (int q = 0; q < W; ++q) nk += s_k[warp][q];
-  for (int q = lane; q < W; q += 32) {
-    if (!s_k[warp][q]) continue;
-    const int mi = s_i[warp][q];
-    int pos = 0;
-    for (int o = 0; o < W; ++o) pos += (s_k[warp][o] && s_i[warp][o] < mi) ? 1 : 0;
-    idx[u * Ksel + pos] = mi;
-    if (score) score[u * Ksel + pos] = s_s[warp][q];
-    if (head_lse)   // unit u = (b*Hkv + kv)*N + i -> rows (b*Hq + kv*G + h)*N + i
-      for (int h = 0; h < G; ++h)
-        head_lse[(((u / N) * G + h) * N + u % N) * Ksel + pos] = chead[(u * W + q) * G + h];
+  int rank[2] = {0, 0};
+  for (int jj = 0; jj < J; ++jj)
+    for (int o = 0; o < 32; ++o) {
+      const float so = __shfl_sync(0xffffffffu, cs[jj], o);
+      const int io = __shfl_sync(0xffffffffu, ci[jj], o);
+      if (io < 0) continue;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) rank[j] += beats(so, io, cs[j], ci[j]) ? 1 : 0;
+    }
+  bool keep[2];
+  int pos[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) keep[j] = ci[j] >= 0 && rank[j] < Ksel;
+  for (int jj = 0; jj < J; ++jj)
+    for (int o = 0; o < 32; ++o) {
+      const int io = __shfl_sync(0xffffffffu, keep[jj] ? ci[jj] : -1, o);
+      if (io < 0) continue;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) pos[j] += io < ci[j] ? 1 : 0;
+    }
+  const int nk = __popc(__ballot_sync(0xffffffffu, keep[0])) + __popc(__ballot_sync(0xffffffffu, keep[1]));
+  // unit u = (b*Hkv + kv)*N + i -> head_lse rows (b*Hq + kv*G + h)*N + i
+  const int64_t hrow0 = (u / N) * G * N + u % N;
+  for (int j = 0; j < J; ++j) {
+    if (!keep[j]) continue;
+    idx[u * Ksel + pos[j]] = ci[j];
+    if (score) score[u * Ksel + pos[j]] = cs[j];
+    if (head_lse) {
+      const float* src = chead + (u * W + lane + 32 * j) * G;
+      for (int h = 0; h < G; ++h) head_lse[(hrow0 + static_cast<int64_t>(h) * N) * Ksel + pos[j]] = src[h];
+    }
   }
   for (int q = nk + lane; q < Ksel; q += 32) {
     idx[u * Ksel + q] = -1;
     if (score) score[u * Ksel + q] = neg_inf();
     if (head_lse)
-      for (int h = 0; h < G; ++h) head_lse[(((u / N) * G + h) * N + u % N) * Ksel + q] = neg_inf();
+      for (int h = 0; h < G; ++h) head_lse[(hrow0 + static_cast<int64_t>(h) * N) * Ksel + q] = neg_inf();
   }
 }
 
