@@ -147,10 +147,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def source_hash() -> str:
+# Sources whose change invalidates a kernel's committed DRAM traffic figure: the kernel's own
+# file, the headers it includes and the grouping that shapes its work items.
+KERNEL_SOURCES = {
+    "route": ["select.cu", "device.cuh", "pyramid.cu"],
+    "leaf_score": ["leaf_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "select.cu"],
+    "attn_fwd_tc": ["attn_ws.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "attn.cu"],
+}
+
+
+def source_hash(files=None) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "pyramid_top_selection_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -164,7 +173,7 @@ def traffic_for(kernel: str, units_per_launch: float):
     try:
         d = json.load(open(p))
         e = d.get(kernel)
-        if not e or e.get("source_hash") != source_hash():
+        if not e or e.get("source_hash") != source_hash(KERNEL_SOURCES.get(kernel)):
             return None
         return e["dram_bytes_per_unit"] * units_per_launch
     except Exception:

@@ -25,12 +25,13 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
 
 namespace {
 
-// Query chunks of about 64 MiB of one KV head's fp32 accumulator rows (G heads x d): the
-// rows that the running items add into stay in L2, and items are long enough that the
-// per-item start (keys, V^T) is paid rarely; at most 1024 queries per work item.
+// Query chunks of about 128 MiB of one KV head's fp32 accumulator rows (G heads x d): the
+// items running at one time add into one chunk's rows, and items are long enough that the
+// per-item start (keys, V^T) is paid rarely; at most 512 queries per work item (measured
+// best with the dynamic item order; 16-64 MiB chunks and 1024-2048 caps were slower).
 GroupPlan fwd_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 4;
-  return make_group_plan(s, s.K, (int64_t(64) << 20) / per_query, 1024);
+  return make_group_plan(s, s.K, (int64_t(128) << 20) / per_query, 512);
 }
 
 }  // namespace

@@ -178,7 +178,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
       const uint32_t dst = aQ + st * L::Q_BYTES;
       const int c = lane % CH;
-#pragma unroll
+#pragma unroll 4
       for (int k = 0; k < CH; ++k) {
         const int rl = k * RPI + lane / CH;
         const int qi = __shfl_sync(0xffffffffu, pk, rl) >> 6;
@@ -305,7 +305,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       const int ps = T % kNP;
       unsigned char* pt = sm + L::oP + ps * L::P_BYTES;
       // the row's 64 keys in two halves of 32 (fewer live registers)
-#pragma unroll
+#pragma unroll 1     // rolled, like the epilogue's rounds: instruction-cache footprint
       for (int half = 0; half < 2; ++half) {
         float sv[32];
         tc::tmem_ld32(tmem_base + 64 * sg + 32 * half + lane_off, sv);
@@ -314,13 +314,8 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
           tc::bar_arrive(&s_empty[sg]);
         }
         const int lh = lim - 32 * half;
-        if (lh >= 31) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sv[c] = tc::ex2(fmaf(sv[c], c1, -l2));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) sv[c] = c <= lh ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
-        }
+        for (int c = 0; c < 32; ++c) sv[c] = c <= lh ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
         if (half == 0) {
           const bool ok2 = tc::bar_wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, ok2)) {
@@ -369,7 +364,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::after_sync();
       const bool issuer = h == 0 && pk >= 0;
       const int unit = (cur.v.b * s.N + (pk < 0 ? 0 : (pk >> 6))) * s.Hkv + cur.v.kv;
-#pragma unroll
+#pragma unroll 1     // rolled: a smaller kernel body keeps the roles' code in the instruction cache
       for (int rd = 0; rd < D / 32; ++rd, ++rd_all) {
         float ov[32];
         tc::tmem_ld32(tmem_base + L::tmem_o + os * D + 32 * rd + lane_off, ov);
