@@ -241,12 +241,11 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const float lv[2] = {l0, l1}, rvv[2] = {r0, r1};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float x0 = s.scale * lv[e] / cnt0;
+        const float x0 = lv[e] * (s.scale / cnt0);
         float l;
-        if (rv) {
-          const float x1 = s.scale * rvv[e] / cnt1;
-          const float mx = fmaxf(x0, x1);
-          l = mx + logf(expf(x0 - mx) + expf(x1 - mx));
+        if (rv) {       // LSE of two terms: max + log(1 + exp(-|difference|))
+          const float x1 = rvv[e] * (s.scale / cnt1);
+          l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
         } else {
           l = x0;
         }
