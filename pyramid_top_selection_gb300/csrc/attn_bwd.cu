@@ -12,9 +12,10 @@
 // the rows = (query, head of the group) that selected it) and adds its share of that
 // block's dK/dV into fp32 accumulators with vector reductions. Each of the 4
 // warps owns 16 of the 64 keys and keeps their dK/dV in registers across all row chunks;
-// rows come in chunks of 32, staged in shared memory row-major and transposed. dQ of a
-// (row, block) pair is a partial written to the workspace; a second kernel sums the <= K
-// partials of every row.
+// rows come in chunks of 32, staged in shared memory row-major; the operands that contract
+// over rows or keys (dO and Q for dV/dK, K for dQ) are read transposed by ldmatrix.trans.
+// dQ of a (row, block) pair is a partial written to the workspace; a second kernel sums the
+// <= K partials of every row.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -30,21 +31,29 @@ constexpr int kRows = 32;       // rows per chunk
 
 template <int D>
 struct BwdSmem {
-  static constexpr int KROW = D + 16;     // row-major tiles (8-byte fragment loads)
-  static constexpr int TROW = 64 + 8;     // transposed K tile [dim][key]
-  static constexpr int RROW = kRows + 8;  // transposed row tiles [dim][row]
+  static constexpr int KROW = D + 16;     // row-major tiles (8-byte fragment loads, 16-byte ldmatrix rows)
   static constexpr int SROW = 64 + 8;     // dS [row][key]
   static constexpr int oK = 0;
   static constexpr int oV = oK + 64 * KROW;
-  static constexpr int oKt = oV + 64 * KROW;
-  static constexpr int oQ = oKt + D * TROW;
+  static constexpr int oQ = oV + 64 * KROW;
   static constexpr int odO = oQ + kRows * KROW;
-  static constexpr int oQt = odO + kRows * KROW;
-  static constexpr int odOt = oQt + D * RROW;
-  static constexpr int odS = odOt + D * RROW;
+  static constexpr int odS = odO + kRows * KROW;
   static constexpr int n_bf16 = odS + kRows * SROW;
   static constexpr int bytes = n_bf16 * 2 + kRows * (4 + 4 + 4 + 4 + 4);
 };
+
+// Four 8x8 bf16 matrices, transposed: the B fragments (k = 16 rows from `row0`, n = dims
+// n8*8.. and n8*8+8..) of two m16n8k16 MMAs from a row-major [k][n] tile with `stride`
+// elements per row. Lane l addresses row row0 + (l & 15), column block n8 + (l >> 4).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&b)[4], const __nv_bfloat16* tile, int stride, int row0,
+                                              int n8) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a = static_cast<uint32_t>(
+      __cvta_generic_to_shared(tile + (row0 + (lane & 15)) * stride + (n8 + (lane >> 4)) * 8));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+               : "r"(a));
+}
 
 // D_row = dO_row . O_row (fp32), one warp per row.
 template <int D>
@@ -77,8 +86,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   constexpr int KS = D / 16, ND = D / 8, QPC = kRows / G;
   extern __shared__ __align__(16) unsigned char smraw[];
   __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smraw);
-  __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sKt = sb + L::oKt, *sQ = sb + L::oQ,
-                *sdO = sb + L::odO, *sQt = sb + L::oQt, *sdOt = sb + L::odOt, *sdS = sb + L::odS;
+  __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sQ = sb + L::oQ, *sdO = sb + L::odO, *sdS = sb + L::odS;
   float* s_lse = reinterpret_cast<float*>(sb + L::n_bf16);
   float* s_D = s_lse + kRows;
   int* s_i = reinterpret_cast<int*>(s_D + kRows);
@@ -95,7 +103,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   const int g = lane >> 2, p = lane & 3;
   const int kbase = t * 64;
 
-  // leaf tiles: K, V row-major, K transposed
+  // leaf tiles: K, V row-major
   for (int it = threadIdx.x; it < 64 * (D / 8); it += blockDim.x) {
     const int r = it / (D / 8), c = it % (D / 8);
     const int64_t j = static_cast<int64_t>(kbase) + r;
@@ -107,9 +115,6 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     }
     *reinterpret_cast<uint4*>(&sK[r * L::KROW + c * 8]) = kk;
     *reinterpret_cast<uint4*>(&sV[r * L::KROW + c * 8]) = vv;
-    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kk);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sKt[(c * 8 + e) * L::TROW + r] = ke[e];
   }
 
   float dv[ND][4], dk[ND][4];
@@ -135,13 +140,6 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
       }
       *reinterpret_cast<uint4*>(&sQ[r * L::KROW + c * 8]) = qq;
       *reinterpret_cast<uint4*>(&sdO[r * L::KROW + c * 8]) = oo;
-      const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(&qq);
-      const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&oo);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        sQt[(c * 8 + u) * L::RROW + r] = qe[u];
-        sdOt[(c * 8 + u) * L::RROW + r] = oe[u];
-      }
     }
     if (threadIdx.x < kRows) {
       const int r = threadIdx.x, e = e0 + r / G, h = r % G;
@@ -207,11 +205,14 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
                               pack_bf16(dp[2 * kk + 1][0], dp[2 * kk + 1][1]),
                               pack_bf16(dp[2 * kk + 1][2], dp[2 * kk + 1][3])};
 #pragma unroll
-      for (int nd = 0; nd < ND; ++nd) {
-        const __nv_bfloat16* orow = &sdOt[(nd * 8 + g) * L::RROW + 16 * kk + 2 * p];
-        const __nv_bfloat16* qrow = &sQt[(nd * 8 + g) * L::RROW + 16 * kk + 2 * p];
-        mma_bf16(dv[nd], ap, *reinterpret_cast<const uint32_t*>(orow), *reinterpret_cast<const uint32_t*>(orow + 8));
-        mma_bf16(dk[nd], as, *reinterpret_cast<const uint32_t*>(qrow), *reinterpret_cast<const uint32_t*>(qrow + 8));
+      for (int nd = 0; nd < ND; nd += 2) {
+        uint32_t bo[4], bq[4];
+        ldsm_x4_trans(bo, sdO, L::KROW, 16 * kk, nd);
+        ldsm_x4_trans(bq, sQ, L::KROW, 16 * kk, nd);
+        mma_bf16(dv[nd], ap, bo[0], bo[1]);
+        mma_bf16(dv[nd + 1], ap, bo[2], bo[3]);
+        mma_bf16(dk[nd], as, bq[0], bq[1]);
+        mma_bf16(dk[nd + 1], as, bq[2], bq[3]);
       }
     }
     // dS -> shared memory as [row][key] for dQ
@@ -239,9 +240,11 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
         const uint32_t a[4] = {*reinterpret_cast<const uint32_t*>(a0), *reinterpret_cast<const uint32_t*>(a1),
                                *reinterpret_cast<const uint32_t*>(a0 + 8), *reinterpret_cast<const uint32_t*>(a1 + 8)};
 #pragma unroll
-        for (int nd = 0; nd < ND / 2; ++nd) {
-          const __nv_bfloat16* br = &sKt[(d0 + nd * 8 + g) * L::TROW + 16 * kk + 2 * p];
-          mma_bf16(dq[nd], a, *reinterpret_cast<const uint32_t*>(br), *reinterpret_cast<const uint32_t*>(br + 8));
+        for (int nd = 0; nd < ND / 2; nd += 2) {
+          uint32_t bk[4];
+          ldsm_x4_trans(bk, sK, L::KROW, 16 * kk, d0 / 8 + nd);
+          mma_bf16(dq[nd], a, bk[0], bk[1]);
+          mma_bf16(dq[nd + 1], a, bk[2], bk[3]);
         }
       }
 #pragma unroll
