@@ -12,13 +12,15 @@
 // the rows = (query, head of the group) that selected it) and adds its share of that
 // block's dK/dV into fp32 accumulators with vector reductions. Each of the 4
 // warps owns 16 of the 64 keys and keeps their dK/dV in registers across all row chunks;
-// rows come in chunks of 32, staged in shared memory row-major; the operands that contract
-// over rows or keys (dO and Q for dV/dK, K for dQ) are read transposed by ldmatrix.trans.
+// rows come in chunks of 32, staged in shared memory row-major by cp.async into two buffers
+// (the next chunk's rows land while this one is computed); the operands that contract over
+// rows or keys (dO and Q for dV/dK, K for dQ) are read transposed by ldmatrix.trans.
 // dQ of a (row, block) pair is a partial written to the workspace; a second kernel sums the
 // <= K partials of every row.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
+#include "tc.cuh"
 
 namespace pisa {
 
@@ -35,11 +37,11 @@ struct BwdSmem {
   static constexpr int SROW = 64 + 8;     // dS [row][key]
   static constexpr int oK = 0;
   static constexpr int oV = oK + 64 * KROW;
-  static constexpr int oQ = oV + 64 * KROW;
-  static constexpr int odO = oQ + kRows * KROW;
-  static constexpr int odS = odO + kRows * KROW;
+  static constexpr int oQ = oV + 64 * KROW;            // two buffers each of Q and dO rows
+  static constexpr int odO = oQ + 2 * kRows * KROW;
+  static constexpr int odS = odO + 2 * kRows * KROW;
   static constexpr int n_bf16 = odS + kRows * SROW;
-  static constexpr int bytes = n_bf16 * 2 + kRows * (4 + 4 + 4 + 4 + 4);
+  static constexpr int bytes = n_bf16 * 2 + 2 * kRows * (4 + 4 + 4 + 4 + 4);
 };
 
 // Four 8x8 bf16 matrices, transposed: the B fragments (k = 16 rows from `row0`, n = dims
@@ -86,12 +88,9 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   constexpr int KS = D / 16, ND = D / 8, QPC = kRows / G;
   extern __shared__ __align__(16) unsigned char smraw[];
   __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smraw);
-  __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sQ = sb + L::oQ, *sdO = sb + L::odO, *sdS = sb + L::odS;
-  float* s_lse = reinterpret_cast<float*>(sb + L::n_bf16);
-  float* s_D = s_lse + kRows;
-  int* s_i = reinterpret_cast<int*>(s_D + kRows);
-  int* s_slot = s_i + kRows;
-  int* s_h = s_slot + kRows;
+  __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sdS = sb + L::odS;
+  // per row buffer: lse, D, query, slot, head (kRows words each)
+  int* s_meta = reinterpret_cast<int*>(sb + L::n_bf16);
 
   if (static_cast<int>(blockIdx.x) >= *n_items) return;
   const int4 item = items[blockIdx.x];
@@ -125,42 +124,82 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
 
   const int n_ent = end - beg;
   const int key0 = 16 * warp;        // this warp's keys: key0 + g, key0 + g + 8
-  for (int e0 = 0; e0 < n_ent; e0 += QPC) {
-    __syncthreads();                 // previous chunk fully consumed
-    // stage the chunk's rows (query, head): row r = entry r / G, head r % G
-    for (int it = threadIdx.x; it < kRows * (D / 8); it += blockDim.x) {
-      const int r = it / (D / 8), c = it % (D / 8);
-      const int e = e0 + r / G, h = r % G;
-      uint4 qq = make_uint4(0, 0, 0, 0), oo = make_uint4(0, 0, 0, 0);
-      if (e < n_ent) {
-        const int pk = list[beg + e];
-        const int64_t row = (static_cast<int64_t>(b) * s.N + (pk >> 6)) * s.Hq + kv * G + h;
-        qq = ldg_u4(Q + row * D + c * 8);
-        oo = ldg_u4(dO + row * D + c * 8);
-      }
-      *reinterpret_cast<uint4*>(&sQ[r * L::KROW + c * 8]) = qq;
-      *reinterpret_cast<uint4*>(&sdO[r * L::KROW + c * 8]) = oo;
+  // chunk staging: thread tid copies chunk (tid % CPR) of rows tid / CPR + RSTEP * u
+  constexpr int CPR = D / 8, NIT = kRows * CPR / (kWarps * 32), RSTEP = kWarps * 32 / CPR;
+  const int sc_c = threadIdx.x % CPR, sc_r = threadIdx.x / CPR;
+  auto entries = [&](int e0, int (&pk)[NIT]) {     // list entries of the thread's rows (-1: none)
+#pragma unroll
+    for (int u = 0; u < NIT; ++u) {
+      const int e = e0 + (sc_r + RSTEP * u) / G;
+      pk[u] = e < n_ent ? list[beg + e] : -1;
     }
-    if (threadIdx.x < kRows) {
-      const int r = threadIdx.x, e = e0 + r / G, h = r % G;
-      if (e < n_ent) {
-        const int pk = list[beg + e];
-        const int i = pk >> 6;
-        const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
-        s_lse[r] = lse[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i];
-        s_D[r] = delta[row];
-        s_i[r] = i;
-        s_slot[r] = pk & 63;
-        s_h[r] = h;
-      } else {
-        s_lse[r] = __int_as_float(0x7f800000);   // +inf: P = 0 on padding rows
-        s_D[r] = 0.f;
-        s_i[r] = -1;
-        s_slot[r] = 0;
-        s_h[r] = 0;
-      }
+  };
+  auto issue = [&](int bf, const int (&pk)[NIT]) {
+#pragma unroll
+    for (int u = 0; u < NIT; ++u) {
+      const int r = sc_r + RSTEP * u, h = r % G;
+      const int64_t row = (static_cast<int64_t>(b) * s.N + (pk[u] < 0 ? 0 : (pk[u] >> 6))) * s.Hq + kv * G + h;
+      const uint32_t o = static_cast<uint32_t>(((bf * kRows + r) * L::KROW + sc_c * 8) * 2);
+      tc::cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(sb + L::oQ)) + o, Q + row * D + sc_c * 8, pk[u] >= 0);
+      tc::cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(sb + L::odO)) + o, dO + row * D + sc_c * 8,
+                     pk[u] >= 0);
     }
-    __syncthreads();
+  };
+  // row metadata of a chunk (threads < kRows), loaded into registers and stored later
+  struct Meta { float lse, D; int i, slot, h; };
+  auto meta_load = [&](int e0) {
+    Meta m{__int_as_float(0x7f800000), 0.f, -1, 0, 0};   // +inf lse: P = 0 on padding rows
+    const int r = threadIdx.x, e = e0 + r / G, h = r % G;
+    if (e < n_ent) {
+      const int pk = list[beg + e];
+      const int i = pk >> 6;
+      const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
+      m.lse = lse[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i];
+      m.D = delta[row];
+      m.i = i;
+      m.slot = pk & 63;
+      m.h = h;
+    }
+    return m;
+  };
+  auto meta_store = [&](int bf, const Meta& m) {
+    int* mb = s_meta + bf * 5 * kRows;
+    const int r = threadIdx.x;
+    mb[r] = __float_as_int(m.lse);
+    mb[kRows + r] = __float_as_int(m.D);
+    mb[2 * kRows + r] = m.i;
+    mb[3 * kRows + r] = m.slot;
+    mb[4 * kRows + r] = m.h;
+  };
+  int pk_next[NIT];
+  Meta m_next{};
+  if (n_ent > 0) {
+    entries(0, pk_next);
+    issue(0, pk_next);
+    if (threadIdx.x < kRows) meta_store(0, meta_load(0));
+    entries(QPC, pk_next);
+  }
+  tc::cp_async_commit();
+  for (int e0 = 0, bf = 0; e0 < n_ent; e0 += QPC, bf ^= 1) {
+    // the next chunk's rows into the other buffer (freed by the previous iteration's last
+    // barrier); its list entries for the chunk after it load meanwhile
+    const bool more = e0 + QPC < n_ent;
+    if (more) {
+      issue(bf ^ 1, pk_next);
+      if (threadIdx.x < kRows) m_next = meta_load(e0 + QPC);
+      entries(e0 + 2 * QPC, pk_next);
+    }
+    tc::cp_async_commit();
+    tc::cp_async_wait<1>();
+    __syncthreads();                 // this chunk's rows and metadata are in place
+    const __nv_bfloat16* sQ = sb + L::oQ + bf * kRows * L::KROW;
+    const __nv_bfloat16* sdO = sb + L::odO + bf * kRows * L::KROW;
+    const int* mb = s_meta + bf * 5 * kRows;
+    const float* s_lse = reinterpret_cast<const float*>(mb);
+    const float* s_D = reinterpret_cast<const float*>(mb + kRows);
+    const int* s_i = mb + 2 * kRows;
+    const int* s_slot = mb + 3 * kRows;
+    const int* s_h = mb + 4 * kRows;
 
     // S^T and dP^T for keys key0+{g, g+8} x the 32 rows (4 n-tiles of 8 rows)
     float st[4][4], dp[4][4];
@@ -259,7 +298,10 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
               pack_bf16(s.scale * dq[nd][2 * half], s.scale * dq[nd][2 * half + 1]);
       }
     }
+    if (more && threadIdx.x < kRows) meta_store(bf ^ 1, m_next);
+    __syncthreads();                 // this chunk's buffers are free for the chunk after next
   }
+  tc::cp_async_wait<0>();
   // this item's share of the leaf block's dK and dV (unscaled dK), added into fp32
   // accumulators with vector reductions: items of one leaf run in different CTAs
 #pragma unroll
