@@ -39,8 +39,13 @@ constexpr int kWarps = 4;
 constexpr int kMaxCand = 64;   // 2K for K <= 32
 
 
-// fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}.
-__global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4) {
+// fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}. Chunk c of a
+// row (dims 4c..4c+3; k-step ks = c / 4, lane p = c % 4 of an m16n8k16 fragment) is stored at
+// (ks / 2) * 8 + 2p + ks % 2, so that one lane's chunks for two consecutive k-steps are adjacent
+// and the four lanes of a fragment row read one whole 128-byte line with 32-byte loads.
+__host__ __device__ constexpr int split_pos(int c) { return ((c >> 3) << 3) + ((c & 3) << 1) + ((c >> 2) & 1); }
+
+__global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4, int rq) {
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n4;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 v = src[q];
@@ -54,24 +59,38 @@ __global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__
     o.y = (uint32_t)__bfloat16_as_ushort(h[2]) | ((uint32_t)__bfloat16_as_ushort(h[3]) << 16);
     o.z = (uint32_t)__bfloat16_as_ushort(l[0]) | ((uint32_t)__bfloat16_as_ushort(l[1]) << 16);
     o.w = (uint32_t)__bfloat16_as_ushort(l[2]) | ((uint32_t)__bfloat16_as_ushort(l[3]) << 16);
-    dst[q] = o;
+    const int c = static_cast<int>(q % rq);
+    dst[q - c + split_pos(c)] = o;
   }
 }
 
-// Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid; invalid
-// rows contribute zeros.
+// 32-byte read-only load: the chunks of k-steps 2kp and 2kp+1 of one fragment lane.
+__device__ __forceinline__ void ldg_pair(const uint4* a, uint4& x, uint4& y) {
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w), "=r"(y.x), "=r"(y.y), "=r"(y.z), "=r"(y.w)
+      : "l"(a));
+}
+
+// Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid (always valid
+// addresses); invalid rows contribute zeros.
 template <int KS>
 __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0, bool v0,
                                                const uint4* r1, bool v1, int p,
                                                const uint32_t (&qb)[KS][2]) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint4 x0 = v0 ? __ldg(r0 + 4 * ks + p) : make_uint4(0, 0, 0, 0);
-    uint4 x1 = v1 ? __ldg(r1 + 4 * ks + p) : make_uint4(0, 0, 0, 0);
-    uint32_t ahi[4] = {x0.x, x1.x, x0.y, x1.y};
-    uint32_t alo[4] = {x0.z, x1.z, x0.w, x1.w};
-    mma_bf16(acc, ahi, qb[ks][0], qb[ks][1]);
-    mma_bf16(acc, alo, qb[ks][0], qb[ks][1]);
+  for (int kp = 0; kp < KS / 2; ++kp) {
+    uint4 x0[2], x1[2];
+    ldg_pair(r0 + 8 * kp + 2 * p, x0[0], x0[1]);
+    ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint4 a = v0 ? x0[e] : z, c = v1 ? x1[e] : z;
+      const uint32_t ahi[4] = {a.x, c.x, a.y, c.y};
+      const uint32_t alo[4] = {a.z, c.z, a.w, c.w};
+      mma_bf16(acc, ahi, qb[2 * kp + e][0], qb[2 * kp + e][1]);
+      mma_bf16(acc, alo, qb[2 * kp + e][0], qb[2 * kp + e][1]);
+    }
   }
 }
 
@@ -486,11 +505,17 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
     const uint4* row = spl0 + static_cast<int64_t>(vb ? tl : 0) * RQ;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint4 x = vb ? __ldg(row + 4 * ks + p) : make_uint4(0, 0, 0, 0);
-      mma_bf16(acc, ahi[ks], x.x, x.y);
-      mma_bf16(acc, ahi[ks], x.z, x.w);
-      mma_bf16(acc, alo[ks], x.x, x.y);
+    for (int kp = 0; kp < KS / 2; ++kp) {
+      uint4 xx[2];
+      ldg_pair(row + 8 * kp + 2 * p, xx[0], xx[1]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int ks = 2 * kp + e;
+        const uint4 x = vb ? xx[e] : make_uint4(0, 0, 0, 0);
+        mma_bf16(acc, ahi[ks], x.x, x.y);
+        mma_bf16(acc, ahi[ks], x.z, x.w);
+        mma_bf16(acc, alo[ks], x.x, x.y);
+      }
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -630,7 +655,7 @@ size_t flat_ws(const Dims& s, const Geo& g) {
 int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
   const int64_t n4 = static_cast<int64_t>(s.B) * s.Hkv * g.nodes * s.d / 4;
   ProfScope ps(st, "split_pyramid");
-  split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4);
+  split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4, s.d / 4);
   return cudaGetLastError();
 }
 
