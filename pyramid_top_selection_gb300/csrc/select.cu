@@ -615,11 +615,12 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
   }
 }
 
-// Stage-2 grouping: query chunks of about 16 MiB of one head's query rows; about 1024
-// (query, head) rows per work item.
+// Stage-2 grouping: query chunks of about 64 MiB of one KV head's query rows; about 4096
+// (query, head) rows per work item (with the dynamic item order, longer items measured faster:
+// 1.60 -> 1.53 ms at 64K, and fewer bins shorten the scans).
 GroupPlan leaf_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2;
-  return make_group_plan(s, 2 * s.K, (int64_t(16) << 20) / per_query, 1024 / s.G);
+  return make_group_plan(s, 2 * s.K, (int64_t(64) << 20) / per_query, 4096 / s.G);
 }
 
 inline int grid_for(int64_t n, int threads) {
