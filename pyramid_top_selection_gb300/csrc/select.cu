@@ -39,13 +39,15 @@ constexpr int kWarps = 4;
 constexpr int kMaxCand = 64;   // 2K for K <= 32
 
 
-// fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}. Chunk c of a
-// row (dims 4c..4c+3; k-step ks = c / 4, lane p = c % 4 of an m16n8k16 fragment) is stored at
-// (ks / 2) * 8 + 2p + ks % 2, so that one lane's chunks for two consecutive k-steps are adjacent
-// and the four lanes of a fragment row read one whole 128-byte line with 32-byte loads.
-__host__ __device__ constexpr int split_pos(int c) { return ((c >> 3) << 3) + ((c & 3) << 1) + ((c >> 2) & 1); }
+// Dimension order of the m16n8k16 fragments (a dot product may take its terms in any order,
+// as long as both operands agree): lane p's four k-slots of k-step ks hold dims kdim(ks, p) ..
+// + 3, so a lane's dims for k-steps 2kp and 2kp+1 are 8 adjacent ones. The four lanes of a
+// fragment row then read a whole 128-byte line of a split row (32-byte loads) and 64
+// contiguous bytes of a bf16 row (16-byte loads) per pair of k-steps.
+__host__ __device__ constexpr int kdim(int ks, int p) { return 32 * (ks >> 1) + 8 * p + 4 * (ks & 1); }
 
-__global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4, int rq) {
+// fp32 [rows, D] -> hi/lo bf16 rows: per 4 dims, 16 bytes {hi0..hi3, lo0..lo3}.
+__global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n4) {
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n4;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 v = src[q];
@@ -59,12 +61,11 @@ __global__ void split_kernel(const float4* __restrict__ src, uint4* __restrict__
     o.y = (uint32_t)__bfloat16_as_ushort(h[2]) | ((uint32_t)__bfloat16_as_ushort(h[3]) << 16);
     o.z = (uint32_t)__bfloat16_as_ushort(l[0]) | ((uint32_t)__bfloat16_as_ushort(l[1]) << 16);
     o.w = (uint32_t)__bfloat16_as_ushort(l[2]) | ((uint32_t)__bfloat16_as_ushort(l[3]) << 16);
-    const int c = static_cast<int>(q % rq);
-    dst[q - c + split_pos(c)] = o;
+    dst[q] = o;
   }
 }
 
-// 32-byte read-only load: the chunks of k-steps 2kp and 2kp+1 of one fragment lane.
+// 32-byte read-only load: one fragment lane's split chunks for k-steps 2kp and 2kp+1.
 __device__ __forceinline__ void ldg_pair(const uint4* a, uint4& x, uint4& y) {
   asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
       : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w), "=r"(y.x), "=r"(y.y), "=r"(y.z), "=r"(y.w)
@@ -129,7 +130,7 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         Q + ((static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + min(g, G - 1)) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      uint2 v = g < G ? ldg_u2(qrow + 16 * ks + 4 * p) : make_uint2(0, 0);
+      uint2 v = g < G ? ldg_u2(qrow + kdim(ks, p)) : make_uint2(0, 0);
       qb[ks][0] = v.x;
       qb[ks][1] = v.y;
     }
@@ -146,11 +147,12 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const __nv_bfloat16* k0 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r0) * s.Hkv + kv) * D;
       const __nv_bfloat16* k1 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r1) * s.Hkv + kv) * D;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint2 x0 = r0 < nkeys ? ldg_u2(k0 + 16 * ks + 4 * p) : make_uint2(0, 0);
-        uint2 x1 = r1 < nkeys ? ldg_u2(k1 + 16 * ks + 4 * p) : make_uint2(0, 0);
-        uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
-        mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
+      for (int kp = 0; kp < KS / 2; ++kp) {
+        const uint4 x0 = r0 < nkeys ? ldg_u4(k0 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
+        const uint4 x1 = r1 < nkeys ? ldg_u4(k1 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
+        const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y}, a1[4] = {x0.z, x1.z, x0.w, x1.w};
+        mma_bf16(acc, a0, qb[2 * kp][0], qb[2 * kp][1]);
+        mma_bf16(acc, a1, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
       }
       pda += acc[0] + acc[2];
       pdb += acc[1] + acc[3];
@@ -449,12 +451,12 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
     float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int h = 0; h < G; ++h) {
       if (ok0) {
-        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i0) * s.Hq + kv * G + h) * D + 16 * ks + 4 * p);
+        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i0) * s.Hq + kv * G + h) * D + kdim(ks, p));
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
         for (int u = 0; u < 4; ++u) f0[u] += __bfloat162float(e[u]);
       }
       if (ok1) {
-        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i1) * s.Hq + kv * G + h) * D + 16 * ks + 4 * p);
+        uint2 v = ldg_u2(Q + ((static_cast<int64_t>(b) * s.N + i1) * s.Hq + kv * G + h) * D + kdim(ks, p));
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
         for (int u = 0; u < 4; ++u) f1[u] += __bfloat162float(e[u]);
       }
@@ -536,10 +538,12 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
       const __nv_bfloat16* kr = K + ((static_cast<int64_t>(b) * s.N + (vk ? j : 0)) * s.Hkv + kv) * D;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint2 x = vk ? ldg_u2(kr + 16 * ks + 4 * p) : make_uint2(0, 0);
-        mma_bf16(acc, ahi[ks], x.x, x.y);
-        mma_bf16(acc, alo[ks], x.x, x.y);
+      for (int kp = 0; kp < KS / 2; ++kp) {
+        const uint4 x = vk ? ldg_u4(kr + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
+        mma_bf16(acc, ahi[2 * kp], x.x, x.y);
+        mma_bf16(acc, alo[2 * kp], x.x, x.y);
+        mma_bf16(acc, ahi[2 * kp + 1], x.z, x.w);
+        mma_bf16(acc, alo[2 * kp + 1], x.z, x.w);
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -656,7 +660,7 @@ size_t flat_ws(const Dims& s, const Geo& g) {
 int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
   const int64_t n4 = static_cast<int64_t>(s.B) * s.Hkv * g.nodes * s.d / 4;
   ProfScope ps(st, "split_pyramid");
-  split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4, s.d / 4);
+  split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4);
   return cudaGetLastError();
 }
 
