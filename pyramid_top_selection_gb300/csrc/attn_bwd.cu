@@ -15,8 +15,8 @@
 // rows come in chunks of 32, staged in shared memory row-major by cp.async into two buffers
 // (the next chunk's rows land while this one is computed); the operands that contract over
 // rows or keys (dO and Q for dV/dK, K for dQ) are read transposed by ldmatrix.trans.
-// dQ of a (row, block) pair is a partial written to the workspace; a second kernel sums the
-// <= K partials of every row.
+// dQ of a (row, block) pair is added into an fp32 accumulator with vector reductions (the
+// rows of a query chunk stay in L2); a last kernel converts dQ, dK and dV to bf16.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -82,7 +82,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
                 const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ dO,
                 const float* __restrict__ lse, const float* __restrict__ delta,
                 const int32_t* __restrict__ list, const int4* __restrict__ items,
-                const int32_t* __restrict__ n_items, __nv_bfloat16* __restrict__ part_dq,
+                const int32_t* __restrict__ n_items, float* __restrict__ dq_acc,
                 float* __restrict__ dk_acc, float* __restrict__ dv_acc) {
   using L = BwdSmem<D>;
   constexpr int KS = D / 16, ND = D / 8, QPC = kRows / G;
@@ -291,11 +291,11 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
         const int r = r0 + g + 8 * half;
         if (s_i[r] < 0) continue;
         const int64_t row = (static_cast<int64_t>(b) * s.N + s_i[r]) * s.Hq + kv * G + s_h[r];
-        __nv_bfloat16* dst = part_dq + (row * s.K + s_slot[r]) * D + d0;
+        float* dst = dq_acc + row * D + d0;
 #pragma unroll
         for (int nd = 0; nd < ND / 2; ++nd)
-          *reinterpret_cast<uint32_t*>(dst + nd * 8 + 2 * p) =
-              pack_bf16(s.scale * dq[nd][2 * half], s.scale * dq[nd][2 * half + 1]);
+          atomicAdd(reinterpret_cast<float2*>(dst + nd * 8 + 2 * p),
+                    make_float2(s.scale * dq[nd][2 * half], s.scale * dq[nd][2 * half + 1]));
       }
     }
     if (more && threadIdx.x < kRows) meta_store(bf ^ 1, m_next);
@@ -330,37 +330,19 @@ __global__ void dkdv_convert_kernel(int64_t n8, float scale, const float4* __res
   }
 }
 
-// dQ_row = sum over the row's valid slots of the partials; one warp per row.
-template <int D>
-__global__ void __launch_bounds__(256)
-dq_combine_kernel(Dims s, const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_dq,
-                  __nv_bfloat16* __restrict__ dQ) {
-  constexpr int PER = D / 32;
-  const int64_t row = blockIdx.x * 8LL + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<int64_t>(s.B) * s.N * s.Hq) return;
-  const int h = static_cast<int>(row % s.Hq);
-  const int64_t bi = row / s.Hq;
-  const int i = static_cast<int>(bi % s.N), b = static_cast<int>(bi / s.N);
-  const int32_t* id = idx + ((static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i) * s.K;
-  float acc[PER];
-#pragma unroll
-  for (int u = 0; u < PER; ++u) acc[u] = 0.f;
-  for (int q = 0; q < s.K; ++q) {
-    if (id[q] < 0) continue;
-    const __nv_bfloat16* src = part_dq + (row * s.K + q) * D + lane * PER;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) acc[u] += __bfloat162float(src[u]);
+// dQ = bf16(dQ_acc), 8 elements per thread.
+__global__ void dq_convert_kernel(int64_t n8, const float4* __restrict__ dq_acc, uint4* __restrict__ dQ) {
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = dq_acc[2 * q], c = dq_acc[2 * q + 1];
+    dQ[q] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
   }
-  __nv_bfloat16* dst = dQ + row * D + lane * PER;
-#pragma unroll
-  for (int u = 0; u < PER; u += 2) *reinterpret_cast<uint32_t*>(dst + u) = pack_bf16(acc[u], acc[u + 1]);
 }
 
 template <int D, int G>
 int bwd_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                const void* dO, const float* lse, const float* delta, const int32_t* list,
-               const int4* items, const int32_t* n_items, __nv_bfloat16* pdq, float* dk_acc,
+               const int4* items, const int32_t* n_items, float* dqa, float* dk_acc,
                float* dv_acc, cudaStream_t st) {
   const int smem = BwdSmem<D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -369,20 +351,20 @@ int bwd_launch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K,
   attn_bwd_kernel<D, G><<<static_cast<unsigned>(gp.max_items), kWarps * 32, smem, st>>>(
       s, gp, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(dO), lse, delta, list,
-      items, n_items, pdq, dk_acc, dv_acc);
+      items, n_items, dqa, dk_acc, dv_acc);
   return cudaGetLastError();
 }
 
 template <int D>
 int bwd_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                  const void* dO, const float* lse, const float* delta, const int32_t* list,
-                 const int4* items, const int32_t* n_items, __nv_bfloat16* pdq, float* dk_acc,
+                 const int4* items, const int32_t* n_items, float* dqa, float* dk_acc,
                  float* dv_acc, cudaStream_t st) {
   switch (s.G) {
-    case 1: return bwd_launch<D, 1>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
-    case 2: return bwd_launch<D, 2>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
-    case 4: return bwd_launch<D, 4>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
-    default: return bwd_launch<D, 8>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
+    case 1: return bwd_launch<D, 1>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
+    case 2: return bwd_launch<D, 2>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
+    case 4: return bwd_launch<D, 4>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
+    default: return bwd_launch<D, 8>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
   }
 }
 
@@ -402,7 +384,7 @@ AttnBwdWs attn_bwd_ws(const Dims& s) {
   const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
   size_t o = group_ws(bwd_plan(s), 0).end;
   w.delta = o;   o += align256(rows * 4);
-  w.part_dq = o; o += align256(rows * s.K * s.d * 2);
+  w.dq_acc = o;  o += align256(rows * s.d * 4);
   w.dk_acc = o;  o += align256(kvel * 4);
   w.dv_acc = o;  o += align256(kvel * 4);
   w.total = o;
@@ -417,7 +399,7 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   const GroupPlan gp = bwd_plan(s);
   const GroupWs g = group_ws(gp, 0);
   float* delta = reinterpret_cast<float*>(ws + w.delta);
-  __nv_bfloat16* pdq = reinterpret_cast<__nv_bfloat16*>(ws + w.part_dq);
+  float* dqa = reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
   float* dv_acc = reinterpret_cast<float*>(ws + w.dv_acc);
   const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
@@ -425,6 +407,7 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   if (err) return err;
   cudaError_t e = cudaMemsetAsync(dk_acc, 0, kvel * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(dv_acc, 0, kvel * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dqa, 0, static_cast<size_t>(s.B) * s.N * s.Hq * s.d * 4, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
   const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
@@ -441,8 +424,8 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
   const int4* items = reinterpret_cast<const int4*>(ws + g.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
-  err = s.d == 128 ? bwd_dispatch<128>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st)
-                   : bwd_dispatch<64>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, pdq, dk_acc, dv_acc, st);
+  err = s.d == 128 ? bwd_dispatch<128>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st)
+                   : bwd_dispatch<64>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
   if (err) return err;
   {
     ProfScope ps(st, "attn_bwd_dkdv");
@@ -454,10 +437,10 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   }
   {
     ProfScope ps(st, "attn_bwd_dq");
-    if (s.d == 128)
-      dq_combine_kernel<128><<<blocks, 256, 0, st>>>(s, idx, pdq, static_cast<__nv_bfloat16*>(dQ));
-    else
-      dq_combine_kernel<64><<<blocks, 256, 0, st>>>(s, idx, pdq, static_cast<__nv_bfloat16*>(dQ));
+    const int64_t n8 = rows * s.d / 8;
+    const int64_t nb = (n8 + 255) / 256;
+    dq_convert_kernel<<<static_cast<unsigned>(nb < 152 * 32 ? nb : 152 * 32), 256, 0, st>>>(
+        n8, reinterpret_cast<const float4*>(dqa), static_cast<uint4*>(dQ));
   }
   return cudaGetLastError();
 }

@@ -52,7 +52,7 @@ struct AttnFwdWs {
   size_t block_lse, o_acc, status, total;
 };
 struct AttnBwdWs {
-  size_t delta, part_dq, dk_acc, dv_acc, total;
+  size_t delta, dq_acc, dk_acc, dv_acc, total;
 };
 int sm_count();
 SelectWs select_ws(const Dims& s, const Geo& g);
