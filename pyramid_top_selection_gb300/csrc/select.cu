@@ -95,22 +95,24 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
   }
 }
 
-template <int D>
+// MC: the most candidates a level can hold (2K rounded up to 32 or 64); the smaller size lets
+// more CTAs share an SM.
+template <int D, int MC>
 __global__ void __launch_bounds__(kWarps * 32)
 route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
              const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl,
              int32_t* __restrict__ cand_out) {
   constexpr int KS = D / 16;
   constexpr int RQ = D / 4;     // uint4 chunks per split row
-  __shared__ int s_cand[kWarps][kMaxCand];
-  __shared__ int s_kept[kWarps][kMaxCand / 2];
-  __shared__ float s_sc[kWarps][kMaxCand];
+  __shared__ int s_cand[kWarps][MC];
+  __shared__ int s_kept[kWarps][MC / 2];
+  __shared__ float s_sc[kWarps][MC];
   __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
   __shared__ float s_pd[kWarps][PISA_MAX_LEVELS][8];
   // dots of every candidate's two children (q . key sum, per head), two level buffers
-  __shared__ float s_cdot[kWarps][2][kMaxCand][2][8];
-  __shared__ int s_kslot[kWarps][kMaxCand / 2];   // candidate slot each kept node came from
-  __shared__ int s_par[kWarps][kMaxCand];         // 2 * (kept slot of the parent) + which child
+  __shared__ float s_cdot[kWarps][2][MC][2][8];
+  __shared__ int s_kslot[kWarps][MC / 2];   // candidate slot each kept node came from
+  __shared__ int s_par[kWarps][MC];         // 2 * (kept slot of the parent) + which child
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
@@ -680,12 +682,15 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
   ProfScope ps(st, "route");
-  if (s.d == 128)
-    route_kernel<128><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
-                                                     static_cast<const __nv_bfloat16*>(K), spl, cand);
-  else
-    route_kernel<64><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q),
-                                                    static_cast<const __nv_bfloat16*>(K), spl, cand);
+#define PISA_ROUTE(DD, MM) \
+  route_kernel<DD, MM><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
+                                                    static_cast<const __nv_bfloat16*>(K), spl, cand)
+  if (s.d == 128) {
+    if (2 * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
+  } else {
+    if (2 * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
+  }
+#undef PISA_ROUTE
   }
   if ((err = cudaGetLastError())) return err;
   const int W = 2 * s.K;
