@@ -141,17 +141,6 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes) : "memory");
 }
 
-// TMA row gather: rows r0..r3 of a 2-D tensor map (box one row high), columns col ..
-// col + box width, into 4 consecutive box rows at `dst` (the map's swizzle applied).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1,
-                                            int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(su32(bar))
-      : "memory");
-}
-
 // TMA tile load of a 4-D tensor map box at coordinates (c0, c1, c2, c3).
 __device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                           uint64_t* bar) {
@@ -191,14 +180,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// TMA bulk reduction: global[gdst .. +bytes) += shared[ssrc .. +bytes) as fp32, done by the
-// async proxy (both addresses 16-byte aligned, bytes a multiple of 16). The issuing thread
-// must fence its own shared-memory writes with fence_async_smem() first.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-               "r"(ssrc), "r"(bytes)
-               : "memory");
-}
+// Bulk async-proxy groups (the TMA reduce-adds): commit this thread's issued operations as one
+// group; a thread that wrote the shared source must fence_async_smem() before issuing.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory / are pending.
 template <int N>
