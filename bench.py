@@ -7,7 +7,7 @@ head. One step = pyramid build + pyramid Top-K selection + causal block-sparse a
 forward over the selection, on inputs already resident in HBM; tokens/s = B*N / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill_64k|prefill_32k|prefill_4k|sweep|decode|train]
+                  [--workload prefill_64k|prefill_32k|prefill_4k|sweep|quality|decode|train]
                   [--sweep-n 4096,...]
 
 Under torchrun each rank runs the same workload on its own GPU (independent problems, no
@@ -43,6 +43,7 @@ WORKLOADS = {
     "prefill_4k": dict(B=1, N=4096, Hq=4, Hkv=1, d=64, C=64, K=8, g=2, qtile=1, needles=False),
     "prefill_32k": dict(B=1, N=32768, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "sweep": dict(B=1, N=65536, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=4, needles=True),
+    "quality": dict(B=1, N=16384, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "train": dict(B=4, N=16384, Hq=16, Hkv=4, d=128, C=64, K=16, g=2, qtile=4, needles=False),
     "decode": dict(B=32, N=131072, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=1, needles=False),
 }
@@ -59,6 +60,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_64k", choices=sorted(WORKLOADS))
     ap.add_argument("--sweep-n", default="4096,16384,65536,131072,262144")
+    ap.add_argument("--quality-n", default="4096,16384,65536")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -477,6 +479,88 @@ def run_reference(args, cfg, rank, world):
 
 
 # ------------------------------------------------------------------ extra workloads
+def exact_leaf_lse(Qg, Kk, q0, q1, C, scale):
+    """Per-head exact leaf LSEs of queries q0..q1-1 of one KV head: [q, G, visible leaves] fp32,
+    -inf where a leaf has no visible key (a plain dense reference for the quality measurement)."""
+    nk = q1
+    logits = scale * torch.einsum("igd,jd->igj", Qg[q0:q1].float(), Kk[:nk].float())
+    i = torch.arange(q0, q1, device=Kk.device).view(-1, 1, 1)
+    j = torch.arange(nk, device=Kk.device).view(1, 1, -1)
+    logits = logits.masked_fill(j > i, float("-inf"))
+    nl = -(-nk // C)
+    pad = nl * C - nk
+    if pad:
+        logits = torch.nn.functional.pad(logits, (0, pad), value=float("-inf"))
+    return torch.logsumexp(logits.view(q1 - q0, Qg.shape[1], nl, C), dim=-1)
+
+
+def run_quality(args, cfg, local):
+    """Selection quality on the needle data (one JSON line per N): recall of the exhaustive exact
+    top-K, recall of the planted needle leaves (queries aligned with the needle direction), and the
+    share of each head's full causal softmax mass inside the selected leaves; for the pyramid
+    selection, the flat comparator and the exact top-K itself."""
+    import pyramid_top_selection_gb300 as pisa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    for N in [int(x) for x in args.quality_n.split(",")]:
+        c = dict(cfg, N=N)
+        B, Hq, Hkv, d, C, K = c["B"], c["Hq"], c["Hkv"], c["d"], c["C"], c["K"]
+        G, n0 = Hq // Hkv, -(-N // C)
+        Q, Kt, _ = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0, needles=True, device=dev)
+        needles = syn.needle_leaves(B, Hkv, n0, 3, device=dev)
+        shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, c["g"], c["qtile"])
+        pyr = pisa.build_pyramid(Kt, shape)
+        sels = {"pyramid": pisa.select(Q, Kt, pyr, shape, want_score=False)[0],
+                "flat": pisa.select_flat(Q, Kt, pyr, shape, want_score=False)[0]}
+        scale = 1.0 / math.sqrt(d)
+        acc = {k: dict(hit=0.0, units=0, needle=0.0, nunits=0, mass=0.0, munits=0) for k in ("pyramid", "flat", "exact")}
+        QB = 256
+        for b in range(B):
+            for kv in range(Hkv):
+                Qg = Q[b, :, kv * G:(kv + 1) * G, :]
+                Kk = Kt[b, :, kv, :]
+                u = syn.needle_direction(Q, Hkv, b, kv)
+                nd = torch.tensor(needles[b][kv], device=dev)
+                for q0 in range(0, N, QB):
+                    q1 = min(q0 + QB, N)
+                    ll = exact_leaf_lse(Qg, Kk, q0, q1, C, scale)                     # [q, G, nl]
+                    full = torch.logsumexp(ll, dim=-1, keepdim=True)                  # [q, G, 1]
+                    score = ll.sum(1)                                                 # [q, nl]
+                    nl = score.shape[1]
+                    vis = torch.arange(q0, q1, device=dev) // C + 1                   # visible leaves
+                    kk = min(K, nl)
+                    exact = torch.topk(score, kk, dim=-1).indices
+                    exact = exact.masked_fill(torch.arange(kk, device=dev).view(1, -1) >= vis.view(-1, 1), -1)
+                    aligned = (Qg[q0:q1].float() @ u).sum(-1) > 0
+                    vneed = (nd.view(1, -1) < vis.view(-1, 1))                        # [q, 8]
+                    prune = vis > K                                                   # rows where K < visible
+                    for name in acc:
+                        sel = exact if name == "exact" else sels[name][b, kv, q0:q1].long()
+                        hit = (sel.unsqueeze(-1) == exact.unsqueeze(1)) & (sel.unsqueeze(-1) >= 0)
+                        a = acc[name]
+                        a["hit"] += hit.any(-1).sum(-1)[prune].float().sum().item()
+                        a["units"] += int(prune.sum().item()) * K
+                        got = (nd.view(1, 1, -1) == sel.unsqueeze(-1)).any(1) & vneed      # [q, 8]
+                        rows = aligned & vneed.any(-1)
+                        a["needle"] += (got.sum(-1).float() / vneed.sum(-1).clamp_min(1))[rows].sum().item()
+                        a["nunits"] += int(rows.sum().item())
+                        g_ = sel.clamp_min(0).unsqueeze(1).expand(-1, G, -1)
+                        m = torch.exp(torch.gather(ll, 2, g_) - full) * (sel >= 0).unsqueeze(1)
+                        a["mass"] += m.sum(-1).sum().item()
+                        a["munits"] += (q1 - q0) * G
+        out = {name: {"recall_exact_topk": a["hit"] / max(1, a["units"]),
+                      "needle_recall_aligned": a["needle"] / max(1, a["nunits"]),
+                      "attention_mass": a["mass"] / max(1, a["munits"])} for name, a in acc.items()}
+        print(json.dumps({"workload": "selection quality", "N": N, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "C": C,
+                          "K": K, "data": "synthetic (seeded N(0,1) bf16, 8 needle leaf blocks per KV head)",
+                          "reference": "exhaustive exact leaf scores (dense fp32 logits on the GPU, per-head LSE "
+                                       "per leaf summed over the group)",
+                          "recall_rows": "queries with more than K visible leaves",
+                          "needle_rows": "queries with sum_h q.u > 0 and at least one visible needle leaf",
+                          "mass": "mean over (query, head) of the full causal softmax mass inside the selected leaves",
+                          **out}), flush=True)
+
+
 def run_sweep(args, cfg, local):
     """Pyramid selection vs the flat comparator over N (one JSON line per N)."""
     import pyramid_top_selection_gb300 as pisa
@@ -671,6 +755,10 @@ def main():
     if args.workload == "sweep":
         if rank == 0:
             run_sweep(args, cfg, local)
+        return
+    if args.workload == "quality":
+        if rank == 0:
+            run_quality(args, cfg, local)
         return
     if args.workload == "decode":
         run_decode(args, cfg, rank, world, local)

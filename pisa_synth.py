@@ -33,22 +33,33 @@ def randn_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
     return x.to(torch.bfloat16)
 
 
+def needle_direction(Q: torch.Tensor, Hkv: int, b: int, kv: int) -> torch.Tensor:
+    """u = unit(sum over tokens and the group's query heads of q), fp32 [d]."""
+    G = Q.shape[2] // Hkv
+    u = Q[b, :, kv * G:(kv + 1) * G, :].to(torch.float32).sum(dim=(0, 1))
+    return u / u.norm().clamp_min(1e-30)
+
+
+def needle_leaves(B: int, Hkv: int, n0: int, seed: int, n_needles: int = 8, device="cpu"):
+    """The needle leaf indices [b][kv] -> list, drawn exactly as plant_needles draws them."""
+    g = _gen(device, seed)
+    n_pick = min(n_needles, n0)
+    return [[torch.randperm(n0, generator=g, device=device)[:n_pick].tolist() for _ in range(Hkv)]
+            for _ in range(B)]
+
+
 def plant_needles(Q: torch.Tensor, K: torch.Tensor, C: int, seed: int, n_needles: int = 8,
                   strength: float = 3.0) -> torch.Tensor:
     """Return a copy of K [B,N,Hkv,d] with needle leaf blocks planted (see module doc)."""
     B, N, Hq, d = Q.shape
     Hkv = K.shape[2]
-    G = Hq // Hkv
     n0 = (N + C - 1) // C
     K = K.clone()
-    g = _gen(K.device, seed)
-    n_pick = min(n_needles, n0)
+    leaves = needle_leaves(B, Hkv, n0, seed, n_needles, K.device)
     for b in range(B):
         for kv in range(Hkv):
-            u = Q[b, :, kv * G:(kv + 1) * G, :].to(torch.float32).sum(dim=(0, 1))
-            u = u / u.norm().clamp_min(1e-30)
-            leaves = torch.randperm(n0, generator=g, device=K.device)[:n_pick]
-            for t in leaves.tolist():
+            u = needle_direction(Q, Hkv, b, kv)
+            for t in leaves[b][kv]:
                 s, e = t * C, min((t + 1) * C, N)
                 K[b, s:e, kv, :] = (K[b, s:e, kv, :].to(torch.float32) + strength * u).to(torch.bfloat16)
     return K
