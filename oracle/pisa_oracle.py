@@ -33,7 +33,9 @@ Readings taken where the pages are silent (each one is listed in the design note
   R13 fewer than K visible leaves -> all visible leaves, padded with -1.
   R14 ties: higher score first, then lower node index.
   R15 the output leaf list is sorted ascending.
-Parity unpinned: R7, R8, R11, R12 and R14 are readings that nothing the pages print can
+  R16 the digest's PISA-1 ablation ("scored by the mean"): every block, leaves included, is
+      scored by sum_h s q_h . mu_i(l,m), its own causal mean key; descent and ties unchanged.
+Parity unpinned: R7, R8, R11, R12, R14 and R16 are readings that nothing the pages print can
 confirm; the pins in the tests check the oracle against the mathematics of those readings.
 
 Precision: every input is the exact bf16 value promoted to float64; all arithmetic is fp64.
@@ -212,6 +214,67 @@ def select_unit(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, scale: 
     kept = kept[order]
     pos = [int(np.nonzero(leaf_cand == t)[0][0]) for t in kept]
     return UnitSelection(kept, sc[pos], ph[pos], min_margin, cand_sizes, leaf_cand)
+
+
+# --------------------------------------------------------------------------------------
+# PISA-1 ablation (digest page, "Method key points": in the ablation, PISA-1 scores blocks
+# by the mean instead of the LSE; the full LSE is reported to work better)
+# --------------------------------------------------------------------------------------
+def mean_scores(q: np.ndarray, i: int, l: int, nodes: np.ndarray, summ: CausalKeySummaries,
+                scale: float) -> np.ndarray:
+    """PISA-1 score of nodes at level l (l = 0: leaves): sum_h s q_h . mu_i(l, m)."""
+    mu = summ.means(l, nodes, i)                      # [n, d]
+    return (scale * (q @ mu.T)).sum(axis=0)
+
+
+def select_unit_mean(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, scale: float,
+                     g: int = 2) -> tuple[np.ndarray, np.ndarray, float]:
+    """The coarse-to-fine descent with PISA-1 scores at every level; returns the ascending
+    leaves, their scores and the smallest pruning margin."""
+    assert g == 2, "the pyramid's merge factor is 2, so a node has 2 children"
+    kept = np.array([0], dtype=np.int64)
+    min_margin = np.inf
+    cand = kept
+    for l in range(summ.top - 1, -1, -1):
+        cand = np.array([c for a in kept for c in (2 * int(a), 2 * int(a) + 1)
+                         if summ.visible(l, c, i)], dtype=np.int64)
+        if l == 0:
+            break
+        if len(cand) <= K:
+            kept = cand
+            continue
+        kept, margin = _top_k(cand, mean_scores(q, i, l, cand, summ, scale), K)
+        min_margin = min(min_margin, margin)
+    sc = mean_scores(q, i, 0, cand, summ, scale)
+    kept, margin = _top_k(cand, sc, K)
+    min_margin = min(min_margin, margin)
+    kept = np.sort(kept)
+    pos = [int(np.nonzero(cand == t)[0][0]) for t in kept]
+    return kept, sc[pos], min_margin
+
+
+def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
+    """PISA-1 selection for every (batch, KV head, query): idx [B,Hkv,N,K] ascending (-1 pad),
+    score [B,Hkv,N,K] (the PISA-1 leaf scores, -inf pad), margin [B,Hkv,N]."""
+    Q, K = _as64(Q), _as64(K)
+    B, N, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    G = Hq // Hkv
+    s = default_scale(d) if scale is None else float(scale)
+    qs = range(N) if queries is None else [int(x) for x in queries]
+    idx = np.full((B, Hkv, N, K_sel), -1, dtype=np.int32)
+    score = np.full((B, Hkv, N, K_sel), np.nan)
+    margin = np.full((B, Hkv, N), np.nan)
+    for b in range(B):
+        for kv in range(Hkv):
+            summ = CausalKeySummaries(K[b, :, kv, :], C)
+            for i in qs:
+                leaves, sc, mg = select_unit_mean(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s)
+                idx[b, kv, i, :len(leaves)] = leaves
+                score[b, kv, i, :] = NEG_INF
+                score[b, kv, i, :len(leaves)] = sc
+                margin[b, kv, i] = mg
+    return dict(idx=idx, score=score, margin=margin)
 
 
 def _as64(x) -> np.ndarray:

@@ -108,7 +108,18 @@ def _bf_score(q, K, l, m, i, C, s):
     return tot
 
 
-def _bf_select(q, K, i, C, Ksel, s):
+def _bf_mean_score(q, K, l, m, i, C, s):
+    """PISA-1 score by token loops: sum_h s q_h . mean of the node's keys j <= i."""
+    N = K.shape[0]
+    toks = [j for j in range(m * (C << l), min((m + 1) * (C << l), N)) if j <= i]
+    tot = 0.0
+    for h in range(q.shape[0]):
+        tot += s * sum(q[h, k] * sum(K[j, k] for j in toks) / len(toks) for k in range(K.shape[1]))
+    return tot
+
+
+def _bf_select(q, K, i, C, Ksel, s, score_fn=None):
+    score_fn = score_fn or _bf_score
     N = K.shape[0]
     n = [-(-N // C)]
     while n[-1] > 1:
@@ -117,7 +128,7 @@ def _bf_select(q, K, i, C, Ksel, s):
     for l in range(len(n)):
         for m in range(n[l]):
             if m * (C << l) <= i:
-                table[(l, m)] = _bf_score(q, K, l, m, i, C, s)
+                table[(l, m)] = score_fn(q, K, l, m, i, C, s)
     kept = {0}
     for l in range(len(n) - 2, -1, -1):
         cand = sorted({c for a in kept for c in (2 * a, 2 * a + 1) if (l, c) in table})
@@ -148,6 +159,41 @@ def test_descent_matches_brute_force(N, C, Ksel, G, seed):
         assert list(got[got >= 0]) == leaves, (i, got, leaves)
         np.testing.assert_allclose(out["score"][0, 0, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
         assert np.all(out["score"][0, 0, i, len(leaves):] == -np.inf)
+
+
+@pytest.mark.parametrize("N,C,Ksel,G,seed", [
+    (64, 4, 1, 1, 0), (96, 4, 3, 2, 2), (128, 8, 3, 2, 4), (61, 4, 2, 2, 5), (200, 8, 1, 2, 6)])
+def test_pisa1_descent_matches_brute_force(N, C, Ksel, G, seed):
+    d = 4
+    Q = _rand((1, N, G, d), 40 + seed, scale=2.0)
+    K = _rand((1, N, 1, d), 50 + seed, scale=2.0)
+    s = 0.7
+    out = po.select_mean(Q, K, C, Ksel, scale=s)
+    rng = np.random.default_rng(seed)
+    for i in sorted(set(rng.integers(0, N, 12).tolist()) | {0, N - 1}):
+        leaves, scores = _bf_select(Q[0, i], K[0, :, 0, :], i, C, Ksel, s, _bf_mean_score)
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == leaves, (i, got, leaves)
+        np.testing.assert_allclose(out["score"][0, 0, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
+        assert np.all(out["score"][0, 0, i, len(leaves):] == -np.inf)
+
+
+def test_pisa1_keep_all_and_no_pruning_cases():
+    N, C, G, d = 96, 8, 2, 6
+    Q = _rand((1, N, G, d), 60)
+    K = _rand((1, N, 1, d), 61)
+    n0 = -(-N // C)
+    # K >= n0: every visible leaf, in order
+    out = po.select_mean(Q, K, C, n0)
+    for i in range(N):
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == list(range(i // C + 1))
+    # 2K >= n0: no intermediate level prunes, so the leaf stage sees every visible leaf and
+    # PISA-1 is the flat top-K of the mean scores
+    Ksel = -(-n0 // 2)
+    a = po.select_mean(Q, K, C, Ksel)
+    b = po.select_flat(Q, K, C, Ksel)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
 
 
 def test_descent_invariants():
