@@ -511,9 +511,11 @@ def run_quality(args, cfg, local):
         shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, c["g"], c["qtile"])
         pyr = pisa.build_pyramid(Kt, shape)
         sels = {"pyramid": pisa.select(Q, Kt, pyr, shape, want_score=False)[0],
+                "pisa1_mean": pisa.select_mean(Q, Kt, pyr, shape, want_score=False)[0],
                 "flat": pisa.select_flat(Q, Kt, pyr, shape, want_score=False)[0]}
         scale = 1.0 / math.sqrt(d)
-        acc = {k: dict(hit=0.0, units=0, needle=0.0, nunits=0, mass=0.0, munits=0) for k in ("pyramid", "flat", "exact")}
+        acc = {k: dict(hit=0.0, units=0, needle=0.0, nunits=0, mass=0.0, munits=0)
+               for k in ("pyramid", "pisa1_mean", "flat", "exact")}
         QB = 256
         for b in range(B):
             for kv in range(Hkv):
@@ -576,7 +578,8 @@ def run_sweep(args, cfg, local):
         idx = torch.empty(c["B"], c["Hkv"], N, c["K"], dtype=torch.int32, device=dev)
         ws_p, ws_f = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 1, dev)
         out = {}
-        for name, fn, ws in (("pyramid", pisa.select, ws_p), ("flat", pisa.select_flat, ws_f)):
+        for name, fn, ws in (("pyramid", pisa.select, ws_p), ("pisa1_mean", pisa.select_mean, ws_p),
+                             ("flat", pisa.select_flat, ws_f)):
             for _ in range(max(1, args.warmup)):
                 fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)
             ts = []
@@ -596,7 +599,9 @@ def run_sweep(args, cfg, local):
                           "d": c["d"], "K": c["K"], "pyramid_select_ms": out["pyramid"],
                           "flat_select_ms": out["flat"], "flat_over_pyramid": out["flat"] / out["pyramid"],
                           "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3),
-                          "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"]}),
+                          "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"],
+                          "pisa1_mean_select_ms": out["pisa1_mean"],
+                          "pisa1_mean_kernels_ms": out["pisa1_mean_kernels"]}),
               flush=True)
         del Q, Kt, pyr, idx, ws_p, ws_f
         torch.cuda.empty_cache()

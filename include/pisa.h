@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define PISA_VERSION 2
+#define PISA_VERSION 3
 #define PISA_MAX_LEVELS 32
 
 enum {
@@ -138,6 +138,16 @@ int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
  * over every visible leaf; top K with the same tie rule and output layout as
  * pisa_select. Workspace: PISA_OP_SELECT_FLAT. */
 int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
+                     const float* pyr_sum, int32_t* idx, float* score, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* PISA-1 ablation selection (digest page, "Method key points": the ablation that scores
+ * blocks by the mean instead of the LSE): the same coarse-to-fine descent as pisa_select,
+ * but every block, leaves included, scores sum_h s q_{i,h} . mu_i(l,m), its own causal mean
+ * key; no exact leaf stage. score (nullable) receives these mean scores of the selected
+ * leaves (-inf padding). Same arguments, layouts, tie rule and errors as pisa_select minus
+ * head_lse. Workspace: PISA_OP_SELECT. */
+int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
                      const float* pyr_sum, int32_t* idx, float* score, void* ws,
                      size_t ws_bytes, void* stream);
 

@@ -33,9 +33,9 @@ Readings taken where the pages are silent (each one is listed in the design note
   R13 fewer than K visible leaves -> all visible leaves, padded with -1.
   R14 ties: higher score first, then lower node index.
   R15 the output leaf list is sorted ascending.
-  R16 the digest's PISA-1 ablation ("scored by the mean"): every block, leaves included, is
+  R22 the digest's PISA-1 ablation ("scored by the mean"): every block, leaves included, is
       scored by sum_h s q_h . mu_i(l,m), its own causal mean key; descent and ties unchanged.
-Parity unpinned: R7, R8, R11, R12, R14 and R16 are readings that nothing the pages print can
+Parity unpinned: R7, R8, R11, R12, R14 and R22 are readings that nothing the pages print can
 confirm; the pins in the tests check the oracle against the mathematics of those readings.
 
 Precision: every input is the exact bf16 value promoted to float64; all arithmetic is fp64.

@@ -19,14 +19,14 @@ LIB_PATH = os.path.join(_HERE, "libpisa.so")
 PISA_OK, PISA_EINVAL, PISA_EUNSUPPORTED, PISA_EWORKSPACE, PISA_ECUDA, PISA_ETIMEOUT = range(6)
 OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD = range(4)
 MAX_LEVELS = 32
-ABI_VERSION = 2          # PISA_VERSION of the header these argument lists follow
+ABI_VERSION = 3          # PISA_VERSION of the header these argument lists follow
 
 EXPORTS = (
     "pisa_version", "pisa_last_error", "pisa_pyramid_layout", "pisa_workspace_size",
     "pisa_build_pyramid", "pisa_select", "pisa_select_flat", "pisa_sparse_attn_fwd",
     "pisa_sparse_attn_bwd", "pisa_decode_pyramid_layout", "pisa_decode_build_pyramid",
     "pisa_decode_step", "pisa_profile_start", "pisa_profile_stop", "pisa_profile_read",
-    "pisa_select_noalloc",
+    "pisa_select_noalloc", "pisa_select_mean",
 )
 
 
@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.pisa_build_pyramid.argtypes = [P(Shape), vp, vp, vp]
         L.pisa_select.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_select_flat.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
+        L.pisa_select_mean.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_sparse_attn_fwd.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_sparse_attn_bwd.argtypes = [P(Shape)] + [vp] * 10 + [vp, sz, vp]
         L.pisa_decode_pyramid_layout.argtypes = [P(DecodeShape), P(i32), P(i64), P(i64)]
@@ -193,6 +194,18 @@ def select_flat(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, sc
     if ws is None:
         ws = _workspace(shape, OP_SELECT_FLAT, dev)
     _check(lib().pisa_select_flat(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
+                                  _ptr(ws), ws.numel(), _stream(dev)))
+    return idx, score
+
+
+def select_mean(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, score=None):
+    """PISA-1 ablation selection: the pyramid descent with every block scored by its mean key."""
+    _select_in(Q, Kt, pyr)
+    dev = Q.device
+    idx, score = _select_out(Q, shape, want_score, idx, score)
+    if ws is None:
+        ws = _workspace(shape, OP_SELECT, dev)
+    _check(lib().pisa_select_mean(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
                                   _ptr(ws), ws.numel(), _stream(dev)))
     return idx, score
 

@@ -196,6 +196,22 @@ int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
                  "pisa_select_flat");
 }
 
+int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
+                     const float* pyr_sum, int32_t* idx, float* score, void* ws,
+                     size_t ws_bytes, void* stream) {
+  PISA_CHECK(check_shape(shape));
+  PISA_CHECK(check_ptr(Q, "Q"));
+  PISA_CHECK(check_ptr(K, "K"));
+  PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
+  PISA_CHECK(check_ptr(idx, "idx"));
+  PISA_CHECK(check_ptr(score, "score", true));
+  const pisa::Dims d = dims_of(shape);
+  const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  PISA_CHECK(check_ws(d, g, PISA_OP_SELECT, ws, ws_bytes));
+  return cuda_rc(pisa::launch_select_mean(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
+                 "pisa_select_mean");
+}
+
 int pisa_sparse_attn_fwd(const pisa_shape_t* shape, const void* Q, const void* K, const void* V,
                          const int32_t* idx, const float* head_lse, void* O, float* lse, void* ws,
                          size_t ws_bytes, void* stream) {

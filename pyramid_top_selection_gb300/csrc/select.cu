@@ -96,12 +96,14 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
 }
 
 // MC: the most candidates a level can hold (2K rounded up to 32 or 64); the smaller size lets
-// more CTAs share an SM.
-template <int D, int MC>
+// more CTAs share an SM. MEAN: the PISA-1 ablation -- every block, leaves included, is scored
+// by s q . (its causal key sum) / (its visible key count), summed over the G heads; the leaf
+// candidates' scores go to cscore_out (same layout as cand_out) for the final top-K.
+template <int D, int MC, bool MEAN>
 __global__ void __launch_bounds__(kWarps * 32)
 route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
              const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl,
-             int32_t* __restrict__ cand_out) {
+             int32_t* __restrict__ cand_out, float* __restrict__ cscore_out) {
   constexpr int KS = D / 16;
   constexpr int RQ = D / 4;     // uint4 chunks per split row
   __shared__ int s_cand[kWarps][MC];
@@ -264,13 +266,17 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const float lv[2] = {l0, l1}, rvv[2] = {r0, r1};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float x0 = lv[e] * (s.scale / cnt0);
         float l;
-        if (rv) {       // LSE of two terms: max + log(1 + exp(-|difference|))
-          const float x1 = rvv[e] * (s.scale / cnt1);
-          l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
+        if constexpr (MEAN) {   // the node's own mean key: (left + right sums) / (their counts)
+          l = rv ? (lv[e] + rvv[e]) * (s.scale / (cnt0 + cnt1)) : lv[e] * (s.scale / cnt0);
         } else {
-          l = x0;
+          const float x0 = lv[e] * (s.scale / cnt0);
+          if (rv) {     // LSE of two terms: max + log(1 + exp(-|difference|))
+            const float x1 = rvv[e] * (s.scale / cnt1);
+            l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
+          } else {
+            l = x0;
+          }
         }
         if (2 * p + e < G) part += l;
       }
@@ -341,21 +347,59 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
 
   // leaf candidates: visible children of the kept level-1 nodes (or the single leaf)
   int32_t* out = cand_out + ((head * s.N) + i) * (2 * Ksel);
+  int nc = 1;
   if (L == 1) {
-    for (int q = lane; q < 2 * Ksel; q += 32) out[q] = q == 0 ? 0 : -1;
-    return;
-  }
-  {
+    if (lane == 0) cand[0] = 0;
+  } else {
     const int a = lane < nkept ? kept[lane] : -1;
     const bool c0 = a >= 0;
     const bool c1 = a >= 0 && static_cast<int64_t>(2 * a + 1) * C <= i;
     const unsigned m0 = __ballot_sync(0xffffffffu, c0), m1 = __ballot_sync(0xffffffffu, c1);
     const int pos = __popc(m0 & ltm) + __popc(m1 & ltm);
-    const int nc = __popc(m0) + __popc(m1);
-    if (c0) out[pos] = 2 * a;
-    if (c1) out[pos + 1] = 2 * a + 1;
-    for (int q = nc + lane; q < 2 * Ksel; q += 32) out[q] = -1;
+    nc = __popc(m0) + __popc(m1);
+    __syncwarp();
+    if (c0) cand[pos] = 2 * a;
+    if (c1) cand[pos + 1] = 2 * a + 1;
   }
+  __syncwarp();
+  if constexpr (MEAN) {
+    // PISA-1 leaf scores: s q . S(0,t) / count; the query's own leaf uses its causal prefix dot
+    const float pd0 = s_pd[warp][0][2 * p], pd1 = s_pd[warp][0][2 * p + 1];
+    auto leaf_part = [&](int t, float d0, float d1) {
+      if (t < 0) return 0.f;
+      float cnt;
+      if (t == ti) {
+        d0 = pd0;
+        d1 = pd1;
+        cnt = static_cast<float>(i - t * C + 1);
+      } else {
+        cnt = static_cast<float>(min(static_cast<int64_t>(t + 1) * C, static_cast<int64_t>(s.N)) -
+                                 static_cast<int64_t>(t) * C);
+      }
+      const float k = s.scale / cnt;
+      return (2 * p < G ? d0 * k : 0.f) + (2 * p + 1 < G ? d1 * k : 0.f);
+    };
+    for (int mt = 0; mt * 16 < nc; ++mt) {
+      const int csa = mt * 16 + g, csb = csa + 8;
+      const int ta = csa < nc ? cand[csa] : -1, tb = csb < nc ? cand[csb] : -1;
+      const bool la = ta >= 0 && ta != ti, lb = tb >= 0 && tb != ti;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* ra = spl_h + (la ? (geo.off[0] + ta) * RQ : 0);
+      const uint4* rb = spl_h + (lb ? (geo.off[0] + tb) * RQ : 0);
+      mma_split_rows<KS>(acc, ra, la, rb, lb, p, qb);
+      float pa = leaf_part(ta, acc[0], acc[1]), pb = leaf_part(tb, acc[2], acc[3]);
+      pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+      pa += __shfl_xor_sync(0xffffffffu, pa, 2);
+      pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+      pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+      if (p == 0 && csa < nc) sc[csa] = no_nan(pa);
+      if (p == 0 && csb < nc) sc[csb] = no_nan(pb);
+    }
+    __syncwarp();
+    float* outs = cscore_out + ((head * s.N) + i) * (2 * Ksel);
+    for (int q = lane; q < 2 * Ksel; q += 32) outs[q] = q < nc ? sc[q] : neg_inf();
+  }
+  for (int q = lane; q < 2 * Ksel; q += 32) out[q] = q < nc ? cand[q] : -1;
 }
 
 // ---------------------------------------------------------------------------- finish
@@ -683,8 +727,8 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   {
   ProfScope ps(st, "route");
 #define PISA_ROUTE(DD, MM) \
-  route_kernel<DD, MM><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
-                                                    static_cast<const __nv_bfloat16*>(K), spl, cand)
+  route_kernel<DD, MM, false><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
+                                                           static_cast<const __nv_bfloat16*>(K), spl, cand, nullptr)
   if (s.d == 128) {
     if (2 * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
   } else {
@@ -706,6 +750,40 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
     ProfScope ps(st, "topk");
     topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
         units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse);
+  }
+  return cudaGetLastError();
+}
+
+// PISA-1 ablation: the descent with mean scores at every level, the leaf candidates scored by
+// their mean keys inside the routing kernel, then the final top K (no exact leaf stage).
+int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
+                       int32_t* idx, float* score, char* ws, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const SelectWs w = select_ws(s, g);
+  uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
+  int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
+  float* cscore = reinterpret_cast<float*>(ws + w.cscore);
+  int err = launch_split(s, g, pyr, spl, st);
+  if (err) return err;
+  dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
+  {
+    ProfScope ps(st, "route_mean");
+#define PISA_ROUTE(DD, MM) \
+  route_kernel<DD, MM, true><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
+                                                          static_cast<const __nv_bfloat16*>(K), spl, cand, cscore)
+    if (s.d == 128) {
+      if (2 * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
+    } else {
+      if (2 * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
+    }
+#undef PISA_ROUTE
+  }
+  if ((err = cudaGetLastError())) return err;
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  {
+    ProfScope ps(st, "topk");
+    topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+        units, 2 * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr);
   }
   return cudaGetLastError();
 }
