@@ -74,6 +74,28 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of the ranks' values: the slowest rank sets the whole job's time."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_barrier(world: int) -> None:
+    """All ranks meet, then this rank's GPU work drains (both sides of a timed region)."""
+    if world > 1:
+        torch.distributed.barrier()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's units over the (max-over-ranks) step time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -281,11 +303,8 @@ def run_ours(args, cfg, rank, world, local):
         barrier()
     times = [a.elapsed_time(b) for a, b in ev]
     ms = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = B * N * world / (ms / 1e3)
+    ms = max_over_ranks(ms, world, dev)
+    value = job_rate(B * N, world, ms)
 
     # per-kernel times (events around every launch, on the launch stream)
     pisa.profile_start()
@@ -375,13 +394,10 @@ def run_ours(args, cfg, rank, world, local):
         barrier()
         e_ms = run_pipeline(args.steps) / args.steps
         barrier()
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, dev)
         h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV))
         d2h = sum(x.numel() * x.element_size() for x in (hO, hidx, hlse))
-        e2e = {"value": B * N * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+        e2e = {"value": job_rate(B * N, world, e_ms), "unit": "tokens/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "schedule": "3 streams: inputs of step k+1 in and results of step k-1 out while step k computes; "
                            "inputs larger than L2 (no flush)"}
@@ -666,14 +682,14 @@ def run_decode(args, cfg, rank, world, local):
         step()
     stream = torch.cuda.current_stream(dev)
     a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
+    rank_barrier(world)
     with ClockSampler(local) as clk:
         a.record(stream)
         for _ in range(steps):
             step()
         b_.record(stream)
-        torch.cuda.synchronize()
-    ms = a.elapsed_time(b_) / steps
+        rank_barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b_) / steps, world, dev)
     prof_steps = min(8, total - cur[0])
     kernels, dom, launches = profile_kernels(pisa, step, prof_steps)
     assert int(status.sum()) == 0
@@ -686,7 +702,7 @@ def run_decode(args, cfg, rank, world, local):
     roof = roofline_entry("decode_step", "hbm", units * per, "bytes", kernels["decode_step"]["avg_ms"], units, per)
     if rank == 0:
         line = {"workload": "decode", "metric": "decode tokens/s (one fused kernel per step)",
-                "value": B * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+                "value": job_rate(B, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
                 "config": {"B": B, "cache_tokens": L0, "Ncap": Ncap, "Hq": Hq, "Hkv": Hkv, "d": d, "C": C, "K": K,
                            "l2": "working set per step larger than L2 (no flush)"},
@@ -724,22 +740,22 @@ def run_train(args, cfg, rank, world, local):
         step()
     stream = torch.cuda.current_stream(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize()
+    rank_barrier(world)
     with ClockSampler(local) as clk:
         for k in range(args.steps):
             flush.zero_()
             ev[k][0].record(stream)
             step()
             ev[k][1].record(stream)
-        torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        rank_barrier(world)
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world, dev)
     kernels, dom, launches = profile_kernels(pisa, step, args.steps, flush)
     keys = selected_keys(idx.cpu(), C, N)
     units = keys * (Hq // Hkv)
     roof = roofline_entry("attn_bwd", "tensor", units * 10 * d, "flops", kernels["attn_bwd"]["avg_ms"], units, 10 * d)
     if rank == 0:
         line = {"workload": "train", "metric": "training tokens/s (select + sparse attention fwd + bwd)",
-                "value": B * N * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "value": job_rate(B * N, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
                 "config": {k: cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
                 "gpu_launches": int(round(launches)), "kernels": kernels, "dominant": dom, "roofline": roof}
