@@ -71,6 +71,14 @@ def test_host_validation_before_any_cuda_call():
     assert rc == _pisa.PISA_EWORKSPACE
     rc, msg = _rc(L.pisa_select, ctypes.byref(good), A, A, A, A, None, A + 4, A, ws, None)
     assert rc == _pisa.PISA_EINVAL and "head_lse" in msg
+    # the PISA-1 ablation entry validates like pisa_select (same shape checks, workspace op)
+    for shape, code, text in cases[:4]:
+        rc, msg = _rc(L.pisa_select_mean, ctypes.byref(shape), A, A, A, A, None, A, 1 << 40, None)
+        assert rc == code and text in msg, (rc, msg)
+    rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, None, None, A, ws, None)
+    assert rc == _pisa.PISA_EINVAL and "idx is NULL" in msg
+    rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, A, None, A, ws - 1, None)
+    assert rc == _pisa.PISA_EWORKSPACE
     rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, None, A, A, A, 1 << 40, None)
     assert rc == _pisa.PISA_EINVAL and "V is NULL" in msg
     rc, msg = _rc(L.pisa_build_pyramid, None, A, A, None)
