@@ -489,3 +489,133 @@ def test_sampled_backward_equals_full_backward():
         s0, e0 = po.node_range(0, t, C, N)
         np.testing.assert_allclose(sk[(b, kv, t)], dK[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(sv[(b, kv, t)], dV[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- pruning margin
+# The oracle reports, per unit, the smallest gap between the K-th and (K+1)-th ranked scores
+# over every level that prunes (its candidate set holds more than K). The GPU parity tests
+# exempt a unit from the exact index match when that margin is below 1e-3, so the margin
+# itself is pinned here: against a brute-force descent that records the gap of every level
+# from its own score table, and against closed forms.
+def _bf_descent_gaps(q, K, i, C, Ksel, s, score_fn=None):
+    """Brute-force descent (scores from the scalar enumerator) that also returns the
+    K-th vs (K+1)-th gap of every level whose candidate set exceeds K, keyed by level."""
+    score_fn = score_fn or _bf_score
+    N = K.shape[0]
+    n = [-(-N // C)]
+    while n[-1] > 1:
+        n.append(-(-n[-1] // 2))
+    table = {(l, m): score_fn(q, K, l, m, i, C, s)
+             for l in range(len(n)) for m in range(n[l]) if m * (C << l) <= i}
+    kept, gaps = {0}, {}
+    for l in range(len(n) - 2, -1, -1):
+        cand = sorted({c for a in kept for c in (2 * a, 2 * a + 1) if (l, c) in table})
+        ranked = sorted(cand, key=lambda c: (-table[(l, c)], c))
+        if len(cand) > Ksel:
+            gaps[l] = table[(l, ranked[Ksel - 1])] - table[(l, ranked[Ksel])]
+        kept = set(ranked[:Ksel]) if (len(cand) > Ksel or l == 0) else set(cand)
+    return gaps
+
+
+MARGIN_CASES = [(64, 4, 1, 1, 0), (96, 4, 3, 2, 2), (128, 8, 3, 2, 4), (200, 8, 1, 2, 6),
+                (256, 4, 3, 1, 7), (256, 4, 2, 2, 8)]
+
+
+def _check_margins(select_fn, score_fn, seed_base):
+    """Raises AssertionError where select_fn's margin differs from the brute-force minimum gap.
+    Returns which levels supplied the minimum (to show that both kinds are exercised)."""
+    sources = set()
+    for N, C, Ksel, G, seed in MARGIN_CASES:
+        d = 4
+        Q = _rand((1, N, G, d), seed_base + seed, scale=2.0)
+        K = _rand((1, N, 1, d), seed_base + 50 + seed, scale=2.0)
+        s = 0.7
+        rng = np.random.default_rng(seed)
+        qs = sorted(set(rng.integers(0, N, 10).tolist()) | {N - 1})
+        out = select_fn(Q, K, C, Ksel, scale=s, queries=qs)
+        for i in qs:
+            gaps = _bf_descent_gaps(Q[0, i], K[0, :, 0, :], i, C, Ksel, s, score_fn)
+            want = min(gaps.values()) if gaps else np.inf
+            got = out["margin"][0, 0, i]
+            assert (got == want) if not np.isfinite(want) else abs(got - want) <= 1e-12, (N, C, Ksel, i, got, want)
+            if gaps:
+                sources.add("leaf" if min(gaps, key=gaps.get) == 0 else "intermediate")
+    return sources
+
+
+def test_margin_matches_brute_force_gaps_of_every_pruning_level():
+    sources = _check_margins(po.select, _bf_score, 200)
+    assert sources == {"leaf", "intermediate"}       # the minimum comes from both kinds of level
+
+
+def test_pisa1_margin_matches_brute_force_gaps():
+    sources = _check_margins(po.select_mean, _bf_mean_score, 300)
+    assert sources == {"leaf", "intermediate"}
+
+
+def test_margin_constant_leaves_closed_form():
+    # Constant keys inside each leaf and K >= n1 (only the leaf level prunes): the exact leaf
+    # score is sum_h (s q_h.k_t + log n_t) and the flat score s sum_h q_h.k_t, so each margin
+    # is the gap between the K-th and (K+1)-th of those closed forms.
+    N, C, G, d = 128, 8, 2, 6
+    n0 = N // C
+    Ksel = n0 // 2                                   # = n1: no intermediate level prunes
+    Q = _rand((1, N, G, d), 90)
+    kt = _rand((n0, d), 91)
+    K = np.repeat(kt, C, axis=0)[None, :, None, :]
+    s = 0.45
+    qs = [Ksel * C + 3, 100, N - 1]                  # more than K visible leaves
+    sel = po.select(Q, K, C, Ksel, scale=s, queries=qs)
+    flat = po.select_flat(Q, K, C, Ksel, scale=s, queries=qs)
+    for i in qs:
+        vis = np.arange(i // C + 1)
+        base = s * torch.from_numpy(Q[0, i]).sum(0).numpy() @ kt[vis].T
+        n_t = np.array([min((t + 1) * C, i + 1) - t * C for t in vis])
+        for o, sc in ((sel, base + G * np.log(n_t)), (flat, base)):
+            ranked = np.sort(sc)[::-1]
+            assert abs(o["margin"][0, 0, i] - (ranked[Ksel - 1] - ranked[Ksel])) <= 1e-12
+    # fewer than K + 1 visible leaves anywhere: nothing is pruned, the margin is infinite
+    few = po.select(Q, K, C, n0, scale=s, queries=[N - 1])
+    assert few["margin"][0, 0, N - 1] == np.inf
+
+
+def test_margin_pins_catch_planted_mistakes(monkeypatch):
+    # Mistakes planted in the oracle (on the CPU) must fail the pins above.
+    real = po._top_k
+
+    def unsorted_margin(cand, scores, K):
+        kept, m = real(cand, scores, K)
+        return kept, (np.inf if len(cand) <= K else float(scores[K - 1] - scores[K]))
+
+    def flipped_sign(cand, scores, K):
+        kept, m = real(cand, scores, K)
+        return kept, -m
+
+    def next_gap(cand, scores, K):
+        kept, m = real(cand, scores, K)
+        if len(cand) <= K + 1:
+            return kept, m
+        r = np.sort(scores)[::-1]
+        return kept, float(r[K] - r[K + 1])
+
+    for bad in (unsorted_margin, flipped_sign, next_gap):
+        monkeypatch.setattr(po, "_top_k", bad)
+        with pytest.raises(AssertionError):
+            _check_margins(po.select, _bf_score, 200)
+    monkeypatch.setattr(po, "_top_k", real)
+    # A margin taken at the leaf level only, or over the intermediate levels only, differs
+    # from the minimum over all pruning levels for some unit of the pinned cases, so an
+    # oracle that computed it would fail the brute-force pin.
+    leaf_only = inter_only = False
+    for N, C, Ksel, G, seed in MARGIN_CASES:
+        Q = _rand((1, N, G, 4), 200 + seed, scale=2.0)
+        K = _rand((1, N, 1, 4), 250 + seed, scale=2.0)
+        rng = np.random.default_rng(seed)
+        for i in sorted(set(rng.integers(0, N, 10).tolist()) | {N - 1}):
+            gaps = _bf_descent_gaps(Q[0, i], K[0, :, 0, :], i, C, Ksel, 0.7)
+            if not gaps:
+                continue
+            true = min(gaps.values())
+            leaf_only |= gaps.get(0, np.inf) != true
+            inter_only |= min([v for l, v in gaps.items() if l > 0], default=np.inf) != true
+    assert leaf_only and inter_only
