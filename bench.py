@@ -55,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_64k", choices=sorted(WORKLOADS))
@@ -63,6 +63,7 @@ def parse():
     ap.add_argument("--quality-n", default="4096,16384,65536")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     return ap.parse_args()
 
 
@@ -147,6 +148,19 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.fh.close()
+
+    def wait_started(self, busy, timeout_s: float = 3.0):
+        """Run untimed work (busy) until the sampler has written its first line, so that its
+        samples cover the timed region that follows."""
+        t0 = time.perf_counter()
+        while self.proc is not None and time.perf_counter() - t0 < timeout_s:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                pass
+            busy()
+            torch.cuda.synchronize()
 
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
@@ -295,6 +309,7 @@ def run_ours(args, cfg, rank, world, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     with ClockSampler(local) as clk:
+        clk.wait_started(lambda: step(Q, Kt, V))
         for k in range(args.steps):
             flush.zero_()                        # L2 flush, outside the timed events
             ev[k][0].record(stream)
@@ -406,6 +421,12 @@ def run_ours(args, cfg, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, *(x.cpu().double().numpy() for x in (Q, Kt, V)), budget_s=12.0)
 
+    # The other configurations, compact, in the same record (rank 0 only; each rank's GPU is
+    # its own replica, so one rank's figures stand for all).
+    configs = None
+    if rank == 0 and not args.no_extras:
+        configs = other_configs(dev, flush)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -418,6 +439,7 @@ def run_ours(args, cfg, rank, world, local):
                        "step": "build_pyramid + select + sparse_attn_fwd", "parallelism": f"replica x{world}"},
             "gpu_launches": int(round(per_step_launches * args.steps)),
             "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+            "configs": configs,
         }
         if clk.summary() is not None:
             line["clocks"] = clk.summary()
@@ -579,48 +601,127 @@ def run_quality(args, cfg, local):
                           **out}), flush=True)
 
 
+def sweep_point(args, cfg, N, dev, flush):
+    """Pyramid selection, its PISA-1 ablation and the flat comparator at one N (selection only,
+    median of L2-flushed runs), plus the pyramid build's achieved HBM bandwidth."""
+    import pyramid_top_selection_gb300 as pisa
+    c = dict(cfg, N=N)
+    Q, Kt, _ = syn.make_prefill(c["B"], N, c["Hq"], c["Hkv"], c["d"], C=c["C"], seed=0, needles=True, device=dev)
+    shape = pisa.make_shape(c["B"], N, c["Hq"], c["Hkv"], c["d"], c["C"], c["K"], c["g"], c["qtile"])
+    _, _, nodes = pisa.pyramid_layout(shape)
+    pyr = torch.empty(c["B"], c["Hkv"], nodes, c["d"], dtype=torch.float32, device=dev)
+    idx = torch.empty(c["B"], c["Hkv"], N, c["K"], dtype=torch.int32, device=dev)
+    ws_p, ws_f = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 1, dev)
+
+    def timed(fn):
+        for _ in range(max(1, args.warmup)):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = {"build_ms": timed(lambda: pisa.build_pyramid(Kt, shape, out=pyr))}
+    build_bytes = Kt.numel() * 2 + pyr.numel() * 4
+    out["build_gbs"] = build_bytes / (out["build_ms"] / 1e3) / 1e9
+    for name, fn, ws in (("pyramid", pisa.select, ws_p), ("pisa1_mean", pisa.select_mean, ws_p),
+                         ("flat", pisa.select_flat, ws_f)):
+        call = lambda: fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)   # noqa: E731
+        out[name] = timed(call)
+        kern, _, _ = profile_kernels(pisa, call, max(1, args.steps), flush)
+        out[name + "_kernels"] = {k: round(v["avg_ms"], 4) for k, v in kern.items()}
+    pk, _ = peaks()
+    line = {"workload": "selection sweep", "N": N, "B": c["B"], "Hq": c["Hq"], "Hkv": c["Hkv"], "d": c["d"],
+            "K": c["K"], "pyramid_select_ms": out["pyramid"], "flat_select_ms": out["flat"],
+            "flat_over_pyramid": out["flat"] / out["pyramid"],
+            "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3),
+            "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"],
+            "pisa1_mean_select_ms": out["pisa1_mean"], "pisa1_mean_kernels_ms": out["pisa1_mean_kernels"],
+            "build_ms": out["build_ms"], "build_gbs": out["build_gbs"],
+            "build_hbm_frac": out["build_gbs"] / pk["hbm_gbs"]}
+    del Q, Kt, pyr, idx, ws_p, ws_f
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_sweep(args, cfg, local):
     """Pyramid selection vs the flat comparator over N (one JSON line per N)."""
-    import pyramid_top_selection_gb300 as pisa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     for N in [int(x) for x in args.sweep_n.split(",")]:
-        c = dict(cfg, N=N)
-        Q, Kt, _ = syn.make_prefill(c["B"], N, c["Hq"], c["Hkv"], c["d"], C=c["C"], seed=0,
-                                    needles=True, device=dev)
-        shape = pisa.make_shape(c["B"], N, c["Hq"], c["Hkv"], c["d"], c["C"], c["K"], c["g"], c["qtile"])
-        pyr = pisa.build_pyramid(Kt, shape)
-        idx = torch.empty(c["B"], c["Hkv"], N, c["K"], dtype=torch.int32, device=dev)
-        ws_p, ws_f = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 1, dev)
-        out = {}
-        for name, fn, ws in (("pyramid", pisa.select, ws_p), ("pisa1_mean", pisa.select_mean, ws_p),
-                             ("flat", pisa.select_flat, ws_f)):
-            for _ in range(max(1, args.warmup)):
-                fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)
-            ts = []
-            for _ in range(args.steps):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)
-                b.record()
-                torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
-            out[name] = statistics.median(ts)
-            kern, _, _ = profile_kernels(pisa, lambda: fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx),
-                                         max(1, args.steps), flush)
-            out[name + "_kernels"] = {k: round(v["avg_ms"], 4) for k, v in kern.items()}
-        print(json.dumps({"workload": "selection sweep", "N": N, "B": c["B"], "Hq": c["Hq"], "Hkv": c["Hkv"],
-                          "d": c["d"], "K": c["K"], "pyramid_select_ms": out["pyramid"],
-                          "flat_select_ms": out["flat"], "flat_over_pyramid": out["flat"] / out["pyramid"],
-                          "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3),
-                          "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"],
-                          "pisa1_mean_select_ms": out["pisa1_mean"],
-                          "pisa1_mean_kernels_ms": out["pisa1_mean_kernels"]}),
-              flush=True)
-        del Q, Kt, pyr, idx, ws_p, ws_f
-        torch.cuda.empty_cache()
+        print(json.dumps(sweep_point(args, cfg, N, dev, flush)), flush=True)
+
+
+def prefill_point(args, cfg, dev, flush):
+    """Device step time of build + select + attend on one prefill configuration."""
+    import pyramid_top_selection_gb300 as pisa
+    B, N, Hq, Hkv, d, C, K, g, qtile = (cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile"))
+    Q, Kt, V = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0, needles=cfg["needles"], device=dev)
+    shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, g, qtile)
+    _, _, nodes = pisa.pyramid_layout(shape)
+    pyr = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=dev)
+    idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    hl = torch.empty(B, Hq, N, K, dtype=torch.float32, device=dev)
+    O, lse = torch.empty_like(Q), torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    ws_sel, ws_att = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 2, dev)
+
+    def step():
+        pisa.build_pyramid(Kt, shape, out=pyr)
+        pisa.select(Q, Kt, pyr, shape, ws=ws_sel, want_score=False, idx=idx, head_lse=hl)
+        pisa.sparse_attn_fwd(Q, Kt, V, idx, shape, ws=ws_att, out=O, lse=lse, head_lse=hl)
+
+    for _ in range(args.warmup):
+        step()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = sum(ts) / len(ts)
+    kernels, _, _ = profile_kernels(pisa, step, args.steps, flush)
+    return {"workload": f"prefill select+attend, N={N}", "tokens_per_s": B * N / (ms / 1e3), "ms_per_step": ms,
+            "config": {k: cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
+            "kernels_ms": {k: round(v["avg_ms"], 4) for k, v in kernels.items()}}
+
+
+def other_configs(dev, flush):
+    """The other configurations, each measured briefly on this GPU, as compact sub-objects of
+    the headline record: the 4K prefill, the selection sweep (pyramid vs flat) at 64K and 256K
+    with the pyramid build's bandwidth, the batch-32 decode and the training step."""
+    import types
+    sub = types.SimpleNamespace(steps=5, warmup=3)
+    t0 = time.perf_counter()
+    out = {"prefill_4k": prefill_point(sub, WORKLOADS["prefill_4k"], dev, flush)}
+    sw = {}
+    for N in (65536, 262144):
+        p = sweep_point(sub, WORKLOADS["sweep"], N, dev, flush)
+        e = {k: p[k] for k in ("pyramid_select_ms", "flat_select_ms", "flat_over_pyramid", "pisa1_mean_select_ms",
+                               "build_ms", "build_gbs", "build_hbm_frac")}
+        e["route_ms"] = p["pyramid_kernels_ms"].get("route")
+        e["leaf_score_ms"] = p["pyramid_kernels_ms"].get("leaf_score")
+        sw[f"N={N}"] = e
+    out["selection_sweep"] = {"config": {k: WORKLOADS["sweep"][k] for k in ("B", "Hq", "Hkv", "d", "C", "K", "g")},
+                              **sw}
+    dl = run_decode(types.SimpleNamespace(steps=64, warmup=4), WORKLOADS["decode"], 0, 1, dev.index, emit=False)
+    out["decode"] = {"tokens_per_s": dl["value"], "ms_per_step": dl["ms_per_step"], "hbm_gbs": dl["roofline"]["achieved"],
+                     "hbm_frac": dl["roofline"]["frac"], "config": dl["config"]}
+    tr = run_train(types.SimpleNamespace(steps=5, warmup=3), WORKLOADS["train"], 0, 1, dev.index, emit=False)
+    out["train"] = {"tokens_per_s": tr["value"], "ms_per_step": tr["ms_per_step"],
+                    "bwd_ms": tr["kernels"]["attn_bwd"]["avg_ms"], "bwd_tensor_tflops": tr["roofline"]["achieved"],
+                    "bwd_tensor_frac": tr["roofline"]["frac"], "config": tr["config"]}
+    out["seconds"] = time.perf_counter() - t0
+    return out
 
 
 # ------------------------------------------------------------------ decode and training
@@ -652,7 +753,7 @@ def roofline_entry(kernel, bound, amount, unit_kind, avg_ms, units, per):
             "units_per_launch": units, "per_unit": per, "per_unit_kind": unit_kind}
 
 
-def run_decode(args, cfg, rank, world, local):
+def run_decode(args, cfg, rank, world, local, emit=True):
     """Autoregressive decode: a batch of sequences with a long cache, one fused step per token."""
     import pyramid_top_selection_gb300 as pisa
     dev = torch.device("cuda", local)
@@ -700,6 +801,7 @@ def run_decode(args, cfg, rank, world, local):
     per = (2 * K * C * d * 2 + K * C * d * 2 + lv * 2 * K * 2 * d * 4 + C * d * 2 + len(sizes) * 3 * d * 4)
     units = B * Hkv
     roof = roofline_entry("decode_step", "hbm", units * per, "bytes", kernels["decode_step"]["avg_ms"], units, per)
+    line = None
     if rank == 0:
         line = {"workload": "decode", "metric": "decode tokens/s (one fused kernel per step)",
                 "value": job_rate(B, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -709,10 +811,12 @@ def run_decode(args, cfg, rank, world, local):
                 "gpu_launches": steps, "kernels": kernels, "roofline": roof}
         if clk.summary() is not None:
             line["clocks"] = clk.summary()
-        print(json.dumps(line), flush=True)
+        if emit:
+            print(json.dumps(line), flush=True)
+    return line
 
 
-def run_train(args, cfg, rank, world, local):
+def run_train(args, cfg, rank, world, local, emit=True):
     """Training step: pyramid + selection (no gradient) + sparse attention forward and backward."""
     import pyramid_top_selection_gb300 as pisa
     dev = torch.device("cuda", local)
@@ -753,6 +857,7 @@ def run_train(args, cfg, rank, world, local):
     keys = selected_keys(idx.cpu(), C, N)
     units = keys * (Hq // Hkv)
     roof = roofline_entry("attn_bwd", "tensor", units * 10 * d, "flops", kernels["attn_bwd"]["avg_ms"], units, 10 * d)
+    line = None
     if rank == 0:
         line = {"workload": "train", "metric": "training tokens/s (select + sparse attention fwd + bwd)",
                 "value": job_rate(B * N, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -761,7 +866,9 @@ def run_train(args, cfg, rank, world, local):
                 "gpu_launches": int(round(launches)), "kernels": kernels, "dominant": dom, "roofline": roof}
         if clk.summary() is not None:
             line["clocks"] = clk.summary()
-        print(json.dumps(line), flush=True)
+        if emit:
+            print(json.dumps(line), flush=True)
+    return line
 
 
 def main():

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define PISA_VERSION 3
+#define PISA_VERSION 4
 #define PISA_MAX_LEVELS 32
 
 enum {
@@ -50,11 +50,33 @@ enum {
   PISA_EUNSUPPORTED = 2, /* valid per the method but not built here (see the list above) */
   PISA_EWORKSPACE = 3,   /* workspace pointer null or smaller than pisa_workspace_size */
   PISA_ECUDA = 4,        /* a kernel launch or async memset failed */
-  PISA_ETIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
+  PISA_ETIMEOUT = 5      /* never returned by a call: the code the Python binding raises when a
+                            status word carries PISA_STATUS_TIMEOUT */
 };
 
-/* Operations that need a workspace (pisa_workspace_size's `op`). */
-enum { PISA_OP_SELECT = 0, PISA_OP_SELECT_FLAT = 1, PISA_OP_ATTN_FWD = 2, PISA_OP_ATTN_BWD = 3 };
+/* Device status word. Every call that takes a workspace clears the first 4 bytes of it on its
+ * stream and ORs PISA_STATUS_* bits into them as its kernels run; read them (one int32) once
+ * the stream has passed the call. 0 means every step ran to completion. pisa_decode_step
+ * writes the same bits into its `status` argument.
+ *   PISA_STATUS_POS_RANGE: a decode position was outside [0, Ncap); that sequence was skipped.
+ *   PISA_STATUS_TIMEOUT:   a bounded wait inside a tensor-core kernel gave up (see
+ *                          pisa_set_wait_limit). The kernel then stops early, drains the work
+ *                          it had issued and frees its tensor memory; the call's outputs are
+ *                          poisoned: idx = -1 and score/head_lse = NaN for the selections,
+ *                          O = NaN and lse = NaN for the attention forward.
+ * The selection entry point without a workspace (pisa_select_noalloc) reports a timeout
+ * through the poisoned outputs only. */
+enum { PISA_STATUS_POS_RANGE = 1, PISA_STATUS_TIMEOUT = 2 };
+
+/* Operations that need a workspace (pisa_workspace_size's `op`): pisa_select,
+ * pisa_select_flat, pisa_sparse_attn_fwd, pisa_sparse_attn_bwd and pisa_select_mean. */
+enum {
+  PISA_OP_SELECT = 0,
+  PISA_OP_SELECT_FLAT = 1,
+  PISA_OP_ATTN_FWD = 2,
+  PISA_OP_ATTN_BWD = 3,
+  PISA_OP_SELECT_MEAN = 4
+};
 
 /* Prefill/training shape. C = leaf block size in tokens, K = blocks kept per level,
  * g = candidate fan-out per kept node (the merge factor, 2), qtile = scheduling hint for
@@ -76,13 +98,27 @@ int pisa_version(void);
 /* Text of the calling thread's last error ("" if none). Owned by the library. */
 const char* pisa_last_error(void);
 
+/* Upper bound, in nanoseconds of the GPU's global timer, on every single device-side wait of
+ * the tensor-core kernels (a pipeline stage waiting for another). 0 restores the default of
+ * one second. Process-wide; applies to launches enqueued after the call. A wait that reaches
+ * the bound gives up as described under PISA_STATUS_TIMEOUT. Host-only, no CUDA call. */
+int pisa_set_wait_limit(uint64_t limit_ns);
+
+/* Test aid (no counterpart on the pages): with on != 0, the tensor-core kernels of the
+ * following pisa_select and pisa_sparse_attn_fwd launches wait, after their first key tile is
+ * issued and before their first MMA, on a barrier that nothing signals, so that the wait
+ * runs out after the wait limit and the give-up path runs (status PISA_STATUS_TIMEOUT,
+ * poisoned outputs). Process-wide; 0 turns it off. Host-only, no CUDA call. */
+int pisa_test_stall(int on);
+
 /* Pyramid geometry for N tokens: n_levels = ceil(log2(ceil(N/C))) + 1, node offset of
  * every level inside one head's pyramid (level_offset[l], l < n_levels; may be NULL) and
  * the node count per (batch, KV head). Host-only, no CUDA call. */
 int pisa_pyramid_layout(const pisa_shape_t* shape, int32_t* n_levels, int64_t* level_offset,
                         int64_t* nodes_per_head);
 
-/* Bytes of workspace that `op` needs for `shape` (host-only, no CUDA call). */
+/* Bytes of workspace that `op` needs for `shape` (host-only, no CUDA call). The first 256
+ * bytes of every workspace are the status block (status word at offset 0). */
 int pisa_workspace_size(const pisa_shape_t* shape, int op, size_t* bytes);
 
 /* Key pyramid (digest page, "Method key points": leaf blocks of C tokens, mean pooling
@@ -122,14 +158,19 @@ int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const f
  * forbids allocations on the serving path, or a plugin whose host exposes no allocator.
  * Same arguments, results and errors as pisa_select minus head_lse and ws/ws_bytes; it allocates
  * nothing and calls no allocating routine. Its scratch is one fixed 32 MiB array inside
- * the library's device image, held on every GPU that loads the library until the process
- * exits. Shapes whose pisa_workspace_size(shape, PISA_OP_SELECT) exceeds 32 MiB are
- * rejected with PISA_EUNSUPPORTED before any CUDA call (about B*Hkv*N <= 80K units at
- * K = 16). The first call on a device looks up the array's device address (with that
- * device current) and should come before any stream capture. Every call shares the one
- * array and it keeps the last call's contents: the call clears on its stream whatever must
- * start at zero, and calls whose GPU work overlaps in time (different streams or host
- * threads on one device) race on the array. */
+ * the library's device image, held on a GPU from the moment that image is loaded there until
+ * the process exits. Under CUDA's default lazy module loading the image (the array and the
+ * selection kernels) is loaded by the first call on each device, so the driver reserves the
+ * 32 MiB inside that first call: callers that forbid device allocation while serving make one
+ * warm-up call per device at set-up, or run with CUDA_MODULE_LOADING=EAGER. That first call
+ * should also come before any stream capture on the device. Each call looks up the array's
+ * device address with the calling device current. Shapes whose selection workspace without
+ * head_lse exceeds 32 MiB are rejected with PISA_EUNSUPPORTED before any CUDA call (about
+ * B*Hkv*N <= 80K units at K = 16). Every call shares the one array and it keeps the last
+ * call's contents: the call clears on its stream whatever must start at zero, and calls whose
+ * GPU work overlaps in time (different streams or host threads on one device) race on the
+ * array. A bounded wait that gives up is reported through poisoned outputs (idx = -1,
+ * score = NaN), the array's status word being out of the caller's reach. */
 int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
                         const float* pyr_sum, int32_t* idx, float* score, void* stream);
 
@@ -146,7 +187,7 @@ int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
  * but every block, leaves included, scores sum_h s q_{i,h} . mu_i(l,m), its own causal mean
  * key; no exact leaf stage. score (nullable) receives these mean scores of the selected
  * leaves (-inf padding). Same arguments, layouts, tie rule and errors as pisa_select minus
- * head_lse. Workspace: PISA_OP_SELECT. */
+ * head_lse. Workspace: PISA_OP_SELECT_MEAN. */
 int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
                      const float* pyr_sum, int32_t* idx, float* score, void* ws,
                      size_t ws_bytes, void* stream);

@@ -332,6 +332,17 @@ def select(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, g
 # Comparators: flat block selection (digest page, "Motivation": conventional block
 # selection scores every query-block pair, O(N^2/C)) and exhaustive exact scoring
 # --------------------------------------------------------------------------------------
+def select_unit_flat(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int,
+                     scale: float) -> tuple[np.ndarray, np.ndarray, float]:
+    """Flat BSA for one query i of one (batch, KV head): every visible leaf t scores
+    sum_h s q_h . mu_i(0,t); returns the K best ascending, their scores and the margin."""
+    vis = np.arange(i // summ.C + 1)
+    sc = (scale * (q @ summ.means(0, vis, i).T)).sum(axis=0)
+    kept, mg = _top_k(vis, sc, K)
+    kept = np.sort(kept)
+    return kept, sc[kept], mg
+
+
 def select_flat(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
     """Flat BSA: score every visible leaf by sum_h s q_h . mu_i(0,t), keep the top K."""
     Q, K = _as64(Q), _as64(K)
@@ -347,14 +358,10 @@ def select_flat(Q, K, C: int, K_sel: int, scale: float | None = None, queries=No
         for kv in range(Hkv):
             summ = CausalKeySummaries(K[b, :, kv, :], C)
             for i in qs:
-                vis = np.arange(i // C + 1)
-                mu = summ.means(0, vis, i)
-                sc = (s * (Q[b, i, kv * G:(kv + 1) * G, :] @ mu.T)).sum(axis=0)
-                kept, mg = _top_k(vis, sc, K_sel)
-                kept = np.sort(kept)
+                kept, sc, mg = select_unit_flat(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s)
                 idx[b, kv, i, :len(kept)] = kept
                 score[b, kv, i, :] = NEG_INF
-                score[b, kv, i, :len(kept)] = sc[kept]
+                score[b, kv, i, :len(kept)] = sc
                 margin[b, kv, i] = mg
     return dict(idx=idx, score=score, margin=margin)
 

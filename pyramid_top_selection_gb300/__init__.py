@@ -8,4 +8,5 @@ from ._pisa import (  # noqa: F401
     decode_step, default_scale, lib, make_decode_shape, make_shape, profile_read, profile_start,
     profile_stop, pyramid_layout, select, select_mean, workspace,
     select_flat, shape_of, sparse_attn_bwd, sparse_attn_fwd, workspace_size,
+    STATUS_POS_RANGE, STATUS_TIMEOUT, check_status, set_test_stall, set_wait_limit, workspace_status,
 )

@@ -17,16 +17,17 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpisa.so")
 
 PISA_OK, PISA_EINVAL, PISA_EUNSUPPORTED, PISA_EWORKSPACE, PISA_ECUDA, PISA_ETIMEOUT = range(6)
-OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD = range(4)
+OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD, OP_SELECT_MEAN = range(5)
+STATUS_POS_RANGE, STATUS_TIMEOUT = 1, 2
 MAX_LEVELS = 32
-ABI_VERSION = 3          # PISA_VERSION of the header these argument lists follow
+ABI_VERSION = 4          # PISA_VERSION of the header these argument lists follow
 
 EXPORTS = (
     "pisa_version", "pisa_last_error", "pisa_pyramid_layout", "pisa_workspace_size",
     "pisa_build_pyramid", "pisa_select", "pisa_select_flat", "pisa_sparse_attn_fwd",
     "pisa_sparse_attn_bwd", "pisa_decode_pyramid_layout", "pisa_decode_build_pyramid",
     "pisa_decode_step", "pisa_profile_start", "pisa_profile_stop", "pisa_profile_read",
-    "pisa_select_noalloc", "pisa_select_mean",
+    "pisa_select_noalloc", "pisa_select_mean", "pisa_set_wait_limit", "pisa_test_stall",
 )
 
 
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.pisa_profile_start.argtypes = []
         L.pisa_profile_stop.argtypes = []
         L.pisa_profile_read.argtypes = [P(ProfileEntry), i32, P(i32)]
+        L.pisa_set_wait_limit.argtypes = [ctypes.c_uint64]
+        L.pisa_test_stall.argtypes = [ctypes.c_int]
         for f in EXPORTS:
             if f not in ("pisa_version", "pisa_last_error"):
                 getattr(L, f).restype = ctypes.c_int
@@ -204,7 +207,7 @@ def select_mean(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, sc
     dev = Q.device
     idx, score = _select_out(Q, shape, want_score, idx, score)
     if ws is None:
-        ws = _workspace(shape, OP_SELECT, dev)
+        ws = _workspace(shape, OP_SELECT_MEAN, dev)
     _check(lib().pisa_select_mean(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
                                   _ptr(ws), ws.numel(), _stream(dev)))
     return idx, score
@@ -279,6 +282,30 @@ def decode_step(shape: DecodeShape, pos, Kcache, Vcache, pyr, q, k_new, v_new, o
                                   _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(o), _ptr(idx), _ptr(score),
                                   _ptr(status), _stream(dev)))
     return o, idx, score, status
+
+
+def workspace_status(ws: torch.Tensor) -> int:
+    """The status word of the last call that used workspace `ws` (its first 4 bytes, read after
+    the current stream has passed the call): 0, or STATUS_* bits."""
+    torch.cuda.current_stream(ws.device).synchronize()
+    return int(ws[:4].view(torch.int32).item())
+
+
+def check_status(ws: torch.Tensor) -> None:
+    """Raise PisaError(PISA_ETIMEOUT) when the last call on `ws` reported a wait that gave up."""
+    st = workspace_status(ws)
+    if st & STATUS_TIMEOUT:
+        raise PisaError(PISA_ETIMEOUT, f"a bounded device wait gave up (status word {st}); outputs are poisoned")
+
+
+def set_wait_limit(ns: int) -> None:
+    """Bound of every device-side pipeline wait in nanoseconds (0 restores the one-second default)."""
+    _check(lib().pisa_set_wait_limit(int(ns)))
+
+
+def set_test_stall(on: bool) -> None:
+    """Test aid: make the tensor-core kernels wait on a barrier nothing signals (see pisa.h)."""
+    _check(lib().pisa_test_stall(1 if on else 0))
 
 
 def default_scale(d: int) -> float:

@@ -1,5 +1,6 @@
 // C ABI of the PISA GB300 library: argument checks on the host (before any CUDA call),
 // workspace sizing, and dispatch to the kernel launchers.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -10,6 +11,10 @@
 namespace {
 
 thread_local char g_err[512] = "";
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // one second
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall{0};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -97,6 +102,7 @@ int layout_out(const pisa::Geo& g, int32_t* n_levels, int64_t* level_offset, int
 size_t ws_bytes_for(const pisa::Dims& d, const pisa::Geo& g, int op) {
   switch (op) {
     case PISA_OP_SELECT: return pisa::select_ws(d, g).total_head;
+    case PISA_OP_SELECT_MEAN: return pisa::select_ws(d, g).mean_end;
     case PISA_OP_SELECT_FLAT: return pisa::flat_ws(d, g);
     case PISA_OP_ATTN_FWD: return pisa::attn_fwd_ws(d).total;
     case PISA_OP_ATTN_BWD: return pisa::attn_bwd_ws(d).total;
@@ -104,21 +110,39 @@ size_t ws_bytes_for(const pisa::Dims& d, const pisa::Geo& g, int op) {
   }
 }
 
-int check_ws(const pisa::Dims& d, const pisa::Geo& g, int op, const void* ws, size_t ws_bytes) {
-  const size_t need = ws_bytes_for(d, g, op);
+int check_ws_bytes(size_t need, const void* ws, size_t ws_bytes) {
   if (ws_bytes < need) return fail(PISA_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
   if (need > 0 && !ws) return fail(PISA_EWORKSPACE, "workspace is NULL");
   if (ws && !aligned16(ws)) return fail(PISA_EINVAL, "workspace is not 16-byte aligned");
   return PISA_OK;
 }
 
+int check_ws(const pisa::Dims& d, const pisa::Geo& g, int op, const void* ws, size_t ws_bytes) {
+  return check_ws_bytes(ws_bytes_for(d, g, op), ws, ws_bytes);
+}
+
 }  // namespace
+
+namespace pisa {
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int test_stall() { return g_stall.load(std::memory_order_relaxed); }
+}  // namespace pisa
 
 extern "C" {
 
 int pisa_version(void) { return PISA_VERSION; }
 
 const char* pisa_last_error(void) { return g_err; }
+
+int pisa_set_wait_limit(uint64_t limit_ns) {
+  g_wait_ns.store(limit_ns == 0 ? kDefaultWaitNs : limit_ns, std::memory_order_relaxed);
+  return PISA_OK;
+}
+
+int pisa_test_stall(int on) {
+  g_stall.store(on ? 1 : 0, std::memory_order_relaxed);
+  return PISA_OK;
+}
 
 int pisa_pyramid_layout(const pisa_shape_t* shape, int32_t* n_levels, int64_t* level_offset,
                         int64_t* nodes_per_head) {
@@ -129,7 +153,7 @@ int pisa_pyramid_layout(const pisa_shape_t* shape, int32_t* n_levels, int64_t* l
 int pisa_workspace_size(const pisa_shape_t* shape, int op, size_t* bytes) {
   PISA_CHECK(check_shape(shape));
   if (!bytes) return fail(PISA_EINVAL, "bytes is NULL");
-  if (op < PISA_OP_SELECT || op > PISA_OP_ATTN_BWD) return fail(PISA_EINVAL, "unknown op %d", op);
+  if (op < PISA_OP_SELECT || op > PISA_OP_SELECT_MEAN) return fail(PISA_EINVAL, "unknown op %d", op);
   *bytes = ws_bytes_for(dims_of(shape), pisa::make_geo(shape->N, shape->C), op);
   return PISA_OK;
 }
@@ -207,7 +231,7 @@ int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
   PISA_CHECK(check_ptr(score, "score", true));
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
-  PISA_CHECK(check_ws(d, g, PISA_OP_SELECT, ws, ws_bytes));
+  PISA_CHECK(check_ws(d, g, PISA_OP_SELECT_MEAN, ws, ws_bytes));
   return cuda_rc(pisa::launch_select_mean(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
                  "pisa_select_mean");
 }

@@ -40,10 +40,10 @@ AttnFwdWs attn_fwd_ws(const Dims& s) {
   AttnFwdWs w{};
   const GroupPlan gp = fwd_plan(s);
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
-  size_t o = group_ws(gp, 0).end;
+  w.status = 0;                         // first: the caller finds the status word at offset 0
+  size_t o = group_ws(gp, 256).end;
   w.block_lse = o; o += align256(rows * s.K * 4);
   w.o_acc = o;     o += align256(rows * s.d * 4);
-  w.status = o;    o += 256;
   w.total = o;
   return w;
 }
@@ -53,7 +53,7 @@ int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnFwdWs w = attn_fwd_ws(s);
   const GroupPlan gp = fwd_plan(s);
-  const GroupWs g = group_ws(gp, 0);
+  const GroupWs g = group_ws(gp, 256);
   int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;
   cudaError_t e = cudaMemsetAsync(ws + w.status, 0, 256, st);

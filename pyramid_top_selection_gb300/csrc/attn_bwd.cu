@@ -381,7 +381,8 @@ AttnBwdWs attn_bwd_ws(const Dims& s) {
   AttnBwdWs w{};
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
   const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
-  size_t o = group_ws(bwd_plan(s), 0).end;
+  w.status = 0;                         // first: the caller finds the status word at offset 0
+  size_t o = group_ws(bwd_plan(s), 256).end;
   w.delta = o;   o += align256(rows * 4);
   w.dq_acc = o;  o += align256(rows * s.d * 4);
   w.dk_acc = o;  o += align256(kvel * 4);
@@ -396,7 +397,7 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnBwdWs w = attn_bwd_ws(s);
   const GroupPlan gp = bwd_plan(s);
-  const GroupWs g = group_ws(gp, 0);
+  const GroupWs g = group_ws(gp, 256);
   float* delta = reinterpret_cast<float*>(ws + w.delta);
   float* dqa = reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
@@ -404,7 +405,8 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
   int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;
-  cudaError_t e = cudaMemsetAsync(dk_acc, 0, kvel * 4, st);
+  cudaError_t e = cudaMemsetAsync(ws + w.status, 0, 256, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dk_acc, 0, kvel * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(dv_acc, 0, kvel * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(dqa, 0, static_cast<size_t>(s.B) * s.N * s.Hq * s.d * 4, st);
   if (e != cudaSuccess) return e;

@@ -70,11 +70,25 @@ attn_rows_kernel(Dims s, const int32_t* __restrict__ idx, const float* __restric
   lse_out[r0 + lane] = den > 0.f ? m + logf(den) : neg_inf();
 }
 
-// O = bf16(accumulator), 8 elements per thread.
+// O = bf16(accumulator), 8 elements per thread. When the status word carries
+// PISA_STATUS_TIMEOUT (a bounded wait of a tensor-core pass gave up, so some block
+// contributions are missing) O and lse are poisoned instead: every element NaN.
 __global__ void __launch_bounds__(256)
-attn_out_kernel(int64_t n8, const float4* __restrict__ o_acc, uint4* __restrict__ O) {
+attn_out_kernel(Dims s, int64_t n8, const float4* __restrict__ o_acc, uint4* __restrict__ O,
+                float* __restrict__ lse, const int32_t* __restrict__ status) {
+  const bool poison = (*status & PISA_STATUS_TIMEOUT) != 0;
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (poison) {
+      O[q] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+      const int64_t e = q * 8;
+      if (e % s.d == 0) {                      // the row's first chunk: row = (b*N + i)*Hq + h
+        const int64_t row = e / s.d;
+        const int64_t h = row % s.Hq, bi = row / s.Hq;
+        lse[((bi / s.N) * s.Hq + h) * s.N + bi % s.N] = __int_as_float(0x7fc00000);
+      }
+      continue;
+    }
     const float4 a = o_acc[2 * q], c = o_acc[2 * q + 1];
     O[q] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
   }
@@ -112,7 +126,7 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
     const int64_t n8 = rows * s.d / 8;
     const int64_t nb = (n8 + 255) / 256;
     attn_out_kernel<<<static_cast<unsigned>(nb < 152 * 32 ? nb : 152 * 32), 256, 0, st>>>(
-        n8, reinterpret_cast<const float4*>(o_acc), static_cast<uint4*>(O));
+        s, n8, reinterpret_cast<const float4*>(o_acc), static_cast<uint4*>(O), lse, status);
   }
   return cudaGetLastError();
 }

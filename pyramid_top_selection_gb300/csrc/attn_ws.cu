@@ -26,8 +26,11 @@
 //     staging tiles; the lane holding a query's first head adds the query's G heads x 32
 //     columns into the accumulator with one TMA tensor reduce-add;
 //   * scheduler (warp 17, one thread): fills the item queue.
-// Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
-// its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
+// Every wait is bounded (the launch's wait limit); a wait that gives up sets the CTA's abort
+// flag and every role leaves its loop at its next tile. Before the CTA frees its tensor memory
+// the control thread drains what it issued (key tiles in flight, MMAs), the producers and the
+// epilogue their copies and reductions; the kernel then ORs PISA_STATUS_TIMEOUT into the
+// status word, and the output conversion reads it and writes poisoned outputs.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -44,6 +47,7 @@ constexpr int kNQ = 2, kNP = 2, kNKV = 2;   // Q, P, K/V stages; S and O have 2 
 constexpr int kThreads = 576;               // softmax 0-255, epilogue 256-383, producers 384-511, control, scheduler
 constexpr int kConsumerWarps = 17;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
 
 template <int D>
 struct AttnSmem {
@@ -68,6 +72,8 @@ struct AttnArgs {
   const float* lse_rows;   // [B, Hq, N]
   int32_t* status;
   int32_t* next_item;      // zeroed item counter
+  uint64_t wait_ns;        // bound of every pipeline wait
+  int stall;               // test aid: wait on a barrier nothing signals before the first MMA
 };
 
 template <int D, int G>
@@ -78,7 +84,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   constexpr int CH = D / 8;               // 16-byte chunks per Q / V row
   extern __shared__ unsigned char smraw[];
   __shared__ __align__(8) uint64_t q_full[kNQ], q_empty[kNQ], s_full[2], s_empty[2], p_full[kNP], p_empty[kNP],
-      o_full[2], o_empty[2], k_full[kNKV], k_empty[kNKV], v_full[kNKV], v_empty[kNKV];
+      o_full[2], o_empty[2], k_full[kNKV], k_empty[kNKV], v_full[kNKV], v_empty[kNKV], drain, never;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   __shared__ ItemQueue s_q;
@@ -105,7 +111,9 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::bar_init(&v_full[k], kRows);
       tc::bar_init(&v_empty[k], 1);
     }
-    queue_init(s_q, kConsumerWarps);
+    tc::bar_init(&drain, 1);
+    tc::bar_init(&never, 1);
+    queue_init(s_q, kConsumerWarps, a.wait_ns);
     tc::fence_bar_init();
     s_abort = 0;
   }
@@ -114,6 +122,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   __syncthreads();
   tc::after_sync();
   auto give_up = [&]() { atomicOr(&s_abort, 1); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return tc::bar_wait(bar, parity, a.wait_ns); };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
 
   if (warp >= 12 && warp < 16) {
@@ -155,7 +164,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         }
         // V^T of the item (lanes walk keys: no bank conflicts); keys past N are zero
         const int vs = I % kNKV;
-        if (!tc::bar_wait(&v_empty[vs], ((I / kNKV) & 1) ^ 1)) { give_up(); break; }
+        if (!wait(&v_empty[vs], ((I / kNKV) & 1) ^ 1)) { give_up(); break; }
         unsigned char* vt = sm + L::oV + vs * L::V_BYTES;
 #pragma unroll
         for (int u = 0; u < VU; ++u) {
@@ -175,7 +184,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true, lead);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
       const int st = T % kNQ;
-      if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
+      if (!wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
       const uint32_t dst = aQ + st * L::Q_BYTES;
       const int c = lane % CH;
 #pragma unroll 4
@@ -201,14 +210,18 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     // ---------------------------------------------------------------- control
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
+      int k_issued = 0;            // key tiles issued: items 0 .. k_issued - 1
+      int k_landed = 0;            // key tiles whose arrival was waited for
+      bool mma_issued = false;
       // K of the CTA's item number I into stage I % 2
       auto load_k = [&](int I, const ItemView& v) {
         const int ks = I % kNKV;
-        if (!tc::bar_wait(&k_empty[ks], ((I / kNKV) & 1) ^ 1)) { give_up(); return; }
+        if (!wait(&k_empty[ks], ((I / kNKV) & 1) ^ 1)) { give_up(); return; }
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+        k_issued = I + 1;
       };
       // S of tile T (cursor c, item number I)
       auto issue_s = [&](const DynCursor& c, int T, int I) -> bool {
@@ -216,11 +229,13 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         if (c.j == 0) {
           const ItemView v_n = queue_peek(s_q, c.k + 1, &s_abort);
           if (v_n.n_ent >= 0) load_k(I + 1, v_n);
-          if (!tc::bar_wait(&k_full[ks], (I / kNKV) & 1)) return false;
+          if (!wait(&k_full[ks], (I / kNKV) & 1)) return false;
+          k_landed = I + 1;
         }
-        if (!tc::bar_wait(&q_full[st], (T / kNQ) & 1) || !tc::bar_wait(&s_empty[ss], ((T >> 1) & 1) ^ 1))
+        if (!wait(&q_full[st], (T / kNQ) & 1) || !wait(&s_empty[ss], ((T >> 1) & 1) ^ 1))
           return false;
         tc::after_sync();
+        mma_issued = true;
 #pragma unroll
         for (int k2 = 0; k2 < D / 16; ++k2)
           tc::mma(tmem_base + 64 * ss, tc::desc(aQ + st * L::Q_BYTES + (k2 >> 2) * (kRows * 128) + (k2 & 3) * 32),
@@ -233,8 +248,8 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       // P V of tile T
       auto issue_pv = [&](const DynCursor& c, int T, int I) -> bool {
         const int vs = I % kNKV, ps = T % kNP, os = T & 1;
-        if (c.j == 0 && !tc::bar_wait(&v_full[vs], (I / kNKV) & 1)) return false;
-        if (!tc::bar_wait(&p_full[ps], (T / kNP) & 1) || !tc::bar_wait(&o_empty[os], ((T >> 1) & 1) ^ 1))
+        if (c.j == 0 && !wait(&v_full[vs], (I / kNKV) & 1)) return false;
+        if (!wait(&p_full[ps], (T / kNP) & 1) || !wait(&o_empty[os], ((T >> 1) & 1) ^ 1))
           return false;
         tc::after_sync();
 #pragma unroll
@@ -253,7 +268,8 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       int Ts = 0, Is = 0, Tp = 0, Ip = 0;
       if (have_s) {
         load_k(0, cs.v);
-        if (!issue_s(cs, 0, 0)) give_up();
+        if (a.stall && !wait(&never, 0)) give_up();   // runs out after the wait limit
+        if (!aborted() && !issue_s(cs, 0, 0)) give_up();
         Ts = 1;
         have_s = dyn_next(s_q, EPT, &s_abort, cs, false, false, 1u);
         if (have_s && cs.j == 0) Is = 1;
@@ -269,6 +285,14 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         ++Tp;
         have_p = dyn_next(s_q, EPT, &s_abort, cp, true, false, 1u);
         if (have_p && cp.j == 0) ++Ip;
+      }
+      // Drain before the CTA frees its tensor memory and leaves: key tiles still in flight land
+      // (each stage holds at most one: a stage is reloaded only after its item's last S), and
+      // every MMA issued completes (one commit tracks them all).
+      for (int J = k_landed; J < k_issued; ++J) tc::bar_wait(&k_full[J % kNKV], (J / kNKV) & 1, kDrainNs);
+      if (mma_issued) {
+        tc::commit(&drain);
+        tc::bar_wait(&drain, 0, kDrainNs);
       }
     }
   }
@@ -297,7 +321,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
-      const bool ok = tc::bar_wait(&s_full[sg], (T >> 1) & 1);
+      const bool ok = wait(&s_full[sg], (T >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
       tc::after_sync();
       const float l2_n = have_n ? row_lse2(nxt, pk_n) : 0.f;   // in flight during the math
@@ -317,7 +341,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = c <= lh ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
         if (half == 0) {
-          const bool ok2 = tc::bar_wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
+          const bool ok2 = wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, ok2)) {
             give_up();
             break;
@@ -359,7 +383,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;
       const int os = T & 1;
-      const bool ok = tc::bar_wait(&o_full[os], (T >> 1) & 1);
+      const bool ok = wait(&o_full[os], (T >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
       tc::after_sync();
       const bool issuer = h == 0 && pk >= 0;
@@ -397,7 +421,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   }
   tc::before_sync();
   __syncthreads();
-  if (tid == 0 && s_abort) atomicOr(a.status, PISA_ETIMEOUT);
+  if (tid == 0 && s_abort) atomicOr(a.status, PISA_STATUS_TIMEOUT);
   if (warp == 0) {
     tc::after_sync();
     tc::tmem_free(tmem_base, 512);
@@ -448,6 +472,8 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   a.lse_rows = lse_rows;
   a.status = status;
   a.next_item = status + 32;
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
 #define PISA_ATTN_CASE(DD, GG) \

@@ -63,7 +63,7 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   const int G = s.G, Ksel = s.K, C = s.C, Ncap = s.N;
   const int p = pos[b];
   if (p < 0 || p >= Ncap) {
-    if (tid == 0) atomicOr(status, 1);
+    if (tid == 0) atomicOr(status, PISA_STATUS_POS_RANGE);
     return;
   }
   const DecodeSmem L = decode_smem(G, D, Ksel);

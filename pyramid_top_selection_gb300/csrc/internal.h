@@ -42,17 +42,19 @@ struct Dims {
 };
 
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.
-// total: without the per-head leaf terms; total_head: with them (head_lse requested).
-// status: 256 bytes zeroed before the op's kernels; word 0 collects error bits, words 16
-// and 32 are the item counters of the persistent leaf-scoring and attention kernels.
+// total: without the per-head leaf terms; total_head: with them (head_lse requested);
+// mean_end: what the PISA-1 path uses.
+// status: the first 256 bytes of every workspace, zeroed before the op's kernels; word 0
+// collects PISA_STATUS_* bits (the caller reads it there), words 16 and 32 are the item
+// counters of the persistent leaf-scoring and attention kernels.
 struct SelectWs {
-  size_t split, cand, cscore, status, group, total, chead, total_head;
+  size_t status, split, cand, cscore, mean_end, group, total, chead, total_head;
 };
 struct AttnFwdWs {
   size_t block_lse, o_acc, status, total;
 };
 struct AttnBwdWs {
-  size_t delta, dq_acc, dk_acc, dv_acc, total;
+  size_t status, delta, dq_acc, dk_acc, dv_acc, total;
 };
 int sm_count();
 SelectWs select_ws(const Dims& s, const Geo& g);
@@ -79,6 +81,10 @@ int launch_decode_step(const Dims& s, int32_t Ncap, const Geo& g, const int32_t*
                        const void* v_new, void* o, int32_t* idx, float* score, int32_t* status,
                        void* stream);
 const char* cuda_error_string(int err);
+// Bound of every device-side pipeline wait (pisa_set_wait_limit), and the test stall switch
+// (pisa_test_stall), as the launchers pass them to the tensor-core kernels.
+uint64_t wait_limit_ns();
+int test_stall();
 size_t noalloc_scratch_bytes();
 int noalloc_scratch(void** out);
 

@@ -22,8 +22,11 @@
 //     the visible keys; the G rows of a query (adjacent lanes) sum their LSEs into the
 //     candidate's score;
 //   * scheduler (warp 13, one thread): fills the item queue.
-// Every wait is bounded; a wait that gives up sets the CTA's abort flag, every role leaves
-// its loop at its next tile, and the kernel records PISA_ETIMEOUT in the status word.
+// Every wait is bounded (the launch's wait limit); a wait that gives up sets the CTA's abort
+// flag and every role leaves its loop at its next tile. Before the CTA frees its tensor memory
+// the control thread drains what it issued (key tiles in flight, MMAs), the producers their
+// copies; the kernel then ORs PISA_STATUS_TIMEOUT into the status word, and the top-K finish
+// reads it and writes poisoned outputs.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -43,6 +46,7 @@ constexpr int kThreads = 448;     // softmax 0-255 (two warpgroups), producers 2
 constexpr int kConsumerWarps = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
 
 template <int D>
 struct LeafSmem {
@@ -64,6 +68,8 @@ struct LeafArgs {
   float* block_lse;    // when set: per-row LSE [B, Hq, N, W] instead of the scores
   int32_t* status;
   int32_t* next_item;  // zeroed item counter
+  uint64_t wait_ns;    // bound of every pipeline wait
+  int stall;           // test aid: wait on a barrier nothing signals before the first MMA
 };
 
 template <int D, int G>
@@ -74,7 +80,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
   constexpr int CH = D / 8;               // 16-byte chunks per row
   extern __shared__ unsigned char smraw[];
   __shared__ __align__(8) uint64_t q_full[kNQ], q_empty[kNQ], s_full[kNS], s_empty[kNS], k_full[kNK],
-      k_empty[kNK];
+      k_empty[kNK], drain, never;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   __shared__ ItemQueue s_q;
@@ -98,7 +104,9 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       tc::bar_init(&k_full[k], 1);
       tc::bar_init(&k_empty[k], 1);
     }
-    queue_init(s_q, kConsumerWarps);
+    tc::bar_init(&drain, 1);
+    tc::bar_init(&never, 1);
+    queue_init(s_q, kConsumerWarps, a.wait_ns);
     tc::fence_bar_init();
     s_abort = 0;
   }
@@ -107,6 +115,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
   __syncthreads();
   tc::after_sync();
   auto give_up = [&]() { atomicOr(&s_abort, 1); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return tc::bar_wait(bar, parity, a.wait_ns); };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
 
   if (warp >= 8 && warp < 12) {
@@ -126,7 +135,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true, lead);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
       const int st = T % kNQ;
-      if (!tc::bar_wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
+      if (!wait(&q_empty[st], ((T / kNQ) & 1) ^ 1)) { give_up(); break; }
       const uint32_t dst = aQ + st * L::Q_BYTES;
       const int c = lane % CH;
 #pragma unroll
@@ -158,30 +167,37 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     // ---------------------------------------------------------------- control
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
+      int k_issued = 0;            // key tiles issued: items 0 .. k_issued - 1
+      int k_landed = 0;            // key tiles whose arrival was waited for
+      bool mma_issued = false;
       auto load_k = [&](int I, const ItemView& v) {
         const int ks = I % kNK;
-        if (!tc::bar_wait(&k_empty[ks], ((I / kNK) & 1) ^ 1)) { give_up(); return; }
+        if (!wait(&k_empty[ks], ((I / kNK) & 1) ^ 1)) { give_up(); return; }
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
           tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+        k_issued = I + 1;
       };
       int T = 0, I = 0;
       ItemView v = queue_take(s_q, 0, &s_abort);
       if (v.n_ent >= 0) load_k(0, v);
+      if (a.stall && !wait(&never, 0)) give_up();   // runs out after the wait limit
       for (; v.n_ent >= 0 && !aborted(); ++I) {
         const ItemView v_n = queue_take(s_q, I + 1, &s_abort);
         if (v_n.n_ent >= 0) load_k(I + 1, v_n);
         const int ks = I % kNK;
-        if (!tc::bar_wait(&k_full[ks], (I / kNK) & 1)) { give_up(); break; }
+        if (!wait(&k_full[ks], (I / kNK) & 1)) { give_up(); break; }
+        k_landed = I + 1;
         const int n_tiles = (v.n_ent + EPT - 1) / EPT;
         for (int j = 0; j < n_tiles; ++j, ++T) {
           const int st = T % kNQ, ss = T % kNS;
-          if (!tc::bar_wait(&q_full[st], (T / kNQ) & 1) || !tc::bar_wait(&s_empty[ss], ((T / kNS) & 1) ^ 1)) {
+          if (!wait(&q_full[st], (T / kNQ) & 1) || !wait(&s_empty[ss], ((T / kNS) & 1) ^ 1)) {
             give_up();
             break;
           }
           tc::after_sync();
+          mma_issued = true;
 #pragma unroll
           for (int ks2 = 0; ks2 < D / 16; ++ks2)
             tc::mma(tmem_base + 64 * ss,
@@ -192,6 +208,14 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
         }
         tc::commit(&k_empty[ks]);
         v = v_n;
+      }
+      // Drain before the CTA frees its tensor memory and leaves: key tiles still in flight land
+      // (each stage holds at most one: a stage is reloaded only after its item's MMAs), and every
+      // MMA issued completes (one commit tracks them all). Both end in bounded time once issued.
+      for (int J = k_landed; J < k_issued; ++J) tc::bar_wait(&k_full[J % kNK], (J / kNK) & 1, kDrainNs);
+      if (mma_issued) {
+        tc::commit(&drain);
+        tc::bar_wait(&drain, 0, kDrainNs);
       }
     }
   } else if (warp < 8) {
@@ -217,7 +241,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;   // in flight during this tile
       const int ss = T % kNS;
-      const bool ok = tc::bar_wait(&s_full[ss], (T / kNS) & 1);
+      const bool ok = wait(&s_full[ss], (T / kNS) & 1);
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }   // warp-uniform exit
       tc::after_sync();
       float sv[64];
@@ -272,7 +296,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
   }
   tc::before_sync();
   __syncthreads();
-  if (tid == 0 && s_abort) atomicOr(a.status, PISA_ETIMEOUT);
+  if (tid == 0 && s_abort) atomicOr(a.status, PISA_STATUS_TIMEOUT);
   if (warp == 0) {
     tc::after_sync();
     tc::tmem_free(tmem_base, kNS * 64);
@@ -331,6 +355,8 @@ int leaf_tc_run(const Dims& s, const GroupPlan& gp, const void* Q, const void* K
   a.block_lse = block_lse;
   a.status = status;
   a.next_item = status + 16;
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
 #define PISA_LEAF_CASE(DD, GG) \

@@ -406,13 +406,27 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
 // One warp per (b, KV head, query): top K of the <= W (<= 64) candidate scores, output
 // ascending. Lane l holds candidates l and l + 32 in registers; ranks and output positions
 // come from warp shuffles.
+// When the status word carries PISA_STATUS_TIMEOUT (a bounded wait of the leaf stage gave up,
+// so candidate scores may be missing or stale) every output slot is poisoned instead:
+// idx = -1, score = head_lse = NaN.
 __global__ void __launch_bounds__(kWarps * 32)
 topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restrict__ cand,
             const float* __restrict__ csc, const float* __restrict__ chead, int32_t* __restrict__ idx,
-            float* __restrict__ score, float* __restrict__ head_lse) {
+            float* __restrict__ score, float* __restrict__ head_lse, const int32_t* __restrict__ status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = blockIdx.x * static_cast<int64_t>(kWarps) + warp;
   if (u >= units) return;
+  const int64_t hrow = (u / N) * G * N + u % N;
+  if (*status & PISA_STATUS_TIMEOUT) {
+    const float nan = __int_as_float(0x7fc00000);
+    for (int q = lane; q < Ksel; q += 32) {
+      idx[u * Ksel + q] = -1;
+      if (score) score[u * Ksel + q] = nan;
+      if (head_lse)
+        for (int h = 0; h < G; ++h) head_lse[(hrow + static_cast<int64_t>(h) * N) * Ksel + q] = nan;
+    }
+    return;
+  }
   const int J = W > 32 ? 2 : 1;
   int ci[2] = {-1, -1};
   float cs[2] = {neg_inf(), neg_inf()};
@@ -445,7 +459,7 @@ topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restr
     }
   const int nk = __popc(__ballot_sync(0xffffffffu, keep[0])) + __popc(__ballot_sync(0xffffffffu, keep[1]));
   // unit u = (b*Hkv + kv)*N + i -> head_lse rows (b*Hq + kv*G + h)*N + i
-  const int64_t hrow0 = (u / N) * G * N + u % N;
+  const int64_t hrow0 = hrow;
   for (int j = 0; j < J; ++j) {
     if (!keep[j]) continue;
     idx[u * Ksel + pos[j]] = ci[j];
@@ -687,10 +701,11 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   const size_t W = 2 * static_cast<size_t>(s.K);
   size_t o = 0;
+  w.status = o; o += 256;          // first: the caller finds the status word at offset 0
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
-  w.status = o; o += 256;
+  w.mean_end = o;                  // the PISA-1 path needs nothing past here
   w.group = o;
   o = group_ws(leaf_plan(s), o).end;
   w.total = o;           // without the per-head terms
@@ -700,7 +715,7 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
 }
 
 size_t flat_ws(const Dims& s, const Geo& g) {
-  return align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
+  return 256 + align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);   // status word, split rows
 }
 
 int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
@@ -749,7 +764,8 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   {
     ProfScope ps(st, "topk");
     topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse);
+        units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse,
+        reinterpret_cast<const int32_t*>(ws + w.status));
   }
   return cudaGetLastError();
 }
@@ -765,6 +781,7 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
+  if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
     ProfScope ps(st, "route_mean");
@@ -783,7 +800,8 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   {
     ProfScope ps(st, "topk");
     topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, 2 * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr);
+        units, 2 * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr,
+        reinterpret_cast<const int32_t*>(ws + w.status));
   }
   return cudaGetLastError();
 }
@@ -791,9 +809,10 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
 int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
                        const float* pyr, int32_t* idx, float* score, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint4* spl = reinterpret_cast<uint4*>(ws);
-  int err = launch_split(s, g, pyr, spl, st);
+  uint4* spl = reinterpret_cast<uint4*>(ws + 256);
+  int err = cudaMemsetAsync(ws, 0, 256, st);      // status word (no bounded waits here: stays 0)
   if (err) return err;
+  if ((err = launch_split(s, g, pyr, spl, st))) return err;
   dim3 grid(s.n0, s.Hkv, s.B);
   const size_t smem = static_cast<size_t>(kWarps) * 2 * s.K * 32 * 8;
   ProfScope ps(st, "flat_select");

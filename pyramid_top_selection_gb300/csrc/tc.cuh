@@ -62,11 +62,19 @@ __device__ __forceinline__ void fence_bar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Wait until the phase with the given parity has completed; gives up after about a second
-// (returns false) so a broken pipeline cannot hang the GPU.
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+// Wait until the phase with the given parity has completed; gives up (returns false) once
+// limit_ns nanoseconds of the global timer have passed, so a broken pipeline cannot hang the
+// GPU. The limit comes from the launch (one second unless the host set another).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = su32(bar);
-  for (int it = 0; it < (1 << 23); ++it) {
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -75,9 +83,13 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
         : "r"(a), "r"(parity)
         : "memory");
     if (ok) return true;
-    if (it > 64) __nanosleep(100);
+    if (it == 0) {
+      t0 = global_ns();
+    } else if (it > 64) {
+      __nanosleep(100);
+      if ((it & 15) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
   }
-  return false;
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

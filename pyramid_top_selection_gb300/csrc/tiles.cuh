@@ -53,7 +53,8 @@ __device__ __forceinline__ ItemView view_of(const ItemSource& src, const int4 it
 // items that another CTA could have run, and the next record is fetched as soon as one is
 // published, so its latency passes while the consumers work. The scheduler sleeps in
 // mbarrier.try_wait (no polling: a spinning warp takes issue slots from its SM partition).
-// Every wait is bounded (one second) and a wait that gives up sets the CTA's abort flag.
+// Every wait is bounded (the launch's wait limit, one second unless the host set another) and a
+// wait that gives up sets the CTA's abort flag.
 // ---------------------------------------------------------------------------------------
 namespace pisa {
 
@@ -63,6 +64,7 @@ constexpr int kItemAhead = 3;
 struct ItemQueue {
   ItemView view[kItemRing];
   uint64_t full[kItemRing], empty[kItemRing], demand[kItemRing];
+  uint64_t limit_ns;   // bound of every wait on the queue
 };
 
 __device__ __forceinline__ uint32_t queue_addr(const void* p) {
@@ -71,7 +73,8 @@ __device__ __forceinline__ uint32_t queue_addr(const void* p) {
 
 // One thread, before the CTA's first barrier: full and demand slots take one arrival, empty
 // slots one per consumer warp.
-__device__ __forceinline__ void queue_init(ItemQueue& q, int consumer_warps) {
+__device__ __forceinline__ void queue_init(ItemQueue& q, int consumer_warps, uint64_t limit_ns) {
+  q.limit_ns = limit_ns;
   for (int k = 0; k < kItemRing; ++k) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(queue_addr(&q.full[k])), "r"(1));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(queue_addr(&q.empty[k])), "r"(consumer_warps));
@@ -86,8 +89,9 @@ __device__ __forceinline__ uint64_t queue_clock() {
 }
 
 // Waits for the phase of `bar` with the given parity; false (and the abort flag set) after
-// one second, or at once when the CTA has aborted.
-__device__ __forceinline__ bool queue_wait(const uint64_t* bar, uint32_t parity, int* abort_flag) {
+// limit_ns nanoseconds, or at once when the CTA has aborted.
+__device__ __forceinline__ bool queue_wait(const uint64_t* bar, uint32_t parity, int* abort_flag,
+                                           uint64_t limit_ns) {
   const uint32_t a = queue_addr(bar);
   uint64_t t0 = 0;
   for (int it = 0;; ++it) {
@@ -101,7 +105,7 @@ __device__ __forceinline__ bool queue_wait(const uint64_t* bar, uint32_t parity,
     if (ok) return true;
     if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
     if (it == 0) t0 = queue_clock();
-    else if ((it & 63) == 0 && queue_clock() - t0 > 1000000000ull) break;
+    else if ((it & 63) == 0 && queue_clock() - t0 > limit_ns) break;
   }
   atomicOr(abort_flag, 1);
   return false;
@@ -118,9 +122,9 @@ __device__ __forceinline__ void queue_fill(ItemQueue& q, const ItemSource& src, 
   int4 rec = fetch();
   for (int k = 0;; ++k) {
     const int sl = k % kItemRing;
-    if (!queue_wait(&q.empty[sl], ((k / kItemRing) & 1) ^ 1, abort_flag)) return;
+    if (!queue_wait(&q.empty[sl], ((k / kItemRing) & 1) ^ 1, abort_flag, q.limit_ns)) return;
     const int kd = k - kItemAhead;
-    if (kd >= 0 && !queue_wait(&q.demand[kd % kItemRing], (kd / kItemRing) & 1, abort_flag)) return;
+    if (kd >= 0 && !queue_wait(&q.demand[kd % kItemRing], (kd / kItemRing) & 1, abort_flag, q.limit_ns)) return;
     q.view[sl] = rec.x >= 0 ? view_of(src, rec) : ItemView{0, -1, 0, 0, 0, 0, 0};
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(queue_addr(&q.full[sl])) : "memory");
     if (rec.x < 0) return;
@@ -132,7 +136,7 @@ __device__ __forceinline__ void queue_fill(ItemQueue& q, const ItemSource& src, 
 // lanes may call it; they all see the same value.
 __device__ __forceinline__ ItemView queue_peek(ItemQueue& q, int k, int* abort_flag) {
   const int sl = k % kItemRing;
-  if (!queue_wait(&q.full[sl], (k / kItemRing) & 1, abort_flag)) return ItemView{0, -1, 0, 0, 0, 0, 0};
+  if (!queue_wait(&q.full[sl], (k / kItemRing) & 1, abort_flag, q.limit_ns)) return ItemView{0, -1, 0, 0, 0, 0, 0};
   return q.view[sl];
 }
 

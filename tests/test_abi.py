@@ -77,7 +77,9 @@ def test_host_validation_before_any_cuda_call():
         assert rc == code and text in msg, (rc, msg)
     rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, None, None, A, ws, None)
     assert rc == _pisa.PISA_EINVAL and "idx is NULL" in msg
-    rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, A, None, A, ws - 1, None)
+    ws_mean = pisa.workspace_size(good, _pisa.OP_SELECT_MEAN)
+    assert 0 < ws_mean < ws            # no grouping and no per-head terms on the PISA-1 path
+    rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, A, None, A, ws_mean - 1, None)
     assert rc == _pisa.PISA_EWORKSPACE
     rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, None, A, A, A, 1 << 40, None)
     assert rc == _pisa.PISA_EINVAL and "V is NULL" in msg
@@ -88,10 +90,13 @@ def test_host_validation_before_any_cuda_call():
     assert rc == _pisa.PISA_EINVAL and "status" in msg
     rc, msg = _rc(L.pisa_workspace_size, ctypes.byref(good), 7, ctypes.byref(ctypes.c_size_t()))
     assert rc == _pisa.PISA_EINVAL
+    # the wait limit and the test stall are host-only settings: no CUDA call, always accepted
+    assert L.pisa_set_wait_limit(5_000_000) == _pisa.PISA_OK and L.pisa_set_wait_limit(0) == _pisa.PISA_OK
+    assert L.pisa_test_stall(1) == _pisa.PISA_OK and L.pisa_test_stall(0) == _pisa.PISA_OK
 
 
 def test_workspace_sizes_grow_with_problem():
     a = pisa.make_shape(1, 4096, 16, 2, 128, 64, 16)
     b = pisa.make_shape(1, 65536, 16, 2, 128, 64, 16)
-    for op in range(3):
-        assert 0 < pisa.workspace_size(a, op) < pisa.workspace_size(b, op)
+    for op in range(5):
+        assert 256 < pisa.workspace_size(a, op) < pisa.workspace_size(b, op)   # past the status block

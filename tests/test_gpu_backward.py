@@ -17,6 +17,11 @@ C = 64
     (1, 500, 8, 2, 128, 4, 0),      # G = 4, ragged N
     (2, 300, 2, 2, 64, 3, 1),       # G = 1, d = 64
     (1, 700, 16, 2, 128, 16, 2),    # G = 8, K >= visible leaves for early queries
+    (1, 420, 4, 2, 64, 4, 3),       # G = 2, d = 64
+    (1, 390, 8, 2, 64, 5, 4),       # G = 4, d = 64
+    (1, 333, 8, 1, 64, 3, 5),       # G = 8, d = 64, ragged
+    (2, 260, 2, 2, 128, 3, 6),      # G = 1, d = 128
+    (1, 450, 4, 2, 128, 6, 7),      # G = 2, d = 128
 ])
 def test_backward_vs_oracle(B, N, Hq, Hkv, d, K, seed):
     Q, Kt, V = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=seed, needles=True)

@@ -23,6 +23,8 @@ CASES = [
     ("single_partial_leaf", 1, 63, 4, 1, 64, 4, False),
     ("one_token", 1, 1, 2, 1, 128, 4, False),
     ("two_leaves_b2", 2, 65, 8, 1, 128, 1, False),
+    ("g1_d128", 1, 1200, 2, 2, 128, 6, True),                 # G = 1 with d = 128
+    ("g8_d64", 1, 1100, 8, 1, 64, 5, True),                   # G = 8 with d = 64
 ]
 
 
