@@ -532,73 +532,86 @@ def exact_leaf_lse(Qg, Kk, q0, q1, C, scale):
     return torch.logsumexp(logits.view(q1 - q0, Qg.shape[1], nl, C), dim=-1)
 
 
-def run_quality(args, cfg, local):
-    """Selection quality on the needle data (one JSON line per N): recall of the exhaustive exact
-    top-K, recall of the planted needle leaves (queries aligned with the needle direction), and the
-    share of each head's full causal softmax mass inside the selected leaves; for the pyramid
-    selection, the flat comparator and the exact top-K itself."""
+def quality_stats(sels, Q, Kt, C, K, needles, QB=256):
+    """Selection quality of every selection in `sels` (name -> idx [B,Hkv,N,K]) and of the exact
+    top-K itself, against exhaustive exact leaf scores: recall of the exact top-K (queries with
+    more than K visible leaves), recall of the planted needle leaves (queries aligned with the
+    needle direction), and the mean share of each head's full causal softmax mass that falls
+    inside the selected leaves."""
+    B, N, Hq, d = Q.shape
+    Hkv = Kt.shape[2]
+    G = Hq // Hkv
+    dev = Q.device
+    scale = 1.0 / math.sqrt(d)
+    acc = {k: dict(hit=0.0, units=0, needle=0.0, nunits=0, mass=0.0, munits=0) for k in list(sels) + ["exact"]}
+    for b in range(B):
+        for kv in range(Hkv):
+            Qg = Q[b, :, kv * G:(kv + 1) * G, :]
+            Kk = Kt[b, :, kv, :]
+            u = syn.needle_direction(Q, Hkv, b, kv)
+            nd = torch.tensor(needles[b][kv], device=dev)
+            for q0 in range(0, N, QB):
+                q1 = min(q0 + QB, N)
+                ll = exact_leaf_lse(Qg, Kk, q0, q1, C, scale)                     # [q, G, nl]
+                full = torch.logsumexp(ll, dim=-1, keepdim=True)                  # [q, G, 1]
+                score = ll.sum(1)                                                 # [q, nl]
+                nl = score.shape[1]
+                vis = torch.arange(q0, q1, device=dev) // C + 1                   # visible leaves
+                kk = min(K, nl)
+                exact = torch.topk(score, kk, dim=-1).indices
+                exact = exact.masked_fill(torch.arange(kk, device=dev).view(1, -1) >= vis.view(-1, 1), -1)
+                aligned = (Qg[q0:q1].float() @ u).sum(-1) > 0
+                vneed = (nd.view(1, -1) < vis.view(-1, 1))                        # [q, 8]
+                prune = vis > K                                                   # rows where K < visible
+                for name, a in acc.items():
+                    sel = exact if name == "exact" else sels[name][b, kv, q0:q1].long()
+                    hit = (sel.unsqueeze(-1) == exact.unsqueeze(1)) & (sel.unsqueeze(-1) >= 0)
+                    a["hit"] += hit.any(-1).sum(-1)[prune].float().sum().item()
+                    a["units"] += int(prune.sum().item()) * K
+                    got = (nd.view(1, 1, -1) == sel.unsqueeze(-1)).any(1) & vneed      # [q, 8]
+                    rows = aligned & vneed.any(-1)
+                    a["needle"] += (got.sum(-1).float() / vneed.sum(-1).clamp_min(1))[rows].sum().item()
+                    a["nunits"] += int(rows.sum().item())
+                    g_ = sel.clamp_min(0).unsqueeze(1).expand(-1, G, -1)
+                    m = torch.exp(torch.gather(ll, 2, g_) - full) * (sel >= 0).unsqueeze(1)
+                    a["mass"] += m.sum(-1).sum().item()
+                    a["munits"] += (q1 - q0) * G
+    return {name: {"recall_exact_topk": a["hit"] / max(1, a["units"]),
+                   "needle_recall_aligned": a["needle"] / max(1, a["nunits"]),
+                   "attention_mass": a["mass"] / max(1, a["munits"])} for name, a in acc.items()}
+
+
+QUALITY_NOTES = {"reference": "exhaustive exact leaf scores (dense fp32 logits on the GPU, per-head LSE per leaf "
+                              "summed over the group)",
+                 "recall_rows": "queries with more than K visible leaves",
+                 "needle_rows": "queries with sum_h q.u > 0 and at least one visible needle leaf",
+                 "mass": "mean over (query, head) of the full causal softmax mass inside the selected leaves"}
+
+
+def quality_selections(Q, Kt, cfg):
+    """The library's selections compared by the quality workload."""
     import pyramid_top_selection_gb300 as pisa
+    B, N, Hq, d = Q.shape
+    shape = pisa.make_shape(B, N, Hq, Kt.shape[2], d, cfg["C"], cfg["K"], cfg["g"], cfg["qtile"])
+    pyr = pisa.build_pyramid(Kt, shape)
+    return {"pyramid": pisa.select(Q, Kt, pyr, shape, want_score=False)[0],
+            "pisa1_mean": pisa.select_mean(Q, Kt, pyr, shape, want_score=False)[0],
+            "flat": pisa.select_flat(Q, Kt, pyr, shape, want_score=False)[0]}
+
+
+def run_quality(args, cfg, local):
+    """Selection quality on the needle data (one JSON line per N)."""
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     for N in [int(x) for x in args.quality_n.split(",")]:
         c = dict(cfg, N=N)
         B, Hq, Hkv, d, C, K = c["B"], c["Hq"], c["Hkv"], c["d"], c["C"], c["K"]
-        G, n0 = Hq // Hkv, -(-N // C)
         Q, Kt, _ = syn.make_prefill(B, N, Hq, Hkv, d, C=C, seed=0, needles=True, device=dev)
-        needles = syn.needle_leaves(B, Hkv, n0, 3, device=dev)
-        shape = pisa.make_shape(B, N, Hq, Hkv, d, C, K, c["g"], c["qtile"])
-        pyr = pisa.build_pyramid(Kt, shape)
-        sels = {"pyramid": pisa.select(Q, Kt, pyr, shape, want_score=False)[0],
-                "pisa1_mean": pisa.select_mean(Q, Kt, pyr, shape, want_score=False)[0],
-                "flat": pisa.select_flat(Q, Kt, pyr, shape, want_score=False)[0]}
-        scale = 1.0 / math.sqrt(d)
-        acc = {k: dict(hit=0.0, units=0, needle=0.0, nunits=0, mass=0.0, munits=0)
-               for k in ("pyramid", "pisa1_mean", "flat", "exact")}
-        QB = 256
-        for b in range(B):
-            for kv in range(Hkv):
-                Qg = Q[b, :, kv * G:(kv + 1) * G, :]
-                Kk = Kt[b, :, kv, :]
-                u = syn.needle_direction(Q, Hkv, b, kv)
-                nd = torch.tensor(needles[b][kv], device=dev)
-                for q0 in range(0, N, QB):
-                    q1 = min(q0 + QB, N)
-                    ll = exact_leaf_lse(Qg, Kk, q0, q1, C, scale)                     # [q, G, nl]
-                    full = torch.logsumexp(ll, dim=-1, keepdim=True)                  # [q, G, 1]
-                    score = ll.sum(1)                                                 # [q, nl]
-                    nl = score.shape[1]
-                    vis = torch.arange(q0, q1, device=dev) // C + 1                   # visible leaves
-                    kk = min(K, nl)
-                    exact = torch.topk(score, kk, dim=-1).indices
-                    exact = exact.masked_fill(torch.arange(kk, device=dev).view(1, -1) >= vis.view(-1, 1), -1)
-                    aligned = (Qg[q0:q1].float() @ u).sum(-1) > 0
-                    vneed = (nd.view(1, -1) < vis.view(-1, 1))                        # [q, 8]
-                    prune = vis > K                                                   # rows where K < visible
-                    for name in acc:
-                        sel = exact if name == "exact" else sels[name][b, kv, q0:q1].long()
-                        hit = (sel.unsqueeze(-1) == exact.unsqueeze(1)) & (sel.unsqueeze(-1) >= 0)
-                        a = acc[name]
-                        a["hit"] += hit.any(-1).sum(-1)[prune].float().sum().item()
-                        a["units"] += int(prune.sum().item()) * K
-                        got = (nd.view(1, 1, -1) == sel.unsqueeze(-1)).any(1) & vneed      # [q, 8]
-                        rows = aligned & vneed.any(-1)
-                        a["needle"] += (got.sum(-1).float() / vneed.sum(-1).clamp_min(1))[rows].sum().item()
-                        a["nunits"] += int(rows.sum().item())
-                        g_ = sel.clamp_min(0).unsqueeze(1).expand(-1, G, -1)
-                        m = torch.exp(torch.gather(ll, 2, g_) - full) * (sel >= 0).unsqueeze(1)
-                        a["mass"] += m.sum(-1).sum().item()
-                        a["munits"] += (q1 - q0) * G
-        out = {name: {"recall_exact_topk": a["hit"] / max(1, a["units"]),
-                      "needle_recall_aligned": a["needle"] / max(1, a["nunits"]),
-                      "attention_mass": a["mass"] / max(1, a["munits"])} for name, a in acc.items()}
+        needles = syn.needle_leaves(B, Hkv, -(-N // C), 3, device=dev)
+        out = quality_stats(quality_selections(Q, Kt, c), Q, Kt, C, K, needles)
         print(json.dumps({"workload": "selection quality", "N": N, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "C": C,
                           "K": K, "data": "synthetic (seeded N(0,1) bf16, 8 needle leaf blocks per KV head)",
-                          "reference": "exhaustive exact leaf scores (dense fp32 logits on the GPU, per-head LSE "
-                                       "per leaf summed over the group)",
-                          "recall_rows": "queries with more than K visible leaves",
-                          "needle_rows": "queries with sum_h q.u > 0 and at least one visible needle leaf",
-                          "mass": "mean over (query, head) of the full causal softmax mass inside the selected leaves",
-                          **out}), flush=True)
+                          **QUALITY_NOTES, **out}), flush=True)
 
 
 def sweep_point(args, cfg, N, dev, flush):
@@ -720,6 +733,13 @@ def other_configs(dev, flush):
     out["train"] = {"tokens_per_s": tr["value"], "ms_per_step": tr["ms_per_step"],
                     "bwd_ms": tr["kernels"]["attn_bwd"]["avg_ms"], "bwd_tensor_tflops": tr["roofline"]["achieved"],
                     "bwd_tensor_frac": tr["roofline"]["frac"], "config": tr["config"]}
+    qc = dict(WORKLOADS["quality"], N=4096)
+    Q, Kt, _ = syn.make_prefill(qc["B"], qc["N"], qc["Hq"], qc["Hkv"], qc["d"], C=qc["C"], seed=0, needles=True,
+                                device=dev)
+    needles = syn.needle_leaves(qc["B"], qc["Hkv"], -(-qc["N"] // qc["C"]), 3, device=dev)
+    out["selection_quality"] = {"config": {k: qc[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K")},
+                                **quality_stats(quality_selections(Q, Kt, qc), Q, Kt, qc["C"], qc["K"], needles),
+                                **QUALITY_NOTES}
     out["seconds"] = time.perf_counter() - t0
     return out
 
