@@ -35,8 +35,12 @@ Readings taken where the pages are silent (each one is listed in the design note
   R15 the output leaf list is sorted ascending.
   R22 the digest's PISA-1 ablation ("scored by the mean"): every block, leaves included, is
       scored by sum_h s q_h . mu_i(l,m), its own causal mean key; descent and ties unchanged.
-Parity unpinned: R7, R8, R11, R12, R14 and R22 are readings that nothing the pages print can
-confirm; the pins in the tests check the oracle against the mathematics of those readings.
+  R23 the digest's PISA-2 ablation ("mean + variance"): every block, leaves included, is
+      scored by sum_h [s q_h . mu + (s^2 / 2) sum_k q_hk^2 var_k] over its causal keys, with
+      var_k the population variance of dimension k: the second-order cumulant expansion of
+      the block's log-mean-exp with a diagonal covariance; descent and ties unchanged.
+Parity unpinned: R7, R8, R11, R12, R14, R22 and R23 are readings that nothing the pages print
+can confirm; the pins in the tests check the oracle against the mathematics of those readings.
 
 Precision: every input is the exact bf16 value promoted to float64; all arithmetic is fp64.
 """
@@ -116,6 +120,22 @@ class CausalKeySummaries:
             else:
                 out[r] = (self.csum[i + 1] - self.csum[s]) / (i + 1 - s)
         return out
+
+    def variances(self, l: int, nodes: np.ndarray, i: int) -> np.ndarray:
+        """[len(nodes), d] population variance, per dimension, of the causal keys of visible
+        nodes at level l for query i (mean of squares minus squared mean)."""
+        if not hasattr(self, "sq_sums"):
+            self.sq_sums = pyramid_sums(self.K_bk * self.K_bk, self.C)
+            self.csq = np.concatenate([np.zeros((1, self.K_bk.shape[1])), np.cumsum(self.K_bk * self.K_bk, axis=0)])
+        mu = self.means(l, nodes, i)
+        out = np.empty_like(mu)
+        for r, m in enumerate(nodes):
+            s, e = node_range(l, int(m), self.C, self.N)
+            if e - 1 <= i:
+                out[r] = self.sq_sums[l][m] / (e - s)
+            else:
+                out[r] = (self.csq[i + 1] - self.csq[s]) / (i + 1 - s)
+        return out - mu * mu
 
 
 # --------------------------------------------------------------------------------------
@@ -227,11 +247,22 @@ def mean_scores(q: np.ndarray, i: int, l: int, nodes: np.ndarray, summ: CausalKe
     return (scale * (q @ mu.T)).sum(axis=0)
 
 
+def meanvar_scores(q: np.ndarray, i: int, l: int, nodes: np.ndarray, summ: CausalKeySummaries,
+                   scale: float) -> np.ndarray:
+    """PISA-2 score of nodes at level l (l = 0: leaves):
+    sum_h [s q_h . mu_i(l, m) + (s^2 / 2) sum_k q_hk^2 var_i(l, m)_k]."""
+    mu = summ.means(l, nodes, i)                      # [n, d]
+    var = summ.variances(l, nodes, i)                 # [n, d]
+    return (scale * (q @ mu.T) + 0.5 * scale * scale * ((q * q) @ var.T)).sum(axis=0)
+
+
 def select_unit_mean(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, scale: float,
-                     g: int = 2) -> tuple[np.ndarray, np.ndarray, float]:
-    """The coarse-to-fine descent with PISA-1 scores at every level; returns the ascending
-    leaves, their scores and the smallest pruning margin."""
+                     g: int = 2, score_fn=None) -> tuple[np.ndarray, np.ndarray, float]:
+    """The coarse-to-fine descent with one block score at every level, leaves included
+    (PISA-1 mean scores by default, PISA-2 with score_fn=meanvar_scores); returns the
+    ascending leaves, their scores and the smallest pruning margin."""
     assert g == 2, "the pyramid's merge factor is 2, so a node has 2 children"
+    mean_scores_ = score_fn or mean_scores
     kept = np.array([0], dtype=np.int64)
     min_margin = np.inf
     cand = kept
@@ -243,9 +274,9 @@ def select_unit_mean(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, sc
         if len(cand) <= K:
             kept = cand
             continue
-        kept, margin = _top_k(cand, mean_scores(q, i, l, cand, summ, scale), K)
+        kept, margin = _top_k(cand, mean_scores_(q, i, l, cand, summ, scale), K)
         min_margin = min(min_margin, margin)
-    sc = mean_scores(q, i, 0, cand, summ, scale)
+    sc = mean_scores_(q, i, 0, cand, summ, scale)
     kept, margin = _top_k(cand, sc, K)
     min_margin = min(min_margin, margin)
     kept = np.sort(kept)
@@ -253,7 +284,12 @@ def select_unit_mean(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, sc
     return kept, sc[pos], min_margin
 
 
-def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
+def select_meanvar(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
+    """PISA-2 selection (reading R23), same outputs as select_mean."""
+    return select_mean(Q, K, C, K_sel, scale, queries, score_fn=meanvar_scores)
+
+
+def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, score_fn=None):
     """PISA-1 selection for every (batch, KV head, query): idx [B,Hkv,N,K] ascending (-1 pad),
     score [B,Hkv,N,K] (the PISA-1 leaf scores, -inf pad), margin [B,Hkv,N]."""
     Q, K = _as64(Q), _as64(K)
@@ -269,7 +305,8 @@ def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=No
         for kv in range(Hkv):
             summ = CausalKeySummaries(K[b, :, kv, :], C)
             for i in qs:
-                leaves, sc, mg = select_unit_mean(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s)
+                leaves, sc, mg = select_unit_mean(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s,
+                                                  score_fn=score_fn)
                 idx[b, kv, i, :len(leaves)] = leaves
                 score[b, kv, i, :] = NEG_INF
                 score[b, kv, i, :len(leaves)] = sc

@@ -619,3 +619,75 @@ def test_margin_pins_catch_planted_mistakes(monkeypatch):
             leaf_only |= gaps.get(0, np.inf) != true
             inter_only |= min([v for l, v in gaps.items() if l > 0], default=np.inf) != true
     assert leaf_only and inter_only
+
+
+# ---------------------------------------------------------------- PISA-2 ablation (R23)
+def _bf_meanvar_score(q, K, l, m, i, C, s):
+    """PISA-2 score by token loops: mean, then the two-pass population variance per dimension."""
+    N, d = K.shape
+    toks = [j for j in range(m * (C << l), min((m + 1) * (C << l), N)) if j <= i]
+    mu = [sum(K[j, k] for j in toks) / len(toks) for k in range(d)]
+    var = [sum((K[j, k] - mu[k]) ** 2 for j in toks) / len(toks) for k in range(d)]
+    tot = 0.0
+    for h in range(q.shape[0]):
+        tot += s * sum(q[h, k] * mu[k] for k in range(d)) + 0.5 * s * s * sum(q[h, k] ** 2 * var[k] for k in range(d))
+    return tot
+
+
+@pytest.mark.parametrize("N,C,Ksel,G,seed", [
+    (64, 4, 1, 1, 0), (96, 4, 3, 2, 2), (128, 8, 3, 2, 4), (61, 4, 2, 2, 5), (200, 8, 1, 2, 6)])
+def test_pisa2_descent_matches_brute_force(N, C, Ksel, G, seed):
+    d = 4
+    Q = _rand((1, N, G, d), 400 + seed, scale=2.0)
+    K = _rand((1, N, 1, d), 450 + seed, scale=2.0)
+    s = 0.7
+    rng = np.random.default_rng(seed)
+    qs = sorted(set(rng.integers(0, N, 12).tolist()) | {0, N - 1})
+    out = po.select_meanvar(Q, K, C, Ksel, scale=s, queries=qs)
+    for i in qs:
+        leaves, scores = _bf_select(Q[0, i], K[0, :, 0, :], i, C, Ksel, s, _bf_meanvar_score)
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == leaves, (i, got, leaves)
+        np.testing.assert_allclose(out["score"][0, 0, i, :len(leaves)], scores, rtol=1e-10, atol=1e-10)
+        gaps = _bf_descent_gaps(Q[0, i], K[0, :, 0, :], i, C, Ksel, s, _bf_meanvar_score)
+        want = min(gaps.values()) if gaps else np.inf
+        assert out["margin"][0, 0, i] == want if not np.isfinite(want) else abs(out["margin"][0, 0, i] - want) < 1e-10
+
+
+def test_pisa2_is_the_second_order_cumulant_expansion_of_the_block_lse():
+    # For a block whose keys are mu + (+-a, +-b) (uncorrelated dimensions, symmetric), the
+    # exact log-mean-exp of s q.k equals s q.mu + (s^2/2)(q1^2 a^2 + q2^2 b^2) + O(s^4): the
+    # PISA-2 score minus the exact leaf LSE (less log n) must shrink like s^4, not s^2 or s^3.
+    mu, a, b = np.array([0.3, -0.2]), 0.9, 1.7
+    keys = np.array([mu + [sa * a, sb * b] for sa in (1, -1) for sb in (1, -1)])   # one leaf, C = 4
+    q = np.array([[1.3, -0.8]])
+    summ = po.CausalKeySummaries(keys, 4)
+    errs = []
+    for s in (0.2, 0.1, 0.05):
+        pisa2 = po.meanvar_scores(q, 3, 0, np.array([0]), summ, s)[0]
+        exact = po.leaf_scores(q, 3, np.array([0]), keys, 4, s)[0][0] - math.log(4)
+        errs.append(abs(exact - pisa2))
+        assert abs(pisa2 - (s * q[0] @ mu + 0.5 * s * s * (q[0, 0] ** 2 * a * a + q[0, 1] ** 2 * b * b))) < 1e-14
+    assert errs[0] / errs[1] > 12 and errs[1] / errs[2] > 14           # fourth order: ratio -> 16
+
+
+def test_pisa2_keep_all_and_zero_variance_leaves():
+    N, C, G, d = 96, 8, 2, 6
+    Q = _rand((1, N, G, d), 460)
+    kt = _rand((N // C, d), 461)
+    K = np.repeat(kt, C, axis=0)[None, :, None, :]     # constant keys inside each leaf: variance 0
+    n0 = N // C
+    out = po.select_meanvar(Q, K, C, n0)
+    for i in range(N):
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == list(range(i // C + 1))
+    # with zero leaf variance the PISA-2 leaf scores are the PISA-1 ones
+    Ksel = 3
+    a = po.select_meanvar(Q, K, C, Ksel, queries=[N - 1, 50])
+    b = po.select_mean(Q, K, C, Ksel, queries=[N - 1, 50])
+    for i in (N - 1, 50):
+        common = [t for t in a["idx"][0, 0, i] if t in set(b["idx"][0, 0, i].tolist()) and t >= 0]
+        for t in common:
+            sa = a["score"][0, 0, i][list(a["idx"][0, 0, i]).index(t)]
+            sb = b["score"][0, 0, i][list(b["idx"][0, 0, i]).index(t)]
+            assert abs(sa - sb) < 1e-12
