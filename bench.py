@@ -596,6 +596,7 @@ def quality_selections(Q, Kt, cfg):
     pyr = pisa.build_pyramid(Kt, shape)
     return {"pyramid": pisa.select(Q, Kt, pyr, shape, want_score=False)[0],
             "pisa1_mean": pisa.select_mean(Q, Kt, pyr, shape, want_score=False)[0],
+            "pisa2_meanvar": pisa.select_meanvar(Q, Kt, pyr, shape, want_score=False)[0],
             "flat": pisa.select_flat(Q, Kt, pyr, shape, want_score=False)[0]}
 
 
@@ -643,8 +644,9 @@ def sweep_point(args, cfg, N, dev, flush):
     out = {"build_ms": timed(lambda: pisa.build_pyramid(Kt, shape, out=pyr))}
     build_bytes = Kt.numel() * 2 + pyr.numel() * 4
     out["build_gbs"] = build_bytes / (out["build_ms"] / 1e3) / 1e9
+    ws_v = pisa.workspace(shape, 5, dev)
     for name, fn, ws in (("pyramid", pisa.select, ws_p), ("pisa1_mean", pisa.select_mean, ws_p),
-                         ("flat", pisa.select_flat, ws_f)):
+                         ("pisa2_meanvar", pisa.select_meanvar, ws_v), ("flat", pisa.select_flat, ws_f)):
         call = lambda: fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)   # noqa: E731
         out[name] = timed(call)
         kern, _, _ = profile_kernels(pisa, call, max(1, args.steps), flush)
@@ -656,9 +658,10 @@ def sweep_point(args, cfg, N, dev, flush):
             "pyramid_tokens_per_s": c["B"] * N / (out["pyramid"] / 1e3),
             "pyramid_kernels_ms": out["pyramid_kernels"], "flat_kernels_ms": out["flat_kernels"],
             "pisa1_mean_select_ms": out["pisa1_mean"], "pisa1_mean_kernels_ms": out["pisa1_mean_kernels"],
+            "pisa2_meanvar_select_ms": out["pisa2_meanvar"], "pisa2_meanvar_kernels_ms": out["pisa2_meanvar_kernels"],
             "build_ms": out["build_ms"], "build_gbs": out["build_gbs"],
             "build_hbm_frac": out["build_gbs"] / pk["hbm_gbs"]}
-    del Q, Kt, pyr, idx, ws_p, ws_f
+    del Q, Kt, pyr, idx, ws_p, ws_f, ws_v
     torch.cuda.empty_cache()
     return line
 
@@ -720,7 +723,7 @@ def other_configs(dev, flush):
     for N in (65536, 262144):
         p = sweep_point(sub, WORKLOADS["sweep"], N, dev, flush)
         e = {k: p[k] for k in ("pyramid_select_ms", "flat_select_ms", "flat_over_pyramid", "pisa1_mean_select_ms",
-                               "build_ms", "build_gbs", "build_hbm_frac")}
+                               "pisa2_meanvar_select_ms", "build_ms", "build_gbs", "build_hbm_frac")}
         e["route_ms"] = p["pyramid_kernels_ms"].get("route")
         e["leaf_score_ms"] = p["pyramid_kernels_ms"].get("leaf_score")
         sw[f"N={N}"] = e

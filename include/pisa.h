@@ -69,13 +69,15 @@ enum {
 enum { PISA_STATUS_POS_RANGE = 1, PISA_STATUS_TIMEOUT = 2 };
 
 /* Operations that need a workspace (pisa_workspace_size's `op`): pisa_select,
- * pisa_select_flat, pisa_sparse_attn_fwd, pisa_sparse_attn_bwd and pisa_select_mean. */
+ * pisa_select_flat, pisa_sparse_attn_fwd, pisa_sparse_attn_bwd, pisa_select_mean and
+ * pisa_select_meanvar. */
 enum {
   PISA_OP_SELECT = 0,
   PISA_OP_SELECT_FLAT = 1,
   PISA_OP_ATTN_FWD = 2,
   PISA_OP_ATTN_BWD = 3,
-  PISA_OP_SELECT_MEAN = 4
+  PISA_OP_SELECT_MEAN = 4,
+  PISA_OP_SELECT_MEANVAR = 5
 };
 
 /* Prefill/training shape. C = leaf block size in tokens, K = blocks kept per level,
@@ -191,6 +193,20 @@ int pisa_select_flat(const pisa_shape_t* shape, const void* Q, const void* K,
 int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
                      const float* pyr_sum, int32_t* idx, float* score, void* ws,
                      size_t ws_bytes, void* stream);
+
+/* PISA-2 ablation selection (digest page, "Method key points": the ablation that scores
+ * blocks by mean + variance). The pages give no formula; this library reads it as the
+ * second-order cumulant expansion of a block's log-mean-exp with a diagonal covariance:
+ * every block m at level l, leaves included, scores
+ *     sum_h [ s q_{i,h} . mu_i(l,m) + (s^2 / 2) sum_k q_{i,h,k}^2 var_i(l,m)_k ],
+ * mu_i and var_i the mean and the population variance per dimension of the block's keys
+ * j <= i. Descent, K, tie rule, outputs and errors as pisa_select_mean; score (nullable)
+ * receives these scores of the selected leaves. The call builds the squared-key pyramid it
+ * needs inside its workspace (PISA_OP_SELECT_MEANVAR). Runs on the CUDA cores (an ablation,
+ * not the method's hot path). */
+int pisa_select_meanvar(const pisa_shape_t* shape, const void* Q, const void* K,
+                        const float* pyr_sum, int32_t* idx, float* score, void* ws,
+                        size_t ws_bytes, void* stream);
 
 /* Causal block-sparse attention forward over the selected leaves (digest page,
  * "Reference value of the work"): o_{i,h} = sum_{j in J_i} softmax_j(s q_{i,h}.k_j) v_j,

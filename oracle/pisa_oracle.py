@@ -22,6 +22,13 @@ Complexity", PISA; three web pages about it):
 
 Readings taken where the pages are silent (each one is listed in the design notes):
   R2  g = 2 (fan-out equals the merge factor), so a level holds at most 2K candidates.
+  R24 g = 4 (a fan-out above the merge factor 2): each descent step goes down two levels,
+      the candidates being the visible grandchildren of the kept nodes (at most 4K); a last
+      step of one level reaches the leaves when the level count is odd. A candidate is still
+      scored by the LSE over its two children's means (leaves: exact LSE).
+  R25 per-head selection (the explainer's remedy for one head taking the shared budget):
+      every query head selects its own K leaves with its own LSE scores, no sum over the
+      group; the key summaries are those of its KV head.
   R3  the descent starts at the single top node; levels with <= K candidates keep all.
   R7  the LSE temperature is the attention scale s (default 1/sqrt(d)).
   R8  an intermediate node is scored with its (at most 2) immediate children, each
@@ -206,16 +213,27 @@ class UnitSelection:
 
 def select_unit(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, scale: float,
                 g: int = 2) -> UnitSelection:
-    """Pyramid Top-K selection for one query i of one (batch, KV head); q: [G, d]."""
-    assert g == 2, "the pyramid's merge factor is 2, so a node has 2 children"
+    """Pyramid Top-K selection for one query i of one (batch, KV head); q: [G, d] (the heads
+    whose LSEs are summed: the whole group, or one head for a per-head selection).
+
+    g = 2: every step goes one level down (candidates = visible children of the kept nodes);
+    g = 4: two levels (visible grandchildren), the last step one level when that reaches the
+    leaves (reading R24)."""
+    assert g in (2, 4), "fan-out g: 2 (the merge factor) or 4 (two levels per step)"
+    step = 1 if g == 2 else 2
     kept = np.array([0], dtype=np.int64)            # A at the top level
     min_margin = np.inf
     cand_sizes = []
-    for l in range(summ.top - 1, -1, -1):
-        cand = np.array([c for a in kept for c in (2 * int(a), 2 * int(a) + 1)
-                         if summ.visible(l, c, i)], dtype=np.int64)
+    cand = kept                                     # a single leaf: the top node
+    l = summ.top
+    while l > 0:
+        nl = max(l - step, 0)
+        t = l - nl                                  # levels this step goes down
+        cand = np.array([c for a in kept for c in range(int(a) << t, (int(a) + 1) << t)
+                         if summ.visible(nl, c, i)], dtype=np.int64)
         cand_sizes.append(len(cand))
         assert len(cand) <= g * K
+        l = nl
         if l == 0:
             break
         if len(cand) <= K:
@@ -224,8 +242,6 @@ def select_unit(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, scale: 
         sc = node_scores(q, i, l, cand, summ, scale)
         kept, margin = _top_k(cand, sc, K)
         min_margin = min(min_margin, margin)
-    else:
-        cand = kept                                   # a single leaf: the top node
     leaf_cand = cand
     sc, ph = leaf_scores(q, i, leaf_cand, summ.K_bk, summ.C, scale)
     kept, margin = _top_k(leaf_cand, sc, K)
@@ -328,40 +344,45 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def select(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, g: int = 2):
-    """Pyramid Top-K selection for every (batch, KV head, query).
+def select(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, g: int = 2,
+           per_head: bool = False):
+    """Pyramid Top-K selection for every (batch, KV head, query), or with per_head for every
+    (batch, query head, query) (reading R25). U = Hkv units per batch, or Hq with per_head.
 
     Q [B,N,Hq,d], K [B,N,Hkv,d]. Returns a dict with
-      idx   int32 [B,Hkv,N,K]  selected leaves, ascending, -1 padded
-      score f64   [B,Hkv,N,K]  S_i(0,t) (-inf on padding)
+      idx   int32 [B,U,N,K]    selected leaves, ascending, -1 padded
+      score f64   [B,U,N,K]    S_i(0,t) (-inf on padding)
       head_lse f64 [B,Hq,N,K]  per-head leaf LSE of the selected leaves (-inf padding)
-      margin f64  [B,Hkv,N]    smallest pruning margin over all levels (inf if none)
-      cand  int32 [B,Hkv,N,gK] leaf candidates that reached exact scoring (-1 padded)
+      margin f64  [B,U,N]      smallest pruning margin over all levels (inf if none)
+      cand  int32 [B,U,N,gK]   leaf candidates that reached exact scoring (-1 padded)
     Only the queries listed in `queries` (default: all) are filled; the rest stay -1/nan."""
     Q, K = _as64(Q), _as64(K)
     B, N, Hq, d = Q.shape
     Hkv = K.shape[2]
     G = Hq // Hkv
+    U, per = (Hq, 1) if per_head else (Hkv, G)       # units per batch, query heads per unit
     s = default_scale(d) if scale is None else float(scale)
     qs = range(N) if queries is None else [int(x) for x in queries]
-    idx = np.full((B, Hkv, N, K_sel), -1, dtype=np.int32)
-    score = np.full((B, Hkv, N, K_sel), np.nan)
+    idx = np.full((B, U, N, K_sel), -1, dtype=np.int32)
+    score = np.full((B, U, N, K_sel), np.nan)
     head_lse = np.full((B, Hq, N, K_sel), np.nan)
-    margin = np.full((B, Hkv, N), np.nan)
-    cand = np.full((B, Hkv, N, g * K_sel), -1, dtype=np.int32)
+    margin = np.full((B, U, N), np.nan)
+    cand = np.full((B, U, N, g * K_sel), -1, dtype=np.int32)
     for b in range(B):
         for kv in range(Hkv):
             summ = CausalKeySummaries(K[b, :, kv, :], C)
-            for i in qs:
-                u = select_unit(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s, g)
-                n = len(u.leaves)
-                idx[b, kv, i, :n] = u.leaves
-                score[b, kv, i, :] = NEG_INF
-                score[b, kv, i, :n] = u.scores
-                head_lse[b, kv * G:(kv + 1) * G, i, :] = NEG_INF
-                head_lse[b, kv * G:(kv + 1) * G, i, :n] = u.head_lse.T
-                margin[b, kv, i] = u.min_margin
-                cand[b, kv, i, :len(u.leaf_candidates)] = np.sort(u.leaf_candidates)
+            for un in range(kv * G // per, (kv + 1) * G // per):
+                hs = slice(un * per, (un + 1) * per)
+                for i in qs:
+                    u = select_unit(Q[b, i, hs, :], i, summ, K_sel, s, g)
+                    n = len(u.leaves)
+                    idx[b, un, i, :n] = u.leaves
+                    score[b, un, i, :] = NEG_INF
+                    score[b, un, i, :n] = u.scores
+                    head_lse[b, hs, i, :] = NEG_INF
+                    head_lse[b, hs, i, :n] = u.head_lse.T
+                    margin[b, un, i] = u.min_margin
+                    cand[b, un, i, :len(u.leaf_candidates)] = np.sort(u.leaf_candidates)
     return dict(idx=idx, score=score, head_lse=head_lse, margin=margin, cand=cand)
 
 
@@ -444,6 +465,7 @@ def selected_head_lse(Q, K, idx, C: int, scale: float | None = None, queries=Non
     exp(s q_{i,h} . k_j) for h in KV head kv's group (the exact leaf score of the digest
     page's "Method key points" before the GQA heads are summed).
 
+    idx: [B,Hkv,N,K] (a selection shared by the group) or [B,Hq,N,K] (per head).
     Returns [B,Hq,N,K] f64: -inf for -1 slots, nan for queries not computed."""
     Q, K = _as64(Q), _as64(K)
     idx = np.asarray(idx)
@@ -455,23 +477,31 @@ def selected_head_lse(Q, K, idx, C: int, scale: float | None = None, queries=Non
     qs = range(N) if queries is None else [int(x) for x in queries]
     out = np.full((B, Hq, N, Ksel), np.nan)
     for b in range(B):
-        for kv in range(Hkv):
-            hs = slice(kv * G, (kv + 1) * G)
+        for h in range(Hq):
+            kv = h // G
             for i in qs:
+                row = _idx_row(idx, b, h, G, Hkv, i)
                 for k in range(Ksel):
-                    t = int(idx[b, kv, i, k])
+                    t = int(row[k])
                     if t < 0:
-                        out[b, hs, i, k] = -np.inf
+                        out[b, h, i, k] = -np.inf
                         continue
                     lo, hi = node_range(0, t, C, N)
-                    logits = s * (Q[b, i, hs, :] @ K[b, lo:min(hi, i + 1), kv, :].T)   # [G, n]
-                    out[b, hs, i, k] = _logsumexp(logits, axis=1)
+                    logits = s * (Q[b, i, h, :] @ K[b, lo:min(hi, i + 1), kv, :].T)   # [n]
+                    out[b, h, i, k] = _logsumexp(logits, axis=0)
     return out
+
+
+def _idx_row(idx: np.ndarray, b: int, h: int, G: int, Hkv: int, i: int) -> np.ndarray:
+    """The selection row of query head h: its KV head's row of a selection shared by the
+    group (idx [B,Hkv,N,K]) or its own row of a per-head selection (idx [B,Hq,N,K])."""
+    return idx[b, h // G, i] if idx.shape[1] == Hkv else idx[b, h, i]
 
 
 def sparse_attn_fwd(Q, K, V, idx, C: int, scale: float | None = None, queries=None):
     """o_{i,h} = sum_{j in J_i} softmax_j(s q_{i,h} . k_j) v_j ; lse_{i,h} = log sum exp.
 
+    idx: [B,Hkv,N,K] (shared by the group) or [B,Hq,N,K] (per head).
     Returns O [B,N,Hq,d] f64 and lse [B,Hq,N] f64 (nan where not computed)."""
     Q, K, V = _as64(Q), _as64(K), _as64(V)
     idx = np.asarray(idx)
@@ -483,15 +513,14 @@ def sparse_attn_fwd(Q, K, V, idx, C: int, scale: float | None = None, queries=No
     O = np.full((B, N, Hq, d), np.nan)
     lse = np.full((B, Hq, N), np.nan)
     for b in range(B):
-        for kv in range(Hkv):
-            hs = slice(kv * G, (kv + 1) * G)
+        for h in range(Hq):
+            kv = h // G
             for i in qs:
-                J = selected_keys(idx[b, kv, i], i, C, N)
-                logits = s * (Q[b, i, hs, :] @ K[b, J, kv, :].T)   # [G, |J|]
-                l = _logsumexp(logits, axis=1)
-                P = np.exp(logits - l[:, None])
-                O[b, i, hs, :] = P @ V[b, J, kv, :]
-                lse[b, hs, i] = l
+                J = selected_keys(_idx_row(idx, b, h, G, Hkv, i), i, C, N)
+                logits = s * (Q[b, i, h, :] @ K[b, J, kv, :].T)   # [|J|]
+                l = _logsumexp(logits, axis=0)
+                O[b, i, h, :] = np.exp(logits - l) @ V[b, J, kv, :]
+                lse[b, h, i] = l
     return O, lse
 
 
@@ -500,7 +529,8 @@ def sparse_attn_bwd(Q, K, V, dO, idx, C: int, scale: float | None = None):
 
     P_ij = exp(s q_i.k_j - lse_i), D_i = dO_i . o_i, dS_ij = P_ij (dO_i . v_j - D_i),
     dQ_i = s sum_j dS_ij k_j, dK_j = s sum_{i,h in group} dS_ij q_i,
-    dV_j = sum_{i,h in group} P_ij dO_i."""
+    dV_j = sum_{i,h in group} P_ij dO_i.
+    idx: [B,Hkv,N,K] (shared by the group) or [B,Hq,N,K] (per head)."""
     Q, K, V, dO = _as64(Q), _as64(K), _as64(V), _as64(dO)
     idx = np.asarray(idx)
     B, N, Hq, d = Q.shape
@@ -511,19 +541,18 @@ def sparse_attn_bwd(Q, K, V, dO, idx, C: int, scale: float | None = None):
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
     for b in range(B):
-        for kv in range(Hkv):
-            hs = slice(kv * G, (kv + 1) * G)
+        for h in range(Hq):
+            kv = h // G
             for i in range(N):
-                J = selected_keys(idx[b, kv, i], i, C, N)
-                q, kJ, vJ, do = Q[b, i, hs, :], K[b, J, kv, :], V[b, J, kv, :], dO[b, i, hs, :]
-                logits = s * (q @ kJ.T)
-                P = np.exp(logits - _logsumexp(logits, axis=1)[:, None])   # [G, |J|]
-                o = P @ vJ
-                D = np.sum(do * o, axis=1)                                  # [G]
-                dS = P * (do @ vJ.T - D[:, None])
-                dQ[b, i, hs, :] = s * (dS @ kJ)
-                dK[b, J, kv, :] += s * (dS.T @ q)
-                dV[b, J, kv, :] += P.T @ do
+                J = selected_keys(_idx_row(idx, b, h, G, Hkv, i), i, C, N)
+                q, kJ, vJ, do = Q[b, i, h, :], K[b, J, kv, :], V[b, J, kv, :], dO[b, i, h, :]
+                logits = s * (kJ @ q)
+                P = np.exp(logits - _logsumexp(logits, axis=0))            # [|J|]
+                D = do @ (P @ vJ)
+                dS = P * (vJ @ do - D)
+                dQ[b, i, h, :] = s * (dS @ kJ)
+                dK[b, J, kv, :] += s * np.outer(dS, q)
+                dV[b, J, kv, :] += np.outer(P, do)
     return dQ, dK, dV
 
 
@@ -639,6 +668,7 @@ def sparse_attn_bwd_sampled(Q, K, V, dO, idx, C: int, scale: float | None = None
     """The backward's definitions evaluated only where asked: dQ of the listed queries (all
     heads) and dK/dV of the keys of the listed (b, KV head, leaf) triples. dK/dV of a key
     sums over every (query, head) whose selection holds the key's leaf and sees the key.
+    idx: [B,Hkv,N,K] (shared by the group) or [B,Hq,N,K] (per head).
 
     Returns (dQ {(b, i): [Hq, d]}, dK {(b, kv, t): [n_keys, d]}, dV {...})."""
     Q, K, V, dO = _as64(Q), _as64(K), _as64(V), _as64(dO)
@@ -648,35 +678,36 @@ def sparse_attn_bwd_sampled(Q, K, V, dO, idx, C: int, scale: float | None = None
     G = Hq // Hkv
     s = default_scale(d) if scale is None else float(scale)
 
-    def row_terms(b, kv, i):
-        hs = slice(kv * G, (kv + 1) * G)
-        J = selected_keys(idx[b, kv, i], i, C, N)
-        q, kJ, vJ, do = Q[b, i, hs, :], K[b, J, kv, :], V[b, J, kv, :], dO[b, i, hs, :]
-        logits = s * (q @ kJ.T)
-        P = np.exp(logits - _logsumexp(logits, axis=1)[:, None])
-        D = np.sum(do * (P @ vJ), axis=1)
-        dS = P * (do @ vJ.T - D[:, None])
+    def row_terms(b, h, i):
+        kv = h // G
+        J = selected_keys(_idx_row(idx, b, h, G, Hkv, i), i, C, N)
+        q, kJ, vJ, do = Q[b, i, h, :], K[b, J, kv, :], V[b, J, kv, :], dO[b, i, h, :]
+        logits = s * (kJ @ q)
+        P = np.exp(logits - _logsumexp(logits, axis=0))
+        D = do @ (P @ vJ)
+        dS = P * (vJ @ do - D)
         return J, q, kJ, do, P, dS
 
     dQ = {}
     for (b, i) in queries:
         out = np.zeros((Hq, d))
-        for kv in range(Hkv):
-            J, q, kJ, do, P, dS = row_terms(b, kv, i)
-            out[kv * G:(kv + 1) * G] = s * (dS @ kJ)
+        for h in range(Hq):
+            J, q, kJ, do, P, dS = row_terms(b, h, i)
+            out[h] = s * (dS @ kJ)
         dQ[(b, i)] = out
     dK, dV = {}, {}
     for (b, kv, t) in leaves:
         s0, e0 = node_range(0, t, C, N)
         gk = np.zeros((e0 - s0, d))
         gv = np.zeros((e0 - s0, d))
-        users = np.nonzero((idx[b, kv] == t).any(axis=-1))[0]
-        for i in users:
-            J, q, kJ, do, P, dS = row_terms(b, kv, int(i))
-            for c, j in enumerate(J):
-                if s0 <= j < e0:
-                    gk[j - s0] += s * (dS[:, c] @ q)
-                    gv[j - s0] += P[:, c] @ do
+        for h in range(kv * G, (kv + 1) * G):
+            rows = idx[b, kv] if idx.shape[1] == Hkv else idx[b, h]
+            for i in np.nonzero((rows == t).any(axis=-1))[0]:
+                J, q, kJ, do, P, dS = row_terms(b, h, int(i))
+                for c, j in enumerate(J):
+                    if s0 <= j < e0:
+                        gk[j - s0] += s * dS[c] * q
+                        gv[j - s0] += P[c] * do
         dK[(b, kv, t)] = gk
         dV[(b, kv, t)] = gv
     return dQ, dK, dV

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpisa.so")
 
 PISA_OK, PISA_EINVAL, PISA_EUNSUPPORTED, PISA_EWORKSPACE, PISA_ECUDA, PISA_ETIMEOUT = range(6)
-OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD, OP_SELECT_MEAN = range(5)
+OP_SELECT, OP_SELECT_FLAT, OP_ATTN_FWD, OP_ATTN_BWD, OP_SELECT_MEAN, OP_SELECT_MEANVAR = range(6)
 STATUS_POS_RANGE, STATUS_TIMEOUT = 1, 2
 MAX_LEVELS = 32
 ABI_VERSION = 4          # PISA_VERSION of the header these argument lists follow
@@ -28,6 +28,7 @@ EXPORTS = (
     "pisa_sparse_attn_bwd", "pisa_decode_pyramid_layout", "pisa_decode_build_pyramid",
     "pisa_decode_step", "pisa_profile_start", "pisa_profile_stop", "pisa_profile_read",
     "pisa_select_noalloc", "pisa_select_mean", "pisa_set_wait_limit", "pisa_test_stall",
+    "pisa_select_meanvar",
 )
 
 
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.pisa_select.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_select_flat.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_select_mean.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
+        L.pisa_select_meanvar.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_sparse_attn_fwd.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.pisa_sparse_attn_bwd.argtypes = [P(Shape)] + [vp] * 10 + [vp, sz, vp]
         L.pisa_decode_pyramid_layout.argtypes = [P(DecodeShape), P(i32), P(i64), P(i64)]
@@ -210,6 +212,18 @@ def select_mean(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, sc
         ws = _workspace(shape, OP_SELECT_MEAN, dev)
     _check(lib().pisa_select_mean(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
                                   _ptr(ws), ws.numel(), _stream(dev)))
+    return idx, score
+
+
+def select_meanvar(Q, Kt, pyr, shape: Shape, ws=None, want_score=True, idx=None, score=None):
+    """PISA-2 ablation selection: the pyramid descent with every block scored by mean + variance."""
+    _select_in(Q, Kt, pyr)
+    dev = Q.device
+    idx, score = _select_out(Q, shape, want_score, idx, score)
+    if ws is None:
+        ws = _workspace(shape, OP_SELECT_MEANVAR, dev)
+    _check(lib().pisa_select_meanvar(ctypes.byref(shape), _ptr(Q), _ptr(Kt), _ptr(pyr), _ptr(idx), _ptr(score),
+                                     _ptr(ws), ws.numel(), _stream(dev)))
     return idx, score
 
 

@@ -103,6 +103,7 @@ size_t ws_bytes_for(const pisa::Dims& d, const pisa::Geo& g, int op) {
   switch (op) {
     case PISA_OP_SELECT: return pisa::select_ws(d, g).total_head;
     case PISA_OP_SELECT_MEAN: return pisa::select_ws(d, g).mean_end;
+    case PISA_OP_SELECT_MEANVAR: return pisa::meanvar_ws(d, g);
     case PISA_OP_SELECT_FLAT: return pisa::flat_ws(d, g);
     case PISA_OP_ATTN_FWD: return pisa::attn_fwd_ws(d).total;
     case PISA_OP_ATTN_BWD: return pisa::attn_bwd_ws(d).total;
@@ -153,7 +154,7 @@ int pisa_pyramid_layout(const pisa_shape_t* shape, int32_t* n_levels, int64_t* l
 int pisa_workspace_size(const pisa_shape_t* shape, int op, size_t* bytes) {
   PISA_CHECK(check_shape(shape));
   if (!bytes) return fail(PISA_EINVAL, "bytes is NULL");
-  if (op < PISA_OP_SELECT || op > PISA_OP_SELECT_MEAN) return fail(PISA_EINVAL, "unknown op %d", op);
+  if (op < PISA_OP_SELECT || op > PISA_OP_SELECT_MEANVAR) return fail(PISA_EINVAL, "unknown op %d", op);
   *bytes = ws_bytes_for(dims_of(shape), pisa::make_geo(shape->N, shape->C), op);
   return PISA_OK;
 }
@@ -234,6 +235,22 @@ int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
   PISA_CHECK(check_ws(d, g, PISA_OP_SELECT_MEAN, ws, ws_bytes));
   return cuda_rc(pisa::launch_select_mean(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
                  "pisa_select_mean");
+}
+
+int pisa_select_meanvar(const pisa_shape_t* shape, const void* Q, const void* K,
+                        const float* pyr_sum, int32_t* idx, float* score, void* ws,
+                        size_t ws_bytes, void* stream) {
+  PISA_CHECK(check_shape(shape));
+  PISA_CHECK(check_ptr(Q, "Q"));
+  PISA_CHECK(check_ptr(K, "K"));
+  PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
+  PISA_CHECK(check_ptr(idx, "idx"));
+  PISA_CHECK(check_ptr(score, "score", true));
+  const pisa::Dims d = dims_of(shape);
+  const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  PISA_CHECK(check_ws(d, g, PISA_OP_SELECT_MEANVAR, ws, ws_bytes));
+  return cuda_rc(pisa::launch_select_meanvar(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
+                 "pisa_select_meanvar");
 }
 
 int pisa_sparse_attn_fwd(const pisa_shape_t* shape, const void* Q, const void* K, const void* V,

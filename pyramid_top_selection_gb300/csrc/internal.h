@@ -71,6 +71,9 @@ int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K
                        const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
 int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K,
                        const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
+int launch_select_meanvar(const Dims& s, const Geo& g, const void* Q, const void* K,
+                          const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
+size_t meanvar_ws(const Dims& s, const Geo& g);
 int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V, const int32_t* idx,
                     const float* head_lse, void* O, float* lse, char* ws, void* stream);
 int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, const void* O,

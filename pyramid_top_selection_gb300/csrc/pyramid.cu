@@ -21,7 +21,8 @@ constexpr int kLeavesPerCta = 8;   // leaves reduced by one CTA; levels 1..3 fin
 constexpr int kInCtaLevels = 3;
 
 // Grid (ceil(n0/8), Hkv, B); block (D/8) * 8 threads: thread = (leaf, 8-dim chunk).
-template <int D>
+// SQ: sums of squared keys instead (per dimension; same order), for the PISA-2 ablation.
+template <int D, bool SQ>
 __global__ void __launch_bounds__(D)
 build_leaves_kernel(const __nv_bfloat16* __restrict__ K, const int32_t* __restrict__ len,
                     int64_t T, int Hkv, int C, Geo geo, float* __restrict__ pyr) {
@@ -52,14 +53,20 @@ build_leaves_kernel(const __nv_bfloat16* __restrict__ K, const int32_t* __restri
       for (int u = 0; u < 4; ++u) {
         const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v[u]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += __bfloat162float(h[e]);
+        for (int e = 0; e < 8; ++e) {
+          const float x = __bfloat162float(h[e]);
+          acc[e] += SQ ? x * x : x;
+        }
       }
     }
     for (; j < e_; ++j) {
       uint4 v = ldg_u4(base + j * stride);
       const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += __bfloat162float(h[e]);
+      for (int e = 0; e < 8; ++e) {
+        const float x = __bfloat162float(h[e]);
+        acc[e] += SQ ? x * x : x;
+      }
     }
     float4* out = reinterpret_cast<float4*>(pyr_h + (geo.off[0] + t) * D + ch * 8);
     out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -106,12 +113,12 @@ build_upper_kernel(int Hkv, Geo geo, float* __restrict__ pyr) {
   }
 }
 
-template <int D>
+template <int D, bool SQ = false>
 int build_impl(const Dims& s, const Geo& g, const void* K, const int32_t* len, int64_t T,
                float* pyr, cudaStream_t st) {
   dim3 grid((g.size[0] + kLeavesPerCta - 1) / kLeavesPerCta, s.Hkv, s.B);
-  { ProfScope ps(st, "build_leaves");
-  build_leaves_kernel<D><<<grid, (D / 8) * kLeavesPerCta, 0, st>>>(
+  { ProfScope ps(st, SQ ? "build_sq_leaves" : "build_leaves");
+  build_leaves_kernel<D, SQ><<<grid, (D / 8) * kLeavesPerCta, 0, st>>>(
       static_cast<const __nv_bfloat16*>(K), len, T, s.Hkv, s.C, g, pyr); }
   if (g.n_levels > kInCtaLevels + 1) {
     ProfScope ps(st, "build_upper");
@@ -127,6 +134,12 @@ int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.d == 128) return build_impl<128>(s, g, K, len, tokens_per_seq, pyr, st);
   return build_impl<64>(s, g, K, len, tokens_per_seq, pyr, st);
+}
+
+// Pyramid of per-dimension sums of squared keys (same layout and summation order).
+int launch_build_pyramid_sq(const Dims& s, const Geo& g, const void* K, float* sq, cudaStream_t st) {
+  if (s.d == 128) return build_impl<128, true>(s, g, K, nullptr, s.N, sq, st);
+  return build_impl<64, true>(s, g, K, nullptr, s.N, sq, st);
 }
 
 const char* cuda_error_string(int err) {

@@ -696,6 +696,17 @@ inline int grid_for(int64_t n, int threads) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The top-K finish over `units` rows of W candidates (ascending output, -1 / -inf padding,
+// poisoned outputs when the status word reports a timeout).
+int launch_topk(const Dims& s, int W, const int32_t* cand, const float* cscore, const float* chead,
+                int32_t* idx, float* score, float* head_lse, const int32_t* status, cudaStream_t st) {
+  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
+  ProfScope ps(st, "topk");
+  topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+      units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse, status);
+  return cudaGetLastError();
+}
+
 SelectWs select_ws(const Dims& s, const Geo& g) {
   SelectWs w{};
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;

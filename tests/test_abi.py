@@ -81,6 +81,11 @@ def test_host_validation_before_any_cuda_call():
     assert 0 < ws_mean < ws            # no grouping and no per-head terms on the PISA-1 path
     rc, msg = _rc(L.pisa_select_mean, ctypes.byref(good), A, A, A, A, None, A, ws_mean - 1, None)
     assert rc == _pisa.PISA_EWORKSPACE
+    ws_mv = pisa.workspace_size(good, _pisa.OP_SELECT_MEANVAR)
+    rc, msg = _rc(L.pisa_select_meanvar, ctypes.byref(good), A, A, A, A, None, A, ws_mv - 1, None)
+    assert rc == _pisa.PISA_EWORKSPACE
+    rc, msg = _rc(L.pisa_select_meanvar, ctypes.byref(cases[0][0]), A, A, A, A, None, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EUNSUPPORTED and "head dim" in msg
     rc, msg = _rc(L.pisa_sparse_attn_fwd, ctypes.byref(good), A, A, None, A, None, A, A, A, 1 << 40, None)
     assert rc == _pisa.PISA_EINVAL and "V is NULL" in msg
     rc, msg = _rc(L.pisa_build_pyramid, None, A, A, None)
@@ -98,5 +103,5 @@ def test_host_validation_before_any_cuda_call():
 def test_workspace_sizes_grow_with_problem():
     a = pisa.make_shape(1, 4096, 16, 2, 128, 64, 16)
     b = pisa.make_shape(1, 65536, 16, 2, 128, 64, 16)
-    for op in range(5):
+    for op in range(6):
         assert 256 < pisa.workspace_size(a, op) < pisa.workspace_size(b, op)   # past the status block
