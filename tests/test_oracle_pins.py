@@ -691,3 +691,152 @@ def test_pisa2_keep_all_and_zero_variance_leaves():
             sa = a["score"][0, 0, i][list(a["idx"][0, 0, i]).index(t)]
             sb = b["score"][0, 0, i][list(b["idx"][0, 0, i]).index(t)]
             assert abs(sa - sb) < 1e-12
+
+
+# ---------------------------------------------------------------- fan-out g = 4 (R24)
+def _bf_select_g4(q, K, i, C, Ksel, s):
+    """Brute-force descent with fan-out 4 over the scalar enumerator's full score table:
+    visible grandchildren of the kept nodes at every step, one level for the last step when
+    two would pass the leaves."""
+    N = K.shape[0]
+    n = [-(-N // C)]
+    while n[-1] > 1:
+        n.append(-(-n[-1] // 2))
+    table = {(l, m): _bf_score(q, K, l, m, i, C, s)
+             for l in range(len(n)) for m in range(n[l]) if m * (C << l) <= i}
+    kept, l = [0], len(n) - 1
+    while l > 0:
+        nl = max(l - 2, 0)
+        cand = sorted({c for a in kept for c in range(a << (l - nl), (a + 1) << (l - nl)) if (nl, c) in table})
+        assert len(cand) <= 4 * Ksel
+        l = nl
+        if len(cand) > Ksel or l == 0:
+            kept = sorted(cand, key=lambda c: (-table[(l, c)], c))[:Ksel]
+        else:
+            kept = cand
+    leaves = sorted(kept)
+    return leaves, [table[(0, t)] for t in leaves]
+
+
+@pytest.mark.parametrize("N,C,Ksel,G,seed", [
+    (64, 4, 1, 1, 0), (96, 4, 2, 2, 1), (128, 4, 3, 2, 2), (200, 8, 1, 2, 3), (256, 4, 2, 1, 4), (61, 4, 2, 2, 5)])
+def test_g4_descent_matches_brute_force(N, C, Ksel, G, seed):
+    d = 4
+    Q = _rand((1, N, G, d), 500 + seed, scale=2.0)
+    K = _rand((1, N, 1, d), 550 + seed, scale=2.0)
+    s = 0.7
+    rng = np.random.default_rng(seed)
+    qs = sorted(set(rng.integers(0, N, 12).tolist()) | {0, N - 1})
+    out = po.select(Q, K, C, Ksel, scale=s, queries=qs, g=4)
+    for i in qs:
+        leaves, scores = _bf_select_g4(Q[0, i], K[0, :, 0, :], i, C, Ksel, s)
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == leaves, (i, got, leaves)
+        np.testing.assert_allclose(out["score"][0, 0, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
+
+
+def test_g4_invariants_and_keep_all():
+    N, C, Ksel, G, d = 512, 4, 3, 2, 4
+    Q = _rand((1, N, G, d), 560)
+    K = _rand((1, N, 1, d), 561)
+    summ = po.CausalKeySummaries(K[0, :, 0, :], C)
+    for i in range(0, N, 9):
+        u = po.select_unit(Q[0, i], i, summ, Ksel, 0.5, g=4)
+        assert all(c <= 4 * Ksel for c in u.cand_sizes)            # at most gK candidates per step
+        assert len(u.cand_sizes) == -(-(len(summ.sizes) - 1) // 2)  # ceil(top / 2) steps to the leaves
+        assert len(u.leaves) == min(Ksel, i // C + 1) and np.all(u.leaves <= i // C)
+        assert set(u.leaves.tolist()) <= set(u.leaf_candidates.tolist())
+    out = po.select(Q, K, C, -(-N // C), g=4)
+    for i in range(0, N, 5):
+        got = out["idx"][0, 0, i]
+        assert list(got[got >= 0]) == list(range(i // C + 1))
+
+
+# ---------------------------------------------------------------- per-head selection (R25)
+def test_per_head_selection_matches_single_head_brute_force():
+    N, C, Ksel, Hq, Hkv, d = 128, 4, 2, 4, 2, 4
+    Q = _rand((1, N, Hq, d), 570, scale=2.0)
+    K = _rand((1, N, Hkv, d), 571, scale=2.0)
+    s = 0.6
+    qs = [0, 17, 63, 100, N - 1]
+    out = po.select(Q, K, C, Ksel, scale=s, queries=qs, per_head=True)
+    assert out["idx"].shape == (1, Hq, N, Ksel) and out["head_lse"].shape == (1, Hq, N, Ksel)
+    for h in range(Hq):
+        for i in qs:
+            leaves, scores = _bf_select(Q[0, i, h:h + 1], K[0, :, h // (Hq // Hkv), :], i, C, Ksel, s)
+            got = out["idx"][0, h, i]
+            assert list(got[got >= 0]) == leaves, (h, i)
+            np.testing.assert_allclose(out["score"][0, h, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(out["head_lse"][0, h, i, :len(leaves)], scores, rtol=1e-12, atol=1e-12)
+
+
+def test_per_head_equals_shared_when_the_group_queries_coincide():
+    # identical queries in every head of a group: the shared score is G times a per-head
+    # score, so both rankings (and tie rules) agree
+    N, C, Ksel, Hq, Hkv, d = 160, 8, 3, 6, 2, 6
+    q = _rand((1, N, Hkv, d), 580)
+    Q = np.repeat(q, Hq // Hkv, axis=2)
+    K = _rand((1, N, Hkv, d), 581)
+    shared = po.select(Q, K, C, Ksel)
+    per = po.select(Q, K, C, Ksel, per_head=True)
+    for h in range(Hq):
+        np.testing.assert_array_equal(per["idx"][0, h], shared["idx"][0, h // (Hq // Hkv)])
+
+
+def _dense_masked_attention(Q, K, V, idx, C, s):
+    """Per head: torch softmax over dense logits masked to the head's own selected leaves."""
+    B, N, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, N, Hq, d))
+    j = torch.arange(N)
+    for b in range(B):
+        for h in range(Hq):
+            logits = torch.from_numpy(Q[b, :, h, :] @ K[b, :, h // G, :].T) * s          # [N, N]
+            rows = idx[b, h] if idx.shape[1] == Hq else idx[b, h // G]
+            keep = torch.zeros(N, N, dtype=torch.bool)
+            for i in range(N):
+                for t in rows[i]:
+                    if t >= 0:
+                        keep[i] |= (j // C == int(t)) & (j <= i)
+            O[b, :, h, :] = (torch.softmax(logits.masked_fill(~keep, float("-inf")), dim=-1) @
+                             torch.from_numpy(V[b, :, h // G, :])).numpy()
+    return O
+
+
+def test_per_head_attention_and_backward():
+    B, N, Hq, Hkv, d, C = 1, 40, 4, 2, 4, 8
+    Q, K, V = _rand((B, N, Hq, d), 590), _rand((B, N, Hkv, d), 591), _rand((B, N, Hkv, d), 592)
+    dO = _rand((B, N, Hq, d), 593)
+    idx = _random_idx(B, Hq, N, C, 2, 594)                    # a different selection per query head
+    s = 0.5
+    O, lse = po.sparse_attn_fwd(Q, K, V, idx, C, scale=s)
+    np.testing.assert_allclose(O, _dense_masked_attention(Q, K, V, idx, C, s), rtol=1e-10, atol=1e-12)
+    hl = po.selected_head_lse(Q, K, idx, C, scale=s)
+    np.testing.assert_allclose(torch.logsumexp(torch.from_numpy(hl), dim=-1).numpy(), lse, rtol=1e-12, atol=1e-12)
+    dQ, dK, dV = po.sparse_attn_bwd(Q, K, V, dO, idx, C, scale=s)
+
+    def loss(Q_, K_, V_):
+        O_, _ = po.sparse_attn_fwd(Q_, K_, V_, idx, C, scale=s)
+        return float((O_ * dO).sum())
+
+    eps = 1e-6
+    rng = np.random.default_rng(1)
+    for name, X, G_ in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        for _ in range(5):
+            pos = tuple(int(rng.integers(0, n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[pos] += eps
+            Xm[pos] -= eps
+            args_p = {"Q": (Xp, K, V), "K": (Q, Xp, V), "V": (Q, K, Xp)}[name]
+            args_m = {"Q": (Xm, K, V), "K": (Q, Xm, V), "V": (Q, K, Xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - G_[pos]) < 1e-6 * max(1.0, abs(fd)), (name, pos, fd, G_[pos])
+    sq, sk, sv = po.sparse_attn_bwd_sampled(Q, K, V, dO, idx, C, scale=s, queries=[(0, 7), (0, 39)],
+                                            leaves=[(0, 0, 0), (0, 1, 3)])
+    for (b, i) in ((0, 7), (0, 39)):
+        np.testing.assert_allclose(sq[(b, i)], dQ[b, i], rtol=1e-12, atol=1e-13)
+    for (b, kv, t) in ((0, 0, 0), (0, 1, 3)):
+        s0, e0 = po.node_range(0, t, C, N)
+        np.testing.assert_allclose(sk[(b, kv, t)], dK[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(sv[(b, kv, t)], dV[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
