@@ -27,9 +27,10 @@
  *    any CUDA call; a failed check returns PISA_EINVAL / PISA_EUNSUPPORTED /
  *    PISA_EWORKSPACE and enqueues nothing. A launch failure returns PISA_ECUDA. The text
  *    of the last error of the calling thread is returned by pisa_last_error().
- *  - Supported in this build: d in {64,128}, C = 64, g = 2, 1 <= K <= 32,
- *    G in {1,2,4,8}, 1 <= N <= 2^24, B*Hkv*N*2K < 2^31 and B*N*Hq < 2^31. Anything else
- *    returns PISA_EUNSUPPORTED.
+ *  - Supported in this build: d in {64,128}, C = 64, g in {2,4} (4 for the entry points
+ *    named under pisa_shape_t), 1 <= K <= 32 with gK <= 64, G in {1,2,4,8},
+ *    1 <= N <= 2^24, B*U*N*gK < 2^31 (U = Hkv, or Hq for a per-head selection) and
+ *    B*N*Hq < 2^31. Anything else returns PISA_EUNSUPPORTED.
  */
 #ifndef PISA_H_
 #define PISA_H_
@@ -81,15 +82,25 @@ enum {
 };
 
 /* Prefill/training shape. C = leaf block size in tokens, K = blocks kept per level,
- * g = candidate fan-out per kept node (the merge factor, 2), qtile = scheduling hint for
- * how many queries sharing a leaf block form one tile (results never depend on it),
- * scale = LSE and softmax temperature (0 selects 1/sqrt(d)). */
+ * g = candidate fan-out per kept node: 2 (the merge factor: candidates are the visible
+ * children of the kept nodes) or 4 (two levels per step: the visible grandchildren, the last
+ * step one level when that reaches the leaves; pisa_select and pisa_select_noalloc only;
+ * the flat comparator has no descent and ignores g), qtile = scheduling hint for how many queries sharing a leaf block
+ * form one tile (results never depend on it), scale = LSE and softmax temperature (0 selects
+ * 1/sqrt(d)).
+ * per_head = 0: the G query heads of a KV head sum their LSEs and share one selection;
+ * selections are [B,Hkv,N,K]. per_head = 1 (explainer page, "five pitfalls" item 2: a
+ * per-head top-K budget so that no head takes the others' share): every query head selects
+ * its own K leaves with its own LSE scores over its KV head's keys; selections (idx, score)
+ * are [B,Hq,N,K], and pisa_sparse_attn_fwd/bwd read such a selection per query head. The
+ * pyramid always belongs to the KV heads ([B,Hkv,nodes,d]). */
 typedef struct {
   int32_t B, N, Hq, Hkv, d, C, K, g, qtile;
   float scale;
+  int32_t per_head;
 } pisa_shape_t;
 
-/* Decode shape: Ncap = KV-cache capacity in tokens per sequence. */
+/* Decode shape: Ncap = KV-cache capacity in tokens per sequence (g = 2, shared selection). */
 typedef struct {
   int32_t B, Ncap, Hq, Hkv, d, C, K, g;
   float scale;
@@ -133,8 +144,9 @@ int pisa_workspace_size(const pisa_shape_t* shape, int op, size_t* bytes);
 int pisa_build_pyramid(const pisa_shape_t* shape, const void* K, float* pyr_sum, void* stream);
 
 /* Pyramid Top-K selection (abstract; digest page "Method key points"): for every
- * (b, KV head, query i), descend from the top node; at every level whose candidate set
- * (the visible children of the kept nodes, at most gK) exceeds K, score the candidates
+ * (b, KV head, query i) -- (b, query head, i) with per_head -- descend from the top node; at
+ * every level whose candidate set (the visible children of the kept nodes, at most gK;
+ * grandchildren with g = 4) exceeds K, score the candidates
  * and keep the K best (higher score first, then lower index). Intermediate node m at
  * level l scores sum_{h in group} log sum_{visible child c} exp(s q_{i,h} . mu_i(l-1,c)),
  * leaf t scores sum_h log sum_{j in t, j <= i} exp(s q_{i,h} . k_j). A node is visible to

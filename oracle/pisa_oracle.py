@@ -300,33 +300,43 @@ def select_unit_mean(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int, sc
     return kept, sc[pos], min_margin
 
 
-def select_meanvar(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
+def select_meanvar(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, per_head: bool = False):
     """PISA-2 selection (reading R23), same outputs as select_mean."""
-    return select_mean(Q, K, C, K_sel, scale, queries, score_fn=meanvar_scores)
+    return select_mean(Q, K, C, K_sel, scale, queries, score_fn=meanvar_scores, per_head=per_head)
 
 
-def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, score_fn=None):
-    """PISA-1 selection for every (batch, KV head, query): idx [B,Hkv,N,K] ascending (-1 pad),
-    score [B,Hkv,N,K] (the PISA-1 leaf scores, -inf pad), margin [B,Hkv,N]."""
+def _units(Hq: int, Hkv: int, per_head: bool):
+    """Selection units per batch and query heads per unit: the KV heads with their groups, or
+    every query head on its own (per-head selection, reading R25)."""
+    return (Hq, 1) if per_head else (Hkv, Hq // Hkv)
+
+
+def select_mean(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, score_fn=None,
+                per_head: bool = False):
+    """PISA-1 selection for every (batch, unit, query): idx [B,U,N,K] ascending (-1 pad),
+    score [B,U,N,K] (the PISA-1 leaf scores, -inf pad), margin [B,U,N]; U = Hkv, or Hq with
+    per_head."""
     Q, K = _as64(Q), _as64(K)
     B, N, Hq, d = Q.shape
     Hkv = K.shape[2]
     G = Hq // Hkv
+    U, per = _units(Hq, Hkv, per_head)
     s = default_scale(d) if scale is None else float(scale)
     qs = range(N) if queries is None else [int(x) for x in queries]
-    idx = np.full((B, Hkv, N, K_sel), -1, dtype=np.int32)
-    score = np.full((B, Hkv, N, K_sel), np.nan)
-    margin = np.full((B, Hkv, N), np.nan)
+    idx = np.full((B, U, N, K_sel), -1, dtype=np.int32)
+    score = np.full((B, U, N, K_sel), np.nan)
+    margin = np.full((B, U, N), np.nan)
     for b in range(B):
         for kv in range(Hkv):
             summ = CausalKeySummaries(K[b, :, kv, :], C)
-            for i in qs:
-                leaves, sc, mg = select_unit_mean(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s,
-                                                  score_fn=score_fn)
-                idx[b, kv, i, :len(leaves)] = leaves
-                score[b, kv, i, :] = NEG_INF
-                score[b, kv, i, :len(leaves)] = sc
-                margin[b, kv, i] = mg
+            for un in range(kv * G // per, (kv + 1) * G // per):
+                for i in qs:
+                    leaves, sc, mg = select_unit_mean(Q[b, i, un * per:(un + 1) * per, :], i, summ, K_sel, s,
+                                                      score_fn=score_fn)
+                    idx[b, un, i, :len(leaves)] = leaves
+                    score[b, un, i, :] = NEG_INF
+                    score[b, un, i, :len(leaves)] = sc
+                    margin[b, un, i] = mg
     return dict(idx=idx, score=score, margin=margin)
 
 
@@ -360,7 +370,7 @@ def select(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, g
     B, N, Hq, d = Q.shape
     Hkv = K.shape[2]
     G = Hq // Hkv
-    U, per = (Hq, 1) if per_head else (Hkv, G)       # units per batch, query heads per unit
+    U, per = _units(Hq, Hkv, per_head)
     s = default_scale(d) if scale is None else float(scale)
     qs = range(N) if queries is None else [int(x) for x in queries]
     idx = np.full((B, U, N, K_sel), -1, dtype=np.int32)
@@ -401,26 +411,29 @@ def select_unit_flat(q: np.ndarray, i: int, summ: CausalKeySummaries, K: int,
     return kept, sc[kept], mg
 
 
-def select_flat(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None):
-    """Flat BSA: score every visible leaf by sum_h s q_h . mu_i(0,t), keep the top K."""
+def select_flat(Q, K, C: int, K_sel: int, scale: float | None = None, queries=None, per_head: bool = False):
+    """Flat BSA: score every visible leaf by sum_h s q_h . mu_i(0,t), keep the top K (per
+    (batch, KV head, query), or per query head with per_head)."""
     Q, K = _as64(Q), _as64(K)
     B, N, Hq, d = Q.shape
     Hkv = K.shape[2]
     G = Hq // Hkv
+    U, per = _units(Hq, Hkv, per_head)
     s = default_scale(d) if scale is None else float(scale)
     qs = range(N) if queries is None else [int(x) for x in queries]
-    idx = np.full((B, Hkv, N, K_sel), -1, dtype=np.int32)
-    score = np.full((B, Hkv, N, K_sel), np.nan)
-    margin = np.full((B, Hkv, N), np.nan)
+    idx = np.full((B, U, N, K_sel), -1, dtype=np.int32)
+    score = np.full((B, U, N, K_sel), np.nan)
+    margin = np.full((B, U, N), np.nan)
     for b in range(B):
         for kv in range(Hkv):
             summ = CausalKeySummaries(K[b, :, kv, :], C)
-            for i in qs:
-                kept, sc, mg = select_unit_flat(Q[b, i, kv * G:(kv + 1) * G, :], i, summ, K_sel, s)
-                idx[b, kv, i, :len(kept)] = kept
-                score[b, kv, i, :] = NEG_INF
-                score[b, kv, i, :len(kept)] = sc
-                margin[b, kv, i] = mg
+            for un in range(kv * G // per, (kv + 1) * G // per):
+                for i in qs:
+                    kept, sc, mg = select_unit_flat(Q[b, i, un * per:(un + 1) * per, :], i, summ, K_sel, s)
+                    idx[b, un, i, :len(kept)] = kept
+                    score[b, un, i, :] = NEG_INF
+                    score[b, un, i, :len(kept)] = sc
+                    margin[b, un, i] = mg
     return dict(idx=idx, score=score, margin=margin)
 
 

@@ -40,7 +40,7 @@ class PisaError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")] + \
-               [("scale", ctypes.c_float)]
+               [("scale", ctypes.c_float), ("per_head", ctypes.c_int32)]
 
 
 class ProfileEntry(ctypes.Structure):
@@ -108,13 +108,18 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def make_shape(B, N, Hq, Hkv, d, C=64, K=16, g=2, qtile=1, scale=0.0) -> Shape:
-    return Shape(B, N, Hq, Hkv, d, C, K, g, qtile, float(scale))
+def make_shape(B, N, Hq, Hkv, d, C=64, K=16, g=2, qtile=1, scale=0.0, per_head=False) -> Shape:
+    return Shape(B, N, Hq, Hkv, d, C, K, g, qtile, float(scale), 1 if per_head else 0)
 
 
-def shape_of(Q: torch.Tensor, Kt: torch.Tensor, C=64, K=16, g=2, qtile=1, scale=0.0) -> Shape:
+def shape_of(Q: torch.Tensor, Kt: torch.Tensor, C=64, K=16, g=2, qtile=1, scale=0.0, per_head=False) -> Shape:
     B, N, Hq, d = Q.shape
-    return make_shape(B, N, Hq, Kt.shape[2], d, C, K, g, qtile, scale)
+    return make_shape(B, N, Hq, Kt.shape[2], d, C, K, g, qtile, scale, per_head)
+
+
+def _units(shape: Shape) -> int:
+    """Selection units per batch: the KV heads, or the query heads of a per-head selection."""
+    return shape.Hq if shape.per_head else shape.Hkv
 
 
 def pyramid_layout(shape: Shape):
@@ -159,9 +164,9 @@ def build_pyramid(Kt: torch.Tensor, shape: Shape, out: torch.Tensor | None = Non
 def _select_out(Q, shape, want_score, idx, score):
     dev = Q.device
     if idx is None:
-        idx = torch.empty(shape.B, shape.Hkv, shape.N, shape.K, dtype=torch.int32, device=dev)
+        idx = torch.empty(shape.B, _units(shape), shape.N, shape.K, dtype=torch.int32, device=dev)
     if score is None and want_score:
-        score = torch.empty(shape.B, shape.Hkv, shape.N, shape.K, dtype=torch.float32, device=dev)
+        score = torch.empty(shape.B, _units(shape), shape.N, shape.K, dtype=torch.float32, device=dev)
     return idx, score
 
 

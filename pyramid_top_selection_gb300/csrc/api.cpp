@@ -46,14 +46,16 @@ int check_common(int B, int N, int Hq, int Hkv, int d, int C, int K, int g) {
   const int G = Hq / Hkv;
   if (d != 64 && d != 128) return fail(PISA_EUNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
   if (C != 64) return fail(PISA_EUNSUPPORTED, "leaf block C=%d (supported: 64)", C);
-  if (g != 2) return fail(PISA_EUNSUPPORTED, "fan-out g=%d (supported: 2, the merge factor)", g);
+  if (g != 2 && g != 4)
+    return fail(PISA_EUNSUPPORTED, "fan-out g=%d (supported: 2, the merge factor, and 4, two levels per step)", g);
   if (K > 32) return fail(PISA_EUNSUPPORTED, "K=%d (supported: 1..32)", K);
+  if (g * K > 64) return fail(PISA_EUNSUPPORTED, "g*K=%d candidates (supported: at most 64)", g * K);
   if (G != 1 && G != 2 && G != 4 && G != 8)
     return fail(PISA_EUNSUPPORTED, "GQA group G=%d (supported: 1, 2, 4, 8)", G);
   if (N > (1 << 24)) return fail(PISA_EUNSUPPORTED, "N=%d exceeds 2^24", N);
-  const int64_t pairs = static_cast<int64_t>(B) * Hkv * N * 2 * K;
+  const int64_t pairs = static_cast<int64_t>(B) * Hkv * N * g * K;
   if (pairs >= (int64_t(1) << 31))
-    return fail(PISA_EUNSUPPORTED, "B*Hkv*N*2K=%lld exceeds 2^31", static_cast<long long>(pairs));
+    return fail(PISA_EUNSUPPORTED, "B*Hkv*N*gK=%lld exceeds 2^31", static_cast<long long>(pairs));
   const int64_t rows = static_cast<int64_t>(B) * N * Hq;   // TMA row coordinates are int32
   if (rows >= (int64_t(1) << 31))
     return fail(PISA_EUNSUPPORTED, "B*N*Hq=%lld exceeds 2^31", static_cast<long long>(rows));
@@ -64,6 +66,12 @@ int check_shape(const pisa_shape_t* s) {
   if (!s) return fail(PISA_EINVAL, "shape is NULL");
   PISA_CHECK(check_common(s->B, s->N, s->Hq, s->Hkv, s->d, s->C, s->K, s->g));
   if (s->qtile < 0) return fail(PISA_EINVAL, "qtile=%d is negative", s->qtile);
+  if (s->per_head != 0 && s->per_head != 1) return fail(PISA_EINVAL, "per_head=%d (0 or 1)", s->per_head);
+  if (s->per_head) {          // the units are the query heads
+    const int64_t pairs = static_cast<int64_t>(s->B) * s->Hq * s->N * s->g * s->K;
+    if (pairs >= (int64_t(1) << 31))
+      return fail(PISA_EUNSUPPORTED, "B*Hq*N*gK=%lld exceeds 2^31 (per-head selection)", static_cast<long long>(pairs));
+  }
   if (!(s->scale >= 0.f) || std::isinf(s->scale)) return fail(PISA_EINVAL, "scale must be finite and >= 0");
   return PISA_OK;
 }
@@ -74,7 +82,23 @@ pisa::Dims dims_of(const pisa_shape_t* s) {
   d.G = s->Hq / s->Hkv;
   d.n0 = (s->N + s->C - 1) / s->C;
   d.scale = s->scale > 0.f ? s->scale : 1.0f / std::sqrt(static_cast<float>(s->d));
+  d.Hkv_r = s->Hkv;
+  d.kvr = 1;
+  d.g = s->g;
+  if (s->per_head) {          // every query head a selection unit of its own
+    d.kvr = d.G;
+    d.Hkv = s->Hq;
+    d.G = 1;
+  }
   return d;
+}
+
+// The real (per KV head) view of a shape, for the pyramid build: the pyramid always belongs to
+// the KV heads.
+pisa::Dims kv_dims_of(const pisa_shape_t* s) {
+  pisa_shape_t r = *s;
+  r.per_head = 0;
+  return dims_of(&r);
 }
 
 pisa::Dims dims_of(const pisa_decode_shape_t* s) {
@@ -83,6 +107,9 @@ pisa::Dims dims_of(const pisa_decode_shape_t* s) {
   d.G = s->Hq / s->Hkv;
   d.n0 = (s->Ncap + s->C - 1) / s->C;
   d.scale = s->scale > 0.f ? s->scale : 1.0f / std::sqrt(static_cast<float>(s->d));
+  d.Hkv_r = s->Hkv;
+  d.kvr = 1;
+  d.g = s->g;
   return d;
 }
 
@@ -163,7 +190,7 @@ int pisa_build_pyramid(const pisa_shape_t* shape, const void* K, float* pyr_sum,
   PISA_CHECK(check_shape(shape));
   PISA_CHECK(check_ptr(K, "K"));
   PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
-  const pisa::Dims d = dims_of(shape);
+  const pisa::Dims d = kv_dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
   return cuda_rc(pisa::launch_build_pyramid(d, g, K, nullptr, d.N, pyr_sum, stream), "pisa_build_pyramid");
 }
@@ -232,6 +259,7 @@ int pisa_select_mean(const pisa_shape_t* shape, const void* Q, const void* K,
   PISA_CHECK(check_ptr(score, "score", true));
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
+  if (shape->g != 2) return fail(PISA_EUNSUPPORTED, "pisa_select_mean: fan-out g=%d (supported: 2)", shape->g);
   PISA_CHECK(check_ws(d, g, PISA_OP_SELECT_MEAN, ws, ws_bytes));
   return cuda_rc(pisa::launch_select_mean(d, g, Q, K, pyr_sum, idx, score, static_cast<char*>(ws), stream),
                  "pisa_select_mean");
@@ -246,6 +274,7 @@ int pisa_select_meanvar(const pisa_shape_t* shape, const void* Q, const void* K,
   PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
   PISA_CHECK(check_ptr(idx, "idx"));
   PISA_CHECK(check_ptr(score, "score", true));
+  if (shape->g != 2) return fail(PISA_EUNSUPPORTED, "pisa_select_meanvar: fan-out g=%d (supported: 2)", shape->g);
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
   PISA_CHECK(check_ws(d, g, PISA_OP_SELECT_MEANVAR, ws, ws_bytes));
@@ -289,6 +318,7 @@ int pisa_decode_pyramid_layout(const pisa_decode_shape_t* shape, int32_t* n_leve
                                int64_t* level_offset, int64_t* nodes_per_head) {
   if (!shape) return fail(PISA_EINVAL, "shape is NULL");
   PISA_CHECK(check_common(shape->B, shape->Ncap, shape->Hq, shape->Hkv, shape->d, shape->C, shape->K, shape->g));
+  if (shape->g != 2) return fail(PISA_EUNSUPPORTED, "decode: fan-out g=%d (supported: 2)", shape->g);
   return layout_out(pisa::make_geo(shape->Ncap, shape->C), n_levels, level_offset, nodes_per_head);
 }
 
@@ -296,6 +326,7 @@ int pisa_decode_build_pyramid(const pisa_decode_shape_t* shape, const void* Kcac
                               const int32_t* len, float* pyr_sum, void* stream) {
   if (!shape) return fail(PISA_EINVAL, "shape is NULL");
   PISA_CHECK(check_common(shape->B, shape->Ncap, shape->Hq, shape->Hkv, shape->d, shape->C, shape->K, shape->g));
+  if (shape->g != 2) return fail(PISA_EUNSUPPORTED, "decode: fan-out g=%d (supported: 2)", shape->g);
   PISA_CHECK(check_ptr(Kcache, "Kcache"));
   PISA_CHECK(check_ptr(len, "len"));
   PISA_CHECK(check_ptr(pyr_sum, "pyr_sum"));
@@ -311,6 +342,7 @@ int pisa_decode_step(const pisa_decode_shape_t* shape, const int32_t* pos, void*
                      void* stream) {
   if (!shape) return fail(PISA_EINVAL, "shape is NULL");
   PISA_CHECK(check_common(shape->B, shape->Ncap, shape->Hq, shape->Hkv, shape->d, shape->C, shape->K, shape->g));
+  if (shape->g != 2) return fail(PISA_EUNSUPPORTED, "decode: fan-out g=%d (supported: 2)", shape->g);
   if (!(shape->scale >= 0.f) || std::isinf(shape->scale)) return fail(PISA_EINVAL, "scale must be finite and >= 0");
   const void* in[] = {pos, Kcache, Vcache, pyr_sum, q, k_new, v_new, o, idx, status};
   const char* names[] = {"pos", "Kcache", "Vcache", "pyr_sum", "q", "k_new", "v_new", "o", "idx", "status"};

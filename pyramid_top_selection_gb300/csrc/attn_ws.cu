@@ -151,7 +151,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         const int lin = pt + kRows * u, key = lin % 64, c = lin / 64;
         const int64_t j = static_cast<int64_t>(v.kbase) + key;
         vreg[u] = make_uint4(0, 0, 0, 0);
-        if (j < s.N) vreg[u] = ldg_u4(a.V + ((static_cast<int64_t>(v.b) * s.N + j) * s.Hkv + v.kv) * D + c * 8);
+        if (j < s.N) vreg[u] = ldg_u4(a.V + ((static_cast<int64_t>(v.b) * s.N + j) * s.Hkv_r + v.kv / s.kvr) * D + c * 8);
       }
     };
     if (have) load_v(cur.v);
@@ -220,7 +220,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &k_full[ks]);
         k_issued = I + 1;
       };
       // S of tile T (cursor c, item number I)
@@ -448,9 +448,9 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   CUtensorMap km, om;
   const uint64_t d = static_cast<uint64_t>(s.d);
   {
-    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv), static_cast<uint64_t>(s.N),
+    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv_r), static_cast<uint64_t>(s.N),
                               static_cast<uint64_t>(s.B)};
-    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv, d * 2 * s.Hkv * s.N};
+    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv_r, d * 2 * s.Hkv_r * s.N};
     const uint32_t box[4] = {64, 1, 64, 1};
     if (int e = encode_tmap(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, strides, box)) return e;
   }

@@ -36,9 +36,14 @@ inline Geo make_geo(int64_t N, int C) {
 }
 
 // Plain-old-data view of a prefill shape with derived values, passed to kernels by value.
+// Selection units are (b, kv) with kv < Hkv and G query heads kv*G .. kv*G+G-1 each. With a
+// per-head selection every query head is a unit of its own: Hkv = Hq and G = 1 here, and the
+// keys, values and pyramid of unit kv are those of KV head kv / kvr of the Hkv_r real ones
+// (kvr = the real group size). Otherwise Hkv_r = Hkv and kvr = 1. g: candidate fan-out.
 struct Dims {
   int32_t B, N, Hq, Hkv, d, C, K, G, n0;
   float scale;
+  int32_t Hkv_r, kvr, g;
 };
 
 // Workspace carving for each op; every sub-buffer is 256-byte aligned.

@@ -176,7 +176,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv, v.kbase, v.b, &k_full[ks]);
+          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &k_full[ks]);
         k_issued = I + 1;
       };
       int T = 0, I = 0;
@@ -335,9 +335,9 @@ int leaf_tc_run(const Dims& s, const GroupPlan& gp, const void* Q, const void* K
   CUtensorMap km;
   {
     const uint64_t d = static_cast<uint64_t>(s.d);
-    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv), static_cast<uint64_t>(s.N),
+    const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv_r), static_cast<uint64_t>(s.N),
                               static_cast<uint64_t>(s.B)};
-    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv, d * 2 * s.Hkv * s.N};
+    const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv_r, d * 2 * s.Hkv_r * s.N};
     const uint32_t box[4] = {64, 1, 64, 1};
     if (int e = encode_tmap(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, strides, box)) return e;
   }

@@ -136,10 +136,15 @@ int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32
   return build_impl<64>(s, g, K, len, tokens_per_seq, pyr, st);
 }
 
-// Pyramid of per-dimension sums of squared keys (same layout and summation order).
+// Pyramid of per-dimension sums of squared keys (same layout and summation order), one per
+// real KV head also when the selection units are query heads.
 int launch_build_pyramid_sq(const Dims& s, const Geo& g, const void* K, float* sq, cudaStream_t st) {
-  if (s.d == 128) return build_impl<128, true>(s, g, K, nullptr, s.N, sq, st);
-  return build_impl<64, true>(s, g, K, nullptr, s.N, sq, st);
+  Dims k = s;
+  k.Hkv = s.Hkv_r;
+  k.G = s.Hq / s.Hkv_r;
+  k.kvr = 1;
+  if (s.d == 128) return build_impl<128, true>(k, g, K, nullptr, s.N, sq, st);
+  return build_impl<64, true>(k, g, K, nullptr, s.N, sq, st);
 }
 
 const char* cuda_error_string(int err) {

@@ -95,6 +95,25 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
   }
 }
 
+// Fan-out 4: the visible grandchildren 4a .. 4a+3 at the level below the next (node span
+// `span` tokens; visible when the first token is <= i) of the kept node `a` held by each lane
+// (-1: none), compacted in lane order into cand. Returns their number. A node's visible
+// grandchildren are a prefix of the four, so a lane's count tells them all.
+__device__ __forceinline__ int expand4(int a, int64_t span, int i, int* cand, unsigned ltm) {
+  int n = 0;
+  if (a >= 0)
+    for (int c = 0; c < 4; ++c) n += static_cast<int64_t>(4 * a + c) * span <= i ? 1 : 0;
+  int pos = 0, tot = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const unsigned m = __ballot_sync(0xffffffffu, n > c);
+    pos += __popc(m & ltm);
+    tot += __popc(m);
+  }
+  for (int c = 0; c < n; ++c) cand[pos + c] = 4 * a + c;
+  return tot;
+}
+
 // MC: the most candidates a level can hold (2K rounded up to 32 or 64); the smaller size lets
 // more CTAs share an SM. MEAN: the PISA-1 ablation -- every block, leaves included, is scored
 // by s q . (its causal key sum) / (its visible key count), summed over the G heads; the leaf
@@ -121,11 +140,12 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   const int b = blockIdx.z, kv = blockIdx.y;
   const int i = blockIdx.x * kWarps + warp;
   if (i >= s.N) return;                   // no block-wide barriers below
-  const int G = s.G, Ksel = s.K, C = s.C;
+  const int G = s.G, Ksel = s.K, C = s.C, W = s.g * s.K;
   const int ti = i / C;
   const int L = geo.n_levels;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
-  const uint4* spl_h = spl + head * geo.nodes * RQ;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;            // selection unit
+  const int kvk = kv / s.kvr;                                           // its KV head
+  const uint4* spl_h = spl + (static_cast<int64_t>(b) * s.Hkv_r + kvk) * geo.nodes * RQ;
 
   // q of the G heads as MMA B fragments (column n = head g; heads >= G are zero).
   uint32_t qb[KS][2];
@@ -148,8 +168,8 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     for (int mt = 0; mt * 16 < nkeys; ++mt) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const int r0 = mt * 16 + g, r1 = r0 + 8;
-      const __nv_bfloat16* k0 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r0) * s.Hkv + kv) * D;
-      const __nv_bfloat16* k1 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r1) * s.Hkv + kv) * D;
+      const __nv_bfloat16* k0 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r0) * s.Hkv_r + kvk) * D;
+      const __nv_bfloat16* k1 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r1) * s.Hkv_r + kvk) * D;
 #pragma unroll
       for (int kp = 0; kp < KS / 2; ++kp) {
         const uint4 x0 = r0 < nkeys ? ldg_u4(k0 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
@@ -219,12 +239,18 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   bool have_pdot = false;   // dots of the current candidates are known (previous level scored)
   int cur = 0;              // s_cdot buffer written by the previous scored level
   int* kslot = s_kslot[warp];
-  for (int lam = L - 2; lam >= 1; --lam) {
-    // candidates at level lam: visible children of the kept nodes of level lam+1; candidate
-    // 2k(+1) of kept node k records (kept slot, which child) for its parent dot
+  // Visited levels: L-1 (the top node), then one level down per step (g = 2) or two (g = 4,
+  // the candidates being the kept nodes' visible grandchildren), down to the leaves; the last
+  // step is one level when two would pass them. Intermediate levels are scored here.
+  const int step = s.g == 4 ? 2 : 1;
+  int lp = L - 1;
+  for (int lam = lp - step; lam >= 1; lp = lam, lam -= step) {
+    // candidates at level lam: visible children of the kept nodes of level lam+1 (g = 2: each
+    // records its kept slot and which child, for the parent-dot shortcut), or visible
+    // grandchildren of the kept nodes of level lam+2 (g = 4: both children scored directly)
     const int64_t span = static_cast<int64_t>(C) << lam;
     int nc;
-    {
+    if (step == 1) {
       const int a = lane < nkept ? kept[lane] : -1;
       const bool c0 = a >= 0;
       const bool c1 = a >= 0 && static_cast<int64_t>(2 * a + 1) * span <= i;
@@ -234,6 +260,9 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       if (c0) { cand[pos] = 2 * a; s_par[warp][pos] = lane * 2 + 0; }
       if (c1) { cand[pos + 1] = 2 * a + 1; s_par[warp][pos + 1] = lane * 2 + 1; }
       nc = __popc(m0) + __popc(m1);
+    } else {
+      nc = expand4(lane < nkept ? kept[lane] : -1, span, i, cand, ltm);
+      have_pdot = false;
     }
     __syncwarp();
     if (nc <= Ksel) {
@@ -345,12 +374,13 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     __syncwarp();
   }
 
-  // leaf candidates: visible children of the kept level-1 nodes (or the single leaf)
-  int32_t* out = cand_out + ((head * s.N) + i) * (2 * Ksel);
+  // leaf candidates: visible descendants of the kept level-lp nodes (children when lp = 1,
+  // grandchildren when lp = 2), or the single leaf
+  int32_t* out = cand_out + ((head * s.N) + i) * W;
   int nc = 1;
   if (L == 1) {
     if (lane == 0) cand[0] = 0;
-  } else {
+  } else if (lp == 1) {
     const int a = lane < nkept ? kept[lane] : -1;
     const bool c0 = a >= 0;
     const bool c1 = a >= 0 && static_cast<int64_t>(2 * a + 1) * C <= i;
@@ -360,6 +390,9 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     __syncwarp();
     if (c0) cand[pos] = 2 * a;
     if (c1) cand[pos + 1] = 2 * a + 1;
+  } else {
+    __syncwarp();
+    nc = expand4(lane < nkept ? kept[lane] : -1, static_cast<int64_t>(C), i, cand, ltm);
   }
   __syncwarp();
   if constexpr (MEAN) {
@@ -396,10 +429,10 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       if (p == 0 && csb < nc) sc[csb] = no_nan(pb);
     }
     __syncwarp();
-    float* outs = cscore_out + ((head * s.N) + i) * (2 * Ksel);
-    for (int q = lane; q < 2 * Ksel; q += 32) outs[q] = q < nc ? sc[q] : neg_inf();
+    float* outs = cscore_out + ((head * s.N) + i) * W;
+    for (int q = lane; q < W; q += 32) outs[q] = q < nc ? sc[q] : neg_inf();
   }
-  for (int q = lane; q < 2 * Ksel; q += 32) out[q] = q < nc ? cand[q] : -1;
+  for (int q = lane; q < W; q += 32) out[q] = q < nc ? cand[q] : -1;
 }
 
 // ---------------------------------------------------------------------------- finish
@@ -501,7 +534,8 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
   const int C = s.C, G = s.G;
   const int qbase = tq * C + warp * 16;
   if (qbase >= s.N) return;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;                       // selection unit
+  const int64_t head_k = static_cast<int64_t>(b) * s.Hkv_r + kv / s.kvr;           // its KV head
   const int i0 = qbase + g, i1 = qbase + g + 8;
   const bool ok0 = i0 < s.N, ok1 = i1 < s.N;
 
@@ -560,7 +594,7 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
   };
 
   const float inv_c = s.scale / static_cast<float>(C);
-  const uint4* spl0 = spl + (head * geo.nodes + geo.off[0]) * RQ;
+  const uint4* spl0 = spl + (head_k * geo.nodes + geo.off[0]) * RQ;
   for (int nt = 0; nt * 8 < tq; ++nt) {
     const int tl = nt * 8 + g;
     const bool vb = tl < tq;
@@ -595,7 +629,7 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
     for (int nt = 0; nt < 8; ++nt) {
       const int64_t j = kb + nt * 8 + g;
       const bool vk = j < s.N;
-      const __nv_bfloat16* kr = K + ((static_cast<int64_t>(b) * s.N + (vk ? j : 0)) * s.Hkv + kv) * D;
+      const __nv_bfloat16* kr = K + ((static_cast<int64_t>(b) * s.N + (vk ? j : 0)) * s.Hkv_r + kv / s.kvr) * D;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kp = 0; kp < KS / 2; ++kp) {
@@ -684,7 +718,7 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
 // 1.60 -> 1.53 ms at 64K, and fewer bins shorten the scans).
 GroupPlan leaf_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2;
-  return make_group_plan(s, 2 * s.K, (int64_t(64) << 20) / per_query, 4096 / s.G);
+  return make_group_plan(s, s.g * s.K, (int64_t(64) << 20) / per_query, 4096 / s.G);
 }
 
 inline int grid_for(int64_t n, int threads) {
@@ -710,10 +744,10 @@ int launch_topk(const Dims& s, int W, const int32_t* cand, const float* cscore, 
 SelectWs select_ws(const Dims& s, const Geo& g) {
   SelectWs w{};
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
-  const size_t W = 2 * static_cast<size_t>(s.K);
+  const size_t W = static_cast<size_t>(s.g) * s.K;
   size_t o = 0;
   w.status = o; o += 256;          // first: the caller finds the status word at offset 0
-  w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
+  w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
   w.mean_end = o;                  // the PISA-1 path needs nothing past here
@@ -726,11 +760,11 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
 }
 
 size_t flat_ws(const Dims& s, const Geo& g) {
-  return 256 + align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);   // status word, split rows
+  return 256 + align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);   // status word, split rows
 }
 
 int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cudaStream_t st) {
-  const int64_t n4 = static_cast<int64_t>(s.B) * s.Hkv * g.nodes * s.d / 4;
+  const int64_t n4 = static_cast<int64_t>(s.B) * s.Hkv_r * g.nodes * s.d / 4;
   ProfScope ps(st, "split_pyramid");
   split_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(pyr), spl, n4);
   return cudaGetLastError();
@@ -756,14 +790,14 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   route_kernel<DD, MM, false><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
                                                            static_cast<const __nv_bfloat16*>(K), spl, cand, nullptr)
   if (s.d == 128) {
-    if (2 * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
+    if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
   } else {
-    if (2 * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
+    if (s.g * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
   }
 #undef PISA_ROUTE
   }
   if ((err = cudaGetLastError())) return err;
-  const int W = 2 * s.K;
+  const int W = s.g * s.K;
   if ((err = launch_group_items(gp, cand, ws, gw, st))) return err;
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + gw.list);
   const int4* items = reinterpret_cast<const int4*>(ws + gw.items);
@@ -800,9 +834,9 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   route_kernel<DD, MM, true><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
                                                           static_cast<const __nv_bfloat16*>(K), spl, cand, cscore)
     if (s.d == 128) {
-      if (2 * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
+      if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
     } else {
-      if (2 * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
+      if (s.g * s.K <= 32) PISA_ROUTE(64, 32); else PISA_ROUTE(64, 64);
     }
 #undef PISA_ROUTE
   }
@@ -811,7 +845,7 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   {
     ProfScope ps(st, "topk");
     topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, 2 * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr,
+        units, s.g * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr,
         reinterpret_cast<const int32_t*>(ws + w.status));
   }
   return cudaGetLastError();

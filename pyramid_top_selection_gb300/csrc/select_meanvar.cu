@@ -50,9 +50,10 @@ meanvar_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_
   if (i >= s.N) return;                       // no block-wide barriers below
   const int G = s.G, Ksel = s.K, C = s.C, L = geo.n_levels;
   const int ti = i / C;
-  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
-  const float* pyr_h = pyr + head * geo.nodes * D;
-  const float* sq_h = sqp + head * geo.nodes * D;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;                       // selection unit
+  const int64_t head_k = static_cast<int64_t>(b) * s.Hkv_r + kv / s.kvr;           // its KV head
+  const float* pyr_h = pyr + head_k * geo.nodes * D;
+  const float* sq_h = sqp + head_k * geo.nodes * D;
   float* pre = smv + static_cast<size_t>(warp) * L * 2 * D;
   const int d0 = lane * E;
 
@@ -76,7 +77,7 @@ meanvar_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_
 #pragma unroll
     for (int e = 0; e < E; ++e) ps[e] = pq[e] = 0.f;
     for (int64_t j = static_cast<int64_t>(ti) * C; j <= i; ++j) {
-      const __nv_bfloat16* kr = Kt + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + d0;
+      const __nv_bfloat16* kr = Kt + ((static_cast<int64_t>(b) * s.N + j) * s.Hkv_r + kv / s.kvr) * D + d0;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const float x = __bfloat162float(kr[e]);
@@ -197,7 +198,7 @@ MeanVarWs meanvar_ws_of(const Dims& s, const Geo& g) {
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   size_t o = 0;
   w.status = o; o += 256;
-  w.sq = o;     o += align256(static_cast<size_t>(s.B) * s.Hkv * g.nodes * s.d * 4);
+  w.sq = o;     o += align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);
   w.cand = o;   o += align256(units * 2 * s.K * 4);
   w.cscore = o; o += align256(units * 2 * s.K * 4);
   w.total = o;

@@ -51,7 +51,7 @@ def test_host_validation_before_any_cuda_call():
     cases = [
         (pisa.make_shape(1, 4096, 4, 1, 96, 64, 8), _pisa.PISA_EUNSUPPORTED, "head dim"),
         (pisa.make_shape(1, 4096, 4, 1, 64, 32, 8), _pisa.PISA_EUNSUPPORTED, "leaf block"),
-        (pisa.make_shape(1, 4096, 4, 1, 64, 64, 8, g=4), _pisa.PISA_EUNSUPPORTED, "fan-out"),
+        (pisa.make_shape(1, 4096, 4, 1, 64, 64, 8, g=3), _pisa.PISA_EUNSUPPORTED, "fan-out"),
         (pisa.make_shape(1, 4096, 4, 1, 64, 64, 33), _pisa.PISA_EUNSUPPORTED, "K=33"),
         (pisa.make_shape(1, 4096, 6, 4, 64, 64, 8), _pisa.PISA_EINVAL, "multiple"),
         (pisa.make_shape(1, 4096, 32, 1, 64, 64, 8), _pisa.PISA_EUNSUPPORTED, "GQA group"),
@@ -95,6 +95,27 @@ def test_host_validation_before_any_cuda_call():
     assert rc == _pisa.PISA_EINVAL and "status" in msg
     rc, msg = _rc(L.pisa_workspace_size, ctypes.byref(good), 7, ctypes.byref(ctypes.c_size_t()))
     assert rc == _pisa.PISA_EINVAL
+    # fan-out 4: at most 64 candidates, and only where a descent is built for it
+    rc, msg = _rc(L.pisa_select, ctypes.byref(pisa.make_shape(1, 4096, 4, 1, 64, 64, 17, g=4)), A, A, A, A,
+                  None, None, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EUNSUPPORTED and "g*K" in msg
+    g4 = pisa.make_shape(1, 4096, 4, 1, 64, 64, 16, g=4)
+    rc, msg = _rc(L.pisa_select_mean, ctypes.byref(g4), A, A, A, A, None, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EUNSUPPORTED and "fan-out" in msg
+    rc, msg = _rc(L.pisa_select_meanvar, ctypes.byref(g4), A, A, A, A, None, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EUNSUPPORTED and "fan-out" in msg
+    rc, msg = _rc(L.pisa_decode_step, ctypes.byref(pisa.make_decode_shape(2, 1000, 8, 2, 128, 64, 8, g=4)),
+                  A, A, A, A, A, A, A, A, A, None, A, None)
+    assert rc == _pisa.PISA_EUNSUPPORTED and "fan-out" in msg
+    bad = pisa.make_shape(1, 4096, 4, 1, 64, 64, 8)
+    bad.per_head = 2
+    rc, msg = _rc(L.pisa_select, ctypes.byref(bad), A, A, A, A, None, None, A, 1 << 40, None)
+    assert rc == _pisa.PISA_EINVAL and "per_head" in msg
+    # a per-head selection has Hq units: its workspace grows with Hq, its pyramid does not
+    ph = pisa.make_shape(1, 4096, 8, 2, 64, 64, 8, per_head=True)
+    sh = pisa.make_shape(1, 4096, 8, 2, 64, 64, 8)
+    assert pisa.workspace_size(ph, _pisa.OP_SELECT) > pisa.workspace_size(sh, _pisa.OP_SELECT)
+    assert pisa.pyramid_layout(ph) == pisa.pyramid_layout(sh)
     # the wait limit and the test stall are host-only settings: no CUDA call, always accepted
     assert L.pisa_set_wait_limit(5_000_000) == _pisa.PISA_OK and L.pisa_set_wait_limit(0) == _pisa.PISA_OK
     assert L.pisa_test_stall(1) == _pisa.PISA_OK and L.pisa_test_stall(0) == _pisa.PISA_OK

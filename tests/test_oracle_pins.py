@@ -840,3 +840,17 @@ def test_per_head_attention_and_backward():
         s0, e0 = po.node_range(0, t, C, N)
         np.testing.assert_allclose(sk[(b, kv, t)], dK[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(sv[(b, kv, t)], dV[b, s0:e0, kv], rtol=1e-12, atol=1e-13)
+
+
+def test_per_head_flat_mean_meanvar_decompose_into_single_head_problems():
+    # a per-head selection of head h is the shared selection of the one-head problem (q_h, its KV head)
+    N, C, Ksel, Hq, Hkv, d = 96, 8, 3, 4, 2, 6
+    Q = _rand((1, N, Hq, d), 600)
+    K = _rand((1, N, Hkv, d), 601)
+    qs = [5, 40, 95]
+    for fn in (po.select_flat, po.select_mean, po.select_meanvar, po.select):
+        per = fn(Q, K, C, Ksel, queries=qs, per_head=True)
+        for h in range(Hq):
+            one = fn(Q[:, :, h:h + 1], K[:, :, h // 2:h // 2 + 1], C, Ksel, queries=qs)
+            np.testing.assert_array_equal(per["idx"][0, h, qs], one["idx"][0, 0, qs])
+            np.testing.assert_allclose(per["score"][0, h, qs], one["score"][0, 0, qs], rtol=0, atol=0)
