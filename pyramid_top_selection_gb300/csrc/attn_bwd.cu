@@ -25,6 +25,10 @@
 namespace pisa {
 
 size_t align256(size_t x);
+int launch_attn_bwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
+                       const void* dO, const float* lse, const float* delta, const int32_t* list,
+                       const int4* items, const int32_t* n_items, float* dq_acc, float* dk_acc, float* dv_acc,
+                       int32_t* status, cudaStream_t st);
 
 namespace {
 
@@ -108,7 +112,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     const int64_t j = static_cast<int64_t>(kbase) + r;
     uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
     if (j < s.N && beg < end) {
-      const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D + c * 8;
+      const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv_r + kv / s.kvr) * D + c * 8;
       kk = ldg_u4(K + o);
       vv = ldg_u4(V + o);
     }
@@ -308,7 +312,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   for (int half = 0; half < 2; ++half) {
     const int64_t j = static_cast<int64_t>(kbase) + key0 + g + 8 * half;
     if (j >= s.N) continue;
-    const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv + kv) * D;
+    const int64_t o = ((static_cast<int64_t>(b) * s.N + j) * s.Hkv_r + kv / s.kvr) * D;
 #pragma unroll
     for (int nd = 0; nd < ND; ++nd) {
       atomicAdd(reinterpret_cast<float2*>(dk_acc + o + nd * 8 + 2 * p), make_float2(dk[nd][2 * half], dk[nd][2 * half + 1]));
@@ -317,12 +321,20 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   }
 }
 
-// dK = bf16(s * dK_acc), dV = bf16(dV_acc), 8 elements per thread.
+constexpr uint32_t kNaN2 = 0x7fc07fc0u;   // two bf16 NaNs
+
+// dK = bf16(s * dK_acc), dV = bf16(dV_acc), 8 elements per thread; NaN everywhere when the
+// status word reports a bounded wait that gave up (the accumulators are then incomplete).
 __global__ void dkdv_convert_kernel(int64_t n8, float scale, const float4* __restrict__ dk_acc,
                                     const float4* __restrict__ dv_acc, uint4* __restrict__ dK,
-                                    uint4* __restrict__ dV) {
+                                    uint4* __restrict__ dV, const int32_t* __restrict__ status) {
+  const bool poison = (*status & PISA_STATUS_TIMEOUT) != 0;
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (poison) {
+      dK[q] = dV[q] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+      continue;
+    }
     const float4 a = dk_acc[2 * q], c = dk_acc[2 * q + 1], e = dv_acc[2 * q], f = dv_acc[2 * q + 1];
     dK[q] = make_uint4(pack_bf16(scale * a.x, scale * a.y), pack_bf16(scale * a.z, scale * a.w),
                        pack_bf16(scale * c.x, scale * c.y), pack_bf16(scale * c.z, scale * c.w));
@@ -330,10 +342,16 @@ __global__ void dkdv_convert_kernel(int64_t n8, float scale, const float4* __res
   }
 }
 
-// dQ = bf16(dQ_acc), 8 elements per thread.
-__global__ void dq_convert_kernel(int64_t n8, const float4* __restrict__ dq_acc, uint4* __restrict__ dQ) {
+// dQ = bf16(dQ_acc), 8 elements per thread (NaN when the status word reports a timeout).
+__global__ void dq_convert_kernel(int64_t n8, const float4* __restrict__ dq_acc, uint4* __restrict__ dQ,
+                                  const int32_t* __restrict__ status) {
+  const bool poison = (*status & PISA_STATUS_TIMEOUT) != 0;
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (poison) {
+      dQ[q] = make_uint4(kNaN2, kNaN2, kNaN2, kNaN2);
+      continue;
+    }
     const float4 a = dq_acc[2 * q], c = dq_acc[2 * q + 1];
     dQ[q] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
   }
@@ -380,7 +398,7 @@ GroupPlan bwd_plan(const Dims& s) {
 AttnBwdWs attn_bwd_ws(const Dims& s) {
   AttnBwdWs w{};
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
-  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
+  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv_r * s.d;
   w.status = 0;                         // first: the caller finds the status word at offset 0
   size_t o = group_ws(bwd_plan(s), 256).end;
   w.delta = o;   o += align256(rows * 4);
@@ -402,7 +420,7 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   float* dqa = reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
   float* dv_acc = reinterpret_cast<float*>(ws + w.dv_acc);
-  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv * s.d;
+  const size_t kvel = static_cast<size_t>(s.B) * s.N * s.Hkv_r * s.d;
   int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;
   cudaError_t e = cudaMemsetAsync(ws + w.status, 0, 256, st);
@@ -425,7 +443,9 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
   const int32_t* list = reinterpret_cast<const int32_t*>(ws + g.list);
   const int4* items = reinterpret_cast<const int4*>(ws + g.items);
   const int32_t* n_items = reinterpret_cast<const int32_t*>(ws + g.icount) + gp.bins;
-  err = s.d == 128 ? bwd_dispatch<128>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st)
+  // d = 128 on the tensor-core kernel (attn_bwd_tc.cu); d = 64 on the warp-MMA kernel above
+  err = s.d == 128 ? launch_attn_bwd_tc(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc,
+                                        reinterpret_cast<int32_t*>(ws + w.status), st)
                    : bwd_dispatch<64>(s, gp, Q, K, V, dO, lse, delta, list, items, n_items, dqa, dk_acc, dv_acc, st);
   if (err) return err;
   {
@@ -434,14 +454,15 @@ int launch_attn_bwd(const Dims& s, const void* Q, const void* K, const void* V, 
     const int64_t nb = (n8 + 255) / 256;
     dkdv_convert_kernel<<<static_cast<unsigned>(nb < 152 * 32 ? nb : 152 * 32), 256, 0, st>>>(
         n8, s.scale, reinterpret_cast<const float4*>(dk_acc), reinterpret_cast<const float4*>(dv_acc),
-        static_cast<uint4*>(dK), static_cast<uint4*>(dV));
+        static_cast<uint4*>(dK), static_cast<uint4*>(dV), reinterpret_cast<const int32_t*>(ws + w.status));
   }
   {
     ProfScope ps(st, "attn_bwd_dq");
     const int64_t n8 = rows * s.d / 8;
     const int64_t nb = (n8 + 255) / 256;
     dq_convert_kernel<<<static_cast<unsigned>(nb < 152 * 32 ? nb : 152 * 32), 256, 0, st>>>(
-        n8, reinterpret_cast<const float4*>(dqa), static_cast<uint4*>(dQ));
+        n8, reinterpret_cast<const float4*>(dqa), static_cast<uint4*>(dQ),
+        reinterpret_cast<const int32_t*>(ws + w.status));
   }
   return cudaGetLastError();
 }

@@ -34,6 +34,24 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory matrix descriptor of an MN-major operand (the M or N dimension contiguous),
+// 128-byte swizzle: an atom is 8 rows of the contraction dimension, each 64 MN elements
+// (128 B), 1024 B in all; atoms follow one another along the contraction dimension (stride
+// 1024 B) and 64-element MN chunks lie `mn_stride` bytes apart. A k-step of 16 moves the start
+// address by 16 rows (2048 B).
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t mn_stride) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M x N; a_mn / b_mn mark
+// an MN-major A / B (transposed relative to the K-major default).
+__host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |

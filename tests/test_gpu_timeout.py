@@ -62,6 +62,13 @@ def test_wait_that_runs_out_is_reported_and_poisons_outputs(stalled):
     st = pisa.workspace_status(ws_a)
     assert st & pisa.STATUS_TIMEOUT, st
     assert bool(O.isnan().all()) and bool(lse.isnan().all())
+    # attention backward (the tensor-core kernel, d = 128)
+    dO = syn.make_grad_out(*Q.shape[:3], Q.shape[3], seed=4).cuda()
+    ws_b = pisa.workspace(shape, _pisa.OP_ATTN_BWD, Q.device)
+    dQ, dK, dV = pisa.sparse_attn_bwd(Q, Kt, V, O0, lse0, dO, idx0, shape, ws=ws_b)
+    st = pisa.workspace_status(ws_b)
+    assert st & pisa.STATUS_TIMEOUT, st
+    assert bool(dQ.isnan().all()) and bool(dK.isnan().all()) and bool(dV.isnan().all())
     # the context is intact: the same calls run normally again and reproduce the results
     pisa.set_test_stall(False)
     pisa.set_wait_limit(0)
@@ -70,3 +77,6 @@ def test_wait_that_runs_out_is_reported_and_poisons_outputs(stalled):
     assert torch.equal(lse1, lse0)
     # block contributions are added in a run-dependent order: equal up to fp32 rounding
     torch.testing.assert_close(O1.float(), O0.float(), atol=1e-2, rtol=1e-2)
+    dQ1, dK1, dV1 = pisa.sparse_attn_bwd(Q, Kt, V, O0, lse0, dO, idx0, shape, ws=ws_b)
+    assert pisa.workspace_status(ws_b) == 0
+    assert not (dQ1.isnan().any() or dK1.isnan().any() or dV1.isnan().any())
