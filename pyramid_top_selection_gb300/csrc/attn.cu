@@ -25,13 +25,19 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
 
 namespace {
 
-// Query chunks of about 128 MiB of one KV head's fp32 accumulator rows (G heads x d): the
-// items running at one time add into one chunk's rows, and items are long enough that the
-// per-item start (keys, V^T) is paid rarely; at most 512 queries per work item (measured
-// best with the dynamic item order; 16-64 MiB chunks and 1024-2048 caps were slower).
+// Query chunks of about 48 MiB of one KV head's fp32 accumulator rows (G heads x d): the
+// items running at one time add into one chunk's rows, which then stay in L2 (128 MiB chunks
+// spilled them to HBM: 2.13 ms per launch at the 64K workload against 1.66 ms at 48 MiB and
+// 1.67 ms at 32 MiB); at most 512 queries per work item (1024 measured slower).
+#ifndef PISA_FWD_CHUNK_MIB
+#define PISA_FWD_CHUNK_MIB 48
+#endif
+#ifndef PISA_FWD_ITEM_CAP
+#define PISA_FWD_ITEM_CAP 512
+#endif
 GroupPlan fwd_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 4;
-  return make_group_plan(s, s.K, (int64_t(128) << 20) / per_query, 512);
+  return make_group_plan(s, s.K, (int64_t(PISA_FWD_CHUNK_MIB) << 20) / per_query, PISA_FWD_ITEM_CAP);
 }
 
 }  // namespace

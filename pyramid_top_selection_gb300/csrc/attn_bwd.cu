@@ -388,9 +388,15 @@ int bwd_dispatch(const Dims& s, const GroupPlan& gp, const void* Q, const void* 
 
 // Query chunks of about 16 MiB of one head's Q and dO rows (their fp32 dQ rows stay in L2);
 // about 4096 (query, head) rows per work item.
+#ifndef PISA_BWD_CHUNK_MIB
+#define PISA_BWD_CHUNK_MIB 16
+#endif
+#ifndef PISA_BWD_ITEM_ROWS
+#define PISA_BWD_ITEM_ROWS 4096
+#endif
 GroupPlan bwd_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2 * 2;
-  return make_group_plan(s, s.K, (int64_t(16) << 20) / per_query, 4096 / s.G);
+  return make_group_plan(s, s.K, (int64_t(PISA_BWD_CHUNK_MIB) << 20) / per_query, PISA_BWD_ITEM_ROWS / s.G);
 }
 
 }  // namespace

@@ -112,32 +112,52 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
     }
   }
 
-  // gather of tile j into buffer bf: thread copies 16-byte chunk (tid & 15) of rows
-  // (tid >> 4) + 16u; threads < 128 also load row tid's metadata
-  auto gather = [&](int j, int bf) {
-    const int c = tid & 15;
-#pragma unroll 2
+  // A tile's list entries, loaded one tile ahead of its gather: entries of the thread's 8
+  // gather rows ((tid >> 4) + 16u) and, for threads < 128, of metadata row tid.
+  struct Entries {
+    int pk[8];
+    int mpk;
+  };
+  auto load_entries = [&](int j, Entries& en) {
+#pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int r = (tid >> 4) + 16 * u, e = j * EPT + r / G;
-      const int pk = e < v.n_ent ? a.src.list[v.beg + e] : -1;
+      const int e = j * EPT + ((tid >> 4) + 16 * u) / G;
+      en.pk[u] = e < v.n_ent ? a.src.list[v.beg + e] : -1;
+    }
+    const int e = j * EPT + (tid & (kRows - 1)) / G;
+    en.mpk = tid < kRows && e < v.n_ent ? a.src.list[v.beg + e] : -1;
+  };
+  // gather of a tile into buffer bf: the thread copies 16-byte chunk (tid & 15) of its rows
+  auto gather = [&](const Entries& en, int bf) {
+    const int c = tid & 15;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = (tid >> 4) + 16 * u, pk = en.pk[u];
       const int64_t row = (static_cast<int64_t>(v.b) * s.N + (pk < 0 ? 0 : (pk >> 6))) * s.Hq + v.kv * G + r % G;
       const uint32_t off = bf * L::TILE + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8);
       tc::cp_async16(aQ + off, a.Q + row * kD + c * 8, pk >= 0);
       tc::cp_async16(adO + off, a.dO + row * kD + c * 8, pk >= 0);
     }
     tc::cp_async_commit();
+  };
+  // metadata of row tid (threads < 128): lse * log2e, D, query (-1: padding); loaded into
+  // registers when the tile's gather is issued, stored to shared memory a phase later
+  float ml2 = 0.f, mD = 0.f;
+  int mqi = -1;
+  auto meta_load = [&](const Entries& en) {
+    const int h = tid % G;
+    mqi = en.mpk < 0 ? -1 : (en.mpk >> 6);
+    ml2 = mD = 0.f;
+    if (mqi >= 0) {
+      ml2 = a.lse[(static_cast<int64_t>(v.b) * s.Hq + v.kv * G + h) * s.N + mqi] * kLog2e;
+      mD = a.delta[(static_cast<int64_t>(v.b) * s.N + mqi) * s.Hq + v.kv * G + h];
+    }
+  };
+  auto meta_store = [&](int bf) {
     if (tid < kRows) {
-      const int r = tid, e = j * EPT + r / G, h = r % G;
-      const int pk = e < v.n_ent ? a.src.list[v.beg + e] : -1;
-      const int qi = pk < 0 ? -1 : (pk >> 6);
-      float l2 = 0.f, D = 0.f;
-      if (qi >= 0) {
-        l2 = a.lse[(static_cast<int64_t>(v.b) * s.Hq + v.kv * G + h) * s.N + qi] * kLog2e;
-        D = a.delta[(static_cast<int64_t>(v.b) * s.N + qi) * s.Hq + v.kv * G + h];
-      }
-      m_lse2[bf][r] = l2;
-      m_D[bf][r] = D;
-      m_qi[bf][r] = qi;
+      m_lse2[bf][tid] = ml2;
+      m_D[bf][tid] = mD;
+      m_qi[bf][tid] = mqi;
     }
   };
 
@@ -155,19 +175,56 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
     mma_phase ^= 1;
     return w;
   };
+  // dQ of the previous tile, row r, columns 64 hf .. 64 hf + 63 (scaled by s), and its query
+  float dqr[2][32];
+  int dq_qi = -1;
+  // the previous tile's dQ into the fp32 accumulator: two rounds of 32 columns per thread half,
+  // staged in the P and dS tiles (free once that tile's MMAs completed), one TMA reduce-add per
+  // query (its G rows) and staging buffer
+  auto dq_out = [&]() {
+    const bool issuer = dq_qi >= 0 && r % G == 0;
+    const int unit = (v.b * s.N + (dq_qi < 0 ? 0 : dq_qi)) * s.Hkv + v.kv;
+    const uint32_t stg_a = hf == 0 ? aP : adS;
+    unsigned char* stg = sm + (hf == 0 ? L::oP : L::odS);
+#pragma unroll
+    for (int rd = 0; rd < 2; ++rd) {
+      const float* x = dqr[rd];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_float4(s.scale * x[4 * c], s.scale * x[4 * c + 1], s.scale * x[4 * c + 2], s.scale * x[4 * c + 3]);
+      tc::fence_async_smem();
+      __syncthreads();
+      if (issuer) {
+        tc::tma_reduce_add3(&qmap, 64 * hf + 32 * rd, 0, unit, stg_a + r * 128);
+        tc::bulk_commit();
+        tc::bulk_wait_read<0>();
+      }
+      __syncthreads();
+    }
+  };
 
-  if (n_tiles > 0) gather(0, 0);
+  Entries ent;
+  if (n_tiles > 0) {
+    load_entries(0, ent);
+    gather(ent, 0);
+    meta_load(ent);
+    meta_store(0);
+    if (n_tiles > 1) load_entries(1, ent);
+  }
   for (int j = 0; j < n_tiles; ++j) {
     const int bf = j & 1;
     if (j + 1 < n_tiles) {
-      gather(j + 1, bf ^ 1);                      // buffer bf ^ 1: tile j - 1's MMAs are complete
+      gather(ent, bf ^ 1);                        // buffer bf ^ 1: tile j - 1's MMAs are complete
+      meta_load(ent);                             // in flight; stored below
+      if (j + 2 < n_tiles) load_entries(j + 2, ent);
       tc::cp_async_wait<1>();
     } else {
       tc::cp_async_wait<0>();
     }
     tc::fence_async_smem();                       // the copies land in the async proxy's view
     __syncthreads();
-    // S and dP
+    // S and dP of tile j
     if (tid == 0) {
       if (!kv_landed) {
         kv_landed = tc::bar_wait(&kv_bar, 0, a.wait_ns);
@@ -188,6 +245,8 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
       }
     }
     if (!__syncthreads_and(ok)) break;
+    // meanwhile, the previous tile's dQ leaves through the P/dS tiles
+    if (j > 0) dq_out();
     ok = wait_mma();
     if (!__syncthreads_and(ok)) break;
     tc::after_sync();
@@ -199,11 +258,17 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
       const int qi = m_qi[bf][r];
       const int lim = qi < 0 ? -1 : qi - v.kbase - 32 * hf;   // key c of the half visible iff c <= lim
       const float l2 = m_lse2[bf][r], D = m_D[bf][r];
+      const uint64_t cc = tc::pack2(c1, c1), ll = tc::pack2(-l2, -l2), dd = tc::pack2(-D, -D);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p = c <= lim ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
-        sv[c] = p;
-        dp[c] = p * (dp[c] - D);
+      for (int c = 0; c < 32; c += 2) {           // packed pairs: exponent arguments, dP - D, P (dP - D)
+        float y0, y1, e0, e1;
+        tc::unpack2(tc::fma2(tc::pack2(sv[c], sv[c + 1]), cc, ll), y0, y1);
+        const float p0 = c <= lim ? tc::ex2(y0) : 0.f, p1 = c + 1 <= lim ? tc::ex2(y1) : 0.f;
+        sv[c] = p0;
+        sv[c + 1] = p1;
+        tc::unpack2(tc::add2(tc::pack2(dp[c], dp[c + 1]), dd), e0, e1);
+        dp[c] = p0 * e0;
+        dp[c + 1] = p1 * e1;
       }
       unsigned char* pt = sm + L::oP;
       unsigned char* st = sm + L::odS;
@@ -217,6 +282,7 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
             make_uint4(pack_bf16(dp[cc * 8 + 0], dp[cc * 8 + 1]), pack_bf16(dp[cc * 8 + 2], dp[cc * 8 + 3]),
                        pack_bf16(dp[cc * 8 + 4], dp[cc * 8 + 5]), pack_bf16(dp[cc * 8 + 6], dp[cc * 8 + 7]));
       }
+      dq_qi = qi;                                 // this tile's query of row r, for its dQ
     }
     tc::fence_async_smem();
     tc::before_sync();
@@ -236,40 +302,15 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
         tc::mma(tm + kColDQ, tc::desc(adS + k * 32), tc::desc_mn(aK + k * 2048, 64 * 128), idQ, k > 0);
       tc::commit(&mma_bar);
     }
+    if (j + 1 < n_tiles) meta_store(bf ^ 1);      // the next tile's metadata (loads issued above)
     ok = wait_mma();
     if (!__syncthreads_and(ok)) break;
     tc::after_sync();
-    // dQ of row r, columns 64 hf .. 64 hf + 63, scaled by s; added in four rounds of 32
-    // columns through one staging tile, one TMA reduce-add per query (its G rows)
-    {
-      float dq[2][32];
-      tc::tmem_ld32(tm + kColDQ + 64 * hf + lane_off, dq[0]);
-      tc::tmem_ld32(tm + kColDQ + 64 * hf + 32 + lane_off, dq[1]);
-      const int qi = m_qi[bf][r];
-      const bool issuer = qi >= 0 && r % G == 0;
-      const int unit = (v.b * s.N + (qi < 0 ? 0 : qi)) * s.Hkv + v.kv;
-      unsigned char* stg = sm + L::oS;
-#pragma unroll 1
-      for (int rd = 0; rd < 4; ++rd) {
-        if ((rd >> 1) == hf) {
-          const float* x = dq[rd & 1];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
-                make_float4(s.scale * x[4 * c], s.scale * x[4 * c + 1], s.scale * x[4 * c + 2], s.scale * x[4 * c + 3]);
-          tc::fence_async_smem();
-        }
-        __syncthreads();
-        if ((rd >> 1) == hf && issuer) {
-          tc::tma_reduce_add3(&qmap, 32 * rd, 0, unit, aS + r * 128);
-          tc::bulk_commit();
-          tc::bulk_wait_read<0>();
-        }
-        __syncthreads();
-      }
-    }
+    tc::tmem_ld32(tm + kColDQ + 64 * hf + lane_off, dqr[0]);
+    tc::tmem_ld32(tm + kColDQ + 64 * hf + 32 + lane_off, dqr[1]);
     tc::before_sync();
   }
+  if (__syncthreads_and(ok) && n_tiles > 0) dq_out();   // the last tile's dQ
   // every thread takes the same branch below (a loop left early leaves per-thread flags apart)
   const bool all_ok = __syncthreads_and(ok);
   // the item's dK and dV columns: warps 0-3 read dV^T, warps 4-7 dK^T (thread = dimension)
@@ -281,12 +322,14 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
     tc::tmem_ld32(tm + col + 32 + lane_off, x[1]);
     float* acc = warp < 4 ? a.dv_acc : a.dk_acc;
     const int dim = (warp & 3) * 32 + lane;
-#pragma unroll 4
-    for (int c = 0; c < 64; ++c) {
-      const int64_t jk = static_cast<int64_t>(v.kbase) + c;
-      if (jk < s.N)
-        atomicAdd(acc + ((static_cast<int64_t>(v.b) * s.N + jk) * s.Hkv_r + kvk) * kD + dim, x[c >> 5][c & 31]);
-    }
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int64_t jk = static_cast<int64_t>(v.kbase) + 32 * h2 + c;
+        if (jk < s.N)
+          atomicAdd(acc + ((static_cast<int64_t>(v.b) * s.N + jk) * s.Hkv_r + kvk) * kD + dim, x[h2][c]);
+      }
   }
   // drain what was issued, then free the tensor memory
   tc::cp_async_wait<0>();

@@ -338,8 +338,14 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
           tc::bar_arrive(&s_empty[sg]);
         }
         const int lh = lim - 32 * half;
+        const uint64_t cc = tc::pack2(c1, c1), ll = tc::pack2(-l2, -l2);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = c <= lh ? tc::ex2(fmaf(sv[c], c1, -l2)) : 0.f;
+        for (int c = 0; c < 32; c += 2) {         // exponent arguments on packed pairs
+          float y0, y1;
+          tc::unpack2(tc::fma2(tc::pack2(sv[c], sv[c + 1]), cc, ll), y0, y1);
+          sv[c] = c <= lh ? tc::ex2(y0) : 0.f;
+          sv[c + 1] = c + 1 <= lh ? tc::ex2(y1) : 0.f;
+        }
         if (half == 0) {
           const bool ok2 = wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, ok2)) {

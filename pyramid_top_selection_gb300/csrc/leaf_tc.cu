@@ -10,18 +10,18 @@
 // rows that have it among their candidates) from a global counter through its item queue
 // (tiles.cuh) and walks them in tiles of 128 rows. Roles, connected by mbarrier rings so
 // that no role waits on another's latency:
-//   * producers (warps 8-11, 32 tile rows per warp): gather the query vectors with cp.async
+//   * producers (4 warps after the softmax ones, 32 tile rows each): gather the query vectors with cp.async
 //     into a 4-stage ring of swizzled Q tiles, each warp instruction copying whole rows
 //     (full 32-byte sectors); a thread confirms a tile's copies (wait, proxy fence,
 //     arrival) once it has issued the next tile;
-//   * control (warp 12, one thread): loads each item's 64 keys by TMA into a 2-stage ring
+//   * control (the next warp, one thread): loads each item's 64 keys by TMA into a 2-stage ring
 //     (the next item's while the current one runs) and issues S = Q K^T (M=128, N=64) as
 //     tcgen05.mma into a 4-stage ring of TMEM accumulators;
-//   * softmax (two warpgroups, warps 0-3 and 4-7, on alternate tiles; thread = TMEM lane =
+//   * softmax (two warpgroups, warps 0-7, taking the tiles in turn; thread = TMEM lane =
 //     tile row): reads its S row, frees the TMEM stage, and reduces the row to its LSE over
 //     the visible keys; the G rows of a query (adjacent lanes) sum their LSEs into the
 //     candidate's score;
-//   * scheduler (warp 13, one thread): fills the item queue.
+//   * scheduler (the last warp, one thread): fills the item queue.
 // Every wait is bounded (the launch's wait limit); a wait that gives up sets the CTA's abort
 // flag and every role leaves its loop at its next tile. Before the CTA frees its tensor memory
 // the control thread drains what it issued (key tiles in flight, MMAs), the producers their
@@ -42,8 +42,14 @@ constexpr int kRows = 128;
 constexpr int kNQ = 4;            // Q tile stages
 constexpr int kNS = 4;            // TMEM S stages (64 columns each)
 constexpr int kNK = 2;            // K tile stages
-constexpr int kThreads = 448;     // softmax 0-255 (two warpgroups), producers 256-383, control, scheduler
-constexpr int kConsumerWarps = 13;
+#ifndef PISA_LEAF_SG
+#define PISA_LEAF_SG 2
+#endif
+constexpr int kSG = PISA_LEAF_SG;                 // softmax warpgroups (tile T goes to group T % kSG;
+                                                  // three measured slower than two: 1.24 vs 1.18 ms)
+constexpr int kWP = 4 * kSG;                      // first producer warp
+constexpr int kThreads = 128 * kSG + 128 + 64;    // softmax, producers (4 warps), control, scheduler
+constexpr int kConsumerWarps = 4 * kSG + 5;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
@@ -118,15 +124,15 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
   auto wait = [&](uint64_t* bar, uint32_t parity) { return tc::bar_wait(bar, parity, a.wait_ns); };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
 
-  if (warp >= 8 && warp < 12) {
+  if (warp >= kWP && warp < kWP + 4) {
     // ---------------------------------------------------------------- producers
     // the next tile's list entries (and item) load while this tile's copies are issued; lane
     // l holds the entry of the warp's row l, and instruction k copies rows k*RPI .. of the
     // warp's 32, chunk (lane % CH) of row (lane / CH)
     constexpr int RPI = 32 / CH;                      // rows per warp instruction
-    const int wr = (warp - 8) * 32;                   // the warp's first tile row
+    const int wr = (warp - kWP) * 32;                 // the warp's first tile row
     DynCursor cur;
-    const bool lead = warp == 8;                      // marks the queue positions demanded
+    const bool lead = warp == kWP;                    // marks the queue positions demanded
     bool have = dyn_first(s_q, EPT, &s_abort, cur, true, lead);
     int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
     int T = 0;
@@ -163,7 +169,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       tc::fence_async_smem();
       tc::bar_arrive(&q_full[(T - 1) % kNQ]);
     }
-  } else if (warp == 12) {
+  } else if (warp == kWP + 4) {
     // ---------------------------------------------------------------- control
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
@@ -218,9 +224,9 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
         tc::bar_wait(&drain, 0, kDrainNs);
       }
     }
-  } else if (warp < 8) {
+  } else if (warp < kWP) {
     // ---------------------------------------------------------------- softmax
-    // warpgroup sg takes the tiles T with T % 2 == sg; its entries for the next such tile
+    // warpgroup sg takes the tiles T with T % kSG == sg; its entries for the next such tile
     // load while the current one is reduced
     const int sg = warp >> 2;
     const int r = tid & (kRows - 1);
@@ -230,15 +236,14 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
     DynCursor cur;
     bool have = dyn_first(s_q, EPT, &s_abort, cur, true);
     int T = 0;
-    if (have && sg == 1) {
-      have = dyn_next(s_q, EPT, &s_abort, cur, true);
-      T = 1;
-    }
+    for (; have && T < sg; ++T) have = dyn_next(s_q, EPT, &s_abort, cur, true);
     int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     while (have && !aborted()) {
       DynCursor nxt = cur;
-      bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
-      if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
+      bool have_n = true;
+#pragma unroll
+      for (int k = 0; k < kSG; ++k)
+        if (have_n) have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, r) : -1;   // in flight during this tile
       const int ss = T % kNS;
       const bool ok = wait(&s_full[ss], (T / kNS) & 1);
@@ -254,18 +259,31 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
       }
-      // four partial chains for the max and the sum (independent instructions in flight)
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // row max: eight chains of three-input maxima; exponent arguments and the sum on packed
+      // pairs (fewer instructions per row: the softmax warps are issue- and latency-bound)
+      float mq[8];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      for (int k = 0; k < 8; ++k) {
+        mq[k] = fmaxf(sv[k], sv[k + 8]);
+#pragma unroll
+        for (int u = 16; u < 64; u += 16) mq[k] = tc::max3(mq[k], sv[k + u], sv[k + u + 8]);
+      }
+      const float mx = fmaxf(tc::max3(mq[0], mq[1], mq[2]), tc::max3(mq[3], tc::max3(mq[4], mq[5], mq[6]), mq[7]));
       float lse = -INFINITY;
       if (mx != -INFINITY) {
         const float m2 = mx * c1;
-        float lq[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t cc = tc::pack2(c1, c1), mm = tc::pack2(-m2, -m2);
+        uint64_t lq[4] = {0, 0, 0, 0};            // packed zero pairs
 #pragma unroll
-        for (int c = 0; c < 64; ++c) lq[c & 3] += tc::ex2(fmaf(sv[c], c1, -m2));
-        lse = (m2 + tc::lg2((lq[0] + lq[1]) + (lq[2] + lq[3]))) * kLn2;
+        for (int p = 0; p < 32; ++p) {
+          float y0, y1;
+          tc::unpack2(tc::fma2(tc::pack2(sv[2 * p], sv[2 * p + 1]), cc, mm), y0, y1);
+          lq[p & 3] = tc::add2(lq[p & 3], tc::pack2(tc::ex2(y0), tc::ex2(y1)));
+        }
+        const uint64_t t = tc::add2(tc::add2(lq[0], lq[1]), tc::add2(lq[2], lq[3]));
+        float t0, t1;
+        tc::unpack2(t, t0, t1);
+        lse = (m2 + tc::lg2(t0 + t1)) * kLn2;
       }
       if (a.block_lse) {
         if (pk >= 0)
@@ -273,7 +291,7 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
         cur = nxt;
         have = have_n;
         pk = pk_n;
-        T += 2;
+        T += kSG;
         continue;
       }
       // G adjacent lanes hold the heads of one query (a padding entry is whole)
@@ -288,9 +306,9 @@ leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
       cur = nxt;
       have = have_n;
       pk = pk_n;
-      T += 2;
+      T += kSG;
     }
-  } else if (warp == 13) {
+  } else if (warp == kWP + 5) {
     // ---------------------------------------------------------------- scheduler
     if (lane == 0) queue_fill(s_q, a.src, a.next_item, n_items, &s_abort);
   }

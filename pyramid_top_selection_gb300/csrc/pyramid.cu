@@ -45,12 +45,12 @@ build_leaves_kernel(const __nv_bfloat16* __restrict__ K, const int32_t* __restri
     const __nv_bfloat16* base = K + (static_cast<int64_t>(b) * T * Hkv + kv) * D + ch * 8;
     const int64_t stride = static_cast<int64_t>(Hkv) * D;
     int64_t j = s;
-    for (; j + 4 <= e_; j += 4) {
-      uint4 v[4];
+    for (; j + 8 <= e_; j += 8) {          // eight rows in flight, added in token order
+      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = ldg_u4(base + (j + u) * stride);
+      for (int u = 0; u < 8; ++u) v[u] = ldg_u4(base + (j + u) * stride);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v[u]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -93,23 +93,43 @@ build_leaves_kernel(const __nv_bfloat16* __restrict__ K, const int32_t* __restri
   }
 }
 
-// Levels 4.. for one (batch, KV head) per CTA, level by level.
+// Upper levels by subtrees: grid (ceil(n_src / 64), heads). A CTA loads 64 nodes of level
+// l_src (those of its subtree) and computes the up to kSubLevels levels above them in shared
+// memory, writing every node it completes (parent = left + right, or left alone).
+constexpr int kSubNodes = 64;
+constexpr int kSubLevels = 6;                  // 64 nodes -> 1
+
 template <int D>
 __global__ void __launch_bounds__(256)
-build_upper_kernel(int Hkv, Geo geo, float* __restrict__ pyr) {
-  const int64_t head = static_cast<int64_t>(blockIdx.y) * Hkv + blockIdx.x;
+build_subtree_kernel(Geo geo, int l_src, float* __restrict__ pyr) {
+  __shared__ __align__(16) float sa[kSubNodes * D];          // levels l_src, l_src + 2, ...
+  __shared__ __align__(16) float sb[(kSubNodes / 2) * D];    // levels l_src + 1, l_src + 3, ...
+  const int64_t head = blockIdx.y;
   float* pyr_h = pyr + head * geo.nodes * D;
-  for (int l = kInCtaLevels + 1; l < geo.n_levels; ++l) {
-    const float* src = pyr_h + geo.off[l - 1] * D;
-    float* dst = pyr_h + geo.off[l] * D;
-    const int n = geo.size[l], nc = geo.size[l - 1];
-    for (int it = threadIdx.x; it < n * D; it += blockDim.x) {
+  const int m0 = blockIdx.x * kSubNodes;
+  const int here = min(kSubNodes, geo.size[l_src] - m0);
+  const float4* src = reinterpret_cast<const float4*>(pyr_h + (geo.off[l_src] + m0) * D);
+  for (int it = threadIdx.x; it < here * D / 4; it += blockDim.x)
+    reinterpret_cast<float4*>(sa)[it] = src[it];
+  __syncthreads();
+  int cnt = here;                              // nodes of the current level inside the subtree
+  const float* cur = sa;
+  float* nxt = sb;
+  for (int l = l_src + 1; l <= l_src + kSubLevels && l < geo.n_levels; ++l) {
+    const int nl = (cnt + 1) / 2, first = m0 >> (l - l_src), nc = geo.size[l - 1];
+    const int c0 = m0 >> (l - 1 - l_src);     // first child index at level l - 1
+    for (int it = threadIdx.x; it < nl * D; it += blockDim.x) {
       const int m = it / D, k = it % D;
-      float v = src[(2 * m) * D + k];
-      if (2 * m + 1 < nc) v = v + src[(2 * m + 1) * D + k];
-      dst[it] = v;
+      float v = cur[(2 * m) * D + k];
+      if (c0 + 2 * m + 1 < nc) v = v + cur[(2 * m + 1) * D + k];
+      nxt[it] = v;
+      if (first + m < geo.size[l]) pyr_h[(geo.off[l] + first + m) * D + k] = v;
     }
     __syncthreads();
+    float* t = const_cast<float*>(cur);
+    cur = nxt;
+    nxt = t;
+    cnt = nl;
   }
 }
 
@@ -120,9 +140,10 @@ int build_impl(const Dims& s, const Geo& g, const void* K, const int32_t* len, i
   { ProfScope ps(st, SQ ? "build_sq_leaves" : "build_leaves");
   build_leaves_kernel<D, SQ><<<grid, (D / 8) * kLeavesPerCta, 0, st>>>(
       static_cast<const __nv_bfloat16*>(K), len, T, s.Hkv, s.C, g, pyr); }
-  if (g.n_levels > kInCtaLevels + 1) {
+  for (int l = kInCtaLevels; l + 1 < g.n_levels; l += kSubLevels) {
     ProfScope ps(st, "build_upper");
-    build_upper_kernel<D><<<dim3(s.Hkv, s.B), 256, 0, st>>>(s.Hkv, g, pyr);
+    const int n = g.size[l];
+    build_subtree_kernel<D><<<dim3((n + kSubNodes - 1) / kSubNodes, s.B * s.Hkv), 256, 0, st>>>(g, l, pyr);
   }
   return static_cast<int>(cudaGetLastError());
 }

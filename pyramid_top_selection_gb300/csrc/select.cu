@@ -442,6 +442,7 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
 // When the status word carries PISA_STATUS_TIMEOUT (a bounded wait of the leaf stage gave up,
 // so candidate scores may be missing or stale) every output slot is poisoned instead:
 // idx = -1, score = head_lse = NaN.
+template <int J>    // candidates per lane: 1 (W <= 32) or 2 (W <= 64)
 __global__ void __launch_bounds__(kWarps * 32)
 topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restrict__ cand,
             const float* __restrict__ csc, const float* __restrict__ chead, int32_t* __restrict__ idx,
@@ -460,7 +461,6 @@ topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restr
     }
     return;
   }
-  const int J = W > 32 ? 2 : 1;
   int ci[2] = {-1, -1};
   float cs[2] = {neg_inf(), neg_inf()};
   for (int j = 0; j < J; ++j) {
@@ -471,24 +471,28 @@ topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restr
     }
   }
   int rank[2] = {0, 0};
+#pragma unroll
   for (int jj = 0; jj < J; ++jj)
+#pragma unroll 8
     for (int o = 0; o < 32; ++o) {
       const float so = __shfl_sync(0xffffffffu, cs[jj], o);
       const int io = __shfl_sync(0xffffffffu, ci[jj], o);
       if (io < 0) continue;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) rank[j] += beats(so, io, cs[j], ci[j]) ? 1 : 0;
+      for (int j = 0; j < J; ++j) rank[j] += beats(so, io, cs[j], ci[j]) ? 1 : 0;
     }
-  bool keep[2];
+  bool keep[2] = {false, false};
   int pos[2] = {0, 0};
 #pragma unroll
-  for (int j = 0; j < 2; ++j) keep[j] = ci[j] >= 0 && rank[j] < Ksel;
+  for (int j = 0; j < J; ++j) keep[j] = ci[j] >= 0 && rank[j] < Ksel;
+#pragma unroll
   for (int jj = 0; jj < J; ++jj)
+#pragma unroll 8
     for (int o = 0; o < 32; ++o) {
       const int io = __shfl_sync(0xffffffffu, keep[jj] ? ci[jj] : -1, o);
       if (io < 0) continue;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) pos[j] += io < ci[j] ? 1 : 0;
+      for (int j = 0; j < J; ++j) pos[j] += io < ci[j] ? 1 : 0;
     }
   const int nk = __popc(__ballot_sync(0xffffffffu, keep[0])) + __popc(__ballot_sync(0xffffffffu, keep[1]));
   // unit u = (b*Hkv + kv)*N + i -> head_lse rows (b*Hq + kv*G + h)*N + i
@@ -716,9 +720,15 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
 // Stage-2 grouping: query chunks of about 64 MiB of one KV head's query rows; about 4096
 // (query, head) rows per work item (with the dynamic item order, longer items measured faster:
 // 1.60 -> 1.53 ms at 64K, and fewer bins shorten the scans).
+#ifndef PISA_LEAF_CHUNK_MIB
+#define PISA_LEAF_CHUNK_MIB 64
+#endif
+#ifndef PISA_LEAF_ITEM_ROWS
+#define PISA_LEAF_ITEM_ROWS 4096
+#endif
 GroupPlan leaf_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2;
-  return make_group_plan(s, s.g * s.K, (int64_t(64) << 20) / per_query, 4096 / s.G);
+  return make_group_plan(s, s.g * s.K, (int64_t(PISA_LEAF_CHUNK_MIB) << 20) / per_query, PISA_LEAF_ITEM_ROWS / s.G);
 }
 
 inline int grid_for(int64_t n, int threads) {
@@ -736,7 +746,7 @@ int launch_topk(const Dims& s, int W, const int32_t* cand, const float* cscore, 
                 int32_t* idx, float* score, float* head_lse, const int32_t* status, cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   ProfScope ps(st, "topk");
-  topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+  (W > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
       units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse, status);
   return cudaGetLastError();
 }
@@ -808,7 +818,7 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
     ProfScope ps(st, "topk");
-    topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+    (W > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
         units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse,
         reinterpret_cast<const int32_t*>(ws + w.status));
   }
@@ -844,7 +854,7 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   {
     ProfScope ps(st, "topk");
-    topk_kernel<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+    (s.g * s.K > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
         units, s.g * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr,
         reinterpret_cast<const int32_t*>(ws + w.status));
   }
