@@ -191,6 +191,7 @@ KERNEL_SOURCES = {
     "route": ["select.cu", "device.cuh", "pyramid.cu"],
     "leaf_score": ["leaf_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "select.cu"],
     "attn_fwd_tc": ["attn_ws.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "attn.cu"],
+    "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h"],
 }
 
 
