@@ -4,9 +4,9 @@ bench.py runs one process per GPU, each on its own replica of the workload (no c
 on the data path); the only cross-rank steps are the barriers around the timed region and
 the max-over-ranks reduction of the step time, which these tests exercise."""
 import os
-import socket
 import subprocess
 import sys
+import tempfile
 
 import pytest
 import torch
@@ -16,18 +16,12 @@ import torch.multiprocessing as mp
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _free_port() -> int:
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _worker(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+def _worker(rank, world, store_file, out):
+    # rendezvous through a file store: no TCP port to race for with other processes
+    os.environ.update(MASTER_ADDR="127.0.0.1", RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
     sys.path.insert(0, ROOT)
     import bench
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", init_method=f"file://{store_file}", rank=rank, world_size=world)
     try:
         r, w, l = bench.dist_env()
         bench.rank_barrier(w)
@@ -39,11 +33,11 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time():
     world = 2
-    port = _free_port()
+    store_file = os.path.join(tempfile.mkdtemp(prefix="pisa_pg_"), "store")
     ctx = mp.get_context("spawn")
     with ctx.Manager() as m:
         out = m.dict()
-        procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
+        procs = [ctx.Process(target=_worker, args=(r, world, store_file, out)) for r in range(world)]
         for p in procs:
             p.start()
         for p in procs:
