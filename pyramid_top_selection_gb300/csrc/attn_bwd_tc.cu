@@ -6,22 +6,27 @@
 // D_i = dO_i . O_i and dS = P (dO . v - D):  dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO.
 //
 // One CTA per work item (a leaf block of one selection unit and the rows = (query, head) that
-// selected it, grouped as for the forward), 8 warps, one CTA per SM. The item's 64 keys and
-// values arrive once by TMA; its rows come in tiles of 128 (row = TMEM lane), gathered by
-// cp.async into two buffers (the next tile's Q and dO rows land while this one is computed).
-// Per tile, one thread issues
-//     S = Q K^T and dP = dO V^T          (M = 128 rows, N = 64 keys, K = d; K-major operands)
-// into TMEM; every row's P and dS are computed by two threads (32 keys each) and written as
-// bf16 tiles [row][key]; then
-//     dV^T += dO^T P and dK^T += Q^T dS  (M = d, N = 64 keys, K = 128 rows; MN-major operands,
-//                                         accumulated in TMEM over the whole item)
-//     dQ = dS K                          (M = 128 rows, N = d, K = 64 keys; K MN-major)
-// and dQ (scaled by s) leaves TMEM through a staging tile as TMA tensor reduce-adds into the
-// fp32 dQ accumulator (the rows of a query chunk stay in L2). At the item's end its dK^T and
-// dV^T columns are added into the fp32 key/value accumulators. Every wait is bounded (the
-// launch's wait limit); a wait that gives up makes the whole CTA leave its loop, drain the MMAs,
-// copies and reductions it issued, free its tensor memory and OR PISA_STATUS_TIMEOUT into the
-// status word, which the output conversion turns into poisoned (NaN) gradients.
+// selected it, grouped as for the forward), one CTA per SM, warp-specialised so that the tensor
+// cores, the softmax arithmetic, the row gathers and the dQ reductions of different tiles run at
+// the same time. The item's 64 keys and values arrive once by TMA; its rows come in tiles of 128
+// (row = TMEM lane). Roles, connected by mbarriers:
+//   * producers (warps 12-15): gather a tile's Q and dO rows by cp.async into one of two stages;
+//   * control (warp 16, one thread): per tile T, S = Q K^T and dP = dO V^T (M = 128 rows, N = 64
+//     keys, K = d; K-major operands) into one of two TMEM stages, issued before tile T - 1's
+//     second group; once T's P and dS tiles are written,
+//         dV^T += dO^T P and dK^T += Q^T dS  (M = d, N = 64 keys, K = 128 rows; MN-major operands,
+//                                             accumulated in TMEM over the whole item)
+//         dQ = dS K                          (M = 128 rows, N = d, K = 64 keys; K MN-major)
+//   * softmax (warps 0-7, two threads per row, 32 keys each): P = exp(s S - lse) and
+//     dS = P (dP - D) from TMEM into bf16 tiles [row][key];
+//   * dQ epilogue (warps 8-11): dQ (scaled by s) from TMEM, 32 columns per round, through two
+//     swizzled staging tiles as TMA tensor reduce-adds of each query's G rows into the fp32 dQ
+//     accumulator (the rows of a query chunk stay in L2); after the item's last tile, its dK^T
+//     and dV^T columns are added into the fp32 key/value accumulators.
+// Every wait is bounded (the launch's wait limit); a wait that gives up sets the CTA's abort
+// flag and every role leaves its loop at its next wait; the CTA drains the MMAs, copies and
+// reductions it issued, frees its tensor memory and ORs PISA_STATUS_TIMEOUT into the status
+// word, which the output conversion turns into poisoned (NaN) gradients.
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
@@ -33,23 +38,23 @@ namespace pisa {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 544;                  // softmax 0-255, epilogue 256-383, producers 384-511, control
 constexpr int kRows = 128;                     // tile rows = TMEM lanes
 constexpr int kD = 128;                        // head dimension of this kernel
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
 
-// TMEM columns: S, dP, dV^T, dK^T (64 each), dQ (128).
-constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDK = 192, kColDQ = 256;
+// TMEM columns: S and dP of stage st at 128 st and 128 st + 64; dV^T, dK^T (64 each); dQ (128).
+constexpr uint32_t kColDV = 256, kColDK = 320, kColDQ = 384;
 
 struct Smem {
   static constexpr int KV = 2 * 64 * 128;            // [64 keys x 128 dims] bf16, two SW128 chunks
   static constexpr int TILE = 2 * kRows * 128;       // [128 rows x 128 dims] bf16, two SW128 chunks
   static constexpr int PS = kRows * 128;             // [128 rows x 64 keys] bf16, SW128
-  static constexpr int STG = kRows * 128;            // [128 rows x 32] fp32, SW128 chunks
+  static constexpr int STG = kRows * 128;            // [128 rows x 32] fp32, SW128
   static constexpr int oK = 0, oV = oK + KV, oQ = oV + KV, odO = oQ + 2 * TILE, oP = odO + 2 * TILE,
                        odS = oP + PS, oS = odS + PS;
-  static constexpr int bytes = oS + STG + 1024;
+  static constexpr int bytes = oS + 2 * STG + 1024;
 };
 
 struct BwdTcArgs {
@@ -74,10 +79,10 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
   using L = Smem;
   constexpr int EPT = kRows / G;                     // list entries (queries) per tile
   extern __shared__ unsigned char smraw[];
-  __shared__ __align__(8) uint64_t kv_bar, mma_bar, drain, never;
+  __shared__ __align__(8) uint64_t kv_bar, q_full[2], q_empty[2], s_full[2], s_empty[2], p_full, p_empty,
+      dq_full, dq_empty, drain, never;
   __shared__ uint32_t tmem_base;
-  __shared__ float m_lse2[2][kRows], m_D[2][kRows];
-  __shared__ int m_qi[2][kRows];
+  __shared__ int s_abort;
 
   const Dims& s = a.s;
   if (static_cast<int>(blockIdx.x) >= *a.n_items) return;
@@ -89,178 +94,161 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
                  aS = tc::su32(sm + L::oS);
   const int n_tiles = (v.n_ent + EPT - 1) / EPT;
   const int kvk = v.kv / s.kvr;                      // the unit's KV head
+  // list entry of tile j's row r (-1: padding), packed as query << 6 | slot
+  auto entry = [&](int j, int r) {
+    const int e = j * EPT + r / G;
+    return e < v.n_ent ? a.src.list[v.beg + e] : -1;
+  };
 
   if (tid == 0) {
     tc::bar_init(&kv_bar, 1);
-    tc::bar_init(&mma_bar, 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::bar_init(&q_full[k], kRows);
+      tc::bar_init(&q_empty[k], 1);
+      tc::bar_init(&s_full[k], 1);
+      tc::bar_init(&s_empty[k], 2 * kRows);
+    }
+    tc::bar_init(&p_full, 2 * kRows);
+    tc::bar_init(&p_empty, 1);
+    tc::bar_init(&dq_full, 1);
+    tc::bar_init(&dq_empty, kRows);
     tc::bar_init(&drain, 1);
     tc::bar_init(&never, 1);
     tc::fence_bar_init();
+    s_abort = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
   tc::before_sync();
   __syncthreads();
   tc::after_sync();
   const uint32_t tm = tmem_base;
+  auto give_up = [&]() { atomicOr(&s_abort, 1); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return tc::bar_wait(bar, parity, a.wait_ns); };
 
-  // the item's keys and values: two 64-dim boxes each, one transaction barrier
-  if (tid == 0) {
-    tc::bar_expect_tx(&kv_bar, 2 * L::KV);
-    for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load4(aK + kb * (64 * 128), &kmap, kb * 64, kvk, v.kbase, v.b, &kv_bar);
-      tc::tma_load4(aV + kb * (64 * 128), &vmap, kb * 64, kvk, v.kbase, v.b, &kv_bar);
-    }
-  }
-
-  // A tile's list entries, loaded one tile ahead of its gather: entries of the thread's 8
-  // gather rows ((tid >> 4) + 16u) and, for threads < 128, of metadata row tid.
-  struct Entries {
-    int pk[8];
-    int mpk;
-  };
-  auto load_entries = [&](int j, Entries& en) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = j * EPT + ((tid >> 4) + 16 * u) / G;
-      en.pk[u] = e < v.n_ent ? a.src.list[v.beg + e] : -1;
-    }
-    const int e = j * EPT + (tid & (kRows - 1)) / G;
-    en.mpk = tid < kRows && e < v.n_ent ? a.src.list[v.beg + e] : -1;
-  };
-  // gather of a tile into buffer bf: the thread copies 16-byte chunk (tid & 15) of its rows
-  auto gather = [&](const Entries& en, int bf) {
-    const int c = tid & 15;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int r = (tid >> 4) + 16 * u, pk = en.pk[u];
-      const int64_t row = (static_cast<int64_t>(v.b) * s.N + (pk < 0 ? 0 : (pk >> 6))) * s.Hq + v.kv * G + r % G;
-      const uint32_t off = bf * L::TILE + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8);
-      tc::cp_async16(aQ + off, a.Q + row * kD + c * 8, pk >= 0);
-      tc::cp_async16(adO + off, a.dO + row * kD + c * 8, pk >= 0);
-    }
-    tc::cp_async_commit();
-  };
-  // metadata of row tid (threads < 128): lse * log2e, D, query (-1: padding); loaded into
-  // registers when the tile's gather is issued, stored to shared memory a phase later
-  float ml2 = 0.f, mD = 0.f;
-  int mqi = -1;
-  auto meta_load = [&](const Entries& en) {
-    const int h = tid % G;
-    mqi = en.mpk < 0 ? -1 : (en.mpk >> 6);
-    ml2 = mD = 0.f;
-    if (mqi >= 0) {
-      ml2 = a.lse[(static_cast<int64_t>(v.b) * s.Hq + v.kv * G + h) * s.N + mqi] * kLog2e;
-      mD = a.delta[(static_cast<int64_t>(v.b) * s.N + mqi) * s.Hq + v.kv * G + h];
-    }
-  };
-  auto meta_store = [&](int bf) {
-    if (tid < kRows) {
-      m_lse2[bf][tid] = ml2;
-      m_D[bf][tid] = mD;
-      m_qi[bf][tid] = mqi;
-    }
-  };
-
-  bool ok = true;
-  bool mma_issued = false, kv_landed = false;
-  const int r = tid & (kRows - 1), hf = tid >> 7;      // a thread's tile row and half of it
-  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const float c1 = s.scale * kLog2e;
-  constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);                  // S, dP
-  constexpr uint32_t idKV = tc::idesc_bf16_major(kD, 64, true, true);   // dV^T, dK^T
-  constexpr uint32_t idQ = tc::idesc_bf16_major(kRows, kD, false, true);  // dQ
-  uint32_t mma_phase = 0;
-  auto wait_mma = [&]() {
-    const bool w = tc::bar_wait(&mma_bar, mma_phase, a.wait_ns);
-    mma_phase ^= 1;
-    return w;
-  };
-  // dQ of the previous tile, row r, columns 64 hf .. 64 hf + 63 (scaled by s), and its query
-  float dqr[2][32];
-  int dq_qi = -1;
-  // the previous tile's dQ into the fp32 accumulator: two rounds of 32 columns per thread half,
-  // staged in the P and dS tiles (free once that tile's MMAs completed), one TMA reduce-add per
-  // query (its G rows) and staging buffer
-  auto dq_out = [&]() {
-    const bool issuer = dq_qi >= 0 && r % G == 0;
-    const int unit = (v.b * s.N + (dq_qi < 0 ? 0 : dq_qi)) * s.Hkv + v.kv;
-    const uint32_t stg_a = hf == 0 ? aP : adS;
-    unsigned char* stg = sm + (hf == 0 ? L::oP : L::odS);
-#pragma unroll
-    for (int rd = 0; rd < 2; ++rd) {
-      const float* x = dqr[rd];
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
-            make_float4(s.scale * x[4 * c], s.scale * x[4 * c + 1], s.scale * x[4 * c + 2], s.scale * x[4 * c + 3]);
-      tc::fence_async_smem();
-      __syncthreads();
-      if (issuer) {
-        tc::tma_reduce_add3(&qmap, 64 * hf + 32 * rd, 0, unit, stg_a + r * 128);
-        tc::bulk_commit();
-        tc::bulk_wait_read<0>();
+  if (warp >= 12 && warp < 16) {
+    // ---------------------------------------------------------------- producers
+    // thread: chunk (lane & 15) of two rows per instruction, rows wr .. wr + 31 of the tile; the
+    // tile's copies are waited for and confirmed before the next stage is awaited, so no
+    // unconfirmed copies are held while blocking (the stages are released only after the
+    // second MMA group, which needs the next tile's S)
+    const int wr = (warp - 12) * 32, c = lane & 15;
+    int pk = n_tiles > 0 ? entry(0, wr + lane) : -1;
+    for (int T = 0; T < n_tiles; ++T) {
+      const int pk_n = T + 1 < n_tiles ? entry(T + 1, wr + lane) : -1;   // in flight meanwhile
+      const int st = T & 1;
+      const bool ok = wait(&q_empty[st], ((T >> 1) & 1) ^ 1);
+      if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int rl = 2 * k + (lane >> 4);
+        const int qpk = __shfl_sync(0xffffffffu, pk, rl);
+        const int r = wr + rl;
+        const int64_t row = (static_cast<int64_t>(v.b) * s.N + (qpk < 0 ? 0 : (qpk >> 6))) * s.Hq + v.kv * G + r % G;
+        const uint32_t off = st * L::TILE + (c >> 3) * (kRows * 128) + tc::sw128(r, (c & 7) * 8);
+        tc::cp_async16(aQ + off, a.Q + row * kD + c * 8, qpk >= 0);
+        tc::cp_async16(adO + off, a.dO + row * kD + c * 8, qpk >= 0);
       }
-      __syncthreads();
-    }
-  };
-
-  Entries ent;
-  if (n_tiles > 0) {
-    load_entries(0, ent);
-    gather(ent, 0);
-    meta_load(ent);
-    meta_store(0);
-    if (n_tiles > 1) load_entries(1, ent);
-  }
-  for (int j = 0; j < n_tiles; ++j) {
-    const int bf = j & 1;
-    if (j + 1 < n_tiles) {
-      gather(ent, bf ^ 1);                        // buffer bf ^ 1: tile j - 1's MMAs are complete
-      meta_load(ent);                             // in flight; stored below
-      if (j + 2 < n_tiles) load_entries(j + 2, ent);
-      tc::cp_async_wait<1>();
-    } else {
+      tc::cp_async_commit();
       tc::cp_async_wait<0>();
+      tc::fence_async_smem();
+      tc::bar_arrive(&q_full[st]);
+      pk = pk_n;
     }
-    tc::fence_async_smem();                       // the copies land in the async proxy's view
-    __syncthreads();
-    // S and dP of tile j
-    if (tid == 0) {
-      if (!kv_landed) {
-        kv_landed = tc::bar_wait(&kv_bar, 0, a.wait_ns);
-        ok = kv_landed;
-        if (ok && a.stall) ok = tc::bar_wait(&never, 0, a.wait_ns);   // test aid: runs out
+    tc::cp_async_wait<0>();
+  } else if (warp == 16) {
+    // ---------------------------------------------------------------- control
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);                   // S, dP
+      constexpr uint32_t idKV = tc::idesc_bf16_major(kD, 64, true, true);   // dV^T, dK^T
+      constexpr uint32_t idQ = tc::idesc_bf16_major(kRows, kD, false, true);  // dQ
+      bool kv_landed = false, mma_issued = false, ok = true;
+      tc::bar_expect_tx(&kv_bar, 2 * L::KV);
+      for (int kb = 0; kb < 2; ++kb) {
+        tc::tma_load4(aK + kb * (64 * 128), &kmap, kb * 64, kvk, v.kbase, v.b, &kv_bar);
+        tc::tma_load4(aV + kb * (64 * 128), &vmap, kb * 64, kvk, v.kbase, v.b, &kv_bar);
       }
-      if (ok) {
+      auto issue_s = [&](int T) -> bool {            // S and dP of tile T
+        const int st = T & 1;
+        if (!wait(&q_full[st], (T >> 1) & 1) || !wait(&s_empty[st], ((T >> 1) & 1) ^ 1)) return false;
         tc::after_sync();
-        const uint32_t q = aQ + bf * L::TILE, o = adO + bf * L::TILE;
+        mma_issued = true;
+        const uint32_t q = aQ + st * L::TILE, o = adO + st * L::TILE;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
           const uint32_t ka = (k >> 2) * (kRows * 128) + (k & 3) * 32, kb = (k >> 2) * (64 * 128) + (k & 3) * 32;
-          tc::mma(tm + kColS, tc::desc(q + ka), tc::desc(aK + kb), idS, k > 0);
-          tc::mma(tm + kColDP, tc::desc(o + ka), tc::desc(aV + kb), idS, k > 0);
+          tc::mma(tm + 128 * st, tc::desc(q + ka), tc::desc(aK + kb), idS, k > 0);
+          tc::mma(tm + 128 * st + 64, tc::desc(o + ka), tc::desc(aV + kb), idS, k > 0);
         }
-        tc::commit(&mma_bar);
-        mma_issued = true;
+        tc::commit(&s_full[st]);
+        return true;
+      };
+      kv_landed = wait(&kv_bar, 0);
+      ok = kv_landed;
+      if (ok && a.stall) ok = wait(&never, 0);      // test aid: runs out after the wait limit
+      if (ok && n_tiles > 0) ok = issue_s(0);
+      for (int T = 0; ok && T < n_tiles; ++T) {
+        if (*reinterpret_cast<volatile int*>(&s_abort)) { ok = false; break; }
+        if (T + 1 < n_tiles && !issue_s(T + 1)) { ok = false; break; }   // runs under T's softmax
+        if (!wait(&p_full, T & 1) || (T > 0 && !wait(&dq_empty, (T - 1) & 1))) { ok = false; break; }
+        tc::after_sync();
+        const int st = T & 1;
+        const uint32_t q = aQ + st * L::TILE, o = adO + st * L::TILE;
+#pragma unroll
+        for (int k = 0; k < kRows / 16; ++k) {
+          const uint32_t rk = k * 2048;             // 16 rows of an MN-major operand
+          tc::mma(tm + kColDV, tc::desc_mn(o + rk, kRows * 128), tc::desc_mn(aP + rk, 0), idKV, T > 0 || k > 0);
+          tc::mma(tm + kColDK, tc::desc_mn(q + rk, kRows * 128), tc::desc_mn(adS + rk, 0), idKV, T > 0 || k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma(tm + kColDQ, tc::desc(adS + k * 32), tc::desc_mn(aK + k * 2048, 64 * 128), idQ, k > 0);
+        tc::commit(&q_empty[st]);
+        tc::commit(&p_empty);
+        tc::commit(&dq_full);
+      }
+      if (!ok) give_up();
+      // drain: the key/value tiles land and every MMA issued completes before the CTA leaves
+      if (!kv_landed) tc::bar_wait(&kv_bar, 0, kDrainNs);
+      if (mma_issued) {
+        tc::commit(&drain);
+        tc::bar_wait(&drain, 0, kDrainNs);
       }
     }
-    if (!__syncthreads_and(ok)) break;
-    // meanwhile, the previous tile's dQ leaves through the P/dS tiles
-    if (j > 0) dq_out();
-    ok = wait_mma();
-    if (!__syncthreads_and(ok)) break;
-    tc::after_sync();
-    // P and dS of the thread's 32 keys of row r
-    {
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax
+    // thread: row r (TMEM lane), keys 32 hs .. 32 hs + 31; the next tile's row metadata
+    // (lse * log2e, D, query) loads during this tile
+    const int r = tid & (kRows - 1), hs = warp >> 2, h = r % G;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c1 = s.scale * kLog2e;
+    auto meta = [&](int j, float& l2, float& D) {
+      const int pk = entry(j, r);
+      l2 = D = 0.f;
+      if (pk >= 0) {
+        const int qi = pk >> 6;
+        l2 = a.lse[(static_cast<int64_t>(v.b) * s.Hq + v.kv * G + h) * s.N + qi] * kLog2e;
+        D = a.delta[(static_cast<int64_t>(v.b) * s.N + qi) * s.Hq + v.kv * G + h];
+      }
+      return pk;
+    };
+    float l2 = 0.f, D = 0.f;
+    int pk = n_tiles > 0 ? meta(0, l2, D) : -1;
+    for (int T = 0; T < n_tiles; ++T) {
+      float l2_n = 0.f, D_n = 0.f;
+      const int pk_n = T + 1 < n_tiles ? meta(T + 1, l2_n, D_n) : -1;
+      const int st = T & 1;
+      const bool ok = wait(&s_full[st], (T >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
+      tc::after_sync();
       float sv[32], dp[32];
-      tc::tmem_ld32(tm + kColS + 32 * hf + lane_off, sv);
-      tc::tmem_ld32(tm + kColDP + 32 * hf + lane_off, dp);
-      const int qi = m_qi[bf][r];
-      const int lim = qi < 0 ? -1 : qi - v.kbase - 32 * hf;   // key c of the half visible iff c <= lim
-      const float l2 = m_lse2[bf][r], D = m_D[bf][r];
+      tc::tmem_ld32(tm + 128 * st + 32 * hs + lane_off, sv);
+      tc::tmem_ld32(tm + 128 * st + 64 + 32 * hs + lane_off, dp);
+      tc::before_sync();
+      tc::bar_arrive(&s_empty[st]);
+      const int lim = pk < 0 ? -1 : (pk >> 6) - v.kbase - 32 * hs;   // key c of the half visible iff c <= lim
       const uint64_t cc = tc::pack2(c1, c1), ll = tc::pack2(-l2, -l2), dd = tc::pack2(-D, -D);
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {           // packed pairs: exponent arguments, dP - D, P (dP - D)
+      for (int c = 0; c < 32; c += 2) {             // packed pairs: exponent arguments, dP - D, P (dP - D)
         float y0, y1, e0, e1;
         tc::unpack2(tc::fma2(tc::pack2(sv[c], sv[c + 1]), cc, ll), y0, y1);
         const float p0 = c <= lim ? tc::ex2(y0) : 0.f, p1 = c + 1 <= lim ? tc::ex2(y1) : 0.f;
@@ -270,80 +258,89 @@ attn_bwd_tc_kernel(const BwdTcArgs a, const __grid_constant__ CUtensorMap kmap,
         dp[c] = p0 * e0;
         dp[c + 1] = p1 * e1;
       }
+      const bool ok2 = wait(&p_empty, (T & 1) ^ 1);   // tile T - 1's second group has read P and dS
+      if (!__all_sync(0xffffffffu, ok2)) { give_up(); break; }
       unsigned char* pt = sm + L::oP;
-      unsigned char* st = sm + L::odS;
+      unsigned char* dt = sm + L::odS;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint32_t off = tc::sw128(r, 32 * hf + cc * 8);
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t off = tc::sw128(r, 32 * hs + k * 8);
         *reinterpret_cast<uint4*>(pt + off) =
-            make_uint4(pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]), pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]),
-                       pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]), pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]));
-        *reinterpret_cast<uint4*>(st + off) =
-            make_uint4(pack_bf16(dp[cc * 8 + 0], dp[cc * 8 + 1]), pack_bf16(dp[cc * 8 + 2], dp[cc * 8 + 3]),
-                       pack_bf16(dp[cc * 8 + 4], dp[cc * 8 + 5]), pack_bf16(dp[cc * 8 + 6], dp[cc * 8 + 7]));
+            make_uint4(pack_bf16(sv[k * 8 + 0], sv[k * 8 + 1]), pack_bf16(sv[k * 8 + 2], sv[k * 8 + 3]),
+                       pack_bf16(sv[k * 8 + 4], sv[k * 8 + 5]), pack_bf16(sv[k * 8 + 6], sv[k * 8 + 7]));
+        *reinterpret_cast<uint4*>(dt + off) =
+            make_uint4(pack_bf16(dp[k * 8 + 0], dp[k * 8 + 1]), pack_bf16(dp[k * 8 + 2], dp[k * 8 + 3]),
+                       pack_bf16(dp[k * 8 + 4], dp[k * 8 + 5]), pack_bf16(dp[k * 8 + 6], dp[k * 8 + 7]));
       }
-      dq_qi = qi;                                 // this tile's query of row r, for its dQ
+      tc::fence_async_smem();
+      tc::bar_arrive(&p_full);
+      pk = pk_n;
+      l2 = l2_n;
+      D = D_n;
     }
-    tc::fence_async_smem();
-    tc::before_sync();
-    __syncthreads();
-    // dV^T += dO^T P, dK^T += Q^T dS (over the tile's 128 rows), dQ = dS K (over the 64 keys)
-    if (tid == 0) {
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- dQ epilogue
+    // row r's dQ, 32 columns per round, into staging tile (round & 1) at +128 r with 16-byte
+    // chunks swizzled by r & 7; every lane commits one bulk group per round (empty unless it
+    // issued), so "all but the newest group read out" means the other tile is free again
+    const int r = tid - 256, h = r % G;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int pk = n_tiles > 0 ? entry(0, r) : -1;
+    int rd_all = 0;
+    bool ok = true;
+    for (int T = 0; T < n_tiles; ++T) {
+      const int pk_n = T + 1 < n_tiles ? entry(T + 1, r) : -1;
+      ok = wait(&dq_full, T & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; give_up(); break; }
       tc::after_sync();
-      const uint32_t q = aQ + bf * L::TILE, o = adO + bf * L::TILE;
+      const bool issuer = h == 0 && pk >= 0;
+      const int unit = (v.b * s.N + (pk < 0 ? 0 : (pk >> 6))) * s.Hkv + v.kv;
+#pragma unroll 1
+      for (int rd = 0; rd < kD / 32; ++rd, ++rd_all) {
+        float x[32];
+        tc::tmem_ld32(tm + kColDQ + 32 * rd + lane_off, x);
+        if (rd == kD / 32 - 1) {                      // dQ's columns are free for tile T + 1
+          tc::before_sync();
+          tc::bar_arrive(&dq_empty);
+        }
+        const int sb = rd_all & 1;
+        tc::bulk_wait_read<1>();
+        __syncwarp();
+        unsigned char* stg = sm + L::oS + sb * L::STG;
 #pragma unroll
-      for (int k = 0; k < kRows / 16; ++k) {
-        const uint32_t rk = k * 2048;             // 16 rows of an MN-major operand
-        tc::mma(tm + kColDV, tc::desc_mn(o + rk, kRows * 128), tc::desc_mn(aP + rk, 0), idKV, j > 0 || k > 0);
-        tc::mma(tm + kColDK, tc::desc_mn(q + rk, kRows * 128), tc::desc_mn(adS + rk, 0), idKV, j > 0 || k > 0);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_float4(s.scale * x[4 * c], s.scale * x[4 * c + 1], s.scale * x[4 * c + 2], s.scale * x[4 * c + 3]);
+        tc::fence_async_smem();
+        __syncwarp();
+        if (issuer) tc::tma_reduce_add3(&qmap, 32 * rd, 0, unit, aS + sb * L::STG + r * 128);
+        tc::bulk_commit();
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma(tm + kColDQ, tc::desc(adS + k * 32), tc::desc_mn(aK + k * 2048, 64 * 128), idQ, k > 0);
-      tc::commit(&mma_bar);
+      pk = pk_n;
     }
-    if (j + 1 < n_tiles) meta_store(bf ^ 1);      // the next tile's metadata (loads issued above)
-    ok = wait_mma();
-    if (!__syncthreads_and(ok)) break;
-    tc::after_sync();
-    tc::tmem_ld32(tm + kColDQ + 64 * hf + lane_off, dqr[0]);
-    tc::tmem_ld32(tm + kColDQ + 64 * hf + 32 + lane_off, dqr[1]);
-    tc::before_sync();
-  }
-  if (__syncthreads_and(ok) && n_tiles > 0) dq_out();   // the last tile's dQ
-  // every thread takes the same branch below (a loop left early leaves per-thread flags apart)
-  const bool all_ok = __syncthreads_and(ok);
-  // the item's dK and dV columns: warps 0-3 read dV^T, warps 4-7 dK^T (thread = dimension)
-  if (all_ok && n_tiles > 0) {
-    tc::after_sync();
-    float x[2][32];
-    const uint32_t col = warp < 4 ? kColDV : kColDK;
-    tc::tmem_ld32(tm + col + lane_off, x[0]);
-    tc::tmem_ld32(tm + col + 32 + lane_off, x[1]);
-    float* acc = warp < 4 ? a.dv_acc : a.dk_acc;
-    const int dim = (warp & 3) * 32 + lane;
+    // the item's dK and dV columns (dQ's last commit covers every MMA): thread = dimension r
+    if (ok && n_tiles > 0) {
+      tc::after_sync();
+#pragma unroll 1
+      for (int w = 0; w < 2; ++w) {
+        float* acc = w == 0 ? a.dv_acc : a.dk_acc;
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float x[32];
+          tc::tmem_ld32(tm + (w == 0 ? kColDV : kColDK) + 32 * h2 + lane_off, x);
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int64_t jk = static_cast<int64_t>(v.kbase) + 32 * h2 + c;
-        if (jk < s.N)
-          atomicAdd(acc + ((static_cast<int64_t>(v.b) * s.N + jk) * s.Hkv_r + kvk) * kD + dim, x[h2][c]);
+          for (int c = 0; c < 32; ++c) {
+            const int64_t jk = static_cast<int64_t>(v.kbase) + 32 * h2 + c;
+            if (jk < s.N) atomicAdd(acc + ((static_cast<int64_t>(v.b) * s.N + jk) * s.Hkv_r + kvk) * kD + r, x[c]);
+          }
+        }
       }
-  }
-  // drain what was issued, then free the tensor memory
-  tc::cp_async_wait<0>();
-  tc::bulk_wait<0>();
-  if (tid == 0) {
-    if (!kv_landed) tc::bar_wait(&kv_bar, 0, kDrainNs);
-    if (mma_issued) {
-      tc::commit(&drain);
-      tc::bar_wait(&drain, 0, kDrainNs);
     }
-    if (!all_ok) atomicOr(a.status, PISA_STATUS_TIMEOUT);
+    tc::bulk_wait<0>();
   }
   tc::before_sync();
   __syncthreads();
+  if (tid == 0 && s_abort) atomicOr(a.status, PISA_STATUS_TIMEOUT);
   if (warp == 0) {
     tc::after_sync();
     tc::tmem_free(tm, 512);
