@@ -25,12 +25,14 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
 
 namespace {
 
-// Query chunks of about 48 MiB of one KV head's fp32 accumulator rows (G heads x d): the
-// items running at one time add into one chunk's rows, which then stay in L2 (128 MiB chunks
-// spilled them to HBM: 2.13 ms per launch at the 64K workload against 1.66 ms at 48 MiB and
-// 1.67 ms at 32 MiB); at most 512 queries per work item (1024 measured slower).
+// Query chunks of about 32 MiB of one KV head's fp32 accumulator rows (G heads x d): the
+// items running at one time add into one chunk's rows, which then stay in L2. At the 64K
+// workload 128 / 48 / 32 / 24 / 16 MiB took 2.13 / 1.68 / 1.67 / 1.70 / 1.74 ms per launch, and
+// at 32K the launch moved 1.51 / 1.15 / 1.02 / 0.75 GB of DRAM traffic at 48 / 32 / 24 / 16 MiB
+// (smaller chunks keep more of the accumulator in L2 but make smaller work items); at most 512
+// queries per work item (1024 measured slower).
 #ifndef PISA_FWD_CHUNK_MIB
-#define PISA_FWD_CHUNK_MIB 48
+#define PISA_FWD_CHUNK_MIB 32
 #endif
 #ifndef PISA_FWD_ITEM_CAP
 #define PISA_FWD_ITEM_CAP 512
