@@ -118,8 +118,46 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+class _NvmlReader:
+    """SM clock, its maximum and the active clock-event reasons of one GPU through the driver's
+    NVML library (read-only queries; nothing is set)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        bus = None
+        try:
+            props = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        except Exception:
+            bus = None
+        rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.dev)) if bus else 1
+        if rc != 0 and self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def read(self):
+        c, m, r = self.ct.c_uint(), self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, self.ct.byref(c)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, self.ct.byref(m))
+        self.reason_fn(self.dev, self.ct.byref(r))
+        return float(c.value), float(m.value), [n for bit, n in self.REASONS.items() if r.value & bit]
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 50 ms during the timed region."""
+    """SM clocks and throttle reasons sampled during the timed region: every 10 ms through NVML
+    from a host thread, or (without NVML) every 50 ms by nvidia-smi."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -128,9 +166,29 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.nvml = None
+        self.samples = []
         self.path = os.path.join("/tmp", f"pisa_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        try:
+            self.nvml = _NvmlReader(self.index)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.stop = threading.Event()
+
+            def loop():
+                while not self.stop.is_set():
+                    x = self.nvml.read()
+                    if x is not None:
+                        self.samples.append(x)
+                    self.stop.wait(0.01)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
@@ -141,6 +199,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self.nvml.close()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -150,39 +212,49 @@ class ClockSampler:
             self.fh.close()
 
     def wait_started(self, busy, timeout_s: float = 3.0):
-        """Run untimed work (busy) until the sampler has written its first line, so that its
+        """Run untimed work (busy) until the sampler has taken its first sample, so that its
         samples cover the timed region that follows."""
         t0 = time.perf_counter()
-        while self.proc is not None and time.perf_counter() - t0 < timeout_s:
-            try:
-                if os.path.getsize(self.path) > 0:
+        while time.perf_counter() - t0 < timeout_s:
+            if self.nvml is not None:
+                if self.samples:
                     return
-            except OSError:
-                pass
+            elif self.proc is None:
+                return
+            else:
+                try:
+                    if os.path.getsize(self.path) > 0:
+                        return
+                except OSError:
+                    pass
             busy()
             torch.cuda.synchronize()
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return None
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        if self.nvml is not None:
+            for c, m, r in self.samples:
+                sm.append(c)
+                mx.append(m)
+                reasons.update(r)
+        elif self.proc is not None and os.path.exists(self.path):
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 # Sources whose change invalidates a kernel's committed DRAM traffic figure: the kernel's own
@@ -714,14 +786,22 @@ def prefill_point(args, cfg, dev, flush):
 
 def other_configs(dev, flush):
     """The other configurations, each measured briefly on this GPU, as compact sub-objects of
-    the headline record: the 4K prefill, the selection sweep (pyramid vs flat) at 64K and 256K
-    with the pyramid build's bandwidth, the batch-32 decode and the training step."""
+    the headline record: the 4K prefill, the headline shape's throughput at 4K-256K, the
+    selection sweep (pyramid vs flat) at 16K-256K with the pyramid build's bandwidth, the
+    batch-32 decode and the training step."""
     import types
     sub = types.SimpleNamespace(steps=5, warmup=3)
     t0 = time.perf_counter()
     out = {"prefill_4k": prefill_point(sub, WORKLOADS["prefill_4k"], dev, flush)}
+    # the headline's select+attend throughput against N (4K-256K) on its own head shape
+    curve = {}
+    for N in (4096, 16384, 131072, 262144):
+        pp = prefill_point(sub, dict(WORKLOADS["prefill_64k"], N=N), dev, flush)
+        curve[f"N={N}"] = {"tokens_per_s": pp["tokens_per_s"], "ms_per_step": pp["ms_per_step"]}
+    out["prefill_vs_n"] = {"config": {k: WORKLOADS["prefill_64k"][k] for k in ("B", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
+                           "note": "N=65536 is the headline line itself", **curve}
     sw = {}
-    for N in (65536, 262144):
+    for N in (16384, 65536, 131072, 262144):
         p = sweep_point(sub, WORKLOADS["sweep"], N, dev, flush)
         e = {k: p[k] for k in ("pyramid_select_ms", "flat_select_ms", "flat_over_pyramid", "pisa1_mean_select_ms",
                                "pisa2_meanvar_select_ms", "build_ms", "build_gbs", "build_hbm_frac")}
