@@ -13,11 +13,11 @@
 // One CTA per SM takes work items (a selected leaf of one KV head and the (query, head) rows
 // that chose it) from a global counter through its item queue (tiles.cuh) and walks them in
 // tiles of 128 rows. Roles, connected by mbarrier rings:
-//   * producers (warps 12-15): per item, V^T (d x 64) transposed into a 2-stage ring; per
-//     tile, the query rows gathered with cp.async (whole rows per warp instruction) into a
-//     2-stage ring of swizzled Q tiles, confirmed one tile later (the next item's V rows
-//     load into registers meanwhile);
-//   * control (warp 16, one thread): each item's keys by TMA into a 2-stage ring; S = Q K^T
+//   * producers (warps 12-15): per tile, the query rows gathered with cp.async (whole rows per
+//     warp instruction) into a 2-stage ring of swizzled Q tiles, confirmed one tile later;
+//   * control (warp 16, one thread): each item's keys and values by TMA into 2-stage rings
+//     (the values as stored, [keys][d], read by the P V MMA as an MN-major operand, so no
+//     warp transposes them: that took a producer warp 7 % of the kernel's time); S = Q K^T
 //     (M=128, N=64) into one of 2 TMEM stages and O = P V (M=128, N=d) into one of 2 TMEM
 //     stages, issuing the next tile's S before this tile's P V;
 //   * softmax (two warpgroups, warps 0-3 and 4-7, alternate tiles): S row -> P = 2^(s log2e S
@@ -55,7 +55,7 @@ struct AttnSmem {
   static constexpr int Q_BYTES = KB * kRows * 128;
   static constexpr int P_BYTES = kRows * 128;       // 128 rows x 64 keys bf16
   static constexpr int K_BYTES = KB * 64 * 128;
-  static constexpr int V_BYTES = D * 128;           // V^T: D rows of 64 keys
+  static constexpr int V_BYTES = KB * 64 * 128;     // [64 keys x D] bf16 as K, MN-major operand
   static constexpr int STG = kRows * 128;           // 128 rows x 32 fp32
   static constexpr int oQ = 0, oP = oQ + kNQ * Q_BYTES, oK = oP + kNP * P_BYTES, oV = oK + kNKV * K_BYTES,
                        oS = oV + kNKV * V_BYTES;
@@ -67,7 +67,6 @@ struct AttnArgs {
   Dims s;
   ItemSource src;
   const __nv_bfloat16* Q;
-  const __nv_bfloat16* V;
   const int32_t* n_items;
   const float* lse_rows;   // [B, Hq, N]
   int32_t* status;
@@ -78,7 +77,8 @@ struct AttnArgs {
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap) {
+attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const __grid_constant__ CUtensorMap omap) {
   using L = AttnSmem<D>;
   constexpr int EPT = kRows / G;
   constexpr int CH = D / 8;               // 16-byte chunks per Q / V row
@@ -108,7 +108,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::bar_init(&o_empty[k], kRows);
       tc::bar_init(&k_full[k], 1);
       tc::bar_init(&k_empty[k], 1);
-      tc::bar_init(&v_full[k], kRows);
+      tc::bar_init(&v_full[k], 1);
       tc::bar_init(&v_empty[k], 1);
     }
     tc::bar_init(&drain, 1);
@@ -128,58 +128,19 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   if (warp >= 12 && warp < 16) {
     // ---------------------------------------------------------------- producers
     constexpr int RPI = 32 / CH;                      // Q rows per warp instruction
-    const int pt = tid - 384;                         // 0..127
     const int wr = (warp - 12) * 32;
     DynCursor cur;
     const bool lead = warp == 12;                     // marks the queue positions demanded
     bool have = dyn_first(s_q, EPT, &s_abort, cur, true, lead);
     int pk = have ? row_entry(a.src, cur, EPT, G, wr + lane) : -1;
-    int T = 0, I = 0;
+    int T = 0;
     bool pending = false;                             // tile T-1 issued, not yet confirmed
     auto confirm_last = [&](bool newer_outstanding) {
       if (newer_outstanding) tc::cp_async_wait<1>(); else tc::cp_async_wait<0>();
       tc::fence_async_smem();
       tc::bar_arrive(&q_full[(T - 1) % kNQ]);
     };
-    // V rows of an item: thread pt holds chunks (key, c) = (lin % 64, lin / 64) for
-    // lin = pt + 128 u; loaded one item ahead, transposed into the V stage at the item start
-    constexpr int VU = 64 * CH / kRows;
-    uint4 vreg[VU];
-    auto load_v = [&](const ItemView& v) {
-#pragma unroll
-      for (int u = 0; u < VU; ++u) {
-        const int lin = pt + kRows * u, key = lin % 64, c = lin / 64;
-        const int64_t j = static_cast<int64_t>(v.kbase) + key;
-        vreg[u] = make_uint4(0, 0, 0, 0);
-        if (j < s.N) vreg[u] = ldg_u4(a.V + ((static_cast<int64_t>(v.b) * s.N + j) * s.Hkv_r + v.kv / s.kvr) * D + c * 8);
-      }
-    };
-    if (have) load_v(cur.v);
     while (have && !aborted()) {
-      if (cur.j == 0) {
-        // the control thread may need the pending tile before it can free a V stage
-        if (pending) {
-          confirm_last(false);
-          pending = false;
-        }
-        // V^T of the item (lanes walk keys: no bank conflicts); keys past N are zero
-        const int vs = I % kNKV;
-        if (!wait(&v_empty[vs], ((I / kNKV) & 1) ^ 1)) { give_up(); break; }
-        unsigned char* vt = sm + L::oV + vs * L::V_BYTES;
-#pragma unroll
-        for (int u = 0; u < VU; ++u) {
-          const int lin = pt + kRows * u, key = lin % 64, c = lin / 64;
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&vreg[u]);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) *reinterpret_cast<__nv_bfloat16*>(vt + tc::sw128(c * 8 + q, key)) = e[q];
-        }
-        tc::fence_async_smem();
-        tc::bar_arrive(&v_full[vs]);
-        ++I;
-        // the next item's V rows load while this item's tiles are gathered
-        const ItemView v_n = queue_peek(s_q, cur.k + 1, &s_abort);
-        if (v_n.n_ent >= 0) load_v(v_n);
-      }
       DynCursor nxt = cur;
       const bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true, lead);
       const int pk_n = have_n ? row_entry(a.src, nxt, EPT, G, wr + lane) : -1;
@@ -209,9 +170,11 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   } else if (warp == 16) {
     // ---------------------------------------------------------------- control
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64), idO = tc::idesc_bf16(kRows, D);
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
+      constexpr uint32_t idO = tc::idesc_bf16_major(kRows, D, false, true);   // B = V, MN-major
       int k_issued = 0;            // key tiles issued: items 0 .. k_issued - 1
       int k_landed = 0;            // key tiles whose arrival was waited for
+      int v_issued = 0, v_landed = 0;   // the same for value tiles
       bool mma_issued = false;
       // K of the CTA's item number I into stage I % 2
       auto load_k = [&](int I, const ItemView& v) {
@@ -222,6 +185,16 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         for (int kb = 0; kb < L::KB; ++kb)
           tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &k_full[ks]);
         k_issued = I + 1;
+      };
+      // V of item I into stage I % 2 (its stage was freed by item I - 2's last P V)
+      auto load_v = [&](int I, const ItemView& v) {
+        const int vs = I % kNKV;
+        if (!wait(&v_empty[vs], ((I / kNKV) & 1) ^ 1)) { give_up(); return; }
+        tc::bar_expect_tx(&v_full[vs], L::V_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+          tc::tma_load4(aV + vs * L::V_BYTES + kb * (64 * 128), &vmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &v_full[vs]);
+        v_issued = I + 1;
       };
       // S of tile T (cursor c, item number I)
       auto issue_s = [&](const DynCursor& c, int T, int I) -> bool {
@@ -248,17 +221,25 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       // P V of tile T
       auto issue_pv = [&](const DynCursor& c, int T, int I) -> bool {
         const int vs = I % kNKV, ps = T % kNP, os = T & 1;
-        if (c.j == 0 && !wait(&v_full[vs], (I / kNKV) & 1)) return false;
+        if (c.j == 0) {
+          if (!wait(&v_full[vs], (I / kNKV) & 1)) return false;
+          v_landed = I + 1;
+        }
         if (!wait(&p_full[ps], (T / kNP) & 1) || !wait(&o_empty[os], ((T >> 1) & 1) ^ 1))
           return false;
         tc::after_sync();
+        // K step kk: keys 16 kk .. 16 kk + 15, 2048 bytes of each 64-column chunk of V
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc::mma(tmem_base + L::tmem_o + os * D, tc::desc(aP + ps * L::P_BYTES + kk * 32),
-                  tc::desc(aV + vs * L::V_BYTES + kk * 32), idO, kk > 0);
+                  tc::desc_mn(aV + vs * L::V_BYTES + kk * 2048, 64 * 128), idO, kk > 0);
         tc::commit(&o_full[os]);
         tc::commit(&p_empty[ps]);
         if (c.j + 1 == c.n_tiles) tc::commit(&v_empty[vs]);   // the item's last P V
+        if (c.j == 0) {                                          // the next item's values: their
+          const ItemView v_n = queue_peek(s_q, c.k + 1, &s_abort);   // stage is item I - 1's
+          if (v_n.n_ent >= 0) load_v(I + 1, v_n);
+        }
         return true;
       };
       // cs (S, one tile ahead) only looks; cp (P V) frees the positions it leaves
@@ -268,6 +249,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       int Ts = 0, Is = 0, Tp = 0, Ip = 0;
       if (have_s) {
         load_k(0, cs.v);
+        load_v(0, cs.v);
         if (a.stall && !wait(&never, 0)) give_up();   // runs out after the wait limit
         if (!aborted() && !issue_s(cs, 0, 0)) give_up();
         Ts = 1;
@@ -290,6 +272,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       // (each stage holds at most one: a stage is reloaded only after its item's last S), and
       // every MMA issued completes (one commit tracks them all).
       for (int J = k_landed; J < k_issued; ++J) tc::bar_wait(&k_full[J % kNKV], (J / kNKV) & 1, kDrainNs);
+      for (int J = v_landed; J < v_issued; ++J) tc::bar_wait(&v_full[J % kNKV], (J / kNKV) & 1, kDrainNs);
       if (mma_issued) {
         tc::commit(&drain);
         tc::bar_wait(&drain, 0, kDrainNs);
@@ -435,12 +418,13 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
 }
 
 template <int D, int G>
-int attn_ws_launch(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& om, int grid, cudaStream_t st) {
+int attn_ws_launch(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& om, int grid,
+                   cudaStream_t st) {
   const int smem = AttnSmem<D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(attn_ws_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope ps(st, "attn_fwd_tc");
-  attn_ws_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km, om);
+  attn_ws_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km, vm, om);
   return cudaGetLastError();
 }
 
@@ -451,7 +435,7 @@ int attn_ws_launch(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& 
 int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
                        const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
                        float* o_acc, int32_t* status, cudaStream_t st) {
-  CUtensorMap km, om;
+  CUtensorMap km, vm, om;
   const uint64_t d = static_cast<uint64_t>(s.d);
   {
     const uint64_t dims[4] = {d, static_cast<uint64_t>(s.Hkv_r), static_cast<uint64_t>(s.N),
@@ -459,6 +443,7 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
     const uint64_t strides[3] = {d * 2, d * 2 * s.Hkv_r, d * 2 * s.Hkv_r * s.N};
     const uint32_t box[4] = {64, 1, 64, 1};
     if (int e = encode_tmap(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, K, dims, strides, box)) return e;
+    if (int e = encode_tmap(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, V, dims, strides, box)) return e;
   }
   {
     const uint64_t dims[3] = {d, static_cast<uint64_t>(s.G), static_cast<uint64_t>(s.B) * s.N * s.Hkv};
@@ -473,7 +458,6 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   a.src.list = list;
   a.src.Hkv = s.Hkv;
   a.Q = static_cast<const __nv_bfloat16*>(Q);
-  a.V = static_cast<const __nv_bfloat16*>(V);
   a.n_items = n_items;
   a.lse_rows = lse_rows;
   a.status = status;
@@ -483,7 +467,7 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
 #define PISA_ATTN_CASE(DD, GG) \
-  if (s.d == DD && s.G == GG) return attn_ws_launch<DD, GG>(a, km, om, grid, st);
+  if (s.d == DD && s.G == GG) return attn_ws_launch<DD, GG>(a, km, vm, om, grid, st);
   PISA_ATTN_CASE(128, 1) PISA_ATTN_CASE(128, 2) PISA_ATTN_CASE(128, 4) PISA_ATTN_CASE(128, 8)
   PISA_ATTN_CASE(64, 1) PISA_ATTN_CASE(64, 2) PISA_ATTN_CASE(64, 4) PISA_ATTN_CASE(64, 8)
 #undef PISA_ATTN_CASE
