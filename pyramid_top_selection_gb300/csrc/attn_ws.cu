@@ -21,7 +21,8 @@
 //     (M=128, N=64) into one of 2 TMEM stages and O = P V (M=128, N=d) into one of 2 TMEM
 //     stages, issuing the next tile's S before this tile's P V;
 //   * softmax (two warpgroups, warps 0-3 and 4-7, alternate tiles): S row -> P = 2^(s log2e S
-//     - log2e lse) on the visible keys, bf16, into a 2-stage ring of swizzled P tiles;
+//     - log2e lse) on the visible keys, bf16, stored into one of 2 TMEM stages (P V then reads
+//     its A operand from tensor memory, no shared-memory tile);
 //   * epilogue (warps 8-11): O row from TMEM, 32 columns at a time, through two swizzled
 //     staging tiles; the lane holding a query's first head adds the query's G heads x 32
 //     columns into the accumulator with one TMA tensor reduce-add;
@@ -43,7 +44,7 @@ namespace pisa {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kNQ = 2, kNP = 2, kNKV = 2;   // Q, P, K/V stages; S and O have 2 TMEM stages
+constexpr int kNQ = 2, kNP = 2, kNKV = 2;   // Q, P, K/V stages; S, P and O stages are in TMEM
 constexpr int kThreads = 576;               // softmax 0-255, epilogue 256-383, producers 384-511, control, scheduler
 constexpr int kConsumerWarps = 17;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -53,14 +54,14 @@ template <int D>
 struct AttnSmem {
   static constexpr int KB = D / 64;
   static constexpr int Q_BYTES = KB * kRows * 128;
-  static constexpr int P_BYTES = kRows * 128;       // 128 rows x 64 keys bf16
   static constexpr int K_BYTES = KB * 64 * 128;
   static constexpr int V_BYTES = KB * 64 * 128;     // [64 keys x D] bf16 as K, MN-major operand
   static constexpr int STG = kRows * 128;           // 128 rows x 32 fp32
-  static constexpr int oQ = 0, oP = oQ + kNQ * Q_BYTES, oK = oP + kNP * P_BYTES, oV = oK + kNKV * K_BYTES,
+  static constexpr int oQ = 0, oK = oQ + kNQ * Q_BYTES, oV = oK + kNKV * K_BYTES,
                        oS = oV + kNKV * V_BYTES;
   static constexpr int bytes = oS + 2 * STG + 1024;
   static constexpr int tmem_o = 128;                // O stage k at column 128 + k * D
+  static constexpr int tmem_p = 128 + 2 * D;        // P stage k (bf16 pairs) at tmem_p + 32 k
 };
 
 struct AttnArgs {
@@ -92,7 +93,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   const Dims& s = a.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char* sm = smraw + ((1024 - (tc::su32(smraw) & 1023)) & 1023);
-  const uint32_t aQ = tc::su32(sm + L::oQ), aP = tc::su32(sm + L::oP), aK = tc::su32(sm + L::oK),
+  const uint32_t aQ = tc::su32(sm + L::oQ), aK = tc::su32(sm + L::oK),
                  aV = tc::su32(sm + L::oV), aS = tc::su32(sm + L::oS);
   const int n_items = *a.n_items;
 
@@ -231,8 +232,8 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         // K step kk: keys 16 kk .. 16 kk + 15, 2048 bytes of each 64-column chunk of V
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma(tmem_base + L::tmem_o + os * D, tc::desc(aP + ps * L::P_BYTES + kk * 32),
-                  tc::desc_mn(aV + vs * L::V_BYTES + kk * 2048, 64 * 128), idO, kk > 0);
+          tc::mma_ts(tmem_base + L::tmem_o + os * D, tmem_base + L::tmem_p + 32 * ps + 8 * kk,
+                     tc::desc_mn(aV + vs * L::V_BYTES + kk * 2048, 64 * 128), idO, kk > 0);
         tc::commit(&o_full[os]);
         tc::commit(&p_empty[ps]);
         if (c.j + 1 == c.n_tiles) tc::commit(&v_empty[vs]);   // the item's last P V
@@ -310,7 +311,6 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       const float l2_n = have_n ? row_lse2(nxt, pk_n) : 0.f;   // in flight during the math
       const int lim = pk < 0 ? -1 : (pk >> 6) - cur.v.kbase;    // key c is visible iff c <= lim
       const int ps = T % kNP;
-      unsigned char* pt = sm + L::oP + ps * L::P_BYTES;
       // the row's 64 keys in two halves of 32 (fewer live registers)
 #pragma unroll 1     // rolled, like the epilogue's rounds: instruction-cache footprint
       for (int half = 0; half < 2; ++half) {
@@ -336,18 +336,14 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
             break;
           }
         }
+        uint32_t pkd[16];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint4 pkd;
-          pkd.x = pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]);
-          pkd.y = pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]);
-          pkd.z = pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]);
-          pkd.w = pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]);
-          *reinterpret_cast<uint4*>(pt + tc::sw128(r, 32 * half + cc * 8)) = pkd;
-        }
+        for (int c = 0; c < 16; ++c) pkd[c] = pack_bf16(sv[2 * c], sv[2 * c + 1]);
+        tc::tmem_st16(tmem_base + L::tmem_p + 32 * ps + 16 * half + lane_off, pkd);
       }
       if (aborted()) break;
-      tc::fence_async_smem();
+      tc::tmem_wait_st();                                      // P in TMEM before the arrival
+      tc::before_sync();
       tc::bar_arrive(&p_full[ps]);
       cur = nxt;
       have = have_n;
