@@ -29,7 +29,7 @@
 //   * scheduler (warp 17, one thread): fills the item queue.
 // Every wait is bounded (the launch's wait limit); a wait that gives up sets the CTA's abort
 // flag and every role leaves its loop at its next tile. Before the CTA frees its tensor memory
-// the control thread drains what it issued (key tiles in flight, MMAs), the producers and the
+// the control thread drains what it issued (key and value tiles in flight, MMAs), the producers and the
 // epilogue their copies and reductions; the kernel then ORs PISA_STATUS_TIMEOUT into the
 // status word, and the output conversion reads it and writes poisoned outputs.
 #include "device.cuh"
