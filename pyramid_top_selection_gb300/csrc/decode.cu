@@ -41,8 +41,10 @@ __host__ __device__ inline DecodeSmem decode_smem(int G, int D, int K) {
   return m;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads)
+// GT: the query heads per KV head (1, 2, 4 or 8), a compile-time constant so that every
+// per-head loop unrolls and the attention loop reads a key's G probabilities in one load.
+template <int D, int GT>
+__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM: a batch of sequences x KV heads in one wave
 decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* Kc,
               __nv_bfloat16* Vc, float* pyr, const __nv_bfloat16* __restrict__ qn,
               const __nv_bfloat16* __restrict__ kn, const __nv_bfloat16* __restrict__ vn,
@@ -60,7 +62,8 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   const int kv = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, pq = lane & 3;
-  const int G = s.G, Ksel = s.K, C = s.C, Ncap = s.N;
+  constexpr int G = GT;
+  const int Ksel = s.K, C = s.C, Ncap = s.N;
   const int p = pos[b];
   if (p < 0 || p >= Ncap) {
     if (tid == 0) atomicOr(status, PISA_STATUS_POS_RANGE);
@@ -344,9 +347,9 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
     // their V rows (lane: dims lane*PER ..) in flight before any is used
     constexpr int PER = D / 32;
     constexpr int kKeyBatch = 16;
-    float acc[8][PER];
+    float acc[G][PER];
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int u = 0; u < PER; ++u) acc[h][u] = 0.f;
     const int nkeys = nsel * 64;
@@ -372,21 +375,33 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
         float vv[PER];
 #pragma unroll
         for (int q = 0; q < PER; ++q) vv[q] = __bfloat162float(e[q]);
+        float pw[G];                                  // the key's G probabilities, one load
+        if constexpr (G % 4 == 0) {
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          if (h < G) {
-            const float pw = Pr[h];
-#pragma unroll
-            for (int q = 0; q < PER; ++q) acc[h][q] = fmaf(pw, vv[q], acc[h][q]);
+          for (int h4 = 0; h4 < G / 4; ++h4) {
+            const float4 t = reinterpret_cast<const float4*>(Pr)[h4];
+            pw[4 * h4] = t.x;
+            pw[4 * h4 + 1] = t.y;
+            pw[4 * h4 + 2] = t.z;
+            pw[4 * h4 + 3] = t.w;
           }
+        } else if constexpr (G == 2) {
+          const float2 t = *reinterpret_cast<const float2*>(Pr);
+          pw[0] = t.x;
+          pw[1] = t.y;
+        } else {
+          pw[0] = Pr[0];
         }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int q = 0; q < PER; ++q) acc[h][q] = fmaf(pw[h], vv[q], acc[h][q]);
       }
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
-      if (h < G)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int u = 0; u < PER; ++u) red[(warp * G + h) * D + lane * PER + u] = acc[h][u];
+      for (int u = 0; u < PER; ++u) red[(warp * G + h) * D + lane * PER + u] = acc[h][u];
   }
   __syncthreads();
   for (int it = tid; it < G * D; it += kThreads) {
@@ -409,19 +424,18 @@ int launch_decode_step(const Dims& s, int32_t Ncap, const Geo& g, const int32_t*
   const size_t smem = static_cast<size_t>(L.total) * sizeof(float);
   dim3 grid(s.Hkv, s.B);
   ProfScope ps(st, "decode_step");
-  if (s.d == 128) {
-    cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    decode_kernel<128><<<grid, kThreads, smem, st>>>(
+  auto run = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    kernel<<<grid, kThreads, smem, st>>>(
         d, g, pos, static_cast<__nv_bfloat16*>(Kc), static_cast<__nv_bfloat16*>(Vc), pyr,
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
         static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(o), idx, score, status);
-  } else {
-    cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    decode_kernel<64><<<grid, kThreads, smem, st>>>(
-        d, g, pos, static_cast<__nv_bfloat16*>(Kc), static_cast<__nv_bfloat16*>(Vc), pyr,
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
-        static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(o), idx, score, status);
-  }
+  };
+#define PISA_DECODE_CASE(DD, GG) \
+  if (s.d == DD && s.G == GG) run(decode_kernel<DD, GG>);
+  PISA_DECODE_CASE(128, 1) PISA_DECODE_CASE(128, 2) PISA_DECODE_CASE(128, 4) PISA_DECODE_CASE(128, 8)
+  PISA_DECODE_CASE(64, 1) PISA_DECODE_CASE(64, 2) PISA_DECODE_CASE(64, 4) PISA_DECODE_CASE(64, 8)
+#undef PISA_DECODE_CASE
   return cudaGetLastError();
 }
 
