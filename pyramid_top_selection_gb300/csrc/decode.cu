@@ -353,24 +353,27 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
 #pragma unroll
       for (int u = 0; u < PER; ++u) acc[h][u] = 0.f;
     const int nkeys = nsel * 64;
+    const int64_t vstride = static_cast<int64_t>(s.Hkv) * D;   // cache row stride between tokens
+    // a batch (16 keys, a multiple of 16 from the start) lies inside one selected leaf: its
+    // leaf, first value row and probability row are looked up once
     for (int base = warp * kKeyBatch; base < nkeys; base += kWarps * kKeyBatch) {
+      const int sl = s_sel[base >> 6];
+      const int64_t j0 = static_cast<int64_t>(s_cand[sl]) * C + (base & 63);
+      const __nv_bfloat16* v0 = vrow(j0) + lane * PER;
+      const float* P0 = Sb + static_cast<int64_t>(sl) * (64 * G + 4) + (base & 63) * G;
       uint2 x[kKeyBatch];
 #pragma unroll
       for (int u = 0; u < kKeyBatch; ++u) {
-        const int kk = base + u;
-        const int64_t j = kk < nkeys ? static_cast<int64_t>(s_cand[s_sel[kk >> 6]]) * C + (kk & 63) : p + 1;
         x[u] = make_uint2(0, 0);
-        if (j <= p) {
-          const __nv_bfloat16* vr = vrow(j) + lane * PER;
+        if (j0 + u <= p) {
+          const __nv_bfloat16* vr = v0 + u * vstride;
           if (PER == 4) x[u] = *reinterpret_cast<const uint2*>(vr);
           else x[u].x = *reinterpret_cast<const uint32_t*>(vr);
         }
       }
 #pragma unroll
       for (int u = 0; u < kKeyBatch; ++u) {
-        const int kk = base + u;
-        if (kk >= nkeys) break;
-        const float* Pr = Sb + static_cast<int64_t>(s_sel[kk >> 6]) * (64 * G + 4) + (kk & 63) * G;
+        const float* Pr = P0 + u * G;
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x[u]);
         float vv[PER];
 #pragma unroll
