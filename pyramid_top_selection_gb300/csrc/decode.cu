@@ -208,9 +208,8 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
             const float x0 = dots[(2 * c) * G + h], x1 = dots[(2 * c + 1) * G + h];
             if (x1 == neg_inf()) {
               tot += x0;
-            } else {
-              const float mx = fmaxf(x0, x1);
-              tot += mx + logf(expf(x0 - mx) + expf(x1 - mx));
+            } else {                                 // two-term LSE: max + log(1 + exp(-|difference|))
+              tot += fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
             }
           }
           sc[u] = no_nan(tot);
