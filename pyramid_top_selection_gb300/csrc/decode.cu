@@ -253,33 +253,52 @@ decode_kernel(Dims s, Geo geo, const int32_t* __restrict__ pos, __nv_bfloat16* K
   __syncthreads();
   const int nlc = s_n[1];
   {
+    // k-step 2 kp + e of fragment lane pq takes dims 32 kp + 8 pq + 4 e .. + 3 (a dot product may
+    // take its terms in any order as long as both operands agree): a lane's dims for the two
+    // k-steps of a pair are 8 adjacent ones, one 16-byte load per key row
     uint32_t qb[KS][2];
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const uint2 v = g < G ? ldg_u2(qg + static_cast<int64_t>(g) * D + 16 * ks + 4 * pq) : make_uint2(0, 0);
+      const uint2 v = g < G ? ldg_u2(qg + static_cast<int64_t>(g) * D + 32 * (ks >> 1) + 8 * pq + 4 * (ks & 1))
+                            : make_uint2(0, 0);
       qb[ks][0] = v.x;
       qb[ks][1] = v.y;
     }
     for (int cs = warp; cs < nlc; cs += kWarps) {
       const int64_t t0 = static_cast<int64_t>(s_cand[cs]) * C;
-      for (int mt = 0; mt < 4; ++mt) {
-        const int r0 = mt * 16 + g, r1 = r0 + 8;
-        const bool v0 = t0 + r0 <= p, v1 = t0 + r1 <= p;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float* Sr = Sb + static_cast<int64_t>(cs) * (64 * G + 4);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint2 x0 = v0 ? ldg_u2(krow(t0 + r0) + 16 * ks + 4 * pq) : make_uint2(0, 0);
-          const uint2 x1 = v1 ? ldg_u2(krow(t0 + r1) + 16 * ks + 4 * pq) : make_uint2(0, 0);
-          const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
-          mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
-        }
-        float* Sr = Sb + static_cast<int64_t>(cs) * (64 * G + 4);
+      for (int mh = 0; mh < 2; ++mh) {               // two 16-key tiles per round, all loads in flight
+        uint4 x[2][2][KS / 2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * pq + e;
-          if (h < G) {
-            Sr[r0 * G + h] = v0 ? s.scale * acc[e] : neg_inf();
-            Sr[r1 * G + h] = v1 ? s.scale * acc[2 + e] : neg_inf();
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int rr = (2 * mh + m) * 16 + g + 8 * hr;
+            const bool vr = t0 + rr <= p;
+            const __nv_bfloat16* kr = krow(t0 + rr) + 8 * pq;
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) x[m][hr][kp] = vr ? ldg_u4(kr + 32 * kp) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int r0 = (2 * mh + m) * 16 + g, r1 = r0 + 8;
+          const bool v0 = t0 + r0 <= p, v1 = t0 + r1 <= p;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kp = 0; kp < KS / 2; ++kp) {
+            const uint4 x0 = x[m][0][kp], x1 = x[m][1][kp];
+            const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y}, a1[4] = {x0.z, x1.z, x0.w, x1.w};
+            mma_bf16(acc, a0, qb[2 * kp][0], qb[2 * kp][1]);
+            mma_bf16(acc, a1, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = 2 * pq + e;
+            if (h < G) {
+              Sr[r0 * G + h] = v0 ? s.scale * acc[e] : neg_inf();
+              Sr[r1 * G + h] = v1 ? s.scale * acc[2 + e] : neg_inf();
+            }
           }
         }
       }
