@@ -46,6 +46,8 @@ WORKLOADS = {
     "quality": dict(B=1, N=16384, Hq=16, Hkv=2, d=128, C=64, K=16, g=2, qtile=4, needles=True),
     "train": dict(B=4, N=16384, Hq=16, Hkv=4, d=128, C=64, K=16, g=2, qtile=4, needles=False),
     "decode": dict(B=32, N=131072, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=1, needles=False),
+    # the decode kernel at batch 4 (2 GB of cache): small enough for sectioned profiler captures
+    "decode_small": dict(B=4, N=131072, Hq=32, Hkv=8, d=128, C=64, K=16, g=2, qtile=1, needles=False),
 }
 METRIC = "PISA select+attend tokens/s vs N (4K-256K) on 1 GB300; % of HBM/TC roofline"
 L2_BYTES = 129 * 2 ** 20
@@ -992,7 +994,7 @@ def main():
         if rank == 0:
             run_quality(args, cfg, local)
         return
-    if args.workload == "decode":
+    if args.workload in ("decode", "decode_small"):
         run_decode(args, cfg, rank, world, local)
     elif args.workload == "train":
         run_train(args, cfg, rank, world, local)
