@@ -150,7 +150,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     }
   };
   // row metadata of a chunk (threads < kRows), loaded into registers and stored later
-  struct Meta { float lse, D; int i, slot, h; };
+  struct Meta { float lse, delta; int i, slot, h; };  // delta: D_i = dO_i . O_i
   auto meta_load = [&](int e0) {
     Meta m{__int_as_float(0x7f800000), 0.f, -1, 0, 0};   // +inf lse: P = 0 on padding rows
     const int r = threadIdx.x, e = e0 + r / G, h = r % G;
@@ -159,7 +159,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
       const int i = pk >> 6;
       const int64_t row = (static_cast<int64_t>(b) * s.N + i) * s.Hq + kv * G + h;
       m.lse = lse[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i];
-      m.D = delta[row];
+      m.delta = delta[row];
       m.i = i;
       m.slot = pk & 63;
       m.h = h;
@@ -170,7 +170,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     int* mb = s_meta + bf * 5 * kRows;
     const int r = threadIdx.x;
     mb[r] = __float_as_int(m.lse);
-    mb[kRows + r] = __float_as_int(m.D);
+    mb[kRows + r] = __float_as_int(m.delta);
     mb[2 * kRows + r] = m.i;
     mb[3 * kRows + r] = m.slot;
     mb[4 * kRows + r] = m.h;
