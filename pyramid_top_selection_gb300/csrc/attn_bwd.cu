@@ -45,7 +45,7 @@ struct BwdSmem {
   static constexpr int odO = oQ + 2 * kRows * KROW;
   static constexpr int odS = odO + 2 * kRows * KROW;
   static constexpr int n_bf16 = odS + kRows * SROW;
-  static constexpr int bytes = n_bf16 * 2 + 2 * kRows * (4 + 4 + 4 + 4 + 4);
+  static constexpr int bytes = n_bf16 * 2 + 2 * kRows * (4 + 4 + 4 + 4);
 };
 
 // Four 8x8 bf16 matrices, transposed: the B fragments (k = 16 rows from `row0`, n = dims
@@ -93,7 +93,7 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
   extern __shared__ __align__(16) unsigned char smraw[];
   __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smraw);
   __nv_bfloat16 *sK = sb + L::oK, *sV = sb + L::oV, *sdS = sb + L::odS;
-  // per row buffer: lse, D, query, slot, head (kRows words each)
+  // per row buffer: lse, D, query, head (kRows words each)
   int* s_meta = reinterpret_cast<int*>(sb + L::n_bf16);
 
   if (static_cast<int>(blockIdx.x) >= *n_items) return;
@@ -150,9 +150,9 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     }
   };
   // row metadata of a chunk (threads < kRows), loaded into registers and stored later
-  struct Meta { float lse, delta; int i, slot, h; };  // delta: D_i = dO_i . O_i
+  struct Meta { float lse, delta; int i, h; };  // delta: D_i = dO_i . O_i
   auto meta_load = [&](int e0) {
-    Meta m{__int_as_float(0x7f800000), 0.f, -1, 0, 0};   // +inf lse: P = 0 on padding rows
+    Meta m{__int_as_float(0x7f800000), 0.f, -1, 0};      // +inf lse: P = 0 on padding rows
     const int r = threadIdx.x, e = e0 + r / G, h = r % G;
     if (e < n_ent) {
       const int pk = list[beg + e];
@@ -161,19 +161,17 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
       m.lse = lse[(static_cast<int64_t>(b) * s.Hq + kv * G + h) * s.N + i];
       m.delta = delta[row];
       m.i = i;
-      m.slot = pk & 63;
       m.h = h;
     }
     return m;
   };
   auto meta_store = [&](int bf, const Meta& m) {
-    int* mb = s_meta + bf * 5 * kRows;
+    int* mb = s_meta + bf * 4 * kRows;
     const int r = threadIdx.x;
     mb[r] = __float_as_int(m.lse);
     mb[kRows + r] = __float_as_int(m.delta);
     mb[2 * kRows + r] = m.i;
-    mb[3 * kRows + r] = m.slot;
-    mb[4 * kRows + r] = m.h;
+    mb[3 * kRows + r] = m.h;
   };
   int pk_next[NIT];
   Meta m_next{};
@@ -198,12 +196,11 @@ attn_bwd_kernel(Dims s, GroupPlan gp, const __nv_bfloat16* __restrict__ Q, const
     __syncthreads();                 // this chunk's rows and metadata are in place
     const __nv_bfloat16* sQ = sb + L::oQ + bf * kRows * L::KROW;
     const __nv_bfloat16* sdO = sb + L::odO + bf * kRows * L::KROW;
-    const int* mb = s_meta + bf * 5 * kRows;
+    const int* mb = s_meta + bf * 4 * kRows;
     const float* s_lse = reinterpret_cast<const float*>(mb);
     const float* s_D = reinterpret_cast<const float*>(mb + kRows);
     const int* s_i = mb + 2 * kRows;
-    const int* s_slot = mb + 3 * kRows;
-    const int* s_h = mb + 4 * kRows;
+    const int* s_h = mb + 3 * kRows;
 
     // S^T and dP^T for keys key0+{g, g+8} x the 32 rows (4 n-tiles of 8 rows)
     float st[4][4], dp[4][4];
