@@ -48,6 +48,14 @@ __device__ __forceinline__ BinRange bin_range(const GroupPlan& gp, bool local_ok
   return r;
 }
 
+// The bin key of a selected leaf t: t itself, or with pairs the pair index of an even leaf;
+// -1 for no entry (none, out of range, or the odd member of a pair).
+__device__ __forceinline__ int bin_key(const GroupPlan& gp, int t) {
+  if (t < 0 || (t & ((1 << gp.shift) - 1))) return -1;
+  t >>= gp.shift;
+  return t < gp.n0 ? t : -1;
+}
+
 // Pair k of the block (32-bit arithmetic): its query i, slot and (head, chunk) group.
 __device__ __forceinline__ void pair_at(const GroupPlan& gp, const BinRange& r, int k, int& i, int& slot,
                                         int64_t& g) {
@@ -71,8 +79,8 @@ gcount_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, int3
     __syncthreads();
   }
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = sel[r.e0 + k];
-    if (t < 0 || t >= gp.n0) continue;
+    const int t = bin_key(gp, sel[r.e0 + k]);
+    if (t < 0) continue;
     int i, slot;
     int64_t g;
     pair_at(gp, r, k, i, slot, g);
@@ -136,8 +144,8 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
     __syncthreads();
   }
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = sel[r.e0 + k];
-    if (t < 0 || t >= gp.n0) continue;
+    const int t = bin_key(gp, sel[r.e0 + k]);
+    if (t < 0) continue;
     int i, slot;
     int64_t g;
     pair_at(gp, r, k, i, slot, g);
@@ -159,8 +167,8 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
   }
   __syncthreads();
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = sel[r.e0 + k];
-    if (t < 0 || t >= gp.n0) continue;
+    const int t = bin_key(gp, sel[r.e0 + k]);
+    if (t < 0) continue;
     int i, slot;
     int64_t g;
     pair_at(gp, r, k, i, slot, g);
@@ -194,10 +202,11 @@ inline int grid_for(int64_t n, int threads) {
 
 }  // namespace
 
-GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap) {
+GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap, int shift) {
   GroupPlan gp{};
   gp.N = s.N;
-  gp.n0 = s.n0;
+  gp.shift = shift;
+  gp.n0 = (s.n0 + (1 << shift) - 1) >> shift;
   gp.W = W;
   gp.cap = cap;
   int64_t nq = (nq_target / s.C) * s.C;

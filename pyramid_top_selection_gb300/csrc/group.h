@@ -12,8 +12,11 @@ namespace pisa {
 size_t align256(size_t x);
 
 // Bins are (head = b*Hkv + kv, query chunk, leaf); a work item is {bin, list start, count}.
+// With shift = 1 the bins are pairs of sibling leaves (2m, 2m + 1): only the even leaf of a pair
+// is an entry (its odd sibling, when it is a candidate too, sits at the next slot), n0 counts
+// the pairs, and an item's keys start at leaf 2m.
 struct GroupPlan {
-  int N, n0, W, cap, Nq, nch;
+  int N, n0, W, cap, Nq, nch, shift;
   int64_t heads, bins, total, max_items;
   __host__ __device__ int64_t bin(int64_t head, int i, int t) const {
     return (head * nch + i / Nq) * n0 + t;
@@ -28,7 +31,7 @@ struct GroupWs {
 };
 
 // Nq = the multiple of C nearest below `nq_target` (at least C, at most N).
-GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap);
+GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap, int shift = 0);
 GroupWs group_ws(const GroupPlan& gp, size_t base);
 // Fills off/list/items of `w` from the selection-like array sel [heads, N, W] (-1 = none).
 // The item count is icount[bins] on the device; at most gp.max_items.

@@ -726,9 +726,17 @@ flat_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q, const __nv_bfl
 #ifndef PISA_LEAF_ITEM_ROWS
 #define PISA_LEAF_ITEM_ROWS 4096
 #endif
+#ifndef PISA_LEAF_PAIRS
+#define PISA_LEAF_PAIRS 1
+#endif
+// The leaf candidates of a query come as sibling pairs (2m, 2m + 1) in adjacent slots (the
+// visible children of a kept node; with g = 4 its visible grandchildren 4a .. 4a + 3 in order),
+// so the leaf stage groups them by pair: a work item holds both leaves' 128 keys and gathers each
+// query row once for the two of them.
 GroupPlan leaf_plan(const Dims& s) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 2;
-  return make_group_plan(s, s.g * s.K, (int64_t(PISA_LEAF_CHUNK_MIB) << 20) / per_query, PISA_LEAF_ITEM_ROWS / s.G);
+  return make_group_plan(s, s.g * s.K, (int64_t(PISA_LEAF_CHUNK_MIB) << 20) / per_query, PISA_LEAF_ITEM_ROWS / s.G,
+                         PISA_LEAF_PAIRS);
 }
 
 inline int grid_for(int64_t n, int threads) {

@@ -29,7 +29,7 @@ __device__ __forceinline__ ItemView view_of(const ItemSource& src, const int4 it
   ItemView v;
   v.beg = item.y;
   v.n_ent = item.z;
-  v.kbase = src.gp.leaf_of(item.x) * 64;
+  v.kbase = src.gp.leaf_of(item.x) * (64 << src.gp.shift);
   v.head = src.gp.head_of(item.x);
   v.b = static_cast<int>(v.head / src.Hkv);
   v.kv = static_cast<int>(v.head % src.Hkv);
