@@ -37,16 +37,23 @@ namespace {
 #ifndef PISA_FWD_ITEM_CAP
 #define PISA_FWD_ITEM_CAP 512
 #endif
-GroupPlan fwd_plan(const Dims& s) {
+// With the per-block LSEs given, the output pass takes sibling leaves (2m, 2m + 1) together:
+// a row that selected both is gathered and reduced once for the pair. The S-only LSE pass
+// (head_lse NULL) keeps one leaf per item, since it writes one LSE per (row, slot).
+#ifndef PISA_FWD_PAIRS
+#define PISA_FWD_PAIRS 1
+#endif
+GroupPlan fwd_plan(const Dims& s, bool pairs) {
   const int64_t per_query = static_cast<int64_t>(s.G) * s.d * 4;
-  return make_group_plan(s, s.K, (int64_t(PISA_FWD_CHUNK_MIB) << 20) / per_query, PISA_FWD_ITEM_CAP);
+  const int sh = pairs && PISA_FWD_PAIRS ? 1 : 0;
+  return make_group_plan(s, s.K, (int64_t(PISA_FWD_CHUNK_MIB) << 20) / per_query, PISA_FWD_ITEM_CAP, sh, sh);
 }
 
 }  // namespace
 
 AttnFwdWs attn_fwd_ws(const Dims& s) {
   AttnFwdWs w{};
-  const GroupPlan gp = fwd_plan(s);
+  const GroupPlan gp = fwd_plan(s, false);   // the larger of the two plans' buffers
   const size_t rows = static_cast<size_t>(s.B) * s.N * s.Hq;
   w.status = 0;                         // first: the caller finds the status word at offset 0
   size_t o = group_ws(gp, 256).end;
@@ -60,7 +67,7 @@ int launch_attn_fwd(const Dims& s, const void* Q, const void* K, const void* V, 
                     const float* head_lse, void* O, float* lse, char* ws, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnFwdWs w = attn_fwd_ws(s);
-  const GroupPlan gp = fwd_plan(s);
+  const GroupPlan gp = fwd_plan(s, head_lse != nullptr);
   const GroupWs g = group_ws(gp, 256);
   int err = launch_group_items(gp, idx, ws, g, st);
   if (err) return err;

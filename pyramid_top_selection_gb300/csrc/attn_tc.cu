@@ -18,8 +18,8 @@ int launch_block_lse_tc(const Dims& s, const GroupPlan& gp, const void* Q, const
                         const int4* items, const int32_t* n_items, float* block_lse, int32_t* status,
                         cudaStream_t st);
 int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
-                       const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
-                       float* o_acc, int32_t* status, cudaStream_t st);
+                       const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+                       const float* lse_rows, float* o_acc, int32_t* status, cudaStream_t st);
 
 namespace {
 
@@ -120,7 +120,7 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
         s, idx, hl, lse);
   }
   if ((err = cudaGetLastError())) return err;
-  if ((err = launch_attn_out_ws(s, gp, Q, K, V, list, items, n_items, lse, o_acc, status, st))) return err;
+  if ((err = launch_attn_out_ws(s, gp, Q, K, V, idx, list, items, n_items, lse, o_acc, status, st))) return err;
   {
     ProfScope ps(st, "attn_out");
     const int64_t n8 = rows * s.d / 8;

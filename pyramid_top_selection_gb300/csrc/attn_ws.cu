@@ -50,18 +50,25 @@ constexpr int kConsumerWarps = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
 
-template <int D>
+// PR = 1: an item is a pair of sibling leaves (128 keys) and a row selected one or both of
+// them; PR = 0: one leaf.
+template <int D, int PR>
 struct AttnSmem {
   static constexpr int KB = D / 64;
+  static constexpr int NK = 64 << PR;               // keys per item
   static constexpr int Q_BYTES = KB * kRows * 128;
-  static constexpr int K_BYTES = KB * 64 * 128;
-  static constexpr int V_BYTES = KB * 64 * 128;     // [64 keys x D] bf16 as K, MN-major operand
+  static constexpr int K_BYTES = KB * NK * 128;
+  static constexpr int V_BYTES = KB * NK * 128;     // [NK keys x D] bf16 as K, MN-major operand
   static constexpr int STG = kRows * 128;           // 128 rows x 32 fp32
   static constexpr int oQ = 0, oK = oQ + kNQ * Q_BYTES, oV = oK + kNKV * K_BYTES,
                        oS = oV + kNKV * V_BYTES;
   static constexpr int bytes = oS + 2 * STG + 1024;
-  static constexpr int tmem_o = 128;                // O stage k at column 128 + k * D
-  static constexpr int tmem_p = 128 + 2 * D;        // P stage k (bf16 pairs) at tmem_p + 32 k
+  // TMEM columns: S stage k at NK k; O stage k at 2 NK + k D; P stage k (bf16 pairs) at
+  // tmem_p + 32 k, or (PR = 1, where S and O fill the 512 columns) over the first NK / 2
+  // columns of S stage k, written after the softmax has read them
+  static constexpr int tmem_o = 2 * NK;
+  static constexpr int tmem_p = 2 * NK + 2 * D;
+  static __device__ __forceinline__ uint32_t p_col(int k) { return PR ? NK * k : tmem_p + 32 * k; }
 };
 
 struct AttnArgs {
@@ -70,17 +77,19 @@ struct AttnArgs {
   const __nv_bfloat16* Q;
   const int32_t* n_items;
   const float* lse_rows;   // [B, Hq, N]
+  const int32_t* idx;      // the selection [B, Hkv, N, K] (pairs: which leaves of a pair a row chose)
   int32_t* status;
   int32_t* next_item;      // zeroed item counter
   uint64_t wait_ns;        // bound of every pipeline wait
   int stall;               // test aid: wait on a barrier nothing signals before the first MMA
 };
 
-template <int D, int G>
+template <int D, int G, int PR>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const __grid_constant__ CUtensorMap omap) {
-  using L = AttnSmem<D>;
+  using L = AttnSmem<D, PR>;
+  constexpr int NK = L::NK;
   constexpr int EPT = kRows / G;
   constexpr int CH = D / 8;               // 16-byte chunks per Q / V row
   extern __shared__ unsigned char smraw[];
@@ -102,7 +111,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::bar_init(&q_full[k], kRows);
       tc::bar_init(&q_empty[k], 1);
       tc::bar_init(&s_full[k], 1);
-      tc::bar_init(&s_empty[k], kRows);
+      tc::bar_init(&s_empty[k], PR ? 1 : kRows);   // pairs: freed by the P V that read P from it
       tc::bar_init(&p_full[k], kRows);
       tc::bar_init(&p_empty[k], 1);
       tc::bar_init(&o_full[k], 1);
@@ -171,7 +180,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   } else if (warp == 16) {
     // ---------------------------------------------------------------- control
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(kRows, 64);
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, NK);
       constexpr uint32_t idO = tc::idesc_bf16_major(kRows, D, false, true);   // B = V, MN-major
       int k_issued = 0;            // key tiles issued: items 0 .. k_issued - 1
       int k_landed = 0;            // key tiles whose arrival was waited for
@@ -184,7 +193,10 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::bar_expect_tx(&k_full[ks], L::K_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tc::tma_load4(aK + ks * L::K_BYTES + kb * (64 * 128), &kmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &k_full[ks]);
+#pragma unroll
+          for (int hp = 0; hp <= PR; ++hp)    // a pair's second leaf may lie past N: zero fill
+            tc::tma_load4(aK + ks * L::K_BYTES + kb * (NK * 128) + hp * (64 * 128), &kmap, kb * 64, v.kv / s.kvr,
+                          v.kbase + 64 * hp, v.b, &k_full[ks]);
         k_issued = I + 1;
       };
       // V of item I into stage I % 2 (its stage was freed by item I - 2's last P V)
@@ -194,7 +206,10 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::bar_expect_tx(&v_full[vs], L::V_BYTES);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb)
-          tc::tma_load4(aV + vs * L::V_BYTES + kb * (64 * 128), &vmap, kb * 64, v.kv / s.kvr, v.kbase, v.b, &v_full[vs]);
+#pragma unroll
+          for (int hp = 0; hp <= PR; ++hp)
+            tc::tma_load4(aV + vs * L::V_BYTES + kb * (NK * 128) + hp * (64 * 128), &vmap, kb * 64, v.kv / s.kvr,
+                          v.kbase + 64 * hp, v.b, &v_full[vs]);
         v_issued = I + 1;
       };
       // S of tile T (cursor c, item number I)
@@ -212,8 +227,8 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         mma_issued = true;
 #pragma unroll
         for (int k2 = 0; k2 < D / 16; ++k2)
-          tc::mma(tmem_base + 64 * ss, tc::desc(aQ + st * L::Q_BYTES + (k2 >> 2) * (kRows * 128) + (k2 & 3) * 32),
-                  tc::desc(aK + ks * L::K_BYTES + (k2 >> 2) * (64 * 128) + (k2 & 3) * 32), idS, k2 > 0);
+          tc::mma(tmem_base + NK * ss, tc::desc(aQ + st * L::Q_BYTES + (k2 >> 2) * (kRows * 128) + (k2 & 3) * 32),
+                  tc::desc(aK + ks * L::K_BYTES + (k2 >> 2) * (NK * 128) + (k2 & 3) * 32), idS, k2 > 0);
         tc::commit(&s_full[ss]);
         tc::commit(&q_empty[st]);
         if (c.j + 1 == c.n_tiles) tc::commit(&k_empty[ks]);   // the item's last S
@@ -231,11 +246,11 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::after_sync();
         // K step kk: keys 16 kk .. 16 kk + 15, 2048 bytes of each 64-column chunk of V
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_ts(tmem_base + L::tmem_o + os * D, tmem_base + L::tmem_p + 32 * ps + 8 * kk,
-                     tc::desc_mn(aV + vs * L::V_BYTES + kk * 2048, 64 * 128), idO, kk > 0);
+        for (int kk = 0; kk < NK / 16; ++kk)
+          tc::mma_ts(tmem_base + L::tmem_o + os * D, tmem_base + L::p_col(ps) + 8 * kk,
+                     tc::desc_mn(aV + vs * L::V_BYTES + kk * 2048, NK * 128), idO, kk > 0);
         tc::commit(&o_full[os]);
-        tc::commit(&p_empty[ps]);
+        tc::commit(PR ? &s_empty[ps] : &p_empty[ps]);   // pairs: P lives in its S stage
         if (c.j + 1 == c.n_tiles) tc::commit(&v_empty[vs]);   // the item's last P V
         if (c.j == 0) {                                          // the next item's values: their
           const ItemView v_n = queue_peek(s_q, c.k + 1, &s_abort);   // stage is item I - 1's
@@ -291,6 +306,15 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       if (pkv < 0) return 0.f;
       return a.lse_rows[(static_cast<int64_t>(c.v.b) * s.Hq + c.v.kv * G + h) * s.N + (pkv >> 6)] * kLog2e;
     };
+    // pairs: bit l set when the row chose leaf l of the pair (its entry holds the slot of the
+    // first chosen one; the selection is ascending, so a chosen second leaf follows it)
+    auto row_sel = [&](const DynCursor& c, int pkv) -> int {
+      if (!PR || pkv < 0) return 1;
+      const int64_t base = (c.v.head * s.N + (pkv >> 6)) * s.K;
+      const int slot = pkv & 63, t0 = a.idx[base + slot];
+      if (t0 & 1) return 2;
+      return slot + 1 < s.K && a.idx[base + slot + 1] == t0 + 1 ? 3 : 1;
+    };
     DynCursor cur;
     bool have = dyn_first(s_q, EPT, &s_abort, cur, true);
     int T = 0;
@@ -300,6 +324,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
     }
     int pk = have ? row_entry(a.src, cur, EPT, G, r) : -1;
     float l2 = have ? row_lse2(cur, pk) : 0.f;
+    int sel = have ? row_sel(cur, pk) : 1;
     while (have && !aborted()) {
       DynCursor nxt = cur;
       bool have_n = dyn_next(s_q, EPT, &s_abort, nxt, true);
@@ -309,18 +334,20 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       if (!__all_sync(0xffffffffu, ok)) { give_up(); break; }
       tc::after_sync();
       const float l2_n = have_n ? row_lse2(nxt, pk_n) : 0.f;   // in flight during the math
+      const int sel_n = have_n ? row_sel(nxt, pk_n) : 1;
       const int lim = pk < 0 ? -1 : (pk >> 6) - cur.v.kbase;    // key c is visible iff c <= lim
       const int ps = T % kNP;
-      // the row's 64 keys in two halves of 32 (fewer live registers)
+      // the row's keys in quarters of 32 (fewer live registers); with pairs, P overwrites the
+      // front of the S stage, columns the later quarters do not read
 #pragma unroll 1     // rolled, like the epilogue's rounds: instruction-cache footprint
-      for (int half = 0; half < 2; ++half) {
+      for (int q = 0; q < NK / 32; ++q) {
         float sv[32];
-        tc::tmem_ld32(tmem_base + 64 * sg + 32 * half + lane_off, sv);
-        if (half == 1) {                                       // the S stage is free for S(T + 2)
+        tc::tmem_ld32(tmem_base + NK * sg + 32 * q + lane_off, sv);
+        if (!PR && q == 1) {                                   // the S stage is free for S(T + 2)
           tc::before_sync();
           tc::bar_arrive(&s_empty[sg]);
         }
-        const int lh = lim - 32 * half;
+        const int lh = (sel >> (q >> 1)) & 1 ? lim - 32 * q : -1;   // a leaf the row did not choose: P = 0
         const uint64_t cc = tc::pack2(c1, c1), ll = tc::pack2(-l2, -l2);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {         // exponent arguments on packed pairs
@@ -329,7 +356,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
           sv[c] = c <= lh ? tc::ex2(y0) : 0.f;
           sv[c + 1] = c + 1 <= lh ? tc::ex2(y1) : 0.f;
         }
-        if (half == 0) {
+        if (!PR && q == 0) {
           const bool ok2 = wait(&p_empty[ps], ((T / kNP) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, ok2)) {
             give_up();
@@ -339,7 +366,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
         uint32_t pkd[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) pkd[c] = pack_bf16(sv[2 * c], sv[2 * c + 1]);
-        tc::tmem_st16(tmem_base + L::tmem_p + 32 * ps + 16 * half + lane_off, pkd);
+        tc::tmem_st16(tmem_base + L::p_col(ps) + 16 * q + lane_off, pkd);
       }
       if (aborted()) break;
       tc::tmem_wait_st();                                      // P in TMEM before the arrival
@@ -349,6 +376,7 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
       have = have_n;
       pk = pk_n;
       l2 = l2_n;
+      sel = sel_n;
       T += 2;
     }
   } else if (warp < 12) {
@@ -413,24 +441,26 @@ attn_ws_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap, const
   }
 }
 
-template <int D, int G>
+template <int D, int G, int PR>
 int attn_ws_launch(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& om, int grid,
                    cudaStream_t st) {
-  const int smem = AttnSmem<D>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(attn_ws_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = AttnSmem<D, PR>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_ws_kernel<D, G, PR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope ps(st, "attn_fwd_tc");
-  attn_ws_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km, vm, om);
+  attn_ws_kernel<D, G, PR><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km, vm, om);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// Attention output pass over the grouped (selected leaf, query) pairs: adds every row's
-// normalised block contributions into the fp32 accumulator o_acc [B, N, Hq, d].
+// Attention output pass over the grouped (selected leaf, query) entries: adds every row's
+// normalised block contributions into the fp32 accumulator o_acc [B, N, Hq, d]. With a plan
+// of sibling pairs (gp.shift = 1, deduplicated) an item covers both leaves of a pair and a
+// row's entry stands for the members it selected (read back from idx).
 int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const void* K, const void* V,
-                       const int32_t* list, const int4* items, const int32_t* n_items, const float* lse_rows,
-                       float* o_acc, int32_t* status, cudaStream_t st) {
+                       const int32_t* idx, const int32_t* list, const int4* items, const int32_t* n_items,
+                       const float* lse_rows, float* o_acc, int32_t* status, cudaStream_t st) {
   CUtensorMap km, vm, om;
   const uint64_t d = static_cast<uint64_t>(s.d);
   {
@@ -456,14 +486,17 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
   a.Q = static_cast<const __nv_bfloat16*>(Q);
   a.n_items = n_items;
   a.lse_rows = lse_rows;
+  a.idx = idx;
   a.status = status;
   a.next_item = status + 32;
   a.wait_ns = wait_limit_ns();
   a.stall = test_stall();
   const int64_t mi = gp.max_items;
   const int grid = static_cast<int>(mi < sm_count() ? mi : sm_count());
-#define PISA_ATTN_CASE(DD, GG) \
-  if (s.d == DD && s.G == GG) return attn_ws_launch<DD, GG>(a, km, vm, om, grid, st);
+#define PISA_ATTN_CASE(DD, GG)                                                                         \
+  if (s.d == DD && s.G == GG)                                                                          \
+    return gp.shift ? attn_ws_launch<DD, GG, 1>(a, km, vm, om, grid, st)                               \
+                    : attn_ws_launch<DD, GG, 0>(a, km, vm, om, grid, st);
   PISA_ATTN_CASE(128, 1) PISA_ATTN_CASE(128, 2) PISA_ATTN_CASE(128, 4) PISA_ATTN_CASE(128, 8)
   PISA_ATTN_CASE(64, 1) PISA_ATTN_CASE(64, 2) PISA_ATTN_CASE(64, 4) PISA_ATTN_CASE(64, 8)
 #undef PISA_ATTN_CASE

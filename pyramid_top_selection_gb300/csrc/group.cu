@@ -48,12 +48,21 @@ __device__ __forceinline__ BinRange bin_range(const GroupPlan& gp, bool local_ok
   return r;
 }
 
-// The bin key of a selected leaf t: t itself, or with pairs the pair index of an even leaf;
-// -1 for no entry (none, out of range, or the odd member of a pair).
-__device__ __forceinline__ int bin_key(const GroupPlan& gp, int t) {
-  if (t < 0 || (t & ((1 << gp.shift) - 1))) return -1;
-  t >>= gp.shift;
+// The bin key of a selected leaf t (prev: the unit's previous slot, -1 at slot 0): t itself, or
+// with pairs the pair index; -1 for no entry (none, out of range, or a pair's member that is
+// not its first entry).
+__device__ __forceinline__ int bin_key(const GroupPlan& gp, int t, int prev) {
+  if (t < 0) return -1;
+  if (gp.shift) {
+    if (t & 1) {
+      if (!gp.dedup || prev == t - 1) return -1;
+    }
+    t >>= 1;
+  }
   return t < gp.n0 ? t : -1;
+}
+__device__ __forceinline__ int entry_key(const GroupPlan& gp, const int32_t* __restrict__ sel, int64_t e, int k) {
+  return bin_key(gp, sel[e], gp.dedup && k % gp.W ? sel[e - 1] : -1);
 }
 
 // Pair k of the block (32-bit arithmetic): its query i, slot and (head, chunk) group.
@@ -79,7 +88,7 @@ gcount_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, int3
     __syncthreads();
   }
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = bin_key(gp, sel[r.e0 + k]);
+    const int t = entry_key(gp, sel, r.e0 + k, k);
     if (t < 0) continue;
     int i, slot;
     int64_t g;
@@ -144,7 +153,7 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
     __syncthreads();
   }
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = bin_key(gp, sel[r.e0 + k]);
+    const int t = entry_key(gp, sel, r.e0 + k, k);
     if (t < 0) continue;
     int i, slot;
     int64_t g;
@@ -167,7 +176,7 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
   }
   __syncthreads();
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
-    const int t = bin_key(gp, sel[r.e0 + k]);
+    const int t = entry_key(gp, sel, r.e0 + k, k);
     if (t < 0) continue;
     int i, slot;
     int64_t g;
@@ -202,10 +211,11 @@ inline int grid_for(int64_t n, int threads) {
 
 }  // namespace
 
-GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap, int shift) {
+GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap, int shift, int dedup) {
   GroupPlan gp{};
   gp.N = s.N;
   gp.shift = shift;
+  gp.dedup = dedup;
   gp.n0 = (s.n0 + (1 << shift) - 1) >> shift;
   gp.W = W;
   gp.cap = cap;
