@@ -72,8 +72,15 @@ __device__ __forceinline__ void ldg_pair(const uint4* a, uint4& x, uint4& y) {
       : "l"(a));
 }
 
+#ifndef PISA_ROUTE_PRED
+#define PISA_ROUTE_PRED 1
+#endif
+#ifndef PISA_ROUTE_SUFFIX
+#define PISA_ROUTE_SUFFIX 1
+#endif
 // Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid (always valid
-// addresses); invalid rows contribute zeros.
+// addresses); invalid rows contribute zeros and load nothing (a lane group whose row is
+// invalid issues no request, so sparse row sets cost only their valid rows).
 template <int KS>
 __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0, bool v0,
                                                const uint4* r1, bool v1, int p,
@@ -81,9 +88,9 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
   const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int kp = 0; kp < KS / 2; ++kp) {
-    uint4 x0[2], x1[2];
-    ldg_pair(r0 + 8 * kp + 2 * p, x0[0], x0[1]);
-    ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
+    uint4 x0[2] = {z, z}, x1[2] = {z, z};
+    if (v0 || !PISA_ROUTE_PRED) ldg_pair(r0 + 8 * kp + 2 * p, x0[0], x0[1]);
+    if (v1 || !PISA_ROUTE_PRED) ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const uint4 a = v0 ? x0[e] : z, c = v1 ? x1[e] : z;
@@ -160,26 +167,38 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     }
   }
 
-  // pd0[h] = sum over keys j in [ti*C, i] of q_h . k_j  (keys are exact bf16).
+  // pd0[h] = sum over keys j in [ti*C, i] of q_h . k_j  (keys are exact bf16). Past the middle
+  // of the leaf it is taken as q_h . S(0, ti) minus the keys after i: fewer rows to read.
   float pda = 0.f, pdb = 0.f;
   {
     const int64_t j0 = static_cast<int64_t>(ti) * C;
     const int nkeys = i - static_cast<int>(j0) + 1;
-    for (int mt = 0; mt * 16 < nkeys; ++mt) {
+    const int cnt = static_cast<int>(min(j0 + C, static_cast<int64_t>(s.N)) - j0);   // keys of leaf ti
+    const bool suf = PISA_ROUTE_SUFFIX && 2 * nkeys > cnt + 2;
+    const int64_t k0 = suf ? static_cast<int64_t>(i) + 1 : j0;     // explicit key rows k0 ..
+    const int nr = suf ? cnt - nkeys : nkeys;                      // .. k0 + nr - 1
+    for (int mt = 0; mt * 16 < nr; ++mt) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const int r0 = mt * 16 + g, r1 = r0 + 8;
-      const __nv_bfloat16* k0 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r0) * s.Hkv_r + kvk) * D;
-      const __nv_bfloat16* k1 = Kt + ((static_cast<int64_t>(b) * s.N + j0 + r1) * s.Hkv_r + kvk) * D;
+      const __nv_bfloat16* kr0 = Kt + ((static_cast<int64_t>(b) * s.N + k0 + r0) * s.Hkv_r + kvk) * D;
+      const __nv_bfloat16* kr1 = Kt + ((static_cast<int64_t>(b) * s.N + k0 + r1) * s.Hkv_r + kvk) * D;
 #pragma unroll
       for (int kp = 0; kp < KS / 2; ++kp) {
-        const uint4 x0 = r0 < nkeys ? ldg_u4(k0 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
-        const uint4 x1 = r1 < nkeys ? ldg_u4(k1 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
+        const uint4 x0 = r0 < nr ? ldg_u4(kr0 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
+        const uint4 x1 = r1 < nr ? ldg_u4(kr1 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
         const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y}, a1[4] = {x0.z, x1.z, x0.w, x1.w};
         mma_bf16(acc, a0, qb[2 * kp][0], qb[2 * kp][1]);
         mma_bf16(acc, a1, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
       }
       pda += acc[0] + acc[2];
       pdb += acc[1] + acc[3];
+    }
+    if (suf) {   // the leaf's sum as A row 0 (lanes g = 0); the other lanes hold minus their part
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* lr = spl_h + (geo.off[0] + ti) * RQ;
+      mma_split_rows<KS>(acc, lr, g == 0, lr, false, p, qb);
+      pda = acc[0] - pda;
+      pdb = acc[1] - pdb;
     }
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -514,6 +533,150 @@ topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restr
   }
 }
 
+// One thread per (b, KV head, query) for W <= 32: the warp version above spends most of its
+// time in shuffles (two per candidate and lane). Here a CTA stages its units' candidate rows
+// in shared memory with coalesced loads, and every thread sorts its own row in registers with
+// two bitonic networks: the (score, leaf) pairs by the selection order, then the first K of
+// them by leaf index. A pair is one 64-bit key, the order-preserving bits of the score above
+// the complemented leaf index (lower leaf wins a tie) and the candidate slot; an empty slot
+// is key 0, below every candidate. Same outputs and poisoning as the warp version.
+#ifndef PISA_TOPK_THREAD
+#define PISA_TOPK_THREAD 1
+#endif
+constexpr int kTopkUnits = 128;   // units (threads) per CTA
+constexpr uint32_t kLeafMask = (1u << 26) - 1;   // leaf indices < 2^26 (N < 2^32 tokens of C = 64)
+
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+  const uint32_t u = __float_as_uint(x + 0.f);   // -0 -> +0: equal scores tie on the leaf
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+template <typename T>
+__device__ __forceinline__ void bitonic32(T (&a)[32], bool descending) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool first_high = ((i & k) == 0) == descending;   // a[i] should end up the larger
+          const T x = a[i], y = a[l];
+          const bool sw = first_high ? x < y : x > y;
+          a[i] = sw ? y : x;
+          a[l] = sw ? x : y;
+        }
+      }
+}
+
+__global__ void __launch_bounds__(kTopkUnits)
+topk_thread_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restrict__ cand,
+                   const float* __restrict__ csc, const float* __restrict__ chead, int32_t* __restrict__ idx,
+                   float* __restrict__ score, float* __restrict__ head_lse, const int32_t* __restrict__ status) {
+  __shared__ int32_t s_c[kTopkUnits * 33];
+  __shared__ float s_s[kTopkUnits * 33];
+  const int tid = threadIdx.x;
+  const int64_t u0 = blockIdx.x * static_cast<int64_t>(kTopkUnits);
+  const int nu = static_cast<int>(min(static_cast<int64_t>(kTopkUnits), units - u0));
+  const int stride = W | 1;                  // odd row stride: a thread's row reads are conflict-free
+  const bool timeout = (*status & PISA_STATUS_TIMEOUT) != 0;
+  if (!timeout) {
+    for (int e = tid; e < nu * W; e += kTopkUnits) {
+      const int r = e / W, c = e - r * W;
+      s_c[r * stride + c] = cand[u0 * W + e];
+      s_s[r * stride + c] = csc[u0 * W + e];
+    }
+  }
+  __syncthreads();
+  if (timeout) {
+    if (tid >= nu) return;
+    const int64_t u = u0 + tid;
+    const int64_t hrow = (u / N) * G * N + u % N;    // head_lse row of head 0
+    const float nan = __int_as_float(0x7fc00000);
+    for (int q = 0; q < Ksel; ++q) {
+      idx[u * Ksel + q] = -1;
+      if (score) score[u * Ksel + q] = nan;
+      if (head_lse)
+        for (int h = 0; h < G; ++h) head_lse[(hrow + static_cast<int64_t>(h) * N) * Ksel + q] = nan;
+    }
+    return;
+  }
+  if (tid < nu) {
+    uint64_t key[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      key[j] = 0;
+      if (j < W) {
+        const int c = s_c[tid * stride + j];
+        if (c >= 0)
+          key[j] = (static_cast<uint64_t>(ordered_bits(no_nan(s_s[tid * stride + j]))) << 32) |
+                   ((kLeafMask - static_cast<uint32_t>(c)) << 6) | static_cast<uint32_t>(j);
+      }
+    }
+    bitonic32(key, true);
+    // the first K non-empty keys, re-keyed as (leaf, slot) and sorted by leaf; the rest last
+    uint32_t k2[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const bool keep = j < Ksel && key[j] != 0;
+      const uint32_t lo = static_cast<uint32_t>(key[j]);
+      k2[j] = keep ? (((kLeafMask - (lo >> 6)) << 6) | (lo & 63u)) : 0xffffffffu;
+    }
+    bitonic32(k2, false);
+    // the thread's own row, overwritten in place: slot q < K holds (leaf << 6 | source slot)
+    // or -1, and the score (read before any write: a source slot may lie below q)
+    float sq[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q)
+      sq[q] = q < Ksel && k2[q] != 0xffffffffu ? no_nan(s_s[tid * stride + (k2[q] & 63u)]) : neg_inf();
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      if (q >= Ksel) break;
+      s_c[tid * stride + q] = k2[q] == 0xffffffffu ? -1 : static_cast<int32_t>(k2[q]);
+      s_s[tid * stride + q] = sq[q];
+    }
+  }
+  __syncthreads();
+  // coalesced stores: the CTA's units are consecutive, so its idx / score rows are one range,
+  // and per head its head_lse rows are one range within each (batch, KV head)
+  for (int e = tid; e < nu * Ksel; e += kTopkUnits) {
+    const int t = e / Ksel, q = e - t * Ksel;
+    const int32_t v = s_c[t * stride + q];
+    idx[u0 * Ksel + e] = v < 0 ? -1 : (v >> 6);
+    if (score) score[u0 * Ksel + e] = s_s[t * stride + q];
+  }
+  if (head_lse) {
+    // a lane reads one kept candidate's G per-head terms (one contiguous row) and writes them
+    // to the G head rows: per head, the warp's stores are consecutive
+    for (int e = tid; e < nu * Ksel; e += kTopkUnits) {
+      const int t = e / Ksel, q = e - t * Ksel;
+      const int64_t u = u0 + t;
+      const int32_t v = s_c[t * stride + q];
+      float hv[8];
+      const float* src = chead + (u * W + (v & 63)) * G;
+      if (v >= 0 && G % 4 == 0) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        hv[0] = a.x; hv[1] = a.y; hv[2] = a.z; hv[3] = a.w;
+        if (G == 8) {
+          const float4 c = __ldg(reinterpret_cast<const float4*>(src) + 1);
+          hv[4] = c.x; hv[5] = c.y; hv[6] = c.z; hv[7] = c.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 8; ++h) hv[h] = v >= 0 && h < G ? src[h] : neg_inf();
+      }
+      float* dst = head_lse + ((u / N) * G * N + u % N) * Ksel + q;
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < G) dst[static_cast<int64_t>(h) * N * Ksel] = hv[h];
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------- flat BSA
 // One CTA per (query leaf block tq, KV head, batch), 4 warps x 16 queries. Leaf t < tq is
 // scored by s * qbar . S(0,t) / C with qbar = sum_h q_h (a dot product is linear, so the
@@ -754,8 +917,13 @@ int launch_topk(const Dims& s, int W, const int32_t* cand, const float* cscore, 
                 int32_t* idx, float* score, float* head_lse, const int32_t* status, cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
   ProfScope ps(st, "topk");
-  (W > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-      units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse, status);
+  if (W <= 32 && PISA_TOPK_THREAD)
+    topk_thread_kernel<<<static_cast<unsigned>((units + kTopkUnits - 1) / kTopkUnits), kTopkUnits, 0, st>>>(
+        units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse, status);
+  else
+    (W > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32,
+                                                  0, st>>>(units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score,
+                                                           head_lse, status);
   return cudaGetLastError();
 }
 
@@ -823,14 +991,8 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   if ((err = launch_leaf_tc(s, gp, Q, K, list, items, n_items, W, cscore, chead,
                             reinterpret_cast<int32_t*>(ws + w.status), st)))
     return err;
-  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
-  {
-    ProfScope ps(st, "topk");
-    (W > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, W, s.K, s.N, s.G, cand, cscore, chead, idx, score, head_lse,
-        reinterpret_cast<const int32_t*>(ws + w.status));
-  }
-  return cudaGetLastError();
+  return launch_topk(s, W, cand, cscore, chead, idx, score, head_lse, reinterpret_cast<const int32_t*>(ws + w.status),
+                     st);
 }
 
 // PISA-1 ablation: the descent with mean scores at every level, the leaf candidates scored by
@@ -859,14 +1021,8 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
 #undef PISA_ROUTE
   }
   if ((err = cudaGetLastError())) return err;
-  const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * s.N;
-  {
-    ProfScope ps(st, "topk");
-    (s.g * s.K > 32 ? topk_kernel<2> : topk_kernel<1>)<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
-        units, s.g * s.K, s.K, s.N, s.G, cand, cscore, nullptr, idx, score, nullptr,
-        reinterpret_cast<const int32_t*>(ws + w.status));
-  }
-  return cudaGetLastError();
+  return launch_topk(s, s.g * s.K, cand, cscore, nullptr, idx, score, nullptr,
+                     reinterpret_cast<const int32_t*>(ws + w.status), st);
 }
 
 int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
