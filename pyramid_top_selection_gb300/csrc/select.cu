@@ -93,13 +93,24 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
     if (v1 || !PISA_ROUTE_PRED) ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const uint4 a = v0 ? x0[e] : z, c = v1 ? x1[e] : z;
+      const uint4 a = v0 || PISA_ROUTE_PRED ? x0[e] : z, c = v1 || PISA_ROUTE_PRED ? x1[e] : z;
       const uint32_t ahi[4] = {a.x, c.x, a.y, c.y};
       const uint32_t alo[4] = {a.z, c.z, a.w, c.w};
       mma_bf16(acc, ahi, qb[2 * kp + e][0], qb[2 * kp + e][1]);
       mma_bf16(acc, alo, qb[2 * kp + e][0], qb[2 * kp + e][1]);
     }
   }
+}
+
+// Order-preserving unsigned image of a score (after no_nan): x < y iff ordered_bits(x) <
+// ordered_bits(y); -0 and +0 map to the same value, so equal scores tie on the index.
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+  const uint32_t u = __float_as_uint(x + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// A node's selection key: higher score first, then lower node index (the order of beats()).
+__device__ __forceinline__ uint64_t node_key(float sc, int node) {
+  return (static_cast<uint64_t>(ordered_bits(sc)) << 32) | (0x7fffffffu - static_cast<uint32_t>(node));
 }
 
 // Fan-out 4: the visible grandchildren 4a .. 4a+3 at the level below the next (node span
@@ -135,6 +146,7 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   __shared__ int s_cand[kWarps][MC];
   __shared__ int s_kept[kWarps][MC / 2];
   __shared__ float s_sc[kWarps][MC];
+  __shared__ uint64_t s_key[kWarps][MC];   // node_key of every scored candidate
   __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
   __shared__ float s_pd[kWarps][PISA_MAX_LEVELS][8];
   // dots of every candidate's two children (q . key sum, per head), two level buffers
@@ -246,6 +258,7 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   int* cand = s_cand[warp];
   int* kept = s_kept[warp];
   float* sc = s_sc[warp];
+  uint64_t* key = s_key[warp];
   int nkept = 1;
   if (lane == 0) kept[0] = 0;
   __syncwarp();
@@ -298,14 +311,15 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     float (*cd)[2][8] = s_cdot[warp][nxt];
     float (*pdots)[2][8] = s_cdot[warp][cur];
     // child dots for one candidate slot cs (lane's two heads): returns the score part
+    // Key counts: a visible child off the query's path ends before i, so it is full (cspan
+    // keys); the path child holds the keys up to i. Scale factors s / count, once per level.
+    const float cnt_path = static_cast<float>(i - static_cast<int64_t>(pathc) * cspan + 1);
+    const float f_full = s.scale / static_cast<float>(cspan), f_path = s.scale / cnt_path;
     auto finish = [&](int cs, int c, float l0, float l1, float r0, float r1, bool rv) {
       const int ch0 = 2 * c, ch1 = 2 * c + 1;
-      const int64_t st0 = static_cast<int64_t>(ch0) * cspan, st1 = static_cast<int64_t>(ch1) * cspan;
-      float cnt0, cnt1;
-      if (ch0 == pathc) { l0 = pd0; l1 = pd1; cnt0 = static_cast<float>(i - st0 + 1); }
-      else cnt0 = static_cast<float>(min(st0 + cspan, static_cast<int64_t>(s.N)) - st0);
-      if (ch1 == pathc) { r0 = pd0; r1 = pd1; cnt1 = static_cast<float>(i - st1 + 1); }
-      else cnt1 = static_cast<float>(min(st1 + cspan, static_cast<int64_t>(s.N)) - st1);
+      float f0 = f_full, f1 = f_full;
+      if (ch0 == pathc) { l0 = pd0; l1 = pd1; f0 = f_path; }
+      if (ch1 == pathc) { r0 = pd0; r1 = pd1; f1 = f_path; }
       if (cs < nc) {
         cd[cs][0][2 * p] = l0; cd[cs][0][2 * p + 1] = l1;
         cd[cs][1][2 * p] = r0; cd[cs][1][2 * p + 1] = r1;
@@ -316,11 +330,13 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       for (int e = 0; e < 2; ++e) {
         float l;
         if constexpr (MEAN) {   // the node's own mean key: (left + right sums) / (their counts)
-          l = rv ? (lv[e] + rvv[e]) * (s.scale / (cnt0 + cnt1)) : lv[e] * (s.scale / cnt0);
+          const float cnt0 = ch0 == pathc ? cnt_path : static_cast<float>(cspan);
+          const float cnt1 = ch1 == pathc ? cnt_path : static_cast<float>(cspan);
+          l = rv ? (lv[e] + rvv[e]) * (s.scale / (cnt0 + cnt1)) : lv[e] * f0;
         } else {
-          const float x0 = lv[e] * (s.scale / cnt0);
+          const float x0 = lv[e] * f0;
           if (rv) {     // LSE of two terms: max + log(1 + exp(-|difference|))
-            const float x1 = rvv[e] * (s.scale / cnt1);
+            const float x1 = rvv[e] * f1;
             l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
           } else {
             l = x0;
@@ -357,8 +373,8 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         pa += __shfl_xor_sync(0xffffffffu, pa, 2);
         pb += __shfl_xor_sync(0xffffffffu, pb, 1);
         pb += __shfl_xor_sync(0xffffffffu, pb, 2);
-        if (p == 0 && csa < nc) sc[csa] = no_nan(pa);
-        if (p == 0 && csb < nc) sc[csb] = no_nan(pb);
+        if (p == 0 && csa < nc) key[csa] = node_key(no_nan(pa), ca);
+        if (p == 0 && csb < nc) key[csb] = node_key(no_nan(pb), cb);
       }
     } else {
       // 8 candidates per MMA tile: row g and g+8 are candidate g's two children
@@ -376,15 +392,16 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         if (c >= 0) part = finish(cs, c, acc[0], acc[1], acc[2], acc[3], v1);
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (p == 0 && cs < nc) sc[cs] = no_nan(part);
+        if (p == 0 && cs < nc) key[cs] = node_key(no_nan(part), c);
       }
     }
     __syncwarp();
     for (int s2 = lane; s2 < nc; s2 += 32) {
-      const float my = sc[s2];
+      const uint64_t my = key[s2];
       const int mi = cand[s2];
       int rank = 0;
-      for (int o = 0; o < nc; ++o) rank += beats(sc[o], cand[o], my, mi) ? 1 : 0;
+#pragma unroll 8
+      for (int o = 0; o < nc; ++o) rank += key[o] > my ? 1 : 0;
       if (rank < Ksel) { kept[rank] = mi; kslot[rank] = s2; }
     }
     nkept = Ksel;
@@ -546,13 +563,6 @@ topk_kernel(int64_t units, int W, int Ksel, int N, int G, const int32_t* __restr
 constexpr int kTopkUnits = 128;   // units (threads) per CTA
 constexpr uint32_t kLeafMask = (1u << 26) - 1;   // leaf indices < 2^26 (N < 2^32 tokens of C = 64)
 
-__device__ __forceinline__ uint32_t ordered_bits(float x) {
-  const uint32_t u = __float_as_uint(x + 0.f);   // -0 -> +0: equal scores tie on the leaf
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float from_ordered(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
 
 template <typename T>
 __device__ __forceinline__ void bitonic32(T (&a)[32], bool descending) {
