@@ -24,50 +24,55 @@ int launch_attn_out_ws(const Dims& s, const GroupPlan& gp, const void* Q, const 
 namespace {
 
 // lse = log sum_k exp(block_lse_k) over each row's valid slots, written to the caller's lse
-// ([B,Hq,N]); rows in lse order. A warp takes 32 consecutive rows: it reads their 32 x K
-// block LSEs and slot indices with coalesced loads into shared memory (rows padded to K+1
-// words), then each lane reduces one row.
-constexpr int kRowWarps = 4;
+// ([B,Hq,N]); rows in lse order, one thread per row. A row's K block LSEs are contiguous, and
+// so are its slot indices (shared by the G heads of its KV head): 16-byte loads when K is a
+// multiple of 4.
+constexpr int kRowThreads = 256;
 constexpr int kMaxK = 32;
 
-__global__ void __launch_bounds__(kRowWarps * 32)
+template <bool V4>
+__global__ void __launch_bounds__(kRowThreads)
 attn_rows_kernel(Dims s, const int32_t* __restrict__ idx, const float* __restrict__ block_lse,
                  float* __restrict__ lse_out) {
-  __shared__ float s_l[kRowWarps][32 * (kMaxK + 1)];
-  __shared__ int32_t s_i[kRowWarps][32 * (kMaxK + 1)];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(s.B) * s.N * s.Hq;
-  const int64_t r0 = (blockIdx.x * static_cast<int64_t>(kRowWarps) + warp) * 32;   // (b*Hq + h)*N + i
-  if (r0 >= rows) return;
-  const int K = s.K, nr = static_cast<int>(rows - r0 < 32 ? rows - r0 : 32);
-  int64_t id_base = 0;                     // lane r: start of row r's slot indices
-  if (lane < nr) {
-    const int64_t lrow = r0 + lane;
-    const int i = static_cast<int>(lrow % s.N);
-    const int64_t bh = lrow / s.N;
-    const int h = static_cast<int>(bh % s.Hq), b = static_cast<int>(bh / s.Hq);
-    id_base = ((static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i) * K;
-  }
-  for (int e = lane; e < 32 * K; e += 32) {
-    const int r = e / K, k = e - r * K;
-    const int64_t base = __shfl_sync(0xffffffffu, id_base, r);
-    if (r < nr) {
-      s_l[warp][r * (K + 1) + k] = block_lse[r0 * K + e];
-      s_i[warp][r * (K + 1) + k] = idx[base + k];
+  const int64_t lrow = blockIdx.x * static_cast<int64_t>(kRowThreads) + threadIdx.x;   // (b*Hq + h)*N + i
+  if (lrow >= rows) return;
+  const int K = s.K;
+  const int i = static_cast<int>(lrow % s.N);
+  const int64_t bh = lrow / s.N;
+  const int h = static_cast<int>(bh % s.Hq), b = static_cast<int>(bh / s.Hq);
+  const int32_t* id = idx + ((static_cast<int64_t>(b) * s.Hkv + h / s.G) * s.N + i) * K;
+  const float* bl = block_lse + lrow * K;
+  float v[kMaxK];
+  if constexpr (V4) {
+#pragma unroll
+    for (int k = 0; k < kMaxK; k += 4) {
+      if (k >= K) break;
+      const float4 l = __ldg(reinterpret_cast<const float4*>(bl + k));
+      const int4 t = __ldg(reinterpret_cast<const int4*>(id + k));
+      v[k] = t.x >= 0 ? l.x : neg_inf();
+      v[k + 1] = t.y >= 0 ? l.y : neg_inf();
+      v[k + 2] = t.z >= 0 ? l.z : neg_inf();
+      v[k + 3] = t.w >= 0 ? l.w : neg_inf();
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      if (k >= K) break;
+      v[k] = __ldg(id + k) >= 0 ? __ldg(bl + k) : neg_inf();
     }
   }
-  __syncwarp();
-  if (lane >= nr) return;
-  const float* bl = s_l[warp] + lane * (K + 1);
-  const int32_t* id = s_i[warp] + lane * (K + 1);
   float m = neg_inf();
-  for (int k = 0; k < K; ++k)
-    if (id[k] >= 0) m = fmaxf(m, bl[k]);
+#pragma unroll
+  for (int k = 0; k < kMaxK; ++k)
+    if (k < K) m = fmaxf(m, v[k]);
   float den = 0.f;
-  if (m != neg_inf())
-    for (int k = 0; k < K; ++k)
-      if (id[k] >= 0) den += expf(bl[k] - m);
-  lse_out[r0 + lane] = den > 0.f ? m + logf(den) : neg_inf();
+  if (m != neg_inf()) {
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k)
+      if (k < K && v[k] != neg_inf()) den += expf(v[k] - m);
+  }
+  lse_out[lrow] = den > 0.f ? m + logf(den) : neg_inf();
 }
 
 // O = bf16(accumulator), 8 elements per thread. When the status word carries
@@ -115,9 +120,11 @@ int launch_attn_fwd_tc(const Dims& s, const GroupPlan& gp, const void* Q, const 
   }
   {
     ProfScope ps(st, "attn_rows");
-    const int64_t per_block = kRowWarps * 32;
-    attn_rows_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), kRowWarps * 32, 0, st>>>(
-        s, idx, hl, lse);
+    const unsigned nb = static_cast<unsigned>((rows + kRowThreads - 1) / kRowThreads);
+    if (s.K % 4 == 0)
+      attn_rows_kernel<true><<<nb, kRowThreads, 0, st>>>(s, idx, hl, lse);
+    else
+      attn_rows_kernel<false><<<nb, kRowThreads, 0, st>>>(s, idx, hl, lse);
   }
   if ((err = cudaGetLastError())) return err;
   if ((err = launch_attn_out_ws(s, gp, Q, K, V, idx, list, items, n_items, lse, o_acc, status, st))) return err;

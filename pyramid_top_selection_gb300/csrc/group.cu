@@ -104,40 +104,54 @@ gcount_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, int3
   }
 }
 
-// In-place exclusive scan of n counts (counts[n] receives the total), one 1024-thread block.
-__global__ void __launch_bounds__(1024) gscan_kernel(int32_t* counts, int64_t n) {
-  __shared__ int32_t warp_tot[32];
-  const int tid = threadIdx.x;
+// An in-place exclusive scan and the work items in one 1024-thread block: off (n = gp.bins counts) becomes
+// the exclusive scan with off[n] = the total, every bin's list is cut into items of at most
+// gp.cap pairs, written in bin order to items[], and icount[n] receives the item count.
+__global__ void __launch_bounds__(1024) gscan_items_kernel(GroupPlan gp, int32_t* off, int32_t* icount,
+                                                           int4* __restrict__ items) {
+  __shared__ int32_t warp_tot[2][32];
+  const int64_t n = gp.bins;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int64_t per = (n + 1023) / 1024;
   const int64_t s0 = min(tid * per, n), s1 = min(s0 + per, n);
-  int32_t local = 0;
-  for (int64_t k = s0; k < s1; ++k) local += counts[k];
-  const int lane = tid & 31, w = tid >> 5;
-  int32_t v = local;
+  int32_t lp = 0, li = 0;                    // this thread's pairs and items
+  for (int64_t k = s0; k < s1; ++k) {
+    const int32_t c = off[k];
+    lp += c;
+    li += (c + gp.cap - 1) / gp.cap;
+  }
+  int32_t vp = lp, vi = li;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
+    const int32_t yp = __shfl_up_sync(0xffffffffu, vp, o), yi = __shfl_up_sync(0xffffffffu, vi, o);
+    if (lane >= o) { vp += yp; vi += yi; }
   }
-  if (lane == 31) warp_tot[w] = v;
+  if (lane == 31) { warp_tot[0][w] = vp; warp_tot[1][w] = vi; }
   __syncthreads();
   if (w == 0) {
-    int32_t t = warp_tot[lane];
+    int32_t tp = warp_tot[0][lane], ti = warp_tot[1][lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
+      const int32_t yp = __shfl_up_sync(0xffffffffu, tp, o), yi = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) { tp += yp; ti += yi; }
     }
-    warp_tot[lane] = t;
+    warp_tot[0][lane] = tp;
+    warp_tot[1][lane] = ti;
   }
   __syncthreads();
-  int32_t run = v - local + (w > 0 ? warp_tot[w - 1] : 0);
+  int32_t run = vp - lp + (w > 0 ? warp_tot[0][w - 1] : 0);
+  int32_t irun = vi - li + (w > 0 ? warp_tot[1][w - 1] : 0);
   for (int64_t k = s0; k < s1; ++k) {
-    const int32_t c = counts[k];
-    counts[k] = run;
+    const int32_t c = off[k];
+    off[k] = run;
+    for (int32_t q = 0; q < c; q += gp.cap)
+      items[irun++] = make_int4(static_cast<int>(k), run + q, min(gp.cap, c - q), 0);
     run += c;
   }
-  if (tid == 1023) counts[n] = run;
+  if (tid == 1023) {
+    off[n] = run;
+    icount[n] = irun;
+  }
 }
 
 // Scatter: a local block ranks its pairs within each bin in shared memory, reserves each
@@ -183,30 +197,6 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
     pair_at(gp, r, k, i, slot, g);
     list[hist[(g - r.g0) * gp.n0 + t] + rank[k]] = (i << 6) | slot;
   }
-}
-
-__global__ void icount_kernel(GroupPlan gp, const int32_t* __restrict__ off, int32_t* __restrict__ icount) {
-  for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < gp.bins;
-       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int len = off[b + 1] - off[b];
-    icount[b] = (len + gp.cap - 1) / gp.cap;
-  }
-}
-
-__global__ void ifill_kernel(GroupPlan gp, const int32_t* __restrict__ off, const int32_t* __restrict__ ioff,
-                             int4* __restrict__ items) {
-  for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < gp.bins;
-       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int beg = off[b], len = off[b + 1] - beg;
-    int k = 0;
-    for (int s = 0; s < len; s += gp.cap, ++k)
-      items[ioff[b] + k] = make_int4(static_cast<int>(b), beg + s, min(gp.cap, len - s), 0);
-  }
-}
-
-inline int grid_for(int64_t n, int threads) {
-  int64_t b = (n + threads - 1) / threads;
-  return static_cast<int>(b < 1 ? 1 : (b > 152 * 32 ? 152 * 32 : b));
 }
 
 }  // namespace
@@ -274,7 +264,7 @@ int launch_group_items(const GroupPlan& gp, const int32_t* sel, char* ws, const 
     }
     {
       ProfScope ps(st, "group_scan");
-      gscan_kernel<<<1, 1024, 0, st>>>(off, gp.bins);
+      gscan_items_kernel<<<1, 1024, 0, st>>>(gp, off, icount, items);
     }
     {
       ProfScope ps(st, "group_scatter");
@@ -283,13 +273,7 @@ int launch_group_items(const GroupPlan& gp, const int32_t* sel, char* ws, const 
     }
   } else {
     ProfScope ps(st, "group_scan");
-    gscan_kernel<<<1, 1024, 0, st>>>(off, gp.bins);
-  }
-  {
-    ProfScope ps(st, "group_items");
-    icount_kernel<<<grid_for(gp.bins, 256), 256, 0, st>>>(gp, off, icount);
-    gscan_kernel<<<1, 1024, 0, st>>>(icount, gp.bins);
-    ifill_kernel<<<grid_for(gp.bins, 256), 256, 0, st>>>(gp, off, icount, items);
+    gscan_items_kernel<<<1, 1024, 0, st>>>(gp, off, icount, items);
   }
   return cudaGetLastError();
 }
