@@ -25,8 +25,8 @@ constexpr int kGQ = 256;          // units per block
 constexpr int kGThreads = 512;
 
 struct BinRange {
-  int64_t e0, g0, h0;
-  int n, i0;       // pairs in the block; query of its first unit
+  int64_t u0, e0, g0;   // first unit, its first pair, its (head, chunk) group
+  int n;                // pairs in the block
   bool local;
 };
 
@@ -39,11 +39,10 @@ __device__ __forceinline__ BinRange bin_range(const GroupPlan& gp, bool local_ok
   const int64_t u0 = blockIdx.x * static_cast<int64_t>(kGQ);
   const int64_t u1 = min(u0 + kGQ, units);
   BinRange r;
+  r.u0 = u0;
   r.e0 = u0 * gp.W;
   r.n = static_cast<int>((u1 - u0) * gp.W);
   r.g0 = group_of(gp, u0);
-  r.h0 = u0 / gp.N;
-  r.i0 = static_cast<int>(u0 % gp.N);
   r.local = local_ok && group_of(gp, u1 - 1) - r.g0 <= 1;
   return r;
 }
@@ -62,37 +61,48 @@ __device__ __forceinline__ int bin_key(const GroupPlan& gp, int t, int prev) {
   return t < gp.n0 ? t : -1;
 }
 __device__ __forceinline__ int entry_key(const GroupPlan& gp, const int32_t* __restrict__ sel, int64_t e, int k) {
-  return bin_key(gp, sel[e], gp.dedup && k % gp.W ? sel[e - 1] : -1);
+  const bool first = (gp.wlog >= 0 ? k & (gp.W - 1) : k % gp.W) == 0;   // slot 0 of its unit
+  return bin_key(gp, sel[e], gp.dedup && !first ? sel[e - 1] : -1);
 }
 
-// Pair k of the block (32-bit arithmetic): its query i, slot and (head, chunk) group.
-__device__ __forceinline__ void pair_at(const GroupPlan& gp, const BinRange& r, int k, int& i, int& slot,
-                                        int64_t& g) {
-  const int lu = k / gp.W;
-  slot = k - lu * gp.W;
-  i = r.i0 + lu;
-  int64_t h = r.h0;
-  while (i >= gp.N) {
-    i -= gp.N;
-    ++h;
+// Per unit of the block: its query i and its (head, chunk) group relative to r.g0, tabulated
+// once so that a pair needs no division by N or Nq.
+struct UnitTab {
+  int i[kGQ], dg[kGQ];
+};
+__device__ __forceinline__ void fill_units(const GroupPlan& gp, const BinRange& r, UnitTab& tab) {
+  for (int lu = threadIdx.x; lu < kGQ; lu += kGThreads) {
+    const int64_t u = r.u0 + lu, h = u / gp.N;
+    const int i = static_cast<int>(u - h * gp.N);
+    tab.i[lu] = i;
+    tab.dg[lu] = static_cast<int>(h * gp.nch + i / gp.Nq - r.g0);
   }
-  g = h * gp.nch + i / gp.Nq;
+}
+
+// Pair k of the block: its query i, slot and (head, chunk) group.
+__device__ __forceinline__ void pair_at(const GroupPlan& gp, const BinRange& r, const UnitTab& tab, int k, int& i,
+                                        int& slot, int64_t& g) {
+  const int lu = gp.wlog >= 0 ? k >> gp.wlog : k / gp.W;
+  slot = k - lu * gp.W;
+  i = tab.i[lu];
+  g = r.g0 + tab.dg[lu];
 }
 
 __global__ void __launch_bounds__(kGThreads)
 gcount_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, int32_t* __restrict__ counts) {
   extern __shared__ int32_t hist[];                 // [2 * n0]
+  __shared__ UnitTab tab;
   const BinRange r = bin_range(gp, local_ok);
-  if (r.local) {
+  fill_units(gp, r, tab);
+  if (r.local)
     for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) hist[k] = 0;
-    __syncthreads();
-  }
+  __syncthreads();
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
     const int t = entry_key(gp, sel, r.e0 + k, k);
     if (t < 0) continue;
     int i, slot;
     int64_t g;
-    pair_at(gp, r, k, i, slot, g);
+    pair_at(gp, r, tab, k, i, slot, g);
     if (r.local) atomicAdd(&hist[(g - r.g0) * gp.n0 + t], 1);
     else atomicAdd(&counts[g * gp.n0 + t], 1);
   }
@@ -161,17 +171,18 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
                 int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
   extern __shared__ int32_t hist[];                 // [2 * n0] counts, then bases; ranks [kGQ * W]
   int32_t* rank = hist + 2 * gp.n0;
+  __shared__ UnitTab tab;
   const BinRange r = bin_range(gp, local_ok);
-  if (r.local) {
+  fill_units(gp, r, tab);
+  if (r.local)
     for (int k = threadIdx.x; k < 2 * gp.n0; k += kGThreads) hist[k] = 0;
-    __syncthreads();
-  }
+  __syncthreads();
   for (int k = threadIdx.x; k < r.n; k += kGThreads) {
     const int t = entry_key(gp, sel, r.e0 + k, k);
     if (t < 0) continue;
     int i, slot;
     int64_t g;
-    pair_at(gp, r, k, i, slot, g);
+    pair_at(gp, r, tab, k, i, slot, g);
     if (r.local) {
       rank[k] = atomicAdd(&hist[(g - r.g0) * gp.n0 + t], 1);
     } else {
@@ -194,7 +205,7 @@ gscatter_kernel(GroupPlan gp, bool local_ok, const int32_t* __restrict__ sel, co
     if (t < 0) continue;
     int i, slot;
     int64_t g;
-    pair_at(gp, r, k, i, slot, g);
+    pair_at(gp, r, tab, k, i, slot, g);
     list[hist[(g - r.g0) * gp.n0 + t] + rank[k]] = (i << 6) | slot;
   }
 }
@@ -208,6 +219,9 @@ GroupPlan make_group_plan(const Dims& s, int W, int64_t nq_target, int cap, int 
   gp.dedup = dedup;
   gp.n0 = (s.n0 + (1 << shift) - 1) >> shift;
   gp.W = W;
+  gp.wlog = -1;
+  for (int l = 0; l < 31; ++l)
+    if (W == (1 << l)) gp.wlog = l;
   gp.cap = cap;
   int64_t nq = (nq_target / s.C) * s.C;
   if (nq < s.C) nq = s.C;

@@ -20,6 +20,7 @@ size_t align256(size_t x);
 // appears once per pair with the slot of its first selected member.
 struct GroupPlan {
   int N, n0, W, cap, Nq, nch, shift, dedup;
+  int wlog;   // log2(W) when W is a power of two, else -1
   int64_t heads, bins, total, max_items;
   __host__ __device__ int64_t bin(int64_t head, int i, int t) const {
     return (head * nch + i / Nq) * n0 + t;
