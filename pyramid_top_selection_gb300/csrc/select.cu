@@ -148,9 +148,9 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   __shared__ float s_sc[kWarps][MC];
   __shared__ uint64_t s_key[kWarps][MC];   // node_key of every scored candidate
   __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
-  __shared__ float s_pd[kWarps][PISA_MAX_LEVELS][8];
+  __shared__ __align__(16) float s_pd[kWarps][PISA_MAX_LEVELS][8];
   // dots of every candidate's two children (q . key sum, per head), two level buffers
-  __shared__ float s_cdot[kWarps][2][MC][2][8];
+  __shared__ __align__(16) float s_cdot[kWarps][2][MC][2][8];
   __shared__ int s_kslot[kWarps][MC / 2];   // candidate slot each kept node came from
   __shared__ int s_par[kWarps][MC];         // 2 * (kept slot of the parent) + which child
 
@@ -306,94 +306,112 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     }
     const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
     const int pathc = ti >> (lam - 1);
-    const float pd0 = s_pd[warp][lam - 1][2 * p], pd1 = s_pd[warp][lam - 1][2 * p + 1];
     const int nxt = cur ^ 1;
     float (*cd)[2][8] = s_cdot[warp][nxt];
     float (*pdots)[2][8] = s_cdot[warp][cur];
-    // child dots for one candidate slot cs (lane's two heads): returns the score part
-    // Key counts: a visible child off the query's path ends before i, so it is full (cspan
-    // keys); the path child holds the keys up to i. Scale factors s / count, once per level.
-    const float cnt_path = static_cast<float>(i - static_cast<int64_t>(pathc) * cspan + 1);
-    const float f_full = s.scale / static_cast<float>(cspan), f_path = s.scale / cnt_path;
-    auto finish = [&](int cs, int c, float l0, float l1, float r0, float r1, bool rv) {
-      const int ch0 = 2 * c, ch1 = 2 * c + 1;
-      float f0 = f_full, f1 = f_full;
-      if (ch0 == pathc) { l0 = pd0; l1 = pd1; f0 = f_path; }
-      if (ch1 == pathc) { r0 = pd0; r1 = pd1; f1 = f_path; }
-      if (cs < nc) {
-        cd[cs][0][2 * p] = l0; cd[cs][0][2 * p + 1] = l1;
-        cd[cs][1][2 * p] = r0; cd[cs][1][2 * p + 1] = r1;
-      }
-      float part = 0.f;
-      const float lv[2] = {l0, l1}, rvv[2] = {r0, r1};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float l;
-        if constexpr (MEAN) {   // the node's own mean key: (left + right sums) / (their counts)
-          const float cnt0 = ch0 == pathc ? cnt_path : static_cast<float>(cspan);
-          const float cnt1 = ch1 == pathc ? cnt_path : static_cast<float>(cspan);
-          l = rv ? (lv[e] + rvv[e]) * (s.scale / (cnt0 + cnt1)) : lv[e] * f0;
-        } else {
-          const float x0 = lv[e] * f0;
-          if (rv) {     // LSE of two terms: max + log(1 + exp(-|difference|))
-            const float x1 = rvv[e] * f1;
-            l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
-          } else {
-            l = x0;
-          }
-        }
-        if (2 * p + e < G) part += l;
-      }
-      return part;
-    };
+    const int64_t loff = geo.off[lam - 1];
+    // 1. Child dots by MMA (lane (g, p): heads 2p, 2p+1 of A rows g and g + 8) into cd[slot]:
+    //    the left child of 16 candidates per tile when the parents' dots are known, else both
+    //    children of 8 candidates per tile. The path child is not loaded (its dot is the
+    //    causal prefix, set below).
     if (have_pdot) {
-      // 16 candidates per MMA tile: row g and g+8 are the left children of two candidates
       for (int mt = 0; mt * 16 < nc; ++mt) {
         const int csa = mt * 16 + g, csb = csa + 8;
         const int ca = csa < nc ? cand[csa] : -1, cb = csb < nc ? cand[csb] : -1;
         const bool la = ca >= 0 && 2 * ca != pathc, lb = cb >= 0 && 2 * cb != pathc;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4* ra = spl_h + (la ? (geo.off[lam - 1] + 2 * ca) * RQ : 0);
-        const uint4* rb = spl_h + (lb ? (geo.off[lam - 1] + 2 * cb) * RQ : 0);
+        const uint4* ra = spl_h + (la ? (loff + 2 * ca) * RQ : 0);
+        const uint4* rb = spl_h + (lb ? (loff + 2 * cb) * RQ : 0);
         mma_split_rows<KS>(acc, ra, la, rb, lb, p, qb);
-        float pa = 0.f, pb = 0.f;
-        if (ca >= 0) {
-          const int ps = s_par[warp][csa];
-          const float q0 = pdots[kslot[ps >> 1]][ps & 1][2 * p], q1 = pdots[kslot[ps >> 1]][ps & 1][2 * p + 1];
-          const bool rv = static_cast<int64_t>(2 * ca + 1) * cspan <= i;
-          pa = finish(csa, ca, acc[0], acc[1], q0 - acc[0], q1 - acc[1], rv);
-        }
-        if (cb >= 0) {
-          const int ps = s_par[warp][csb];
-          const float q0 = pdots[kslot[ps >> 1]][ps & 1][2 * p], q1 = pdots[kslot[ps >> 1]][ps & 1][2 * p + 1];
-          const bool rv = static_cast<int64_t>(2 * cb + 1) * cspan <= i;
-          pb = finish(csb, cb, acc[2], acc[3], q0 - acc[2], q1 - acc[3], rv);
-        }
-        pa += __shfl_xor_sync(0xffffffffu, pa, 1);
-        pa += __shfl_xor_sync(0xffffffffu, pa, 2);
-        pb += __shfl_xor_sync(0xffffffffu, pb, 1);
-        pb += __shfl_xor_sync(0xffffffffu, pb, 2);
-        if (p == 0 && csa < nc) key[csa] = node_key(no_nan(pa), ca);
-        if (p == 0 && csb < nc) key[csb] = node_key(no_nan(pb), cb);
+        if (csa < nc) *reinterpret_cast<float2*>(&cd[csa][0][2 * p]) = make_float2(acc[0], acc[1]);
+        if (csb < nc) *reinterpret_cast<float2*>(&cd[csb][0][2 * p]) = make_float2(acc[2], acc[3]);
       }
     } else {
-      // 8 candidates per MMA tile: row g and g+8 are candidate g's two children
       for (int mt = 0; mt * 8 < nc; ++mt) {
         const int cs = mt * 8 + g;
         const int c = cs < nc ? cand[cs] : -1;
-        const int ch0 = 2 * c, ch1 = 2 * c + 1;
-        const bool v0 = c >= 0;
-        const bool v1 = c >= 0 && static_cast<int64_t>(ch1) * cspan <= i;
+        const bool v0 = c >= 0 && 2 * c != pathc;
+        const bool v1 = c >= 0 && 2 * c + 1 != pathc && static_cast<int64_t>(2 * c + 1) * cspan <= i;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4* r0 = spl_h + (v0 ? (geo.off[lam - 1] + ch0) * RQ : 0);
-        const uint4* r1 = spl_h + (v1 ? (geo.off[lam - 1] + ch1) * RQ : 0);
+        const uint4* r0 = spl_h + (v0 ? (loff + 2 * c) * RQ : 0);
+        const uint4* r1 = spl_h + (v1 ? (loff + 2 * c + 1) * RQ : 0);
         mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
-        float part = 0.f;
-        if (c >= 0) part = finish(cs, c, acc[0], acc[1], acc[2], acc[3], v1);
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (p == 0 && cs < nc) key[cs] = node_key(no_nan(part), c);
+        if (cs < nc) {
+          *reinterpret_cast<float2*>(&cd[cs][0][2 * p]) = make_float2(acc[0], acc[1]);
+          *reinterpret_cast<float2*>(&cd[cs][1][2 * p]) = make_float2(acc[2], acc[3]);
+        }
       }
+    }
+    __syncwarp();
+    // 2. One lane per candidate: both children's dots for every head (right = parent - left
+    //    when only the left was loaded; the path child takes the causal prefix dot), written
+    //    back for the next level, then the score = sum over the G heads of the LSE of the
+    //    visible children's mean scores (MEAN: of the candidate's own mean).
+    // Key counts: a visible child off the query's path ends before i, so it is full (cspan
+    // keys); the path child holds the keys up to i. Scale factors s / count, once per level.
+    const float cnt_path = static_cast<float>(i - static_cast<int64_t>(pathc) * cspan + 1);
+    const float f_full = s.scale / static_cast<float>(cspan), f_path = s.scale / cnt_path;
+    for (int cs = lane; cs < nc; cs += 32) {
+      const int c = cand[cs];
+      const int ch0 = 2 * c, ch1 = 2 * c + 1;
+      const bool rv = static_cast<int64_t>(ch1) * cspan <= i;
+      float lv[8], rw[8];
+      {
+        const float4 a = *reinterpret_cast<const float4*>(&cd[cs][0][0]);
+        const float4 b = *reinterpret_cast<const float4*>(&cd[cs][0][4]);
+        lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w; lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
+      }
+      if (have_pdot) {
+        const int ps = s_par[warp][cs];
+        const float* par = pdots[kslot[ps >> 1]][ps & 1];
+        const float4 a = *reinterpret_cast<const float4*>(par), b = *reinterpret_cast<const float4*>(par + 4);
+        rw[0] = a.x - lv[0]; rw[1] = a.y - lv[1]; rw[2] = a.z - lv[2]; rw[3] = a.w - lv[3];
+        rw[4] = b.x - lv[4]; rw[5] = b.y - lv[5]; rw[6] = b.z - lv[6]; rw[7] = b.w - lv[7];
+      } else {
+        const float4 a = *reinterpret_cast<const float4*>(&cd[cs][1][0]);
+        const float4 b = *reinterpret_cast<const float4*>(&cd[cs][1][4]);
+        rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w; rw[4] = b.x; rw[5] = b.y; rw[6] = b.z; rw[7] = b.w;
+      }
+      float f0 = f_full, f1 = f_full;
+      if (ch0 == pathc || ch1 == pathc) {
+        const float* pd = s_pd[warp][lam - 1];
+        const float4 a = *reinterpret_cast<const float4*>(pd), b = *reinterpret_cast<const float4*>(pd + 4);
+        const float pv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if (ch0 == pathc) {
+          f0 = f_path;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) lv[h] = pv[h];
+        } else {
+          f1 = f_path;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) rw[h] = pv[h];
+        }
+      }
+      *reinterpret_cast<float4*>(&cd[cs][0][0]) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+      *reinterpret_cast<float4*>(&cd[cs][0][4]) = make_float4(lv[4], lv[5], lv[6], lv[7]);
+      *reinterpret_cast<float4*>(&cd[cs][1][0]) = make_float4(rw[0], rw[1], rw[2], rw[3]);
+      *reinterpret_cast<float4*>(&cd[cs][1][4]) = make_float4(rw[4], rw[5], rw[6], rw[7]);
+      float score = 0.f;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        if (h >= G) break;
+        float l;
+        if constexpr (MEAN) {   // the node's own mean key: (left + right sums) / (their counts)
+          const float cnt0 = ch0 == pathc ? cnt_path : static_cast<float>(cspan);
+          const float cnt1 = ch1 == pathc ? cnt_path : static_cast<float>(cspan);
+          l = rv ? (lv[h] + rw[h]) * (s.scale / (cnt0 + cnt1)) : lv[h] * f0;
+        } else {
+          const float x0 = lv[h] * f0;
+          if (rv) {     // LSE of two terms: max + log(1 + exp(-|difference|))
+            const float x1 = rw[h] * f1;
+            l = fmaxf(x0, x1) + __logf(1.f + __expf(-fabsf(x0 - x1)));
+          } else {
+            l = x0;
+          }
+        }
+        score += l;
+      }
+      key[cs] = node_key(no_nan(score), c);
     }
     __syncwarp();
     for (int s2 = lane; s2 < nc; s2 += 32) {
