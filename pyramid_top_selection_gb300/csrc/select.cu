@@ -113,6 +113,12 @@ __device__ __forceinline__ uint64_t node_key(float sc, int node) {
   return (static_cast<uint64_t>(ordered_bits(sc)) << 32) | (0x7fffffffu - static_cast<uint32_t>(node));
 }
 
+// Dots of a candidate's two children with the G heads (child, head), padded to 80 bytes.
+struct __align__(16) CDot {
+  float v[2][8];
+  float pad[4];
+};
+
 // Fan-out 4: the visible grandchildren 4a .. 4a+3 at the level below the next (node span
 // `span` tokens; visible when the first token is <= i) of the kept node `a` held by each lane
 // (-1: none), compacted in lane order into cand. Returns their number. A node's visible
@@ -150,7 +156,9 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
   __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
   __shared__ __align__(16) float s_pd[kWarps][PISA_MAX_LEVELS][8];
   // dots of every candidate's two children (q . key sum, per head), two level buffers
-  __shared__ __align__(16) float s_cdot[kWarps][2][MC][2][8];
+  // (80-byte rows: a lane per candidate reads and writes its row with 16-byte accesses, and a
+  // 20-word stride spreads 8 consecutive rows over all 32 banks)
+  __shared__ CDot s_cdot[kWarps][2][MC];
   __shared__ int s_kslot[kWarps][MC / 2];   // candidate slot each kept node came from
   __shared__ int s_par[kWarps][MC];         // 2 * (kept slot of the parent) + which child
 
@@ -307,8 +315,8 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
     const int pathc = ti >> (lam - 1);
     const int nxt = cur ^ 1;
-    float (*cd)[2][8] = s_cdot[warp][nxt];
-    float (*pdots)[2][8] = s_cdot[warp][cur];
+    CDot* cd = s_cdot[warp][nxt];
+    const CDot* pdots = s_cdot[warp][cur];
     const int64_t loff = geo.off[lam - 1];
     // 1. Child dots by MMA (lane (g, p): heads 2p, 2p+1 of A rows g and g + 8) into cd[slot]:
     //    the left child of 16 candidates per tile when the parents' dots are known, else both
@@ -323,8 +331,8 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         const uint4* ra = spl_h + (la ? (loff + 2 * ca) * RQ : 0);
         const uint4* rb = spl_h + (lb ? (loff + 2 * cb) * RQ : 0);
         mma_split_rows<KS>(acc, ra, la, rb, lb, p, qb);
-        if (csa < nc) *reinterpret_cast<float2*>(&cd[csa][0][2 * p]) = make_float2(acc[0], acc[1]);
-        if (csb < nc) *reinterpret_cast<float2*>(&cd[csb][0][2 * p]) = make_float2(acc[2], acc[3]);
+        if (csa < nc) *reinterpret_cast<float2*>(&cd[csa].v[0][2 * p]) = make_float2(acc[0], acc[1]);
+        if (csb < nc) *reinterpret_cast<float2*>(&cd[csb].v[0][2 * p]) = make_float2(acc[2], acc[3]);
       }
     } else {
       for (int mt = 0; mt * 8 < nc; ++mt) {
@@ -337,8 +345,8 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
         const uint4* r1 = spl_h + (v1 ? (loff + 2 * c + 1) * RQ : 0);
         mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
         if (cs < nc) {
-          *reinterpret_cast<float2*>(&cd[cs][0][2 * p]) = make_float2(acc[0], acc[1]);
-          *reinterpret_cast<float2*>(&cd[cs][1][2 * p]) = make_float2(acc[2], acc[3]);
+          *reinterpret_cast<float2*>(&cd[cs].v[0][2 * p]) = make_float2(acc[0], acc[1]);
+          *reinterpret_cast<float2*>(&cd[cs].v[1][2 * p]) = make_float2(acc[2], acc[3]);
         }
       }
     }
@@ -357,19 +365,19 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
       const bool rv = static_cast<int64_t>(ch1) * cspan <= i;
       float lv[8], rw[8];
       {
-        const float4 a = *reinterpret_cast<const float4*>(&cd[cs][0][0]);
-        const float4 b = *reinterpret_cast<const float4*>(&cd[cs][0][4]);
+        const float4 a = *reinterpret_cast<const float4*>(&cd[cs].v[0][0]);
+        const float4 b = *reinterpret_cast<const float4*>(&cd[cs].v[0][4]);
         lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w; lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
       }
       if (have_pdot) {
         const int ps = s_par[warp][cs];
-        const float* par = pdots[kslot[ps >> 1]][ps & 1];
+        const float* par = pdots[kslot[ps >> 1]].v[ps & 1];
         const float4 a = *reinterpret_cast<const float4*>(par), b = *reinterpret_cast<const float4*>(par + 4);
         rw[0] = a.x - lv[0]; rw[1] = a.y - lv[1]; rw[2] = a.z - lv[2]; rw[3] = a.w - lv[3];
         rw[4] = b.x - lv[4]; rw[5] = b.y - lv[5]; rw[6] = b.z - lv[6]; rw[7] = b.w - lv[7];
       } else {
-        const float4 a = *reinterpret_cast<const float4*>(&cd[cs][1][0]);
-        const float4 b = *reinterpret_cast<const float4*>(&cd[cs][1][4]);
+        const float4 a = *reinterpret_cast<const float4*>(&cd[cs].v[1][0]);
+        const float4 b = *reinterpret_cast<const float4*>(&cd[cs].v[1][4]);
         rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w; rw[4] = b.x; rw[5] = b.y; rw[6] = b.z; rw[7] = b.w;
       }
       float f0 = f_full, f1 = f_full;
@@ -387,10 +395,10 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
           for (int h = 0; h < 8; ++h) rw[h] = pv[h];
         }
       }
-      *reinterpret_cast<float4*>(&cd[cs][0][0]) = make_float4(lv[0], lv[1], lv[2], lv[3]);
-      *reinterpret_cast<float4*>(&cd[cs][0][4]) = make_float4(lv[4], lv[5], lv[6], lv[7]);
-      *reinterpret_cast<float4*>(&cd[cs][1][0]) = make_float4(rw[0], rw[1], rw[2], rw[3]);
-      *reinterpret_cast<float4*>(&cd[cs][1][4]) = make_float4(rw[4], rw[5], rw[6], rw[7]);
+      *reinterpret_cast<float4*>(&cd[cs].v[0][0]) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+      *reinterpret_cast<float4*>(&cd[cs].v[0][4]) = make_float4(lv[4], lv[5], lv[6], lv[7]);
+      *reinterpret_cast<float4*>(&cd[cs].v[1][0]) = make_float4(rw[0], rw[1], rw[2], rw[3]);
+      *reinterpret_cast<float4*>(&cd[cs].v[1][4]) = make_float4(rw[4], rw[5], rw[6], rw[7]);
       float score = 0.f;
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
