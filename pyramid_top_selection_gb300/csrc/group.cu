@@ -264,10 +264,13 @@ int launch_group_items(const GroupPlan& gp, const int32_t* sel, char* ws, const 
   const bool local_ok = hist_bytes + rank_bytes <= 200 * 1024;
   const size_t sm_count = local_ok ? hist_bytes : 0, sm_scatter = local_ok ? hist_bytes + rank_bytes : 0;
   if (blocks > 0) {
-    if (sm_scatter > 48 * 1024) {
+    // above 48 KB per block (the dynamic part plus the kernels' static unit table) a launch
+    // needs the opt-in; set on every call, since the attribute is per function and process
+    const size_t dflt = 48 * 1024 - sizeof(UnitTab);
+    if (sm_scatter > dflt) {
       e = cudaFuncSetAttribute(gscatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(sm_scatter));
-      if (e == cudaSuccess && sm_count > 48 * 1024)
+      if (e == cudaSuccess && sm_count > dflt)
         e = cudaFuncSetAttribute(gcount_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sm_count));
       if (e != cudaSuccess) return e;
