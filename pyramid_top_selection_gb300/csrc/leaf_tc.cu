@@ -19,7 +19,7 @@
 //   * control (the next warp, one thread): loads each item's 64 or 128 keys by TMA into a 2-stage ring
 //     (the next item's while the current one runs) and issues S = Q K^T (M=128, N=64) as
 //     tcgen05.mma into a 4-stage ring of TMEM accumulators;
-//   * softmax (two warpgroups, warps 0-7, taking the tiles in turn; thread = TMEM lane =
+//   * softmax (two warpgroups, three when G = 8, taking the tiles in turn; thread = TMEM lane =
 //     tile row): reads its S row, frees the TMEM stage, and reduces the row to its LSE over
 //     the visible keys; the G rows of a query (adjacent lanes) sum their LSEs into the
 //     candidate's score;
@@ -44,14 +44,14 @@ constexpr int kRows = 128;
 constexpr int kNQ = 4;            // Q tile stages
 constexpr int kNS = 4;            // TMEM S stages (64 columns each)
 constexpr int kNK = 2;            // K tile stages
-#ifndef PISA_LEAF_SG
-#define PISA_LEAF_SG 2
+// Softmax warpgroups (tile T goes to group T % SG): three when G = 8 (0.760 -> 0.729 ms at the
+// 64K workload), two otherwise (three: 1.433 -> 1.440 ms at the G = 4 sweep shape; 1.24 vs 1.18
+// ms at G = 8 with one leaf per item).
+#ifndef PISA_LEAF_SG8
+#define PISA_LEAF_SG8 3
 #endif
-constexpr int kSG = PISA_LEAF_SG;                 // softmax warpgroups (tile T goes to group T % kSG;
-                                                  // three measured slower than two: 1.24 vs 1.18 ms)
-constexpr int kWP = 4 * kSG;                      // first producer warp
-constexpr int kThreads = 128 * kSG + 128 + 64;    // softmax, producers (4 warps), control, scheduler
-constexpr int kConsumerWarps = 4 * kSG + 5;
+__host__ __device__ constexpr int sg_for(int G) { return G >= 8 ? PISA_LEAF_SG8 : 2; }
+__host__ __device__ constexpr int threads_for(int G) { return 128 * sg_for(G) + 128 + 64; }   // softmax, producers (4 warps), control, scheduler
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the drain waits (work already issued)
@@ -83,12 +83,15 @@ struct LeafArgs {
 };
 
 template <int D, int G, int PR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(G), 1)
 leaf_tc_kernel(const LeafArgs a, const __grid_constant__ CUtensorMap kmap) {
   using L = LeafSmem<D, PR>;
   constexpr int NK = L::NK;
   constexpr int EPT = kRows / G;          // entries (queries) per tile
   constexpr int CH = D / 8;               // 16-byte chunks per row
+  constexpr int kSG = sg_for(G);          // softmax warpgroups
+  constexpr int kWP = 4 * kSG;            // first producer warp
+  constexpr int kConsumerWarps = 4 * kSG + 5;
   extern __shared__ unsigned char smraw[];
   __shared__ __align__(8) uint64_t q_full[kNQ], q_empty[kNQ], s_full[kNS], s_empty[kNS], k_full[kNK],
       k_empty[kNK], drain, never;
@@ -340,7 +343,7 @@ int leaf_tc_launch(const LeafArgs& a, const CUtensorMap& km, int grid, cudaStrea
   cudaError_t e = cudaFuncSetAttribute(leaf_tc_kernel<D, G, PR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope ps(st, a.block_lse ? "attn_lse_tc" : "leaf_score");
-  leaf_tc_kernel<D, G, PR><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, km);
+  leaf_tc_kernel<D, G, PR><<<static_cast<unsigned>(grid), threads_for(G), smem, st>>>(a, km);
   return cudaGetLastError();
 }
 
