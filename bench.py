@@ -690,6 +690,26 @@ def run_quality(args, cfg, local):
                           **QUALITY_NOTES, **out}), flush=True)
 
 
+def graph_of(fn, check=None):
+    """fn() captured once in a CUDA graph (its buffers fixed) for replay in place of the eager
+    calls, so that a launch-bound chain of small kernels runs without host launch gaps. None when
+    the capture fails or a replay's `check` output differs from the eager run's (a selection is
+    bit-exact from run to run)."""
+    torch.cuda.synchronize()
+    ref = check.clone() if check is not None else None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+    except Exception:
+        return None
+    if ref is not None and not torch.equal(ref, check):
+        return None
+    return g
+
+
 def sweep_point(args, cfg, N, dev, flush):
     """Pyramid selection, its PISA-1 ablation and the flat comparator at one N (selection only,
     median of L2-flushed runs), plus the pyramid build's achieved HBM bandwidth."""
@@ -702,28 +722,33 @@ def sweep_point(args, cfg, N, dev, flush):
     idx = torch.empty(c["B"], c["Hkv"], N, c["K"], dtype=torch.int32, device=dev)
     ws_p, ws_f = pisa.workspace(shape, 0, dev), pisa.workspace(shape, 1, dev)
 
-    def timed(fn):
+    launch = []
+
+    def timed(fn, check):
         for _ in range(max(1, args.warmup)):
             fn()
+        g = graph_of(fn, check)
+        launch.append("cuda_graph" if g is not None else "eager")
+        run = g.replay if g is not None else fn
         ts = []
         for _ in range(args.steps):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            run()
             b.record()
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)
 
-    out = {"build_ms": timed(lambda: pisa.build_pyramid(Kt, shape, out=pyr))}
+    out = {"build_ms": timed(lambda: pisa.build_pyramid(Kt, shape, out=pyr), pyr)}
     build_bytes = Kt.numel() * 2 + pyr.numel() * 4
     out["build_gbs"] = build_bytes / (out["build_ms"] / 1e3) / 1e9
     ws_v = pisa.workspace(shape, 5, dev)
     for name, fn, ws in (("pyramid", pisa.select, ws_p), ("pisa1_mean", pisa.select_mean, ws_p),
                          ("pisa2_meanvar", pisa.select_meanvar, ws_v), ("flat", pisa.select_flat, ws_f)):
         call = lambda: fn(Q, Kt, pyr, shape, ws=ws, want_score=False, idx=idx)   # noqa: E731
-        out[name] = timed(call)
+        out[name] = timed(call, idx)
         kern, _, _ = profile_kernels(pisa, call, max(1, args.steps), flush)
         out[name + "_kernels"] = {k: round(v["avg_ms"], 4) for k, v in kern.items()}
     pk, _ = peaks()
@@ -735,7 +760,8 @@ def sweep_point(args, cfg, N, dev, flush):
             "pisa1_mean_select_ms": out["pisa1_mean"], "pisa1_mean_kernels_ms": out["pisa1_mean_kernels"],
             "pisa2_meanvar_select_ms": out["pisa2_meanvar"], "pisa2_meanvar_kernels_ms": out["pisa2_meanvar_kernels"],
             "build_ms": out["build_ms"], "build_gbs": out["build_gbs"],
-            "build_hbm_frac": out["build_gbs"] / pk["hbm_gbs"]}
+            "build_hbm_frac": out["build_gbs"] / pk["hbm_gbs"],
+            "launch": launch[0] if len(set(launch)) == 1 else ",".join(launch)}
     del Q, Kt, pyr, idx, ws_p, ws_f, ws_v
     torch.cuda.empty_cache()
     return line
@@ -770,18 +796,21 @@ def prefill_point(args, cfg, dev, flush):
 
     for _ in range(args.warmup):
         step()
+    g = graph_of(step, idx)
+    run = g.replay if g is not None else step
     ts = []
     for _ in range(args.steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        step()
+        run()
         b.record()
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
     ms = sum(ts) / len(ts)
     kernels, _, _ = profile_kernels(pisa, step, args.steps, flush)
     return {"workload": f"prefill select+attend, N={N}", "tokens_per_s": B * N / (ms / 1e3), "ms_per_step": ms,
+            "launch": "cuda_graph" if g is not None else "eager",
             "config": {k: cfg[k] for k in ("B", "N", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
             "kernels_ms": {k: round(v["avg_ms"], 4) for k, v in kernels.items()}}
 
@@ -799,14 +828,14 @@ def other_configs(dev, flush):
     curve = {}
     for N in (4096, 16384, 131072, 262144):
         pp = prefill_point(sub, dict(WORKLOADS["prefill_64k"], N=N), dev, flush)
-        curve[f"N={N}"] = {"tokens_per_s": pp["tokens_per_s"], "ms_per_step": pp["ms_per_step"]}
+        curve[f"N={N}"] = {"tokens_per_s": pp["tokens_per_s"], "ms_per_step": pp["ms_per_step"], "launch": pp["launch"]}
     out["prefill_vs_n"] = {"config": {k: WORKLOADS["prefill_64k"][k] for k in ("B", "Hq", "Hkv", "d", "C", "K", "g", "qtile")},
                            "note": "N=65536 is the headline line itself", **curve}
     sw = {}
     for N in (16384, 65536, 131072, 262144):
         p = sweep_point(sub, WORKLOADS["sweep"], N, dev, flush)
         e = {k: p[k] for k in ("pyramid_select_ms", "flat_select_ms", "flat_over_pyramid", "pisa1_mean_select_ms",
-                               "pisa2_meanvar_select_ms", "build_ms", "build_gbs", "build_hbm_frac")}
+                               "pisa2_meanvar_select_ms", "build_ms", "build_gbs", "build_hbm_frac", "launch")}
         e["route_ms"] = p["pyramid_kernels_ms"].get("route")
         e["leaf_score_ms"] = p["pyramid_kernels_ms"].get("leaf_score")
         sw[f"N={N}"] = e

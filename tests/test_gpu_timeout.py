@@ -24,8 +24,8 @@ def stalled():
         pisa.set_wait_limit(0)              # back to the default
 
 
-def _problem():
-    B, N, Hq, Hkv, d, K = 1, 3000, 8, 2, 128, 8
+def _problem(N):
+    B, Hq, Hkv, d, K = 1, 8, 2, 128, 8
     Q, Kt, V = (x.cuda() for x in syn.make_prefill(B, N, Hq, Hkv, d, C=64, seed=4, needles=True))
     shape = pisa.make_shape(B, N, Hq, Hkv, d, 64, K, qtile=4)
     return Q, Kt, V, shape
@@ -41,8 +41,11 @@ def _normal_run(Q, Kt, V, shape):
     return pyr, idx, score, hl, O, lse
 
 
-def test_wait_that_runs_out_is_reported_and_poisons_outputs(stalled):
-    Q, Kt, V, shape = _problem()
+# 6000 and 32768 (query, KV head) units: the top-K finish runs its warp and its thread-per-query
+# version, and both must poison
+@pytest.mark.parametrize("N", [3000, 16384])
+def test_wait_that_runs_out_is_reported_and_poisons_outputs(stalled, N):
+    Q, Kt, V, shape = _problem(N)
     pisa.set_test_stall(False)
     pisa.set_wait_limit(0)
     pyr, idx0, score0, hl0, O0, lse0 = _normal_run(Q, Kt, V, shape)
