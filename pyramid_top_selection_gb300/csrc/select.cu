@@ -16,7 +16,9 @@
 //   key sums (fp32-accurate dots), LSE per head, sum over heads, warp top-K by rank.
 //   The node that contains i is causal-partial: its dot is q . (sum of keys j <= i in it),
 //   built bottom-up from the query's own-leaf prefix and the full left siblings on the
-//   ancestor path. Output: <= 2K leaf candidates per query.
+//   ancestor path; a prefix pass (route_prefix_kernel) computes these for 16 (query, head)
+//   rows of one leaf at a time, which share the keys and siblings they read. Output: <= 2K
+//   leaf candidates per query.
 // Grouping: counting sort of (leaf, query) pairs into (KV head, query chunk, leaf) bins,
 //   cut into work items (group.cu).
 // Stage 2 (leaf_tc.cu): a persistent warp-specialised tcgen05 kernel walks the work items;
@@ -25,6 +27,7 @@
 #include "device.cuh"
 #include "group.h"
 #include "profile.h"
+#include "tc.cuh"
 
 namespace pisa {
 
@@ -74,9 +77,6 @@ __device__ __forceinline__ void ldg_pair(const uint4* a, uint4& x, uint4& y) {
 
 #ifndef PISA_ROUTE_PRED
 #define PISA_ROUTE_PRED 1
-#endif
-#ifndef PISA_ROUTE_SUFFIX
-#define PISA_ROUTE_SUFFIX 1
 #endif
 // Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid (always valid
 // addresses); invalid rows contribute zeros and load nothing (a lane group whose row is
@@ -138,23 +138,156 @@ __device__ __forceinline__ int expand4(int a, int64_t span, int i, int* cand, un
   return tot;
 }
 
+// Causal path prefixes for stage 1, one pass before the descent: pd[l][h] = q_h . (sum of the
+// keys j <= i in the ancestor of i's leaf at level l), for the levels l < LP the descent can
+// score. Level 0 is the own-leaf prefix; level l adds the left sibling of the level-(l-1)
+// ancestor when that ancestor is a right child. A CTA takes 16 * NW (query, head) rows of one
+// KV head, all in one leaf, so the leaf's keys (staged once in shared memory) and the siblings
+// on its ancestor path serve all of them; a warp takes 16 rows. Both contractions run on
+// mma.sync with the rows as A (the dimension order of kdim), the keys (exact bf16 products) or
+// the split sibling rows (hi and lo: fp32-accurate) as B.
+__host__ __device__ constexpr int prefix_warps(int G) { return G >= 2 ? 8 : 4; }   // <= 64 queries per CTA
+constexpr int kMaxSib = 25;   // N < 2^31 tokens in leaves of C = 64: at most 26 levels, 25 siblings
+
+template <int D, int G>
+__global__ void __launch_bounds__(prefix_warps(G) * 32)
+route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q,
+                    const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl, float* __restrict__ pd) {
+  constexpr int KS = D / 16, RQ = D / 4, QW = 16 / G, NW = prefix_warps(G), CH = D / 8;
+  __shared__ __align__(16) uint4 s_key[64 * CH];                // the leaf's keys, [key][chunk ^ (key & 7)]
+  __shared__ __align__(16) uint4 s_sib[kMaxSib * 2 * CH];     // split sibling rows, [level][chunk ^ (level & 7)]
+  __shared__ float s_dot[NW][16][32];                          // [row][level]: sibling dots (4 tiles of 8)
+  __shared__ float s_p0[NW][16];                               // [row]: own-leaf prefix dots
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+  const int b = blockIdx.z, kv = blockIdx.y;
+  const int ic = blockIdx.x * NW * QW;                          // the CTA's first query
+  const int i0 = ic + warp * QW;                                // the warp's first query
+  const int ti = ic / s.C, L = geo.n_levels;
+  const int kvk = kv / s.kvr;
+  const int64_t head = static_cast<int64_t>(b) * s.Hkv + kv;
+  const uint4* spl_h = spl + (static_cast<int64_t>(b) * s.Hkv_r + kvk) * geo.nodes * RQ;
+  const int64_t j0 = static_cast<int64_t>(ti) * s.C;
+
+  // A fragments: rows g and g + 8 (query i0 + r / G, head r % G); rows past N read row ic.
+  // Issued first: their latency overlaps the staging below.
+  const int qa = i0 + g / G, qb = i0 + (g + 8) / G;
+  const __nv_bfloat16* rowa =
+      Q + ((static_cast<int64_t>(b) * s.N + (qa < s.N ? qa : ic)) * s.Hq + kv * G + g % G) * D;
+  const __nv_bfloat16* rowb =
+      Q + ((static_cast<int64_t>(b) * s.N + (qb < s.N ? qb : ic)) * s.Hq + kv * G + (g + 8) % G) * D;
+  uint32_t qf[KS][4];
+#pragma unroll
+  for (int kp = 0; kp < KS / 2; ++kp) {
+    const uint4 x0 = ldg_u4(rowa + kdim(2 * kp, p)), x1 = ldg_u4(rowb + kdim(2 * kp, p));
+    qf[2 * kp][0] = x0.x; qf[2 * kp][1] = x1.x; qf[2 * kp][2] = x0.y; qf[2 * kp][3] = x1.y;
+    qf[2 * kp + 1][0] = x0.z; qf[2 * kp + 1][1] = x1.z; qf[2 * kp + 1][2] = x0.w; qf[2 * kp + 1][3] = x1.w;
+  }
+
+  // staged in shared memory for all warps: the keys j0 .. (the CTA's last query) and the left
+  // siblings on the leaf's ancestor path (a level whose ancestor is a left child is zeros),
+  // 16-byte chunks swizzled by row
+  {
+    const int nkc = min(ic + NW * QW - 1, s.N - 1) - static_cast<int>(j0) + 1;
+    for (int e = threadIdx.x; e < nkc * CH; e += NW * 32) {
+      const int key = e / CH, c = e - key * CH;
+      tc::cp_async16(tc::su32(&s_key[key * CH + (c ^ (key & 7))]),
+                     Kt + ((static_cast<int64_t>(b) * s.N + j0 + key) * s.Hkv_r + kvk) * D + c * 8, true);
+    }
+    for (int e = threadIdx.x; e < (L - 1) * 2 * CH; e += NW * 32) {
+      const int l = e / (2 * CH), c = e - l * 2 * CH;
+      const bool sv = (ti >> l) & 1;
+      tc::cp_async16(tc::su32(&s_sib[l * 2 * CH + (c ^ (l & 7))]),
+                     spl_h + (sv ? (geo.off[l] + (ti >> l) - 1) * RQ + c : 0), sv);
+    }
+    tc::cp_async_commit();
+    tc::cp_async_wait<0>();
+    __syncthreads();
+  }
+  if (i0 >= s.N) return;                   // no block-wide barriers below
+
+  // own leaf: keys j0 .. (the warp's last query), 8 per tile (B column = key, read from shared
+  // memory); a row adds the keys up to its query
+  const int nk = min(i0 + QW - 1, s.N - 1) - static_cast<int>(j0) + 1;
+  const int la = qa - static_cast<int>(j0), lb = qb - static_cast<int>(j0);   // key n counts iff n <= la
+  float pa = 0.f, pb = 0.f;
+  for (int nt = 0; nt * 8 < nk; ++nt) {
+    const int n = nt * 8 + g;                 // this lane's key; n & 7 == g
+    const bool kvld = n < nk;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {     // chunk 4 kp + p holds dims kdim(2 kp, p) .. + 7
+      const uint4 x = kvld ? s_key[n * CH + ((4 * kp + p) ^ g)] : make_uint4(0, 0, 0, 0);
+      mma_bf16(acc, qf[2 * kp], x.x, x.y);
+      mma_bf16(acc, qf[2 * kp + 1], x.z, x.w);
+    }
+    const int c0 = nt * 8 + 2 * p;            // this lane's two keys (columns 2p, 2p + 1)
+    pa += (c0 <= la ? acc[0] : 0.f) + (c0 + 1 <= la ? acc[1] : 0.f);
+    pb += (c0 <= lb ? acc[2] : 0.f) + (c0 + 1 <= lb ? acc[3] : 0.f);
+  }
+  pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+  pa += __shfl_xor_sync(0xffffffffu, pa, 2);
+  pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+  pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+  if (p == 0) {
+    s_p0[warp][g] = pa;
+    s_p0[warp][g + 8] = pb;
+  }
+
+  // left siblings on the path, 8 levels per tile (B column = level l): the node left of the
+  // level-l ancestor when that ancestor is a right child, else zero
+  for (int st = 0; st * 8 < L - 1; ++st) {
+    const int l = st * 8 + g;                 // l & 7 == g
+    const bool sv = l < L - 1;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {     // chunks 8 kp + 2p, + 1: dims kdim(2 kp, p) .. + 7
+      uint4 y0 = make_uint4(0, 0, 0, 0), y1 = y0;
+      if (sv) {
+        y0 = s_sib[l * 2 * CH + ((8 * kp + 2 * p) ^ g)];
+        y1 = s_sib[l * 2 * CH + ((8 * kp + 2 * p + 1) ^ g)];
+      }
+      mma_bf16(acc, qf[2 * kp], y0.x, y0.y);           // hi
+      mma_bf16(acc, qf[2 * kp], y0.z, y0.w);           // lo
+      mma_bf16(acc, qf[2 * kp + 1], y1.x, y1.y);
+      mma_bf16(acc, qf[2 * kp + 1], y1.z, y1.w);
+    }
+    const int c0 = st * 8 + 2 * p;
+    s_dot[warp][g][c0] = acc[0];
+    s_dot[warp][g][c0 + 1] = acc[1];
+    s_dot[warp][g + 8][c0] = acc[2];
+    s_dot[warp][g + 8][c0 + 1] = acc[3];
+  }
+  __syncwarp();
+  // lane r < 16: row r's prefix over the levels, written as pd[unit][l][h]
+  if (lane < 16) {
+    const int qi = i0 + lane / G, h = lane % G;
+    if (qi < s.N) {
+      float v = s_p0[warp][lane];
+      float* out = pd + (head * s.N + qi) * LP * G + h;
+      for (int l = 0; l < LP; ++l) {
+        out[l * G] = v;
+        if (l < L - 1) v += s_dot[warp][lane][l];
+      }
+    }
+  }
+}
+
 // MC: the most candidates a level can hold (2K rounded up to 32 or 64); the smaller size lets
 // more CTAs share an SM. MEAN: the PISA-1 ablation -- every block, leaves included, is scored
 // by s q . (its causal key sum) / (its visible key count), summed over the G heads; the leaf
 // candidates' scores go to cscore_out (same layout as cand_out) for the final top-K.
 template <int D, int MC, bool MEAN>
 __global__ void __launch_bounds__(kWarps * 32)
-route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
-             const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl,
-             int32_t* __restrict__ cand_out, float* __restrict__ cscore_out) {
+route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const float* __restrict__ pd,
+             const uint4* __restrict__ spl, int32_t* __restrict__ cand_out, float* __restrict__ cscore_out) {
   constexpr int KS = D / 16;
   constexpr int RQ = D / 4;     // uint4 chunks per split row
   __shared__ int s_cand[kWarps][MC];
   __shared__ int s_kept[kWarps][MC / 2];
   __shared__ float s_sc[kWarps][MC];
   __shared__ uint64_t s_key[kWarps][MC];   // node_key of every scored candidate
-  __shared__ float s_sib[kWarps][PISA_MAX_LEVELS][8];
-  __shared__ __align__(16) float s_pd[kWarps][PISA_MAX_LEVELS][8];
+  __shared__ __align__(16) float s_pd[kWarps][PISA_MAX_LEVELS][8];   // [level][head]: path prefixes
   // dots of every candidate's two children (q . key sum, per head), two level buffers
   // (80-byte rows: a lane per candidate reads and writes its row with 16-byte accesses, and a
   // 20-word stride spreads 8 consecutive rows over all 32 banks)
@@ -187,78 +320,12 @@ route_kernel(Dims s, Geo geo, const __nv_bfloat16* __restrict__ Q,
     }
   }
 
-  // pd0[h] = sum over keys j in [ti*C, i] of q_h . k_j  (keys are exact bf16). Past the middle
-  // of the leaf it is taken as q_h . S(0, ti) minus the keys after i: fewer rows to read.
-  float pda = 0.f, pdb = 0.f;
+  // the causal path prefix dots of the levels the descent scores, from the prefix pass
   {
-    const int64_t j0 = static_cast<int64_t>(ti) * C;
-    const int nkeys = i - static_cast<int>(j0) + 1;
-    const int cnt = static_cast<int>(min(j0 + C, static_cast<int64_t>(s.N)) - j0);   // keys of leaf ti
-    const bool suf = PISA_ROUTE_SUFFIX && 2 * nkeys > cnt + 2;
-    const int64_t k0 = suf ? static_cast<int64_t>(i) + 1 : j0;     // explicit key rows k0 ..
-    const int nr = suf ? cnt - nkeys : nkeys;                      // .. k0 + nr - 1
-    for (int mt = 0; mt * 16 < nr; ++mt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int r0 = mt * 16 + g, r1 = r0 + 8;
-      const __nv_bfloat16* kr0 = Kt + ((static_cast<int64_t>(b) * s.N + k0 + r0) * s.Hkv_r + kvk) * D;
-      const __nv_bfloat16* kr1 = Kt + ((static_cast<int64_t>(b) * s.N + k0 + r1) * s.Hkv_r + kvk) * D;
-#pragma unroll
-      for (int kp = 0; kp < KS / 2; ++kp) {
-        const uint4 x0 = r0 < nr ? ldg_u4(kr0 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
-        const uint4 x1 = r1 < nr ? ldg_u4(kr1 + kdim(2 * kp, p)) : make_uint4(0, 0, 0, 0);
-        const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y}, a1[4] = {x0.z, x1.z, x0.w, x1.w};
-        mma_bf16(acc, a0, qb[2 * kp][0], qb[2 * kp][1]);
-        mma_bf16(acc, a1, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
-      }
-      pda += acc[0] + acc[2];
-      pdb += acc[1] + acc[3];
-    }
-    if (suf) {   // the leaf's sum as A row 0 (lanes g = 0); the other lanes hold minus their part
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint4* lr = spl_h + (geo.off[0] + ti) * RQ;
-      mma_split_rows<KS>(acc, lr, g == 0, lr, false, p, qb);
-      pda = acc[0] - pda;
-      pdb = acc[1] - pdb;
-    }
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      pda += __shfl_xor_sync(0xffffffffu, pda, o);
-      pdb += __shfl_xor_sync(0xffffffffu, pdb, o);
-    }
-  }
-
-  // Dots with the full left sibling of the ancestor at every level l < L-1 whose
-  // ancestor index is odd; prefix sums over levels give q . (keys j <= i of ancestor l).
-  for (int base = 0; base < L - 1; base += 16) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int l0 = base + g, l1 = base + g + 8;
-    const bool v0 = l0 < L - 1 && ((ti >> l0) & 1);
-    const bool v1 = l1 < L - 1 && ((ti >> l1) & 1);
-    const uint4* r0 = spl_h + (v0 ? (geo.off[l0] + (ti >> l0) - 1) * RQ : 0);
-    const uint4* r1 = spl_h + (v1 ? (geo.off[l1] + (ti >> l1) - 1) * RQ : 0);
-    mma_split_rows<KS>(acc, r0, v0, r1, v1, p, qb);
-    if (l0 < PISA_MAX_LEVELS) {
-      s_sib[warp][l0][2 * p] = v0 ? acc[0] : 0.f;
-      s_sib[warp][l0][2 * p + 1] = v0 ? acc[1] : 0.f;
-    }
-    if (l1 < PISA_MAX_LEVELS) {
-      s_sib[warp][l1][2 * p] = v1 ? acc[2] : 0.f;
-      s_sib[warp][l1][2 * p + 1] = v1 ? acc[3] : 0.f;
-    }
-  }
-  __syncwarp();
-  {
-    // lane h < 8 takes head h: pd0 of head h = 2p' + e sits in lane p' (g = 0), as pda
-    // for e = 0 and pdb for e = 1 (identical in every g after the reduction above)
-    const float va = __shfl_sync(0xffffffffu, pda, (lane & 7) >> 1);
-    const float vb = __shfl_sync(0xffffffffu, pdb, (lane & 7) >> 1);
-    if (lane < 8) {
-      float v = (lane & 1) ? vb : va;
-      s_pd[warp][0][lane] = v;
-      for (int l = 1; l < L; ++l) {
-        v = v + s_sib[warp][l - 1][lane];
-        s_pd[warp][l][lane] = v;
-      }
+    const float* src = pd + (head * s.N + i) * LP * G;
+    for (int e = lane; e < LP * 8; e += 32) {
+      const int l = e >> 3, h = e & 7;
+      s_pd[warp][l][h] = h < G ? src[l * G + h] : 0.f;
     }
   }
   __syncwarp();
@@ -965,6 +1032,31 @@ int launch_topk(const Dims& s, int W, const int32_t* cand, const float* cscore, 
   return cudaGetLastError();
 }
 
+// Path-prefix levels the descent can score: l < LP for every scored level l + 1 (a level
+// scores only when it holds more than K nodes); at least level 0 (the PISA-1 leaf scores).
+int prefix_levels(const Dims& s, const Geo& g) {
+  int lp = 1;
+  for (int l = 1; l < g.n_levels; ++l)
+    if (g.size[l] > s.K) lp = l;
+  return lp;
+}
+
+int launch_route_prefix(const Dims& s, const Geo& g, const void* Q, const void* K, const uint4* spl, float* pd,
+                        cudaStream_t st) {
+  const int per_cta = 16 / s.G * prefix_warps(s.G);   // queries per CTA (one leaf at most)
+  dim3 grid((s.N + per_cta - 1) / per_cta, s.Hkv, s.B);
+  const int lp = prefix_levels(s, g);
+  const auto* q = static_cast<const __nv_bfloat16*>(Q);
+  const auto* k = static_cast<const __nv_bfloat16*>(K);
+  ProfScope ps(st, "route_prefix");
+#define PISA_PREFIX_CASE(DD, GG) \
+  if (s.d == DD && s.G == GG) route_prefix_kernel<DD, GG><<<grid, prefix_warps(GG) * 32, 0, st>>>(s, g, lp, q, k, spl, pd);
+  PISA_PREFIX_CASE(128, 1) PISA_PREFIX_CASE(128, 2) PISA_PREFIX_CASE(128, 4) PISA_PREFIX_CASE(128, 8)
+  PISA_PREFIX_CASE(64, 1) PISA_PREFIX_CASE(64, 2) PISA_PREFIX_CASE(64, 4) PISA_PREFIX_CASE(64, 8)
+#undef PISA_PREFIX_CASE
+  return cudaGetLastError();
+}
+
 SelectWs select_ws(const Dims& s, const Geo& g) {
   SelectWs w{};
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
@@ -972,6 +1064,7 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   size_t o = 0;
   w.status = o; o += 256;          // first: the caller finds the status word at offset 0
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);
+  w.pd = o;     o += align256(units * prefix_levels(s, g) * s.G * 4);
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
   w.mean_end = o;                  // the PISA-1 path needs nothing past here
@@ -1004,15 +1097,18 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   float* chead = head_lse ? reinterpret_cast<float*>(ws + w.chead) : nullptr;
   const GroupPlan gp = leaf_plan(s);
   const GroupWs gw = group_ws(gp, w.group);
+  float* pd = reinterpret_cast<float*>(ws + w.pd);
+  const int lp = prefix_levels(s, g);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
   if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
+  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
   ProfScope ps(st, "route");
 #define PISA_ROUTE(DD, MM) \
-  route_kernel<DD, MM, false><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
-                                                           static_cast<const __nv_bfloat16*>(K), spl, cand, nullptr)
+  route_kernel<DD, MM, false><<<rgrid, kWarps * 32, 0, st>>>(s, g, lp, static_cast<const __nv_bfloat16*>(Q), pd, \
+                                                           spl, cand, nullptr)
   if (s.d == 128) {
     if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
   } else {
@@ -1042,15 +1138,18 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
   int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
+  float* pd = reinterpret_cast<float*>(ws + w.pd);
+  const int lp = prefix_levels(s, g);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
   if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
+  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
     ProfScope ps(st, "route_mean");
 #define PISA_ROUTE(DD, MM) \
-  route_kernel<DD, MM, true><<<rgrid, kWarps * 32, 0, st>>>(s, g, static_cast<const __nv_bfloat16*>(Q), \
-                                                          static_cast<const __nv_bfloat16*>(K), spl, cand, cscore)
+  route_kernel<DD, MM, true><<<rgrid, kWarps * 32, 0, st>>>(s, g, lp, static_cast<const __nv_bfloat16*>(Q), pd, \
+                                                          spl, cand, cscore)
     if (s.d == 128) {
       if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
     } else {
