@@ -262,7 +262,7 @@ class ClockSampler:
 # Sources whose change invalidates a kernel's committed DRAM traffic figure: the kernel's own
 # file, the headers it includes and the grouping that shapes its work items.
 KERNEL_SOURCES = {
-    "route": ["select.cu", "device.cuh", "pyramid.cu"],
+    "route": ["select.cu", "device.cuh", "pyramid.cu", "tc.cuh"],
     "leaf_score": ["leaf_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "select.cu"],
     "attn_fwd_tc": ["attn_ws.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "attn.cu"],
     "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h"],
@@ -836,6 +836,7 @@ def other_configs(dev, flush):
         p = sweep_point(sub, WORKLOADS["sweep"], N, dev, flush)
         e = {k: p[k] for k in ("pyramid_select_ms", "flat_select_ms", "flat_over_pyramid", "pisa1_mean_select_ms",
                                "pisa2_meanvar_select_ms", "build_ms", "build_gbs", "build_hbm_frac", "launch")}
+        e["route_prefix_ms"] = p["pyramid_kernels_ms"].get("route_prefix")
         e["route_ms"] = p["pyramid_kernels_ms"].get("route")
         e["leaf_score_ms"] = p["pyramid_kernels_ms"].get("leaf_score")
         sw[f"N={N}"] = e
