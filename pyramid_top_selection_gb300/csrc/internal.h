@@ -53,7 +53,7 @@ struct Dims {
 // collects PISA_STATUS_* bits (the caller reads it there), words 16 and 32 are the item
 // counters of the persistent leaf-scoring and attention kernels.
 struct SelectWs {
-  size_t status, split, pd, cand, cscore, mean_end, group, total, chead, total_head;
+  size_t status, split, pd, cfirst, cand, cscore, mean_end, group, total, chead, total_head;
 };
 struct AttnFwdWs {
   size_t block_lse, o_acc, status, total;

@@ -148,16 +148,19 @@ __device__ __forceinline__ int expand4(int a, int64_t span, int i, int* cand, un
 // the split sibling rows (hi and lo: fp32-accurate) as B.
 __host__ __device__ constexpr int prefix_warps(int G) { return G >= 2 ? 8 : 4; }   // <= 64 queries per CTA
 constexpr int kMaxSib = 25;   // N < 2^31 tokens in leaves of C = 64: at most 26 levels, 25 siblings
+constexpr int kFirstChildren = 64;   // children of the first scored level: at most 4K (K <= 16)
 
 template <int D, int G>
 __global__ void __launch_bounds__(prefix_warps(G) * 32)
 route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q,
-                    const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl, float* __restrict__ pd) {
+                    const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl, float* __restrict__ pd,
+                    float* __restrict__ cfirst) {
   constexpr int KS = D / 16, RQ = D / 4, QW = 16 / G, NW = prefix_warps(G), CH = D / 8;
   __shared__ __align__(16) uint4 s_key[64 * CH];                // the leaf's keys, [key][chunk ^ (key & 7)]
   __shared__ __align__(16) uint4 s_sib[kMaxSib * 2 * CH];     // split sibling rows, [level][chunk ^ (level & 7)]
   __shared__ float s_dot[NW][16][32];                          // [row][level]: sibling dots (4 tiles of 8)
   __shared__ float s_p0[NW][16];                               // [row]: own-leaf prefix dots
+  extern __shared__ __align__(16) uint4 s_ch[];                // first-level children (split rows), when asked
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, p = lane & 3;
   const int b = blockIdx.z, kv = blockIdx.y;
@@ -184,10 +187,27 @@ route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q
     qf[2 * kp + 1][0] = x0.z; qf[2 * kp + 1][1] = x1.z; qf[2 * kp + 1][2] = x0.w; qf[2 * kp + 1][3] = x1.w;
   }
 
-  // staged in shared memory for all warps: the keys j0 .. (the CTA's last query) and the left
-  // siblings on the leaf's ancestor path (a level whose ancestor is a left child is zeros),
-  // 16-byte chunks swizzled by row
+  // the first scored level (g = 2, when asked): its candidates are all visible nodes of the
+  // level, the same for every query of the leaf; their children are the nch first nodes of the
+  // level below
+  int lam0 = 0, nch = 0;
+  if (cfirst != nullptr) {
+    for (int lam = L - 2; lam >= 1; --lam)
+      if ((ti >> lam) + 1 > s.K) {
+        lam0 = lam;
+        break;
+      }
+    if (lam0 >= 1) nch = (ti >> (lam0 - 1)) + 1;               // <= 4K <= kFirstChildren
+  }
+
+  // staged in shared memory for all warps: the keys j0 .. (the CTA's last query), the left
+  // siblings on the leaf's ancestor path (a level whose ancestor is a left child is zeros) and
+  // the first-level children, 16-byte chunks swizzled by row
   {
+    for (int e = threadIdx.x; e < nch * 2 * CH; e += NW * 32) {
+      const int r = e / (2 * CH), c = e - r * 2 * CH;
+      tc::cp_async16(tc::su32(&s_ch[r * 2 * CH + (c ^ (r & 7))]), spl_h + (geo.off[lam0 - 1] + r) * RQ + c, true);
+    }
     const int nkc = min(ic + NW * QW - 1, s.N - 1) - static_cast<int>(j0) + 1;
     for (int e = threadIdx.x; e < nkc * CH; e += NW * 32) {
       const int key = e / CH, c = e - key * CH;
@@ -258,6 +278,42 @@ route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q
     s_dot[warp][g + 8][c0] = acc[2];
     s_dot[warp][g + 8][c0 + 1] = acc[3];
   }
+  // the first scored level's child dots, into cfirst[unit][child][h] (the path child's full
+  // dot too: the descent replaces it with the causal prefix); two tiles of 8 children at a
+  // time, so that two independent MMA chains overlap
+  for (int nt = 0; nt * 8 < nch; nt += 2) {
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int n = (nt + t) * 8 + g;       // n & 7 == g
+        uint4 y0 = make_uint4(0, 0, 0, 0), y1 = y0;
+        if (n < nch) {
+          y0 = s_ch[n * 2 * CH + ((8 * kp + 2 * p) ^ g)];
+          y1 = s_ch[n * 2 * CH + ((8 * kp + 2 * p + 1) ^ g)];
+        }
+        mma_bf16(acc[t], qf[2 * kp], y0.x, y0.y);
+        mma_bf16(acc[t], qf[2 * kp], y0.z, y0.w);
+        mma_bf16(acc[t], qf[2 * kp + 1], y1.x, y1.y);
+        mma_bf16(acc[t], qf[2 * kp + 1], y1.z, y1.w);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int c0 = (nt + t) * 8 + 2 * p;
+      if (qa < s.N) {
+        float* o = cfirst + ((head * s.N + qa) * kFirstChildren + c0) * G + g % G;
+        if (c0 < nch) o[0] = acc[t][0];
+        if (c0 + 1 < nch) o[G] = acc[t][1];
+      }
+      if (qb < s.N) {
+        float* o = cfirst + ((head * s.N + qb) * kFirstChildren + c0) * G + (g + 8) % G;
+        if (c0 < nch) o[0] = acc[t][2];
+        if (c0 + 1 < nch) o[G] = acc[t][3];
+      }
+    }
+  }
   __syncwarp();
   // lane r < 16: row r's prefix over the levels, written as pd[unit][l][h]
   if (lane < 16) {
@@ -280,7 +336,8 @@ route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q
 template <int D, int MC, bool MEAN>
 __global__ void __launch_bounds__(kWarps * 32)
 route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const float* __restrict__ pd,
-             const uint4* __restrict__ spl, int32_t* __restrict__ cand_out, float* __restrict__ cscore_out) {
+             const float* __restrict__ cfirst, const uint4* __restrict__ spl, int32_t* __restrict__ cand_out,
+             float* __restrict__ cscore_out) {
   constexpr int KS = D / 16;
   constexpr int RQ = D / 4;     // uint4 chunks per split row
   __shared__ int s_cand[kWarps][MC];
@@ -344,6 +401,7 @@ route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const
   // only the left one needs loading: q.S(2c+1) = q.S(c) - q.S(2c). The node on the query's
   // path uses its causal prefix dot instead.
   bool have_pdot = false;   // dots of the current candidates are known (previous level scored)
+  bool scored = false;      // a level has been scored
   int cur = 0;              // s_cdot buffer written by the previous scored level
   int* kslot = s_kslot[warp];
   // Visited levels: L-1 (the top node), then one level down per step (g = 2) or two (g = 4,
@@ -382,6 +440,9 @@ route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const
     const int64_t cspan = static_cast<int64_t>(C) << (lam - 1);
     const int pathc = ti >> (lam - 1);
     const int nxt = cur ^ 1;
+    // the first scored level's child dots come from the prefix pass (g = 2); a later level
+    // without parent dots (kept whole after a scored one) loads its own
+    const bool pre = !scored && step == 1 && cfirst != nullptr;
     CDot* cd = s_cdot[warp][nxt];
     const CDot* pdots = s_cdot[warp][cur];
     const int64_t loff = geo.off[lam - 1];
@@ -401,7 +462,7 @@ route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const
         if (csa < nc) *reinterpret_cast<float2*>(&cd[csa].v[0][2 * p]) = make_float2(acc[0], acc[1]);
         if (csb < nc) *reinterpret_cast<float2*>(&cd[csb].v[0][2 * p]) = make_float2(acc[2], acc[3]);
       }
-    } else {
+    } else if (!pre) {
       for (int mt = 0; mt * 8 < nc; ++mt) {
         const int cs = mt * 8 + g;
         const int c = cs < nc ? cand[cs] : -1;
@@ -431,12 +492,21 @@ route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const
       const int ch0 = 2 * c, ch1 = 2 * c + 1;
       const bool rv = static_cast<int64_t>(ch1) * cspan <= i;
       float lv[8], rw[8];
-      {
+      if (pre) {
+        const float* cf = cfirst + ((head * s.N + i) * kFirstChildren + ch0) * G;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          lv[h] = h < G ? cf[h] : 0.f;
+          rw[h] = h < G && rv ? cf[G + h] : 0.f;
+        }
+      } else {
         const float4 a = *reinterpret_cast<const float4*>(&cd[cs].v[0][0]);
         const float4 b = *reinterpret_cast<const float4*>(&cd[cs].v[0][4]);
         lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w; lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
       }
-      if (have_pdot) {
+      if (pre) {
+        // both children from the prefix pass (above)
+      } else if (have_pdot) {
         const int ps = s_par[warp][cs];
         const float* par = pdots[kslot[ps >> 1]].v[ps & 1];
         const float4 a = *reinterpret_cast<const float4*>(par), b = *reinterpret_cast<const float4*>(par + 4);
@@ -499,6 +569,7 @@ route_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q, const
     }
     nkept = Ksel;
     have_pdot = true;
+    scored = true;
     cur = nxt;
     __syncwarp();
   }
@@ -1041,16 +1112,28 @@ int prefix_levels(const Dims& s, const Geo& g) {
   return lp;
 }
 
+// The prefix pass also computes the first scored level's child dots when that level's children
+// fit its slots (fan-out 2, K <= 16) and G <= 4. The dots make a round trip through HBM
+// (kFirstChildren x G x 4 bytes per query), which pays where the descent's own gathers of that
+// level cost more: at the G = 4 sweep shape 0.21 + 2.79 -> 0.47 + 2.31 ms (prefix pass + descent),
+// at the G = 8 64K workload 0.109 + 0.745 -> 0.227 + 0.662 ms.
+bool first_level_pre(const Dims& s) { return s.g == 2 && 4 * s.K <= kFirstChildren && s.G <= 4; }
+
 int launch_route_prefix(const Dims& s, const Geo& g, const void* Q, const void* K, const uint4* spl, float* pd,
-                        cudaStream_t st) {
+                        float* cfirst, cudaStream_t st) {
   const int per_cta = 16 / s.G * prefix_warps(s.G);   // queries per CTA (one leaf at most)
   dim3 grid((s.N + per_cta - 1) / per_cta, s.Hkv, s.B);
   const int lp = prefix_levels(s, g);
   const auto* q = static_cast<const __nv_bfloat16*>(Q);
   const auto* k = static_cast<const __nv_bfloat16*>(K);
   ProfScope ps(st, "route_prefix");
-#define PISA_PREFIX_CASE(DD, GG) \
-  if (s.d == DD && s.G == GG) route_prefix_kernel<DD, GG><<<grid, prefix_warps(GG) * 32, 0, st>>>(s, g, lp, q, k, spl, pd);
+  const int dyn = cfirst != nullptr ? kFirstChildren * s.d / 4 * 16 : 0;   // split rows of the first-level children
+#define PISA_PREFIX_CASE(DD, GG)                                                                             \
+  if (s.d == DD && s.G == GG) {                                                                              \
+    cudaError_t e = cudaFuncSetAttribute(route_prefix_kernel<DD, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn); \
+    if (e != cudaSuccess) return e;                                                                          \
+    route_prefix_kernel<DD, GG><<<grid, prefix_warps(GG) * 32, dyn, st>>>(s, g, lp, q, k, spl, pd, cfirst);  \
+  }
   PISA_PREFIX_CASE(128, 1) PISA_PREFIX_CASE(128, 2) PISA_PREFIX_CASE(128, 4) PISA_PREFIX_CASE(128, 8)
   PISA_PREFIX_CASE(64, 1) PISA_PREFIX_CASE(64, 2) PISA_PREFIX_CASE(64, 4) PISA_PREFIX_CASE(64, 8)
 #undef PISA_PREFIX_CASE
@@ -1065,6 +1148,7 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   w.status = o; o += 256;          // first: the caller finds the status word at offset 0
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);
   w.pd = o;     o += align256(units * prefix_levels(s, g) * s.G * 4);
+  w.cfirst = o; o += first_level_pre(s) ? align256(units * kFirstChildren * s.G * 4) : 0;
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
   w.mean_end = o;                  // the PISA-1 path needs nothing past here
@@ -1098,17 +1182,18 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const GroupPlan gp = leaf_plan(s);
   const GroupWs gw = group_ws(gp, w.group);
   float* pd = reinterpret_cast<float*>(ws + w.pd);
+  float* cfirst = first_level_pre(s) ? reinterpret_cast<float*>(ws + w.cfirst) : nullptr;
   const int lp = prefix_levels(s, g);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
   if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
-  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, st))) return err;
+  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, cfirst, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
   ProfScope ps(st, "route");
 #define PISA_ROUTE(DD, MM) \
   route_kernel<DD, MM, false><<<rgrid, kWarps * 32, 0, st>>>(s, g, lp, static_cast<const __nv_bfloat16*>(Q), pd, \
-                                                           spl, cand, nullptr)
+                                                           cfirst, spl, cand, nullptr)
   if (s.d == 128) {
     if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
   } else {
@@ -1139,17 +1224,18 @@ int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K
   int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
   float* pd = reinterpret_cast<float*>(ws + w.pd);
+  float* cfirst = first_level_pre(s) ? reinterpret_cast<float*>(ws + w.cfirst) : nullptr;
   const int lp = prefix_levels(s, g);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
   if ((err = cudaMemsetAsync(ws + w.status, 0, 256, st))) return err;
-  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, st))) return err;
+  if ((err = launch_route_prefix(s, g, Q, K, spl, pd, cfirst, st))) return err;
   dim3 rgrid((s.N + kWarps - 1) / kWarps, s.Hkv, s.B);
   {
     ProfScope ps(st, "route_mean");
 #define PISA_ROUTE(DD, MM) \
   route_kernel<DD, MM, true><<<rgrid, kWarps * 32, 0, st>>>(s, g, lp, static_cast<const __nv_bfloat16*>(Q), pd, \
-                                                          spl, cand, cscore)
+                                                          cfirst, spl, cand, cscore)
     if (s.d == 128) {
       if (s.g * s.K <= 32) PISA_ROUTE(128, 32); else PISA_ROUTE(128, 64);
     } else {
