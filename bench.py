@@ -262,6 +262,7 @@ class ClockSampler:
 # Sources whose change invalidates a kernel's committed DRAM traffic figure: the kernel's own
 # file, the headers it includes and the grouping that shapes its work items.
 KERNEL_SOURCES = {
+    "route_prefix": ["select.cu", "device.cuh", "tc.cuh"],
     "route": ["select.cu", "device.cuh", "pyramid.cu", "tc.cuh"],
     "leaf_score": ["leaf_tc.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "select.cu"],
     "attn_fwd_tc": ["attn_ws.cu", "tiles.cuh", "tc.cuh", "tmap.cpp", "device.cuh", "group.cu", "group.h", "attn.cu"],
