@@ -180,7 +180,7 @@ int pisa_select(const pisa_shape_t* shape, const void* Q, const void* K, const f
  * should also come before any stream capture on the device. Each call looks up the array's
  * device address with the calling device current. Shapes whose selection workspace without
  * head_lse exceeds 32 MiB are rejected with PISA_EUNSUPPORTED before any CUDA call (about
- * B*Hkv*N <= 80K units at K = 16). Every call shares the one array and it keeps the last
+ * B*Hkv*N <= 60K units at K = 16, G = 8; 70K at G = 4). Every call shares the one array and it keeps the last
  * call's contents: the call clears on its stream whatever must start at zero, and calls whose
  * GPU work overlaps in time (different streams or host threads on one device) race on the
  * array. A bounded wait that gives up is reported through poisoned outputs (idx = -1,

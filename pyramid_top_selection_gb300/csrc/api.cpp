@@ -221,14 +221,14 @@ int pisa_select_noalloc(const pisa_shape_t* shape, const void* Q, const void* K,
   PISA_CHECK(check_ptr(score, "score", true));
   const pisa::Dims d = dims_of(shape);
   const pisa::Geo g = pisa::make_geo(d.N, d.C);
-  const size_t need = pisa::select_ws(d, g).total;
+  const size_t need = pisa::select_ws(d, g, false).total;
   if (need > pisa::noalloc_scratch_bytes())
     return fail(PISA_EUNSUPPORTED,
                 "pisa_select_noalloc: this shape needs %zu bytes of scratch, more than the fixed %zu; "
                 "use pisa_select with a caller workspace", need, pisa::noalloc_scratch_bytes());
   void* ws = nullptr;
   PISA_CHECK(cuda_rc(pisa::noalloc_scratch(&ws), "pisa_select_noalloc scratch set-up"));
-  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, nullptr, static_cast<char*>(ws), stream),
+  return cuda_rc(pisa::launch_select(d, g, Q, K, pyr_sum, idx, score, nullptr, static_cast<char*>(ws), stream, false),
                  "pisa_select_noalloc");
 }
 

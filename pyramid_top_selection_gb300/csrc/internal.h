@@ -62,7 +62,9 @@ struct AttnBwdWs {
   size_t status, delta, dq_acc, dk_acc, dv_acc, total;
 };
 int sm_count();
-SelectWs select_ws(const Dims& s, const Geo& g);
+// first: the first scored level's child dots precomputed where that pays (G <= 4); the
+// fixed-scratch entry point turns it off to keep its scratch per query small.
+SelectWs select_ws(const Dims& s, const Geo& g, bool first = true);
 AttnFwdWs attn_fwd_ws(const Dims& s);
 AttnBwdWs attn_bwd_ws(const Dims& s);
 size_t flat_ws(const Dims& s, const Geo& g);
@@ -71,7 +73,7 @@ size_t flat_ws(const Dims& s, const Geo& g);
 int launch_build_pyramid(const Dims& s, const Geo& g, const void* K, const int32_t* len,
                          int64_t tokens_per_seq, float* pyr, void* stream);
 int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
-                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream);
+                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream, bool first = true);
 int launch_select_flat(const Dims& s, const Geo& g, const void* Q, const void* K,
                        const float* pyr, int32_t* idx, float* score, char* ws, void* stream);
 int launch_select_mean(const Dims& s, const Geo& g, const void* Q, const void* K,

@@ -75,9 +75,6 @@ __device__ __forceinline__ void ldg_pair(const uint4* a, uint4& x, uint4& y) {
       : "l"(a));
 }
 
-#ifndef PISA_ROUTE_PRED
-#define PISA_ROUTE_PRED 1
-#endif
 // Two-row hi/lo MMA: rows r0 (A row g) and r1 (A row g+8) of the split pyramid (always valid
 // addresses); invalid rows contribute zeros and load nothing (a lane group whose row is
 // invalid issues no request, so sparse row sets cost only their valid rows).
@@ -89,11 +86,11 @@ __device__ __forceinline__ void mma_split_rows(float (&acc)[4], const uint4* r0,
 #pragma unroll
   for (int kp = 0; kp < KS / 2; ++kp) {
     uint4 x0[2] = {z, z}, x1[2] = {z, z};
-    if (v0 || !PISA_ROUTE_PRED) ldg_pair(r0 + 8 * kp + 2 * p, x0[0], x0[1]);
-    if (v1 || !PISA_ROUTE_PRED) ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
+    if (v0) ldg_pair(r0 + 8 * kp + 2 * p, x0[0], x0[1]);
+    if (v1) ldg_pair(r1 + 8 * kp + 2 * p, x1[0], x1[1]);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const uint4 a = v0 || PISA_ROUTE_PRED ? x0[e] : z, c = v1 || PISA_ROUTE_PRED ? x1[e] : z;
+      const uint4 a = x0[e], c = x1[e];
       const uint32_t ahi[4] = {a.x, c.x, a.y, c.y};
       const uint32_t alo[4] = {a.z, c.z, a.w, c.w};
       mma_bf16(acc, ahi, qb[2 * kp + e][0], qb[2 * kp + e][1]);
@@ -1140,7 +1137,7 @@ int launch_route_prefix(const Dims& s, const Geo& g, const void* Q, const void* 
   return cudaGetLastError();
 }
 
-SelectWs select_ws(const Dims& s, const Geo& g) {
+SelectWs select_ws(const Dims& s, const Geo& g, bool first) {
   SelectWs w{};
   const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.N;
   const size_t W = static_cast<size_t>(s.g) * s.K;
@@ -1148,7 +1145,7 @@ SelectWs select_ws(const Dims& s, const Geo& g) {
   w.status = o; o += 256;          // first: the caller finds the status word at offset 0
   w.split = o;  o += align256(static_cast<size_t>(s.B) * s.Hkv_r * g.nodes * s.d * 4);
   w.pd = o;     o += align256(units * prefix_levels(s, g) * s.G * 4);
-  w.cfirst = o; o += first_level_pre(s) ? align256(units * kFirstChildren * s.G * 4) : 0;
+  w.cfirst = o; o += first && first_level_pre(s) ? align256(units * kFirstChildren * s.G * 4) : 0;
   w.cand = o;   o += align256(units * W * 4);
   w.cscore = o; o += align256(units * W * 4);
   w.mean_end = o;                  // the PISA-1 path needs nothing past here
@@ -1172,9 +1169,9 @@ int launch_split(const Dims& s, const Geo& g, const float* pyr, uint4* spl, cuda
 }
 
 int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, const float* pyr,
-                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream) {
+                  int32_t* idx, float* score, float* head_lse, char* ws, void* stream, bool first) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const SelectWs w = select_ws(s, g);
+  const SelectWs w = select_ws(s, g, first);
   uint4* spl = reinterpret_cast<uint4*>(ws + w.split);
   int32_t* cand = reinterpret_cast<int32_t*>(ws + w.cand);
   float* cscore = reinterpret_cast<float*>(ws + w.cscore);
@@ -1182,7 +1179,7 @@ int launch_select(const Dims& s, const Geo& g, const void* Q, const void* K, con
   const GroupPlan gp = leaf_plan(s);
   const GroupWs gw = group_ws(gp, w.group);
   float* pd = reinterpret_cast<float*>(ws + w.pd);
-  float* cfirst = first_level_pre(s) ? reinterpret_cast<float*>(ws + w.cfirst) : nullptr;
+  float* cfirst = first && first_level_pre(s) ? reinterpret_cast<float*>(ws + w.cfirst) : nullptr;
   const int lp = prefix_levels(s, g);
   int err = launch_split(s, g, pyr, spl, st);
   if (err) return err;
