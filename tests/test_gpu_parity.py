@@ -20,6 +20,9 @@ CASES = [
     ("g1_b2_d64", 2, 777, 2, 2, 64, 3, False),
     ("g2_keep_all", 1, 1500, 4, 2, 64, 32, False),
     ("k1_d128", 1, 1300, 8, 1, 128, 1, True),
+    # K = 1 at G = 4: the first scored level's child dots come from the prefix pass, and a level
+    # kept whole after it (the kept node's right child not yet visible) must load its own
+    ("k1_g4_d128", 1, 1300, 4, 1, 128, 1, True),
     ("single_partial_leaf", 1, 63, 4, 1, 64, 4, False),
     ("one_token", 1, 1, 2, 1, 128, 4, False),
     ("two_leaves_b2", 2, 65, 8, 1, 128, 1, False),
@@ -137,7 +140,7 @@ def test_attention_random_selection_vs_oracle():
     check_close(lse3.cpu().numpy(), lref, atol=1e-3, rtol=0, what="lse (shuffled slots)")
 
 
-@pytest.mark.parametrize("name,Hq,Hkv,N",[("prefill_64k_gqa8", 16, 2, 65536), ("sweep_64k_gqa4", 32, 8, 65536)])
+@pytest.mark.parametrize("name,Hq,Hkv,N", [("prefill_64k_gqa8", 16, 2, 65536), ("sweep_64k_gqa4", 32, 8, 65536)])
 def test_full_size_sampled_vs_oracle(name, Hq, Hkv, N):
     # The 64K workloads at full size, launched as the benchmark launches them; the oracle
     # checks a deterministic sample of queries (units are independent once the pyramid is
