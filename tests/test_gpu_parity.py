@@ -28,6 +28,7 @@ CASES = [
     ("two_leaves_b2", 2, 65, 8, 1, 128, 1, False),
     ("g1_d128", 1, 1200, 2, 2, 128, 6, True),                 # G = 1 with d = 128
     ("g8_d64", 1, 1100, 8, 1, 64, 5, True),                   # G = 8 with d = 64
+    ("g2_d128", 1, 1100, 4, 2, 128, 6, True),                 # G = 2 with d = 128
 ]
 
 
