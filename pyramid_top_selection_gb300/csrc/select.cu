@@ -155,7 +155,7 @@ route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q
   constexpr int KS = D / 16, RQ = D / 4, QW = 16 / G, NW = prefix_warps(G), CH = D / 8;
   __shared__ __align__(16) uint4 s_key[64 * CH];                // the leaf's keys, [key][chunk ^ (key & 7)]
   __shared__ __align__(16) uint4 s_sib[kMaxSib * 2 * CH];     // split sibling rows, [level][chunk ^ (level & 7)]
-  __shared__ float s_dot[NW][16][32];                          // [row][level]: sibling dots (4 tiles of 8)
+  __shared__ float s_dot[NW][16][kMaxSib];                     // [row][level]: sibling dots
   __shared__ float s_p0[NW][16];                               // [row]: own-leaf prefix dots
   extern __shared__ __align__(16) uint4 s_ch[];                // first-level children (split rows), when asked
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,11 +269,15 @@ route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q
       mma_bf16(acc, qf[2 * kp + 1], y1.x, y1.y);
       mma_bf16(acc, qf[2 * kp + 1], y1.z, y1.w);
     }
-    const int c0 = st * 8 + 2 * p;
-    s_dot[warp][g][c0] = acc[0];
-    s_dot[warp][g][c0 + 1] = acc[1];
-    s_dot[warp][g + 8][c0] = acc[2];
-    s_dot[warp][g + 8][c0 + 1] = acc[3];
+    const int c0 = st * 8 + 2 * p;            // levels c0, c0 + 1 (none past kMaxSib - 1)
+    if (c0 < kMaxSib) {
+      s_dot[warp][g][c0] = acc[0];
+      s_dot[warp][g + 8][c0] = acc[2];
+    }
+    if (c0 + 1 < kMaxSib) {
+      s_dot[warp][g][c0 + 1] = acc[1];
+      s_dot[warp][g + 8][c0 + 1] = acc[3];
+    }
   }
   // the first scored level's child dots, into cfirst[unit][child][h] (the path child's full
   // dot too: the descent replaces it with the causal prefix); two tiles of 8 children at a
