@@ -148,7 +148,7 @@ constexpr int kMaxSib = 25;   // N < 2^31 tokens in leaves of C = 64: at most 26
 constexpr int kFirstChildren = 64;   // children of the first scored level: at most 4K (K <= 16)
 
 template <int D, int G>
-__global__ void __launch_bounds__(prefix_warps(G) * 32)
+__global__ void __launch_bounds__(prefix_warps(G) * 32, G >= 8 ? 4 : 3)   // CTAs per SM: registers, then shared memory
 route_prefix_kernel(Dims s, Geo geo, int LP, const __nv_bfloat16* __restrict__ Q,
                     const __nv_bfloat16* __restrict__ Kt, const uint4* __restrict__ spl, float* __restrict__ pd,
                     float* __restrict__ cfirst) {
