@@ -126,3 +126,17 @@ def test_workspace_sizes_grow_with_problem():
     b = pisa.make_shape(1, 65536, 16, 2, 128, 64, 16)
     for op in range(6):
         assert 256 < pisa.workspace_size(a, op) < pisa.workspace_size(b, op)   # past the status block
+
+
+def test_noalloc_select_rejects_shapes_beyond_its_scratch_on_the_host():
+    # The 32 MiB fixed scratch holds the selection workspace of about 63K (query, KV head) units
+    # at K = 16, G = 8 and 70K at G = 4 (the header's figures). Shapes past that are rejected
+    # before any CUDA call, so fake addresses are safe here; shapes within it would launch, and
+    # are left to the GPU tests.
+    f = pisa.lib().pisa_select_noalloc
+    A = 1 << 20
+    for Hq, Hkv, N in ((16, 2, 32768), (8, 2, 36864), (16, 2, 1 << 20)):
+        shape = pisa.make_shape(1, N, Hq, Hkv, 128, 64, 16)
+        rc = f(ctypes.byref(shape), A, A, A, A, None, None)
+        assert rc == _pisa.PISA_EUNSUPPORTED, (Hq, Hkv, N, rc)
+        assert "scratch" in pisa.lib().pisa_last_error().decode()
